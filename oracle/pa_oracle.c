@@ -1,0 +1,205 @@
+/*
+ * pa_oracle.c -- fp64 CPU oracle for paged-KV grouped-query decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * bench's cpu_baseline / reference arm may load this.  The CUDA path shares no
+ * code with it and never calls it.
+ *
+ * What it computes (the plain definition, no partitions, no online softmax):
+ * one query token per sequence attends over that sequence's context, which is
+ * stored in fixed-size pages reached through a block table.
+ *
+ *   for every sequence b and query head h:
+ *     kvh   = h / g,  g = Hq / Hkv          (contiguous head groups; the
+ *                                           [kv_h, gqa, ...] -> [H, ...] reshape
+ *                                           in the paged_attention_v2_pytorch.py
+ *                                           commit note, GQA broadcast section)
+ *     L     = context_lens[b]
+ *     start = (window > 0 && window < L) ? L - window : 0
+ *                                          (sliding window: the last `window`
+ *                                           positions; apache/tvm PR #20426,
+ *                                           section Correctness)
+ *     for t in [start, L):
+ *        page = block_tables[b][t / page_size], slot = t % page_size
+ *        K_t  = k_cache[page][kvh][slot][:],  V_t likewise
+ *                                          (gather through the page table,
+ *                                           key_cache[blk_ids] in the commit note)
+ *        s_t  = scale * sum_d q[b][h][d] * K_t[d]
+ *     M   = max_t s_t,  Z = sum_t exp(s_t - M),  lse = M + ln Z
+ *     out = sum_t exp(s_t - lse) * V_t     (softmax-weighted sum of V; the
+ *                                           per-partition statistics and the
+ *                                           log-sum-exp merge of the commit
+ *                                           note's Phase 1 / Phase 2 reach
+ *                                           exactly this value)
+ *   L == 0 (nothing attended): out = 0, lse = -inf.
+ *
+ * Arithmetic: every fp16 value is converted exactly to double (binary16 ->
+ * binary64 is exact), all sums and exponentials are in double.  `scale` is
+ * taken as a double.  No blocking, reordering or fusion beyond the definition.
+ *
+ * Parity status: pinned (dense textbook attention, closed forms, invariants;
+ * see tests/test_oracle_pins.py).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define PA_ORACLE_OK 0
+#define PA_ORACLE_BAD_ARG 1
+#define PA_ORACLE_BAD_PAGE 2
+#define PA_ORACLE_NO_MEM 3
+
+/* IEEE 754 binary16 -> binary64, exact: value = (-1)^s * 2^(e-15) * (1 + m/1024)
+ * for 0 < e < 31, (-1)^s * 2^-14 * (m/1024) for e == 0, inf/nan for e == 31. */
+static double half_bits_to_double(uint16_t h) {
+    const int sign = (h >> 15) & 1;
+    const int e = (h >> 10) & 0x1f;
+    const int m = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -24);              /* 2^-14 * m / 2^10 */
+    } else if (e == 31) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + m), e - 25);  /* 2^(e-15) * (1024+m) / 2^10 */
+    }
+    return sign ? -v : v;
+}
+
+double pa_oracle_half_to_double(uint16_t h) { return half_bits_to_double(h); }
+
+/*
+ * q            [B, Hq, D]                    binary16 bits
+ * k_cache      [num_pages, Hkv, page_size, D] binary16 bits
+ * v_cache      same as k_cache
+ * block_tables [B, max_pages_per_seq]         int32 physical page ids
+ * context_lens [B]                            int32
+ * out          [B, Hq, D]  double (written)
+ * lse          [B, Hq]     double (written)
+ * num_threads  OpenMP threads over (b, h); <= 0 means the runtime default.
+ * Returns 0, or a PA_ORACLE_* code (a page id outside [0, num_pages) or a
+ * context longer than the table are reported, never read).
+ */
+int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages,
+                     int max_pages_per_seq, const uint16_t* q, const uint16_t* k_cache,
+                     const uint16_t* v_cache, const int32_t* block_tables,
+                     const int32_t* context_lens, double scale, int window, double* out,
+                     double* lse, int num_threads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || page_size <= 0 ||
+        num_pages < 0 || max_pages_per_seq < 0)
+        return PA_ORACLE_BAD_ARG;
+    const int g = Hq / Hkv;
+    int status = PA_ORACLE_OK;
+
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+    (void)num_threads;
+#endif
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < (long)B * Hq; ++bh) {
+        const int b = (int)(bh / Hq);
+        const int h = (int)(bh % Hq);
+        const int kvh = h / g;
+        const int L = context_lens[b];
+        double* o = out + ((size_t)b * Hq + h) * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (L < 0 || (long)L > (long)max_pages_per_seq * page_size) {
+#pragma omp atomic write
+            status = PA_ORACLE_BAD_ARG;
+            lse[(size_t)b * Hq + h] = NAN;
+            continue;
+        }
+        const int start = (window > 0 && window < L) ? L - window : 0;
+        const int n = L - start;
+        if (n == 0) {
+            lse[(size_t)b * Hq + h] = -INFINITY;
+            continue;
+        }
+        double* s = (double*)malloc(sizeof(double) * (size_t)n);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+        if (!s || !qd) {
+            free(s);
+            free(qd);
+#pragma omp atomic write
+            status = PA_ORACLE_NO_MEM;
+            continue;
+        }
+        const uint16_t* qrow = q + ((size_t)b * Hq + h) * D;
+        for (int d = 0; d < D; ++d) qd[d] = half_bits_to_double(qrow[d]);
+
+        int bad = 0;
+        /* Step 1-2: gather K_t through the table, score it. */
+        for (int t = start; t < L && !bad; ++t) {
+            const int page = block_tables[(size_t)b * max_pages_per_seq + t / page_size];
+            if (page < 0 || page >= num_pages) {
+                bad = 1;
+                break;
+            }
+            const uint16_t* krow =
+                k_cache + (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += qd[d] * half_bits_to_double(krow[d]);
+            s[t - start] = scale * dot;
+        }
+        if (bad) {
+            free(s);
+            free(qd);
+#pragma omp atomic write
+            status = PA_ORACLE_BAD_PAGE;
+            lse[(size_t)b * Hq + h] = NAN;
+            continue;
+        }
+        /* Step 3: max, exp-sum, log-sum-exp. */
+        double M = -INFINITY;
+        for (int i = 0; i < n; ++i)
+            if (s[i] > M) M = s[i];
+        double Z = 0.0;
+        for (int i = 0; i < n; ++i) Z += exp(s[i] - M);
+        const double l = M + log(Z);
+        lse[(size_t)b * Hq + h] = l;
+        /* Step 4: softmax-weighted sum of the gathered V rows. */
+        for (int t = start; t < L; ++t) {
+            const int page = block_tables[(size_t)b * max_pages_per_seq + t / page_size];
+            const uint16_t* vrow =
+                v_cache + (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
+            const double w = exp(s[t - start] - l);
+            for (int d = 0; d < D; ++d) o[d] += w * half_bits_to_double(vrow[d]);
+        }
+        free(s);
+        free(qd);
+    }
+    return status;
+}
+
+/* Scores alone (scale * q . K_t for t in [start, L)) for one (b, h), in the same
+ * arithmetic as pa_oracle_decode; used by tests that check the log-sum-exp
+ * identity against an independent library routine.  Returns the number of
+ * scores written to s_out (capacity cap), or -1 on a bad page / argument. */
+int pa_oracle_scores(int Hq, int Hkv, int D, int page_size, int num_pages, int max_pages_per_seq,
+                     const uint16_t* q, const uint16_t* k_cache, const int32_t* block_tables,
+                     const int32_t* context_lens, double scale, int window, int b, int h,
+                     double* s_out, int cap) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return -1;
+    const int kvh = h / (Hq / Hkv);
+    const int L = context_lens[b];
+    if (L < 0 || (long)L > (long)max_pages_per_seq * page_size) return -1;
+    const int start = (window > 0 && window < L) ? L - window : 0;
+    if (L - start > cap) return -1;
+    const uint16_t* qrow = q + ((size_t)b * Hq + h) * D;
+    for (int t = start; t < L; ++t) {
+        const int page = block_tables[(size_t)b * max_pages_per_seq + t / page_size];
+        if (page < 0 || page >= num_pages) return -1;
+        const uint16_t* krow =
+            k_cache + (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += half_bits_to_double(qrow[d]) * half_bits_to_double(krow[d]);
+        s_out[t - start] = scale * dot;
+    }
+    return L - start;
+}
