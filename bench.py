@@ -1,0 +1,512 @@
+"""Benchmark of paged-KV GQA decode attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload NAME] [--no-cpu-baseline] [--no-per-workload]
+
+One step = one full decode call (partition kernel + log-sum-exp merge) over
+one batch of the workload, inputs resident in HBM.  Rank 0 prints ONE JSON
+line.  The metric is KV-read bandwidth: algorithmic bytes = 4 * Hkv * D bytes
+(fp16 K and V rows) per attended token, divided by the time per step.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (the only
+other path that runs the oracle), on bounded samples of the same workload.
+Under torchrun every rank runs its own replica of the workload (weak scaling,
+no collective on the data path); time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_gqa_pa_gb300 import workloads  # noqa: E402
+
+METRIC = "decode-attn KV-read GB/s (fraction of GB300 HBM peak); µs per decode step"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "gqa6_ctx100k"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes (read + write) per launch of the partition kernel, from one ncu
+# capture, keyed by workload; valid only while the kernel sources hash to
+# `src_sha` (otherwise the bench reports traffic = null).
+NCU_TRAFFIC = {}
+
+
+def kernel_src_sha() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "paged_kv_gqa_pa_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def attended_tokens(case) -> int:
+    n = 0
+    for L in case.context_lens.tolist():
+        n += min(L, case.window) if case.window > 0 else L
+    return n
+
+
+def kv_bytes(case) -> int:
+    return 4 * case.Hkv * case.D * attended_tokens(case)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.idx = "0"
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self.idx = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            if vis:
+                self.idx = vis.split(",")[0]
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class GpuArm:
+    def __init__(self, case, device, partition_size=None):
+        import torch
+        import paged_kv_gqa_pa_gb300 as pa
+        self.torch = torch
+        self.pa = pa
+        self.case = case
+        self.device = device
+        self.q = torch.from_numpy(case.q).to(device)
+        self.k = torch.from_numpy(case.k_cache).to(device)
+        self.v = torch.from_numpy(case.v_cache).to(device)
+        self.bt = torch.from_numpy(case.block_tables).to(device)
+        self.cl = torch.from_numpy(case.context_lens).to(device)
+        B, Hq, D = case.q.shape
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        ps = case.partition_size if partition_size is None else partition_size
+        self.plan = pa.pa_plan(B, Hq, case.Hkv, D, case.page_size, case.num_pages,
+                               case.max_pages_per_seq, case.max_context_len, case.window, ps, sms)
+        self.out = torch.empty((B, Hq, D), dtype=torch.float16, device=device)
+        self.lse = torch.empty((B, Hq), dtype=torch.float32, device=device)
+        self.ws = pa.new_workspace(self.plan, device)
+        self.stream = torch.cuda.current_stream(device)
+        self.launches_per_step = 1 if self.plan.num_partitions == 1 else 2
+
+    def partitions(self):
+        self.pa.pa_decode_partitions(self.plan, self.q, self.k, self.v, self.bt, self.cl,
+                                     self.case.scale, self.case.window, self.out, self.lse,
+                                     self.ws, self.stream)
+
+    def merge(self):
+        self.pa.pa_merge(self.plan, self.cl, self.out, self.lse, self.ws, self.stream)
+
+    def step(self):
+        self.partitions()
+        self.merge()
+
+    def check_error(self):
+        err = self.pa.pa_get_error(self.ws, self.stream)
+        if err:
+            raise RuntimeError(f"device error word {err:#x}")
+
+
+def l2_flush_buffer(torch, device):
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    return torch.empty(max(2 * l2, 1 << 20), dtype=torch.uint8, device=device)
+
+
+def time_steps(arm, steps, warmup):
+    """K back-to-back steps bracketed by two events (inputs larger than L2).
+    Returns ms per step."""
+    torch = arm.torch
+    for _ in range(warmup):
+        arm.step()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(arm.stream)
+    for _ in range(steps):
+        arm.step()
+    end.record(arm.stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def time_partition_kernel(arm, steps, flush=None):
+    """Mean duration of the partition kernel alone: events on its stream around
+    each launch (the merge runs between, outside the events)."""
+    torch = arm.torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        ev[i][0].record(arm.stream)
+        arm.partitions()
+        ev[i][1].record(arm.stream)
+        arm.merge()
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def time_flushed(arm, iters, flush):
+    """Per-iteration step time with an L2 flush (outside the events) before each."""
+    torch = arm.torch
+    for _ in range(3):
+        arm.step()
+    res, kres = [], []
+    for i in range(iters):
+        flush.fill_(i & 0xFF)
+        a, m, b = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(arm.stream)
+        arm.partitions()
+        m.record(arm.stream)
+        arm.merge()
+        b.record(arm.stream)
+        torch.cuda.synchronize()
+        res.append(a.elapsed_time(b))
+        kres.append(a.elapsed_time(m))
+    return statistics.median(res), statistics.median(kres)
+
+
+def e2e_steps(arm, steps, warmup, upload_kv=False):
+    """Through the public API with host buffers: per step, copy the step's inputs
+    from pinned host memory, decode, read out + LSE back to pinned host."""
+    torch = arm.torch
+    c = arm.case
+    hq = torch.from_numpy(c.q).pin_memory()
+    hbt = torch.from_numpy(c.block_tables).pin_memory()
+    hcl = torch.from_numpy(c.context_lens).pin_memory()
+    hout = torch.empty(arm.out.shape, dtype=arm.out.dtype).pin_memory()
+    hlse = torch.empty(arm.lse.shape, dtype=arm.lse.dtype).pin_memory()
+    hk = hv = None
+    if upload_kv:
+        hk = torch.from_numpy(c.k_cache).pin_memory()
+        hv = torch.from_numpy(c.v_cache).pin_memory()
+    h2d = hq.numel() * 2 + hbt.numel() * 4 + hcl.numel() * 4
+    if upload_kv:
+        h2d += hk.numel() * 2 + hv.numel() * 2
+    d2h = hout.numel() * 2 + hlse.numel() * 4
+
+    def one():
+        arm.q.copy_(hq, non_blocking=True)
+        arm.bt.copy_(hbt, non_blocking=True)
+        arm.cl.copy_(hcl, non_blocking=True)
+        if upload_kv:
+            arm.k.copy_(hk, non_blocking=True)
+            arm.v.copy_(hv, non_blocking=True)
+        arm.step()
+        hout.copy_(arm.out, non_blocking=True)
+        hlse.copy_(arm.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(arm.stream)
+    for _ in range(steps):
+        one()
+    b.record(arm.stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return ms, h2d, d2h
+
+
+class OracleSampler:
+    """Times the oracle, as it stands, on a bounded sample of the workload:
+    sequence 0, all its query heads, the last L of its attended tokens, with L
+    sized to a time budget from a one-thread calibration run."""
+
+    def __init__(self, case, threads=0):
+        import oracle
+        self.oracle = oracle
+        self.case = case
+        self.threads = threads or os.cpu_count() or 1
+        L0 = int(case.context_lens[0])
+        self.att = min(L0, case.window) if case.window > 0 else L0
+        probe = max(1, min(self.att, 512))
+        t0 = time.perf_counter()
+        self._run(probe, 1)
+        self.sec_per_token_1thread = max((time.perf_counter() - t0) / probe, 1e-9)
+
+    def _sub(self, L):
+        c = self.case
+        return workloads.Case(name=c.name + "_sample", q=np.ascontiguousarray(c.q[:1]),
+                              k_cache=c.k_cache, v_cache=c.v_cache,
+                              block_tables=c.block_tables[:1],
+                              context_lens=c.context_lens[:1].copy(), scale=c.scale, window=L,
+                              partition_size=0, seed=c.seed)
+
+    def _run(self, L, threads):
+        s = self._sub(L)
+        self.oracle.decode(s.q, s.k_cache, s.v_cache, s.block_tables, s.context_lens, s.scale,
+                           s.window, num_threads=threads)
+
+    def tokens_for(self, budget_s):
+        par = min(self.threads, self.case.Hq)
+        L = int(budget_s * par / self.sec_per_token_1thread)
+        return max(16, min(self.att, L))
+
+    def run(self, L):
+        t0 = time.perf_counter()
+        self._run(L, self.threads)
+        dt = time.perf_counter() - t0
+        c = self.case
+        byts = 4 * c.Hkv * c.D * L
+        used = min(self.threads, c.Hq)
+        desc = (f"sequence 0 of {c.B}, all {c.Hq} query heads, last {L} of {self.att} attended "
+                f"tokens; fp64 C oracle, OpenMP over heads")
+        return byts / dt / 1e9, dt, desc, used
+
+
+def run_reference(args):
+    world, rank, local = dist_setup()
+    if rank != 0:
+        return 0
+    case = workloads.workload(args.workload)
+    sampler = OracleSampler(case)
+    per_step_budget = args.reference_budget_s / max(1, args.steps + args.warmup)
+    L = sampler.tokens_for(per_step_budget)
+    for _ in range(args.warmup):
+        sampler.run(L)
+    vals, secs = [], []
+    desc, used = "", 1
+    for _ in range(args.steps):
+        v, dt, desc, used = sampler.run(L)
+        vals.append(v)
+        secs.append(dt)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.median(secs) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "l2": "host CPU"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    case = workloads.workload(args.workload)
+    arm = GpuArm(case, device)
+    byts = kv_bytes(case)
+    flush = None
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    big = byts > 2 * l2
+    if not big:
+        flush = l2_flush_buffer(torch, device)
+
+    # correctness of the launch configuration being timed (device error word)
+    arm.step()
+    arm.check_error()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(device) as clk:
+        if big:
+            ms = time_steps(arm, args.steps, args.warmup)
+        else:
+            ms, _ = time_flushed(arm, args.steps, flush)
+        kern_ms = time_partition_kernel(arm, min(args.steps, 500), flush)
+    if world > 1:
+        torch.distributed.barrier()
+    arm.check_error()
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = byts * world / (ms_max * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peaks()
+    kern_gbs = byts / (kern_ms * 1e-3) / 1e9
+    sha = kernel_src_sha()
+    tr = NCU_TRAFFIC.get(args.workload)
+    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == sha else None
+
+    e2e_ms, h2d, d2h = e2e_steps(arm, max(10, min(args.steps, 200)), 3)
+    e2e = {"value": byts / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "note": "per step: H2D of q, block table, context lengths (KV cache resident); "
+                   "D2H of out and LSE"}
+    e2e_kv = None
+    if not args.no_kv_upload:
+        kv_ms, kv_h2d, kv_d2h = e2e_steps(arm, 5, 1, upload_kv=True)
+        e2e_kv = {"value": byts / (kv_ms * 1e-3) / 1e9, "unit": UNIT,
+                  "h2d_bytes_per_step": kv_h2d, "d2h_bytes_per_step": kv_d2h,
+                  "ms_per_step": kv_ms}
+    arm.check_error()
+
+    per = None
+    if not args.no_per_workload and rank == 0:
+        per = {}
+        fl = l2_flush_buffer(torch, device)
+        for name in workloads.WORKLOAD_ORDER:
+            c = case if name == args.workload else workloads.workload(name)
+            a = arm if name == args.workload else GpuArm(c, device)
+            b = kv_bytes(c)
+            med, kmed = time_flushed(a, args.per_workload_iters, fl)
+            a.check_error()
+            per[name] = {"us_per_step": med * 1e3, "partition_kernel_us": kmed * 1e3,
+                         "kv_bytes": b, "kv_gbs": b / (med * 1e-3) / 1e9,
+                         "frac_of_measured_hbm": b / (med * 1e-3) / 1e9 / peak,
+                         "frac_of_nominal_8tbs": b / (med * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
+                         "partitions": a.plan.num_partitions,
+                         "partition_size": a.plan.partition_size, "ctas": a.plan.ctas,
+                         "l2": "flushed before each step"}
+            if a is not arm:
+                del a
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        sampler = OracleSampler(case)
+        v, dt, desc, used = sampler.run(sampler.tokens_for(args.cpu_budget_s))
+        cpu = {"value": v, "unit": UNIT, "cores": used, "kind": "oracle", "sample": desc,
+               "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "us_per_step": ms_max * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "batch": case.B, "num_q_heads": case.Hq,
+                       "num_kv_heads": case.Hkv, "head_dim": case.D, "page_size": case.page_size,
+                       "context_lens": "x".join(str(int(x)) for x in
+                                                sorted(set(case.context_lens.tolist()))),
+                       "window": case.window, "partition_size": arm.plan.partition_size,
+                       "partitions": arm.plan.num_partitions, "kv_bytes_per_step": byts,
+                       "l2": "inputs larger than L2" if big else "L2 flushed between steps",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": kern_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": kern_gbs / peak, "traffic": traffic,
+                         "peak_kind": peak_kind, "kernel": "attend_kernel (partition kernel)",
+                         "kernel_us": kern_ms * 1e3, "frac_of_nominal_8tbs":
+                             kern_gbs / NOMINAL_HBM_GBS, "src_sha": sha},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "e2e_with_kv_upload": e2e_kv,
+            "gpu_launches": args.steps * arm.launches_per_step,
+            "clocks": clk.summary(),
+            "per_workload": per,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.WORKLOAD_ORDER)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true")
+    ap.add_argument("--no-kv-upload", action="store_true")
+    ap.add_argument("--per-workload-iters", type=int, default=50)
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,150 @@
+/*
+ * pa.h -- C ABI of the GB300 paged-KV grouped-query decode-attention library
+ * (libpa_gb300.so, built for sm_103a).
+ *
+ * One query token per sequence attends over that sequence's context, stored in
+ * fixed-size pages of a KV cache reached through a block (page) table, with
+ * grouped-query heads: Hq = g * Hkv and query head h reads KV head h / g (the
+ * [kv_h, gqa, ...] -> [H, ...] grouping of the paged_attention_v2_pytorch.py
+ * commit note, GQA broadcast section).  The attended context of each sequence
+ * is cut into partitions; each partition yields a partial output and its
+ * (max, exp-sum), and a log-sum-exp merge combines the partitions into the
+ * final output and LSE (the commit note's Phase 1 and Phase 2).  When one
+ * partition covers the whole attended context the kernel writes the output
+ * directly and no merge runs (the short-context nest kept by apache/tvm PR
+ * #20426, section Change).
+ *
+ * Result computed, for sequence b and query head h (natural log):
+ *   start = (window > 0 && window < L_b) ? L_b - window : 0
+ *   s_t   = scale * q[b,h,:] . K_t   for t in [start, L_b)
+ *   lse   = log sum_t exp(s_t);   out = sum_t exp(s_t - lse) * V_t
+ * L_b == 0 (or an empty attended range) gives out = 0, lse = -inf.
+ *
+ * Layouts (row-major, element strides implied by the shapes):
+ *   q            fp16  [B, Hq, D]
+ *   k_cache      fp16  [num_pages, Hkv, page_size, D]   (v_cache the same)
+ *   block_tables int32 [B, max_pages_per_seq]   entry j = physical page of the
+ *                                               sequence's logical page j
+ *   context_lens int32 [B]
+ *   out          fp16  [B, Hq, D]   (round to nearest even)
+ *   lse          fp32  [B, Hq]
+ * Supported: head_dim in {64, 128, 256}; page_size 16; Hq % Hkv == 0 with
+ * g = Hq / Hkv split into at most ceil(g / 8) equal head chunks per CTA.
+ * q, k_cache, v_cache, out and workspace must be 16-byte aligned.
+ *
+ * Ownership: every pointer is caller-owned device memory (the library
+ * allocates nothing, holds no device memory and keeps no per-call state).
+ * Calls are asynchronous on the given stream (a cudaStream_t passed as void*;
+ * NULL = the legacy default stream) and never synchronise the host, except
+ * pa_get_error.
+ *
+ * Errors: every call returns a pa_status.  Argument checks happen on the host
+ * before anything is launched.  Data-dependent faults found on the device (a
+ * page id outside [0, num_pages), a context length outside
+ * [0, max_context_len] or longer than the table) are never read through: the
+ * kernel sets a bit in the workspace's device error word (pa_get_error) and
+ * writes NaN to the affected output rows.
+ */
+#ifndef PA_GB300_H
+#define PA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad shape or inconsistent plan */
+    PA_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, page_size, group size */
+    PA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    PA_ERR_WORKSPACE = 4      /* workspace missing or smaller than plan.workspace_bytes */
+} pa_status;
+
+/* Bits of the device error word (pa_get_error). */
+#define PA_DEVERR_BAD_PAGE 1u     /* a block-table entry outside [0, num_pages) */
+#define PA_DEVERR_BAD_LENGTH 2u   /* a context length outside the plan's bounds */
+#define PA_DEVERR_TIMEOUT 4u      /* a bounded wait on a bulk copy gave up */
+
+typedef struct pa_plan {
+    int batch;              /* B */
+    int num_q_heads;        /* Hq */
+    int num_kv_heads;       /* Hkv */
+    int head_dim;           /* D */
+    int page_size;          /* tokens per page (16) */
+    int num_pages;          /* pages in the K (and V) pool */
+    int max_pages_per_seq;  /* row length of block_tables */
+    int max_context_len;    /* upper bound on every context_lens[b] */
+    int window;             /* sliding window in tokens, 0 = whole context */
+    int partition_size;     /* tokens per partition, a multiple of page_size */
+    int num_partitions;     /* partitions per (sequence, KV head); 1 = no split, no merge */
+    int heads_per_cta;      /* query heads one CTA serves (g or a divisor of it) */
+    int num_sms;            /* SM count the plan was made for */
+    int ctas;               /* CTAs of the attention kernel */
+    size_t workspace_bytes; /* bytes of device workspace pa_decode needs */
+    int reserved[8];
+} pa_plan_t;
+
+/*
+ * Choose the partitioning for a decode call (host only, no device access
+ * unless num_sms == 0, which queries the current device).
+ *   partition_size  0 = automatic (enough partitions to fill num_sms SMs),
+ *                   else the tokens per partition (multiple of page_size).
+ * The attended span of a sequence is at most ceil(max_context_len / ps) pages,
+ * or ceil((window - 1) / ps) + 1 pages with a window; num_partitions =
+ * ceil(span / (partition_size / ps)).  The 100000-token, 512-token-partition
+ * case of the commit note therefore gets 196 partitions (the last one holds
+ * 160 tokens).
+ * Returns PA_OK and fills *plan, or PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED.
+ */
+int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+            int num_pages, int max_pages_per_seq, int max_context_len, int window,
+            int partition_size, int num_sms, pa_plan_t* plan);
+
+/*
+ * Full decode step: the partition kernel (gather pages, q.K, per-partition
+ * softmax statistics, P.V) and, when plan->num_partitions > 1, the
+ * log-sum-exp merge.  `window` must equal plan->window.
+ * workspace: >= plan->workspace_bytes of device memory, zero-filled once when
+ * allocated (its first word is the device error word); it holds the
+ * partition partials between the two kernels, so concurrent calls must not
+ * share one workspace.
+ */
+int pa_decode(const pa_plan_t* plan, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens, float scale, int window,
+              void* out, float* lse, void* workspace, void* stream);
+
+/*
+ * The two halves of pa_decode, for callers (and the benchmark) that time or
+ * schedule them separately.  pa_decode_partitions writes the partition
+ * partials to the workspace (or, with one partition, out and lse directly);
+ * pa_merge reads them and writes out and lse (a no-op with one partition).
+ * Same arguments and rules as pa_decode.
+ */
+int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cache,
+                         const void* v_cache, const int32_t* block_tables,
+                         const int32_t* context_lens, float scale, int window, void* out,
+                         float* lse, void* workspace, void* stream);
+int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, float* lse,
+             void* workspace, void* stream);
+
+/*
+ * Synchronise `stream`, read the device error word kept in `workspace`
+ * (PA_DEVERR_* bits, 0 = none) into *device_error, and reset it to 0 when
+ * `clear` is non-zero.
+ */
+int pa_get_error(void* workspace, void* stream, int clear, unsigned* device_error);
+
+/* Static text for a pa_status value. */
+const char* pa_status_string(int status);
+
+/* Library version, (major << 16) | minor. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_GB300_H */

@@ -1,0 +1,217 @@
+"""ctypes binding of libpa_gb300.so (include/pa.h), argument marshalling only.
+
+Every function here checks and converts arguments (torch CUDA tensors ->
+device pointers, the current torch stream -> cudaStream_t) and calls the C ABI
+of the same name; all computation runs in the library's CUDA kernels.  There
+is no CPU fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_CUDA = 3
+PA_ERR_WORKSPACE = 4
+PA_DEVERR_BAD_PAGE = 1
+PA_DEVERR_BAD_LENGTH = 2
+PA_DEVERR_TIMEOUT = 4
+
+EXPORTED = ("pa_plan", "pa_decode", "pa_decode_partitions", "pa_merge", "pa_get_error",
+            "pa_status_string", "pa_version")
+
+
+class pa_plan_t(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int),
+        ("num_q_heads", ctypes.c_int),
+        ("num_kv_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int),
+        ("page_size", ctypes.c_int),
+        ("num_pages", ctypes.c_int),
+        ("max_pages_per_seq", ctypes.c_int),
+        ("max_context_len", ctypes.c_int),
+        ("window", ctypes.c_int),
+        ("partition_size", ctypes.c_int),
+        ("num_partitions", ctypes.c_int),
+        ("heads_per_cta", ctypes.c_int),
+        ("num_sms", ctypes.c_int),
+        ("ctas", ctypes.c_int),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("reserved", ctypes.c_int * 8),
+    ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+
+
+class PAError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__(f"{fn} failed: {status} ({pa_status_string(status)})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load the built library (built by paged_kv_gqa_pa_gb300.build / __graft_entry__.build)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is not built; run `python -m paged_kv_gqa_pa_gb300.build` "
+                "(there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i = ctypes.c_int
+        pp = ctypes.POINTER(pa_plan_t)
+        lib.pa_plan.argtypes = [i] * 11 + [pp]
+        lib.pa_plan.restype = i
+        dec = [pp, P, P, P, P, P, ctypes.c_float, i, P, P, P, P]
+        lib.pa_decode.argtypes = dec
+        lib.pa_decode.restype = i
+        lib.pa_decode_partitions.argtypes = dec
+        lib.pa_decode_partitions.restype = i
+        lib.pa_merge.argtypes = [pp, P, P, P, P, P]
+        lib.pa_merge.restype = i
+        lib.pa_get_error.argtypes = [P, P, i, ctypes.POINTER(ctypes.c_uint)]
+        lib.pa_get_error.restype = i
+        lib.pa_status_string.argtypes = [i]
+        lib.pa_status_string.restype = ctypes.c_char_p
+        lib.pa_version.argtypes = []
+        lib.pa_version.restype = i
+        _lib = lib
+        return lib
+
+
+def pa_status_string(status: int) -> str:
+    return load().pa_status_string(int(status)).decode()
+
+
+def pa_version() -> int:
+    return load().pa_version()
+
+
+def pa_plan(batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+            max_pages_per_seq, max_context_len, window=0, partition_size=0,
+            num_sms=0) -> pa_plan_t:
+    plan = pa_plan_t()
+    st = load().pa_plan(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim),
+                        int(page_size), int(num_pages), int(max_pages_per_seq),
+                        int(max_context_len), int(window), int(partition_size), int(num_sms),
+                        ctypes.byref(plan))
+    if st != PA_OK:
+        raise PAError("pa_plan", st)
+    return plan
+
+
+def _dev_ptr(t, name, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _decode_args(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window, out, lse,
+                 workspace, stream):
+    return (ctypes.byref(plan), _dev_ptr(q, "q", torch.float16),
+            _dev_ptr(k_cache, "k_cache", torch.float16),
+            _dev_ptr(v_cache, "v_cache", torch.float16),
+            _dev_ptr(block_tables, "block_tables", torch.int32),
+            _dev_ptr(context_lens, "context_lens", torch.int32), ctypes.c_float(scale),
+            int(window), _dev_ptr(out, "out", torch.float16), _dev_ptr(lse, "lse", torch.float32),
+            _dev_ptr(workspace, "workspace"), _stream_ptr(stream))
+
+
+def pa_decode(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window, out, lse,
+              workspace, stream=None) -> None:
+    st = load().pa_decode(*_decode_args(plan, q, k_cache, v_cache, block_tables, context_lens,
+                                        scale, window, out, lse, workspace, stream))
+    if st != PA_OK:
+        raise PAError("pa_decode", st)
+
+
+def pa_decode_partitions(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window,
+                         out, lse, workspace, stream=None) -> None:
+    st = load().pa_decode_partitions(*_decode_args(plan, q, k_cache, v_cache, block_tables,
+                                                   context_lens, scale, window, out, lse,
+                                                   workspace, stream))
+    if st != PA_OK:
+        raise PAError("pa_decode_partitions", st)
+
+
+def pa_merge(plan, context_lens, out, lse, workspace, stream=None) -> None:
+    st = load().pa_merge(ctypes.byref(plan), _dev_ptr(context_lens, "context_lens", torch.int32),
+                         _dev_ptr(out, "out", torch.float16), _dev_ptr(lse, "lse", torch.float32),
+                         _dev_ptr(workspace, "workspace"), _stream_ptr(stream))
+    if st != PA_OK:
+        raise PAError("pa_merge", st)
+
+
+def pa_get_error(workspace, stream=None, clear=True) -> int:
+    v = ctypes.c_uint(0)
+    st = load().pa_get_error(_dev_ptr(workspace, "workspace"), _stream_ptr(stream),
+                             1 if clear else 0, ctypes.byref(v))
+    if st != PA_OK:
+        raise PAError("pa_get_error", st)
+    return int(v.value)
+
+
+def new_workspace(plan, device=None) -> torch.Tensor:
+    """Zero-filled device workspace of plan.workspace_bytes (uint8)."""
+    return torch.zeros(max(int(plan.workspace_bytes), 256), dtype=torch.uint8, device=device)
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale, window=0,
+           partition_size=0, max_context_len=None, stream=None):
+    """Convenience call: plan, allocate out/lse/workspace with torch, decode.
+
+    max_context_len defaults to the table's capacity (block_tables.shape[1] *
+    page_size), which needs no device read.  Returns (out, lse, plan,
+    device_error) -- device_error is read back, so this call synchronises.
+    """
+    B, Hq, D = q.shape
+    num_pages, Hkv, ps, _ = k_cache.shape
+    maxp = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = maxp * ps
+    plan = pa_plan(B, Hq, Hkv, D, ps, num_pages, maxp, max_context_len, window, partition_size,
+                   torch.cuda.get_device_properties(q.device).multi_processor_count)
+    out = torch.empty((B, Hq, D), dtype=torch.float16, device=q.device)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    ws = new_workspace(plan, q.device)
+    pa_decode(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window, out, lse, ws,
+              stream)
+    err = pa_get_error(ws, stream)
+    return out, lse, plan, err

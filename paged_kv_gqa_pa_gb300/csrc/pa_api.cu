@@ -1,0 +1,389 @@
+// pa_api.cu -- the C ABI (include/pa.h): host-side planning and argument
+// checks, the launch of the partition kernel, and the log-sum-exp merge kernel.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+template <int D>
+cudaError_t launch_attend_d(int G, bool split, const AttendParams& p, dim3 grid,
+                            cudaStream_t stream);
+
+int attend_ctas_per_sm(int D) {
+    switch (D) {
+        case 64: return AttendCfg<64>::kMinBlocks;
+        case 128: return AttendCfg<128>::kMinBlocks;
+        default: return AttendCfg<256>::kMinBlocks;
+    }
+}
+
+cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 grid,
+                          cudaStream_t stream) {
+    switch (D) {
+        case 64: return launch_attend_d<64>(G, split, p, grid, stream);
+        case 128: return launch_attend_d<128>(G, split, p, grid, stream);
+        case 256: return launch_attend_d<256>(G, split, p, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Log-sum-exp merge of the partition partials (the Phase 2 reduction of the
+// paged_attention_v2_pytorch.py commit note):
+//   M = max_p m_p,  w_p = 2^(m_p - M) * l_p,  Lambda = sum_p w_p
+//   out = sum_p w_p * o_p / Lambda,  lse = (M + log2 Lambda) * ln 2
+// with m in the log2 domain and o_p already divided by its own exp-sum l_p.
+// One CTA per (query head, sequence); 256 threads = (1024 / D) partition
+// groups x (D / 4) float4 columns, reduced across groups in shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kMergeThreads = 256;
+
+__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int mask = 16; mask > 0; mask >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, mask);
+        v = is_max ? fmaxf(v, o) : v + o;
+    }
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = red[0];
+    for (int w = 1; w < kMergeThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+    return v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+    constexpr int D4 = D / 4;
+    constexpr int NGRP = kMergeThreads / D4;
+    __shared__ float s_w[kMaxPartitions];
+    __shared__ float s_red[32];
+    __shared__ __align__(16) float s_acc[NGRP][D];
+
+    const int h = blockIdx.x;
+    const int b = blockIdx.y;
+    const size_t bh = (size_t)b * p.Hq + h;
+    const size_t row0 = bh * p.P;
+    const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, p.pages_per_part);
+    __half* orow = p.out + bh * D;
+    if (!sp.valid) {
+        if (threadIdx.x == 0 && h == 0) atomicOr(p.err, PA_DEVERR_BAD_LENGTH);
+        for (int d = threadIdx.x; d < D; d += kMergeThreads) orow[d] = __float2half_rn(NAN);
+        if (threadIdx.x == 0) p.lse[bh] = NAN;
+        return;
+    }
+    const int np = sp.num_parts;
+    if (np == 0) {
+        for (int d = threadIdx.x; d < D; d += kMergeThreads) orow[d] = __float2half_rn(0.f);
+        if (threadIdx.x == 0) p.lse[bh] = -INFINITY;
+        return;
+    }
+    float mx = -INFINITY;
+    for (int i = threadIdx.x; i < np; i += kMergeThreads) mx = fmaxf(mx, p.ws_m[row0 + i]);
+    const float M = block_reduce(mx, s_red, true);
+    float sum = 0.f;
+    for (int i = threadIdx.x; i < np; i += kMergeThreads) {
+        const float l = p.ws_l[row0 + i];
+        // l == 0 marks a partition with nothing attended; a NaN l (a partition
+        // that found a bad page) is kept so the NaN reaches the output.
+        const float w = (l == 0.f) ? 0.f : ex2(p.ws_m[row0 + i] - M) * l;
+        s_w[i] = w;
+        sum += w;
+    }
+    const float lam = block_reduce(sum, s_red, false);  // also orders the s_w writes
+    const float inv = 1.f / lam;
+
+    const int grp = threadIdx.x / D4;
+    const int d = (threadIdx.x % D4) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = grp; i < np; i += NGRP) {
+        const float w = s_w[i];
+        const float4 o = *reinterpret_cast<const float4*>(p.ws_o + (row0 + i) * D + d);
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+    }
+    *reinterpret_cast<float4*>(&s_acc[grp][d]) = acc;
+    __syncthreads();
+    for (int dd = threadIdx.x; dd < D; dd += kMergeThreads) {
+        float a = 0.f;
+#pragma unroll
+        for (int g = 0; g < NGRP; ++g) a += s_acc[g][dd];
+        orow[dd] = __float2half_rn(a * inv);
+    }
+    if (threadIdx.x == 0) p.lse[bh] = (M + log2f(lam)) * 0.69314718055994531f;
+}
+
+cudaError_t launch_merge(int D, const MergeParams& p, cudaStream_t stream) {
+    const dim3 grid(p.Hq, p.B);
+    switch (D) {
+        case 64: merge_kernel<64><<<grid, kMergeThreads, 0, stream>>>(p); break;
+        case 128: merge_kernel<128><<<grid, kMergeThreads, 0, stream>>>(p); break;
+        case 256: merge_kernel<256><<<grid, kMergeThreads, 0, stream>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+// Workspace layout: [control block | m (B*Hq*P) | l (B*Hq*P) | o (B*Hq*P*D)],
+// each region 256-byte aligned.  The control block's first word is the device
+// error word.
+struct WsLayout {
+    size_t m_off, l_off, o_off, total;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static WsLayout ws_layout(int B, int Hq, int D, int P) {
+    WsLayout w;
+    if (P <= 1) {
+        w.m_off = w.l_off = w.o_off = kCtrlBytes;
+        w.total = kCtrlBytes;
+        return w;
+    }
+    const size_t rows = (size_t)B * Hq * P;
+    w.m_off = kCtrlBytes;
+    w.l_off = w.m_off + align256(rows * 4);
+    w.o_off = w.l_off + align256(rows * 4);
+    w.total = w.o_off + align256(rows * D * 4);
+    return w;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_version(void) { return (0 << 16) | 1; }
+
+const char* pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PA_ERR_CUDA: return "CUDA error";
+        case PA_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+            int num_pages, int max_pages_per_seq, int max_context_len, int window,
+            int partition_size, int num_sms, pa_plan_t* plan) {
+    if (!plan) return PA_ERR_INVALID_ARG;
+    memset(plan, 0, sizeof(*plan));
+    if (batch < 0 || batch > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0 || head_dim <= 0 || page_size <= 0 || num_pages <= 0 ||
+        max_pages_per_seq <= 0 || max_context_len < 0 || window < 0 || partition_size < 0 ||
+        num_sms < 0)
+        return PA_ERR_INVALID_ARG;
+    if ((long long)max_context_len > (long long)max_pages_per_seq * page_size)
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (page_size != kPageSize) return PA_ERR_UNSUPPORTED;
+    if (partition_size % page_size != 0) return PA_ERR_INVALID_ARG;
+
+    const int g = num_q_heads / num_kv_heads;
+    const int nchunk = (g + kMaxHeadsPerCta - 1) / kMaxHeadsPerCta;
+    if (g % nchunk != 0) return PA_ERR_UNSUPPORTED;
+    const int G = g / nchunk;
+    if ((long long)num_kv_heads * nchunk > 65535) return PA_ERR_UNSUPPORTED;
+
+    if (num_sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
+    }
+
+    // Pages a sequence can attend: ceil(Lmax / ps), or with a window at most
+    // ceil((window - 1) / ps) + 1 (the window need not start on a page edge).
+    int span = (max_context_len + page_size - 1) / page_size;
+    if (window > 0) {
+        const int wspan = (window - 1 + page_size - 1) / page_size + 1;
+        if (wspan < span) span = wspan;
+    }
+    if (span < 1) span = 1;
+
+    int pp;  // pages per partition
+    if (partition_size > 0) {
+        pp = partition_size / page_size;
+    } else {
+        // Enough CTAs for two waves of the kernel's resident CTAs, with at
+        // least one page per warp; no split when one pass already fills it.
+        const long long per_part = (long long)batch * num_kv_heads * nchunk;
+        const long long want = 2LL * num_sms * attend_ctas_per_sm(head_dim);
+        int parts = per_part > 0 ? (int)((want + per_part - 1) / per_part) : 1;
+        if (parts < 1) parts = 1;
+        pp = (span + parts - 1) / parts;
+        if (pp < kWarps) pp = kWarps;
+        if (pp > kMaxPagesPerPart) pp = kMaxPagesPerPart;
+    }
+    if (pp > kMaxPagesPerPart) return PA_ERR_UNSUPPORTED;
+    const int P = (span + pp - 1) / pp;
+    if (P > kMaxPartitions) return PA_ERR_UNSUPPORTED;
+
+    plan->batch = batch;
+    plan->num_q_heads = num_q_heads;
+    plan->num_kv_heads = num_kv_heads;
+    plan->head_dim = head_dim;
+    plan->page_size = page_size;
+    plan->num_pages = num_pages;
+    plan->max_pages_per_seq = max_pages_per_seq;
+    plan->max_context_len = max_context_len;
+    plan->window = window;
+    plan->partition_size = pp * page_size;
+    plan->num_partitions = P;
+    plan->heads_per_cta = G;
+    plan->num_sms = num_sms;
+    plan->ctas = P * num_kv_heads * nchunk * batch;
+    plan->workspace_bytes = ws_layout(batch, num_q_heads, head_dim, P).total;
+    return PA_OK;
+}
+
+static int check_plan(const pa_plan_t* plan) {
+    if (!plan) return PA_ERR_INVALID_ARG;
+    const int B = plan->batch, Hq = plan->num_q_heads, Hkv = plan->num_kv_heads;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || plan->page_size != kPageSize ||
+        plan->num_partitions < 1 || plan->num_partitions > kMaxPartitions ||
+        plan->partition_size < kPageSize || plan->partition_size % kPageSize != 0 ||
+        plan->partition_size / kPageSize > kMaxPagesPerPart || plan->num_pages <= 0 ||
+        plan->max_pages_per_seq <= 0 || plan->max_context_len < 0 || plan->window < 0)
+        return PA_ERR_INVALID_ARG;
+    if (plan->head_dim != 64 && plan->head_dim != 128 && plan->head_dim != 256)
+        return PA_ERR_UNSUPPORTED;
+    const int g = Hq / Hkv;
+    const int G = plan->heads_per_cta;
+    if (G < 1 || G > kMaxHeadsPerCta || g % G != 0) return PA_ERR_INVALID_ARG;
+    if (plan->workspace_bytes < ws_layout(B, Hq, plan->head_dim, plan->num_partitions).total)
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cache,
+                         const void* v_cache, const int32_t* block_tables,
+                         const int32_t* context_lens, float scale, int window, void* out,
+                         float* lse, void* workspace, void* stream) {
+    int st = check_plan(plan);
+    if (st != PA_OK) return st;
+    if (window != plan->window) return PA_ERR_INVALID_ARG;
+    if (!workspace) return PA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PA_ERR_INVALID_ARG;
+    if (plan->batch == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !lse)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return PA_ERR_INVALID_ARG;
+
+    const int D = plan->head_dim;
+    const int P = plan->num_partitions;
+    const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, D, P);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    AttendParams p;
+    p.q = static_cast<const __half*>(q);
+    p.k = static_cast<const __half*>(k_cache);
+    p.v = static_cast<const __half*>(v_cache);
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = static_cast<__half*>(out);
+    p.lse = lse;
+    p.ws_m = reinterpret_cast<float*>(ws + wl.m_off);
+    p.ws_l = reinterpret_cast<float*>(ws + wl.l_off);
+    p.ws_o = reinterpret_cast<float*>(ws + wl.o_off);
+    p.err = reinterpret_cast<unsigned*>(ws);
+    p.B = plan->batch;
+    p.Hq = plan->num_q_heads;
+    p.Hkv = plan->num_kv_heads;
+    p.g = plan->num_q_heads / plan->num_kv_heads;
+    p.num_pages = plan->num_pages;
+    p.maxp = plan->max_pages_per_seq;
+    p.max_ctx = plan->max_context_len;
+    p.window = plan->window;
+    p.P = P;
+    p.pages_per_part = plan->partition_size / kPageSize;
+    p.nchunk = p.g / plan->heads_per_cta;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    const dim3 grid(P, p.Hkv * p.nchunk, p.B);
+    cudaError_t e = launch_attend(D, plan->heads_per_cta, P > 1, p, grid,
+                                  static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, float* lse,
+             void* workspace, void* stream) {
+    int st = check_plan(plan);
+    if (st != PA_OK) return st;
+    if (!workspace) return PA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PA_ERR_INVALID_ARG;
+    if (plan->batch == 0 || plan->num_partitions == 1) return PA_OK;
+    if (!context_lens || !out || !lse || !aligned16(out)) return PA_ERR_INVALID_ARG;
+    const int D = plan->head_dim;
+    const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, D, plan->num_partitions);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    MergeParams p;
+    p.context_lens = context_lens;
+    p.ws_m = reinterpret_cast<const float*>(ws + wl.m_off);
+    p.ws_l = reinterpret_cast<const float*>(ws + wl.l_off);
+    p.ws_o = reinterpret_cast<const float*>(ws + wl.o_off);
+    p.out = static_cast<__half*>(out);
+    p.lse = lse;
+    p.err = reinterpret_cast<unsigned*>(ws);
+    p.B = plan->batch;
+    p.Hq = plan->num_q_heads;
+    p.D = D;
+    p.P = plan->num_partitions;
+    p.pages_per_part = plan->partition_size / kPageSize;
+    p.maxp = plan->max_pages_per_seq;
+    p.max_ctx = plan->max_context_len;
+    p.window = plan->window;
+    if (launch_merge(D, p, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+int pa_decode(const pa_plan_t* plan, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens, float scale, int window,
+              void* out, float* lse, void* workspace, void* stream) {
+    int st = pa_decode_partitions(plan, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                  window, out, lse, workspace, stream);
+    if (st != PA_OK) return st;
+    return pa_merge(plan, context_lens, out, lse, workspace, stream);
+}
+
+int pa_get_error(void* workspace, void* stream, int clear, unsigned* device_error) {
+    if (!workspace || !device_error) return PA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    *device_error = v;
+    if (clear) {
+        if (cudaMemsetAsync(workspace, 0, sizeof(unsigned), s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess) {
+            cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
+    }
+    return PA_OK;
+}
+
+}  // extern "C"

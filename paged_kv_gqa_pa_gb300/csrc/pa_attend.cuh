@@ -1,0 +1,460 @@
+// pa_attend.cuh -- the partition kernel of paged-KV GQA decode attention.
+//
+// One CTA serves one (partition, KV head, head chunk, sequence).  It walks the
+// partition's pages of K and V through the block table (the page gather of the
+// paged_attention_v2_pytorch.py commit note, key_cache[blk_ids]), loads each
+// page once for all G query heads of its group (the commit note's GQA
+// broadcast: K/V stay at kv-head size), and computes in fp32:
+//   scores  s = scale * q.K        (Phase 1 QK^T)
+//   softmax statistics (max, exp-sum) with an online update per page
+//   P.V, the exp-weighted sum of the V rows
+// It then writes either the partition's normalised output plus its (max,
+// exp-sum) for the log-sum-exp merge (Phase 1 -> Phase 2 of the commit note;
+// SPLIT = true), or, when one partition covers the whole attended context,
+// the final fp16 output and the natural-log LSE (SPLIT = false; the
+// short-context role of the tiled nest in apache/tvm PR #20426, section
+// Change).
+//
+// GB300 mapping.  Four warps per CTA, each an independent pipeline: lane 0 of
+// a warp streams that warp's pages (pages w, w+4, w+8, ... of the partition)
+// with 1-D bulk copies (cp.async.bulk, one 16-token page of one KV head =
+// 16*D*2 contiguous bytes) into a ring of kStages shared-memory slots guarded
+// by mbarriers, so several pages per warp are in flight while the warp
+// computes on an earlier one.  Within a warp a token row is covered by D/8
+// lanes holding 16 bytes (8 dims) each; q for those 8 dims and G heads stays
+// in registers, and the per-lane partial dot products are combined with a
+// reduce-scatter of warp shuffles (each exchange halves the tokens a lane
+// keeps), after which lane l holds the full scores of token l/2 of the page.
+// The four warps' (max, exp-sum, output) states are merged in shared memory at
+// the end, the same log-sum-exp algebra as the cross-partition merge.
+#pragma once
+
+#include <math.h>
+
+#include <atomic>
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+template <int D, int G>
+struct Lanes {
+    static constexpr int R = D / 8;   // lanes per token row, 8 dims each
+    static constexpr int TL = R / 2;  // tokens of a page per lane
+    static constexpr int LOG_TL = TL == 16 ? 4 : (TL == 8 ? 3 : (TL == 4 ? 2 : 0));
+    static constexpr int GP = (G + 3) & ~3;  // row stride of the per-warp P buffer
+    static_assert(D == 64 || D == 128 || D == 256, "head_dim");
+    static_assert(R * kPageSize / 2 == D, "lane layout");
+};
+
+__device__ __forceinline__ void half8_to_float(const uint4 raw, float (&f)[8]) {
+    const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 t = __half22float2(h[j]);
+        f[2 * j] = t.x;
+        f[2 * j + 1] = t.y;
+    }
+}
+
+// Partial dot products of the G heads with token `tok` of the K page (this
+// lane's 8 dims), combined across the 2^LEVEL tokens tok .. tok + 2^LEVEL - 1
+// by a shuffle reduce-scatter: the exchange over lane mask (1 << LEVEL) pairs
+// token bit LEVEL-1, and a lane keeps the token whose bit equals its lane bit.
+template <int D, int G, int LEVEL>
+__device__ __forceinline__ void qk_tree(float (&res)[G], const unsigned char* kpage, int tok,
+                                        int r, int lane, const float (&qf)[G][8]) {
+    if constexpr (LEVEL == 0) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(kpage + tok * (D * 2) + r * 16);
+        float kf[8];
+        half8_to_float(raw, kf);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float a = qf[h][0] * kf[0];
+#pragma unroll
+            for (int j = 1; j < 8; ++j) a = fmaf(qf[h][j], kf[j], a);
+            res[h] = a;
+        }
+    } else {
+        float lo[G], hi[G];
+        qk_tree<D, G, LEVEL - 1>(lo, kpage, tok, r, lane, qf);
+        qk_tree<D, G, LEVEL - 1>(hi, kpage, tok + (1 << (LEVEL - 1)), r, lane, qf);
+        constexpr int kMask = 1 << LEVEL;
+        const bool up = (lane & kMask) != 0;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float send = up ? lo[h] : hi[h];
+            const float keep = up ? hi[h] : lo[h];
+            res[h] = keep + __shfl_xor_sync(0xffffffffu, send, kMask);
+        }
+    }
+}
+
+template <int D, int G, bool SPLIT>
+__device__ __forceinline__ void write_rows(const AttendParams& p, int b, int h0, int part,
+                                           float o_val, float m_val, float l_val,
+                                           float lse_val) {
+    for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+        const int h = idx / D, d = idx % D;
+        const size_t bh = (size_t)b * p.Hq + h0 + h;
+        if constexpr (SPLIT) {
+            const size_t row = bh * p.P + part;
+            p.ws_o[row * D + d] = o_val;
+            if (d == 0) {
+                p.ws_m[row] = m_val;
+                p.ws_l[row] = l_val;
+            }
+        } else {
+            p.out[bh * D + d] = __float2half_rn(o_val);
+            if (d == 0) p.lse[bh] = lse_val;
+        }
+    }
+}
+
+template <int D, int G, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBlocks))
+    attend_kernel(const AttendParams p) {
+    using Cfg = AttendCfg<D>;
+    using LN = Lanes<D, G>;
+    constexpr int R = LN::R;
+    constexpr int TL = LN::TL;
+    constexpr int GP = LN::GP;
+    constexpr int NS = Cfg::kStages;
+    constexpr int PB = Cfg::kPageBytes;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* ring = smem;                                         // [warps][NS][PB]
+    float* pbuf = reinterpret_cast<float*>(smem + Cfg::kRingBytes);     // [warps][16][8]
+    int* s_pid = reinterpret_cast<int*>(pbuf + kWarps * Cfg::kPBufFloats);  // [kMaxPagesPerPart]
+    float* s_ml = reinterpret_cast<float*>(s_pid + kMaxPagesPerPart);   // [warps][2][8]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 2);
+    __shared__ int s_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int part = blockIdx.x;
+    const int kvh = blockIdx.y / p.nchunk;
+    const int h0 = kvh * p.g + (blockIdx.y % p.nchunk) * G;
+    const int b = blockIdx.z;
+
+    const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, p.pages_per_part);
+    if (!sp.valid) {
+        if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0) atomicOr(p.err, PA_DEVERR_BAD_LENGTH);
+        if constexpr (!SPLIT) write_rows<D, G, SPLIT>(p, b, h0, part, NAN, NAN, NAN, NAN);
+        return;  // with a split, the merge writes the NaN rows
+    }
+    if (part >= sp.num_parts) {
+        // Nothing attended in this partition.  Without a split this only
+        // happens for an empty context: out = 0, lse = -inf.
+        if constexpr (!SPLIT) write_rows<D, G, SPLIT>(p, b, h0, part, 0.f, 0.f, 0.f, -INFINITY);
+        return;
+    }
+    const int pg0 = sp.first_page + part * p.pages_per_part;
+    const int npg = min(p.pages_per_part, sp.end_page - pg0);
+
+    if (threadIdx.x == 0) s_flag = 0;
+    const uint32_t bar_w = smem_u32(bars) + warp * NS * 8;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < NS; ++s) mbar_init(bar_w + s * 8, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < npg; j += kThreads) {
+        int id = p.block_tables[(size_t)b * p.maxp + pg0 + j];
+        if (id < 0 || id >= p.num_pages) {
+            s_flag = 1;
+            id = 0;
+        }
+        s_pid[j] = id;
+    }
+    __syncthreads();
+    if (s_flag) {
+        if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+        write_rows<D, G, SPLIT>(p, b, h0, part, NAN, NAN, NAN, NAN);
+        return;
+    }
+
+    // ---- this warp's pages: j = warp, warp + 4, ... ; items K0, V0, K1, V1, ...
+    const int nk = npg > warp ? (npg - warp + kWarps - 1) / kWarps : 0;
+    const int n_items = 2 * nk;
+    const uint32_t ring_w = smem_u32(ring) + warp * NS * PB;
+    const unsigned char* ring_wp = ring + warp * NS * PB;
+    const size_t kv_stride = (size_t)kPageSize * D;  // elements per (page, kv head)
+
+    auto issue = [&](int item) {
+        const int slot = item % NS;
+        const int jj = warp + (item >> 1) * kWarps;
+        const __half* base = (item & 1) ? p.v : p.k;
+        const __half* src = base + ((size_t)s_pid[jj] * p.Hkv + kvh) * kv_stride;
+        const uint32_t bar = bar_w + slot * 8;
+        mbar_arrive_expect_tx(bar, PB);
+        bulk_g2s(ring_w + slot * PB, src, PB, bar);
+    };
+    int issued = 0;
+    if (lane == 0) {
+        for (int i = 0; i < NS && i < n_items; ++i) issue(i);
+    }
+    issued = min(NS, n_items);
+
+    // ---- q for this lane's 8 dims, all G heads (fp32)
+    const int r = lane % R;
+    const int rg = lane / R;
+    float qf[G][8];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const uint4 raw =
+            *reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.Hq + h0 + h) * D + r * 8);
+        half8_to_float(raw, qf[h]);
+    }
+
+    float o[G][8];
+    float m[G], lsum[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m[h] = -INFINITY;
+        lsum[h] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[h][j] = 0.f;
+    }
+    float* pw = pbuf + warp * Cfg::kPBufFloats;
+    const int t_own = lane >> 1;  // token of the page whose scores this lane ends up with
+    bool ok = true;
+    int consumed = 0;
+
+    for (int k = 0; k < nk; ++k) {
+        // ---------------- K page: scores
+        {
+            const int item = 2 * k;
+            const int slot = item % NS;
+            const bool got = mbar_wait_bounded(bar_w + slot * 8, (item / NS) & 1);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            consumed = item + 1;
+        }
+        float s[G];
+        qk_tree<D, G, LN::LOG_TL>(s, ring_wp + ((2 * k) % NS) * PB, rg * TL, r, lane, qf);
+#pragma unroll
+        for (int h = 0; h < G; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], 1);
+        __syncwarp();
+        if (lane == 0 && 2 * k + NS < n_items) {
+            fence_proxy_async_smem();
+            issue(2 * k + NS);
+        }
+        if (2 * k + NS < n_items) issued = 2 * k + NS + 1;
+
+        // ---------------- online softmax over this page (log2 domain)
+        const int pos = (pg0 + warp + k * kWarps) * kPageSize + t_own;
+        const bool valid = pos >= sp.start && pos < sp.L;
+        float pm[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
+            pm[h] = s[h];
+        }
+#pragma unroll
+        for (int mask = 2; mask < 32; mask <<= 1) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) pm[h] = fmaxf(pm[h], __shfl_xor_sync(0xffffffffu, pm[h], mask));
+        }
+        bool grow = false;
+#pragma unroll
+        for (int h = 0; h < G; ++h) grow |= pm[h] > m[h];
+        if (grow) {  // warp-uniform: every lane holds the same m and pm
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float mn = fmaxf(m[h], pm[h]);
+                const float a = (mn == -INFINITY) ? 1.f : ex2(m[h] - mn);
+                m[h] = mn;
+                lsum[h] *= a;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[h][j] *= a;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float e = (s[h] == -INFINITY) ? 0.f : ex2(s[h] - m[h]);
+            lsum[h] += e;
+            s[h] = e;
+        }
+        if ((lane & 1) == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) pw[t_own * GP + h] = s[h];
+        }
+        __syncwarp();
+
+        // ---------------- V page: o += p * V
+        {
+            const int item = 2 * k + 1;
+            const int slot = item % NS;
+            const bool got = mbar_wait_bounded(bar_w + slot * 8, (item / NS) & 1);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            consumed = item + 1;
+        }
+        const unsigned char* vpage = ring_wp + ((2 * k + 1) % NS) * PB;
+#pragma unroll
+        for (int i = 0; i < TL; ++i) {
+            const int t = rg * TL + i;
+            const uint4 raw = *reinterpret_cast<const uint4*>(vpage + t * (D * 2) + r * 16);
+            float vf[8];
+            half8_to_float(raw, vf);
+            float pr[GP];
+#pragma unroll
+            for (int h4 = 0; h4 < GP; h4 += 4) {
+                const float4 t4 = *reinterpret_cast<const float4*>(pw + t * GP + h4);
+                pr[h4] = t4.x;
+                pr[h4 + 1] = t4.y;
+                pr[h4 + 2] = t4.z;
+                pr[h4 + 3] = t4.w;
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[h][j] = fmaf(pr[h], vf[j], o[h][j]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && 2 * k + 1 + NS < n_items) {
+            fence_proxy_async_smem();
+            issue(2 * k + 1 + NS);
+        }
+        if (2 * k + 1 + NS < n_items) issued = 2 * k + 1 + NS + 1;
+    }
+
+    if (!ok) {
+        // A copy did not land in time: record it, give every copy this warp
+        // issued a bounded chance to land (so none writes into shared memory
+        // after the CTA exits), and publish NaN for this CTA.
+        if (lane == 0) atomicOr(p.err, PA_DEVERR_TIMEOUT);
+        for (int item = consumed; item < issued; ++item)
+            (void)mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
+        s_flag = 1;
+    }
+
+    // ---- combine lanes: exp-sums over the 16 tokens (lanes l and l^1 hold the
+    // same token), outputs over the row groups of the warp.
+#pragma unroll
+    for (int mask = 2; mask < 32; mask <<= 1) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], mask);
+    }
+#pragma unroll
+    for (int mask = R; mask < 32; mask <<= 1) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[h][j] += __shfl_xor_sync(0xffffffffu, o[h][j], mask);
+        }
+    }
+    __syncthreads();  // every warp is done with its ring: reuse it for the warp states
+    float* s_o = reinterpret_cast<float*>(ring);  // [warps][G][D]
+    if (lane < R) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float4* dst = reinterpret_cast<float4*>(s_o + (warp * G + h) * D + r * 8);
+            dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+            dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            s_ml[warp * 2 * kMaxHeadsPerCta + h] = m[h];
+            s_ml[warp * 2 * kMaxHeadsPerCta + kMaxHeadsPerCta + h] = lsum[h];
+        }
+    }
+    __syncthreads();
+    if (s_flag) {
+        write_rows<D, G, SPLIT>(p, b, h0, part, NAN, NAN, NAN, NAN);
+        return;
+    }
+
+    // ---- merge the four warp states (same log-sum-exp algebra as Phase 2)
+    constexpr int D4 = D / 4;
+    for (int idx = threadIdx.x; idx < G * D4; idx += kThreads) {
+        const int h = idx / D4;
+        const int d = (idx % D4) * 4;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w * 2 * kMaxHeadsPerCta + h]);
+        float Ls = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float mw = s_ml[w * 2 * kMaxHeadsPerCta + h];
+            const float c = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+            Ls += c * s_ml[w * 2 * kMaxHeadsPerCta + kMaxHeadsPerCta + h];
+            const float4 ow = *reinterpret_cast<const float4*>(s_o + (w * G + h) * D + d);
+            acc.x += c * ow.x;
+            acc.y += c * ow.y;
+            acc.z += c * ow.z;
+            acc.w += c * ow.w;
+        }
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        const size_t bh = (size_t)b * p.Hq + h0 + h;
+        if constexpr (SPLIT) {
+            const size_t row = bh * p.P + part;
+            *reinterpret_cast<float4*>(p.ws_o + row * D + d) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            if (d == 0) {
+                p.ws_m[row] = M;
+                p.ws_l[row] = Ls;
+            }
+        } else {
+            __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
+            __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
+            uint2 packed;
+            packed.x = *reinterpret_cast<uint32_t*>(&lo);
+            packed.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(p.out + bh * D + d) = packed;
+            if (d == 0) p.lse[bh] = Ls > 0.f ? M * 0.69314718055994531f + logf(Ls) : -INFINITY;
+        }
+    }
+}
+
+// Launcher for one head dim: picks the <G, SPLIT> instance, raises its
+// dynamic shared-memory limit once per device, launches on `stream`.
+template <int D>
+cudaError_t launch_attend_d(int G, bool split, const AttendParams& p, dim3 grid,
+                            cudaStream_t stream) {
+    const void* fn = nullptr;
+    switch (G) {
+#define PA_ATTEND_CASE(GG)                                                    \
+    case GG:                                                                  \
+        fn = split ? reinterpret_cast<const void*>(&attend_kernel<D, GG, true>) \
+                   : reinterpret_cast<const void*>(&attend_kernel<D, GG, false>); \
+        break;
+        PA_ATTEND_CASE(1)
+        PA_ATTEND_CASE(2)
+        PA_ATTEND_CASE(3)
+        PA_ATTEND_CASE(4)
+        PA_ATTEND_CASE(5)
+        PA_ATTEND_CASE(6)
+        PA_ATTEND_CASE(7)
+        PA_ATTEND_CASE(8)
+#undef PA_ATTEND_CASE
+        default:
+            return cudaErrorInvalidValue;
+    }
+    constexpr int kMaxDevices = 64;
+    static std::atomic<uint32_t> configured[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint32_t bit = 1u << ((G - 1) * 2 + (split ? 1 : 0));
+    if (dev < 0 || dev >= kMaxDevices || !(configured[dev].load() & bit)) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AttendCfg<D>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) configured[dev].fetch_or(bit);
+    }
+    void* args[] = {const_cast<AttendParams*>(&p)};
+    return cudaLaunchKernel(fn, grid, dim3(kThreads), args, AttendCfg<D>::kSmemBytes, stream);
+}
+
+}  // namespace pa

@@ -1,0 +1,166 @@
+// pa_common.cuh -- shared pieces of the GB300 (sm_103a) paged-KV decode
+// kernels: launch parameters, the per-head-dim kernel configuration, and the
+// inline-PTX wrappers for mbarriers and 1-D bulk copies (cp.async.bulk).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+constexpr int kPageSize = 16;     // tokens per page
+constexpr int kWarps = 4;         // consumer warps per CTA of the attention kernel
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxPagesPerPart = 256;  // page ids a CTA stages in shared memory
+constexpr int kMaxPartitions = 4096;   // partitions the merge kernel reduces
+constexpr int kMaxHeadsPerCta = 8;
+constexpr int kCtrlBytes = 256;        // workspace control block (device error word)
+
+// Bounded waits: a bulk copy that has not landed after this long is reported
+// as PA_DEVERR_TIMEOUT instead of hanging the GPU.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+
+struct AttendParams {
+    const __half* q;
+    const __half* k;
+    const __half* v;
+    const int* block_tables;
+    const int* context_lens;
+    __half* out;
+    float* lse;
+    float* ws_o;   // [B, Hq, P, D] partition outputs, normalised by their exp-sum
+    float* ws_m;   // [B, Hq, P] partition max, log2 domain
+    float* ws_l;   // [B, Hq, P] partition exp-sum
+    unsigned* err; // device error word
+    int B, Hq, Hkv, g, num_pages, maxp, max_ctx, window;
+    int P;                  // partitions (grid.x)
+    int pages_per_part;     // partition size in pages
+    int nchunk;             // head chunks per KV head (grid.y = Hkv * nchunk)
+    float scale_log2;       // scale * log2(e)
+};
+
+struct MergeParams {
+    const int* context_lens;
+    const float* ws_o;
+    const float* ws_m;
+    const float* ws_l;
+    __half* out;
+    float* lse;
+    unsigned* err;
+    int B, Hq, D, P, pages_per_part, maxp, max_ctx, window;
+};
+
+// Pipeline depth (pages of K or V in flight per warp) for each head dim; the
+// resulting shared-memory footprint sets the CTAs per SM.
+template <int D>
+struct AttendCfg {
+    static constexpr int kPageBytes = kPageSize * D * 2;
+    static constexpr int kStages = D == 256 ? 3 : (D == 128 ? 4 : 6);
+    static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
+    static constexpr int kPBufFloats = kPageSize * kMaxHeadsPerCta;  // per warp
+    static constexpr int kSmemBytes = kRingBytes + kWarps * kPBufFloats * 4 +
+                                      kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 2 * 4 +
+                                      kWarps * kStages * 8 + 16;
+    static constexpr int kMinBlocks = D == 256 ? 2 : 3;
+};
+
+// Span of pages a sequence attends, shared by the partition and merge kernels
+// so both agree on the partition count of every sequence.
+struct SeqSpan {
+    int L, start, first_page, end_page, num_parts;
+    bool valid;
+};
+
+__device__ __forceinline__ SeqSpan seq_span(int L, int window, int max_ctx, int maxp,
+                                            int pages_per_part) {
+    SeqSpan s;
+    s.L = L;
+    s.valid = L >= 0 && L <= max_ctx && (L + kPageSize - 1) / kPageSize <= maxp;
+    s.start = (window > 0 && window < L) ? L - window : 0;
+    s.first_page = s.start / kPageSize;
+    s.end_page = (L + kPageSize - 1) / kPageSize;
+    const int np = s.valid ? s.end_page - s.first_page : 0;
+    s.num_parts = np > 0 ? (np + pages_per_part - 1) / pages_per_part : 0;
+    return s;
+}
+
+// ---------------------------------------------------------------------------
+// Inline PTX: mbarrier + bulk copy + fast exp2.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Global -> shared bulk copy that signals `bar` with its byte count on arrival.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of `bar`, giving up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// 2^x with the MUFU approximation (relative error ~2^-22); -inf -> +0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+}  // namespace pa
+
+// Launchers implemented per head dim (pa_attend_d*.cu).
+namespace pa {
+cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 grid,
+                          cudaStream_t stream);
+int attend_ctas_per_sm(int D);
+}  // namespace pa

@@ -1,0 +1,99 @@
+"""Shared helpers of the GPU tests: upload a seeded case, run the CUDA path
+through the C ABI, compare with the fp64 oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_gqa_pa_gb300 as pa
+from paged_kv_gqa_pa_gb300 import build as pa_build
+
+# Tolerances: relative L2 over the whole fp16 output tensor, absolute on the LSE.
+REL_L2_TOL = 1e-3
+LSE_TOL = 1e-4
+
+_built = False
+
+
+def ensure_built():
+    global _built
+    if not _built:
+        pa_build.build()
+        _built = True
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    pa.load()
+
+
+def to_device(case, device="cuda"):
+    return dict(
+        q=torch.from_numpy(case.q).to(device),
+        k=torch.from_numpy(case.k_cache).to(device),
+        v=torch.from_numpy(case.v_cache).to(device),
+        bt=torch.from_numpy(case.block_tables).to(device),
+        cl=torch.from_numpy(case.context_lens).to(device),
+    )
+
+
+def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=None,
+            guard=0):
+    """Plan + pa_decode through the C ABI.  Returns (out fp64 numpy, lse fp64
+    numpy, device error word, plan).  With guard > 0 the outputs and the
+    workspace sit inside larger NaN/0xA5-filled buffers whose guard regions are
+    checked afterwards."""
+    ensure_built()
+    dev = dev or to_device(case)
+    B, Hq, D = case.q.shape
+    if partition_size is None:
+        partition_size = case.partition_size
+    if max_context_len is None:
+        max_context_len = max(case.max_context_len, 0)
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = pa.pa_plan(B, Hq, case.Hkv, D, case.page_size, case.num_pages, case.max_pages_per_seq,
+                      max_context_len, case.window, partition_size, num_sms)
+    n_out = B * Hq * D
+    out_buf = torch.full((n_out + 2 * guard,), float("nan"), dtype=torch.float16, device="cuda")
+    lse_buf = torch.full((B * Hq + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")
+    ws_bytes = int(plan.workspace_bytes)
+    ws_buf = torch.full((ws_bytes + 2 * guard * 16,), 0xA5, dtype=torch.uint8, device="cuda")
+    out = out_buf[guard:guard + n_out].view(B, Hq, D)
+    lse = lse_buf[guard:guard + B * Hq].view(B, Hq)
+    ws = ws_buf[guard * 16:guard * 16 + ws_bytes]
+    ws[:256].zero_()
+    pa.pa_decode(plan, dev["q"], dev["k"], dev["v"], dev["bt"], dev["cl"], case.scale,
+                 case.window, out, lse, ws)
+    err = pa.pa_get_error(ws)
+    torch.cuda.synchronize()
+    if guard:
+        ob = out_buf.cpu()
+        lb = lse_buf.cpu()
+        wb = ws_buf.cpu()
+        assert torch.isnan(ob[:guard]).all() and torch.isnan(ob[guard + n_out:]).all(), "out guard"
+        assert torch.isnan(lb[:guard]).all() and torch.isnan(lb[guard + B * Hq:]).all(), "lse guard"
+        assert (wb[:guard * 16] == 0xA5).all() and (wb[guard * 16 + ws_bytes:] == 0xA5).all(), \
+            "workspace guard"
+    return (out.double().cpu().numpy(), lse.double().cpu().numpy(), err, plan)
+
+
+def rel_l2(a, b):
+    den = np.linalg.norm(b.ravel())
+    num = np.linalg.norm((a - b).ravel())
+    return num / den if den > 0 else num
+
+
+def assert_matches_oracle(case, out, lse, ref=None, what=""):
+    if ref is None:
+        ref = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                            case.context_lens, case.scale, case.window)
+    ref_out, ref_lse = ref
+    assert not np.isnan(out).any(), f"{what}: NaN in output"
+    err = rel_l2(out, ref_out)
+    assert err <= REL_L2_TOL, f"{what}: rel L2 {err:.3e} > {REL_L2_TOL}"
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(lse), fin), f"{what}: LSE finiteness differs"
+    assert np.array_equal(lse[~fin], ref_lse[~fin]), f"{what}: LSE of empty rows"
+    if fin.any():
+        d = np.abs(lse[fin] - ref_lse[fin]).max()
+        assert d <= LSE_TOL, f"{what}: |dLSE| {d:.3e} > {LSE_TOL}"
+    return err

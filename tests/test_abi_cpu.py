@@ -1,0 +1,156 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads and exports
+every symbol include/pa.h declares, pa_plan's partitioning, and the argument
+checks that reject a call before anything is launched."""
+import ctypes
+import json
+import os
+import re
+import subprocess
+
+import pytest
+
+import paged_kv_gqa_pa_gb300 as pa
+from paged_kv_gqa_pa_gb300 import binding
+from paged_kv_gqa_pa_gb300 import build as pa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    pa_build.build()
+    pa.load()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert {"pa_plan", "pa_decode", "pa_merge", "pa_get_error"} <= names
+    lib = ctypes.CDLL(binding.library_path())
+    for n in names:
+        assert hasattr(lib, n), n
+    nm = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()], check=True,
+                        capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (pa_[a-z0-9_]+)$", nm, flags=re.M))
+    assert names <= exported
+    assert set(binding.EXPORTED) == names
+
+
+def test_plan_struct_layout_matches_header():
+    # 14 ints, then a size_t, then 8 reserved ints.
+    assert binding.pa_plan_t.workspace_bytes.offset == 56
+    assert ctypes.sizeof(binding.pa_plan_t) == 56 + 8 + 32
+
+
+def test_status_strings_and_version():
+    assert pa.pa_status_string(0) == "ok"
+    assert "workspace" in pa.pa_status_string(4)
+    assert pa.pa_version() >= 1
+
+
+def test_plan_matches_the_pages_partition_counts():
+    with open(os.path.join(HERE, "golden", "plan_partitions.json")) as f:
+        spec = json.load(f)
+    for c in spec["cases"]:
+        L = c["context"]
+        maxp = -(-L // 16)
+        plan = pa.pa_plan(1, 8, 8, 128, 16, maxp, maxp, L, c["window"], c["partition_size"], 152)
+        assert plan.num_partitions == c["num_partitions"]
+        last = L - (plan.num_partitions - 1) * plan.partition_size
+        assert last == c["last_partition_tokens"]
+
+
+def test_plan_long_context_workload():
+    plan = pa.pa_plan(4, 24, 4, 256, 16, 31250, 6250, 100000, 0, 512, 152)
+    assert plan.num_partitions == 196 and plan.heads_per_cta == 6
+    assert plan.ctas == 196 * 4 * 4
+    rows = 4 * 24 * 196
+    assert plan.workspace_bytes >= 256 + rows * 4 * 2 + rows * 256 * 4
+
+
+@pytest.mark.parametrize("num_sms", [1, 8, 152, 1000])
+@pytest.mark.parametrize("B,Hkv,L,W", [(1, 1, 256, 0), (1, 8, 3060, 0), (8, 8, 4096, 0),
+                                       (4, 4, 8192, 4096), (4, 4, 100000, 0), (1, 1, 17, 16)])
+def test_auto_plan_is_consistent(num_sms, B, Hkv, L, W):
+    maxp = -(-L // 16)
+    plan = pa.pa_plan(B, Hkv * 4, Hkv, 128, 16, maxp * B, maxp, L, W, 0, num_sms)
+    assert plan.partition_size % 16 == 0 and plan.partition_size // 16 <= 256
+    span = maxp if W == 0 else min(maxp, -(-(W - 1) // 16) + 1)
+    assert plan.num_partitions == -(-span // (plan.partition_size // 16))
+    if plan.num_partitions == 1:
+        assert plan.workspace_bytes == 256
+    # The window bound covers every placement of the window.
+    if W:
+        worst = max(-(-Lb // 16) - (Lb - W) // 16 for Lb in range(W, L + 1))
+        assert worst <= span
+
+
+@pytest.mark.parametrize("args,status", [
+    ((1, 8, 3, 128, 16, 10, 10, 100, 0, 0, 152), binding.PA_ERR_INVALID_ARG),   # Hq % Hkv
+    ((1, 8, 8, 96, 16, 10, 10, 100, 0, 0, 152), binding.PA_ERR_UNSUPPORTED),    # head_dim
+    ((1, 8, 8, 128, 32, 10, 10, 100, 0, 0, 152), binding.PA_ERR_UNSUPPORTED),   # page_size
+    ((1, 8, 8, 128, 16, 10, 10, 100, 0, 24, 152), binding.PA_ERR_INVALID_ARG),  # S % 16
+    ((1, 8, 8, 128, 16, 10, 10, 161, 0, 0, 152), binding.PA_ERR_INVALID_ARG),   # Lmax > table
+    ((1, 18, 2, 128, 16, 10, 10, 100, 0, 0, 152), binding.PA_ERR_UNSUPPORTED),  # g = 9
+    ((1, 8, 8, 128, 16, 10, 10, 100, 0, 8192, 152), binding.PA_ERR_UNSUPPORTED),  # S > 256 pages
+    ((-1, 8, 8, 128, 16, 10, 10, 100, 0, 0, 152), binding.PA_ERR_INVALID_ARG),
+    ((1, 8, 8, 128, 16, 10, 10, 100, -1, 0, 152), binding.PA_ERR_INVALID_ARG),
+])
+def test_plan_rejects(args, status):
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_plan(*args)
+    assert e.value.status == status
+
+
+def _call_decode(plan, **over):
+    fake = 0x10000  # aligned, never dereferenced: every case returns before a launch
+    a = dict(q=fake, k=fake, v=fake, bt=fake, cl=fake, scale=0.1, window=plan.window, out=fake,
+             lse=fake, ws=fake, stream=None)
+    a.update(over)
+    lib = pa.load()
+    return lib.pa_decode(ctypes.byref(plan), a["q"], a["k"], a["v"], a["bt"], a["cl"],
+                         ctypes.c_float(a["scale"]), a["window"], a["out"], a["lse"], a["ws"],
+                         a["stream"])
+
+
+def test_decode_argument_checks_return_before_launch():
+    plan = pa.pa_plan(2, 8, 2, 128, 16, 100, 50, 800, 0, 64, 152)
+    assert plan.num_partitions > 1
+    assert _call_decode(plan, q=None) == binding.PA_ERR_INVALID_ARG
+    assert _call_decode(plan, out=None) == binding.PA_ERR_INVALID_ARG
+    assert _call_decode(plan, ws=None) == binding.PA_ERR_WORKSPACE
+    assert _call_decode(plan, window=5) == binding.PA_ERR_INVALID_ARG
+    assert _call_decode(plan, q=0x10002) == binding.PA_ERR_INVALID_ARG      # misaligned
+    assert _call_decode(plan, ws=0x10008) == binding.PA_ERR_INVALID_ARG     # misaligned
+    small = binding.pa_plan_t.from_buffer_copy(plan)
+    small.workspace_bytes = 256
+    assert _call_decode(small) == binding.PA_ERR_INVALID_ARG
+    bad = binding.pa_plan_t.from_buffer_copy(plan)
+    bad.heads_per_cta = 3
+    assert _call_decode(bad) == binding.PA_ERR_INVALID_ARG
+    empty = pa.pa_plan(0, 8, 2, 128, 16, 100, 50, 800, 0, 64, 152)
+    assert _call_decode(empty) == binding.PA_OK   # nothing to do, nothing launched
+    lib = pa.load()
+    assert lib.pa_decode(None, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000, ctypes.c_float(1.0),
+                         0, 0x10000, 0x10000, 0x10000, None) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_merge(ctypes.byref(plan), 0x10000, 0x10000, 0x10000, None, None) == \
+        binding.PA_ERR_WORKSPACE
+    assert lib.pa_get_error(None, None, 0, None) == binding.PA_ERR_INVALID_ARG
+
+
+def test_binding_rejects_host_tensors():
+    import torch
+    plan = pa.pa_plan(1, 4, 1, 64, 16, 16, 16, 256, 0, 0, 152)
+    t = torch.zeros(4, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        pa.pa_decode(plan, t, t, t, t, t, 0.1, 0, t, t, t)

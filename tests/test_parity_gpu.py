@@ -1,0 +1,188 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, element
+by element, on seeded inputs.
+
+Bar: relative L2 <= 1e-3 over the fp16 output tensor and |dLSE| <= 1e-4
+(tests/gpu_helpers.py); bit-exact where the result is exact (single-token
+context, page placement, window >= context)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import assert_matches_oracle, run_gpu, to_device
+from paged_kv_gqa_pa_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+# ---- the five measured workloads, at full size, in the plan the bench uses
+@pytest.mark.parametrize("name", workloads.WORKLOAD_ORDER)
+def test_workload_full_size(name):
+    case = workloads.workload(name)
+    out, lse, err, plan = run_gpu(case)
+    assert err == 0
+    rel = assert_matches_oracle(case, out, lse, what=name)
+    if name == "gqa6_ctx100k":
+        # 100000 tokens in 512-token partitions: 196 partitions, the last one
+        # holding 160 tokens.
+        assert plan.num_partitions == 196
+    print(f"{name}: rel L2 {rel:.2e}, partitions {plan.num_partitions}")
+
+
+# ---- context lengths of the pages' accuracy check (1 .. 3060, odd shard
+# lengths), each head dim, forced split / no split / automatic
+LENS = [1, 2, 15, 16, 17, 255, 256, 257, 511, 513, 3060]
+
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 4, 1), (128, 8, 2), (256, 6, 1)])
+@pytest.mark.parametrize("partition_size", [0, 16, 64, 512, 4096])
+def test_context_length_sweep(D, Hq, Hkv, partition_size):
+    case = workloads.make_case("sweep", len(LENS), Hq, Hkv, D, LENS, seed=100 + D,
+                               partition_size=partition_size)
+    out, lse, err, plan = run_gpu(case)
+    assert err == 0
+    if partition_size == 4096:
+        assert plan.num_partitions == 1  # whole context in one CTA, no merge
+    assert_matches_oracle(case, out, lse, what=f"D{D} S{partition_size}")
+
+
+@pytest.mark.parametrize("g", [1, 2, 3, 5, 7, 8, 12, 16])
+def test_group_sizes(g):
+    Hkv = 2
+    case = workloads.make_case("g", 3, g * Hkv, Hkv, 128, [37, 700, 1500], seed=200 + g,
+                               q_std=2.0)
+    for S in (0, 128):
+        case.partition_size = S
+        out, lse, err, plan = run_gpu(case)
+        assert err == 0
+        assert_matches_oracle(case, out, lse, what=f"g{g} S{S}")
+
+
+@pytest.mark.parametrize("window", [1, 7, 16, 100, 255, 1000, 3059, 3060, 5000])
+def test_sliding_window(window):
+    case = workloads.make_case("w", 3, 8, 4, 256, [3060, 1001, 40], seed=300, window=window,
+                               q_std=3.0)
+    for S in (0, 64, 2048):
+        case.partition_size = S
+        out, lse, err, _ = run_gpu(case)
+        assert err == 0
+        assert_matches_oracle(case, out, lse, what=f"W{window} S{S}")
+
+
+def test_ragged_batch_with_empty_and_unit_sequences():
+    lens = [0, 1, 4096, 17, 0, 1000, 2, 3333]
+    case = workloads.make_case("r", len(lens), 32, 8, 128, lens, seed=400)
+    for S in (0, 256, 4096):
+        case.partition_size = S
+        out, lse, err, _ = run_gpu(case, guard=64)
+        assert err == 0
+        assert np.all(out[[0, 4]] == 0) and np.all(np.isneginf(lse[[0, 4]]))
+        assert_matches_oracle(case, out, lse, what=f"ragged S{S}")
+
+
+def test_all_empty_batch():
+    case = workloads.make_case("e", 2, 4, 2, 64, [0, 0], seed=401, pool_pages=2)
+    out, lse, err, _ = run_gpu(case, max_context_len=16)
+    assert err == 0
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+# ---- invariants
+def test_single_token_is_v_row_bit_exact():
+    case = workloads.make_case("one", 4, 16, 2, 256, [1, 1, 1, 1], seed=500, q_std=3.0)
+    for S in (0, 16):
+        case.partition_size = S
+        out, lse, err, _ = run_gpu(case, max_context_len=16)
+        assert err == 0
+        for b in range(4):
+            page = case.block_tables[b, 0]
+            for h in range(16):
+                vrow = case.v_cache[page, h // 8, 0].astype(np.float64)
+                assert np.array_equal(out[b, h], vrow)
+        ref = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                            case.context_lens, case.scale)
+        assert np.abs(lse - ref[1]).max() <= 1e-4
+
+
+def test_zero_query_gives_mean_of_v():
+    case = workloads.make_case("q0", 2, 4, 2, 128, [777, 3000], seed=501)
+    case.q[:] = 0
+    out, lse, err, _ = run_gpu(case)
+    assert err == 0
+    for b, L in enumerate(case.context_lens):
+        assert np.abs(lse[b] - math.log(L)).max() <= 1e-4
+    assert_matches_oracle(case, out, lse, what="q=0")
+
+
+def test_page_placement_is_bit_exact():
+    case = workloads.make_case("perm", 2, 8, 2, 128, [1500, 999], seed=502)
+    out1, lse1, _, _ = run_gpu(case)
+    # Move every used page to a new physical slot and rewrite the table.
+    rng = np.random.default_rng(7)
+    perm = rng.permutation(case.num_pages).astype(np.int32)  # old -> new
+    k2 = np.empty_like(case.k_cache)
+    v2 = np.empty_like(case.v_cache)
+    k2[perm] = case.k_cache
+    v2[perm] = case.v_cache
+    bt2 = np.where(case.block_tables >= 0, perm[np.maximum(case.block_tables, 0)], -1)
+    case2 = workloads.Case(**{**case.__dict__, "k_cache": k2, "v_cache": v2,
+                              "block_tables": bt2.astype(np.int32)})
+    out2, lse2, _, _ = run_gpu(case2)
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
+
+
+def test_partition_count_invariance():
+    case = workloads.make_case("pc", 2, 24, 4, 256, [20000, 7777], seed=503)
+    ref = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                        case.context_lens, case.scale)
+    outs = []
+    for S in (16, 48, 512, 1024, 4096, 0):
+        case.partition_size = S
+        out, lse, err, _ = run_gpu(case)
+        assert err == 0
+        assert_matches_oracle(case, out, lse, ref=ref, what=f"S{S}")
+        outs.append(out)
+    for o in outs[1:]:
+        assert np.abs(o - outs[0]).max() < 1e-2
+
+
+def test_window_at_least_context_is_no_window():
+    case = workloads.make_case("wl", 2, 8, 2, 64, [500, 64], seed=504)
+    case.partition_size = 128
+    a = run_gpu(case)
+    case.window = 500
+    b = run_gpu(case)
+    case.window = 10 ** 6
+    c = run_gpu(case)
+    for x in (b, c):
+        assert np.array_equal(a[0], x[0]) and np.array_equal(a[1], x[1])
+
+
+def test_outputs_and_workspace_guards_untouched():
+    case = workloads.make_case("guard", 3, 12, 4, 256, [5000, 33, 1200], seed=505)
+    for S in (0, 512, 4096):
+        case.partition_size = S
+        out, lse, err, _ = run_gpu(case, guard=64)
+        assert err == 0
+        assert_matches_oracle(case, out, lse, what=f"guard S{S}")
+
+
+def test_repeated_calls_reuse_workspace():
+    case = workloads.make_case("rep", 2, 8, 2, 128, [900, 3000], seed=506)
+    dev = to_device(case)
+    a = run_gpu(case, dev=dev)
+    b = run_gpu(case, dev=dev)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_max_shapes():
+    # Largest head group per CTA (g = 8) and a two-chunk group (g = 16) at
+    # D = 256, with the largest partition a CTA stages (256 pages).
+    case = workloads.make_case("max", 2, 64, 4, 256, [4096, 4095], seed=507)
+    for S in (4096, 0):
+        case.partition_size = S
+        out, lse, err, _ = run_gpu(case)
+        assert err == 0
+        assert_matches_oracle(case, out, lse, what=f"max S{S}")
