@@ -145,8 +145,12 @@ def dist_setup():
     return world, rank, local
 
 
+KERNEL_IDS = {"simt": 1, "mma": 2}
+KERNEL_NAMES = {v: k for k, v in KERNEL_IDS.items()}
+
+
 class GpuArm:
-    def __init__(self, case, device, partition_size=None):
+    def __init__(self, case, device, partition_size=None, kernel=None):
         import torch
         import paged_kv_gqa_pa_gb300 as pa
         self.torch = torch
@@ -163,6 +167,9 @@ class GpuArm:
         ps = case.partition_size if partition_size is None else partition_size
         self.plan = pa.pa_plan(B, Hq, case.Hkv, D, case.page_size, case.num_pages,
                                case.max_pages_per_seq, case.max_context_len, case.window, ps, sms)
+        self.planner_kernel = self.plan.kernel
+        if kernel:
+            self.plan.kernel = KERNEL_IDS[kernel]
         self.out = torch.empty((B, Hq, D), dtype=torch.float16, device=device)
         self.lse = torch.empty((B, Hq), dtype=torch.float32, device=device)
         self.ws = pa.new_workspace(self.plan, device)
@@ -377,8 +384,8 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     device = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(device)
-    case = workloads.workload(args.workload)
-    arm = GpuArm(case, device)
+    case = workloads.workload(args.workload, batch=args.batch)
+    arm = GpuArm(case, device, kernel=None if args.kernel == "auto" else args.kernel)
     byts = kv_bytes(case)
     flush = None
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -389,6 +396,19 @@ def run_gpu(args):
     # correctness of the launch configuration being timed (device error word)
     arm.step()
     arm.check_error()
+    if args.profile_only:
+        # A short, plain run for ncu: warm-up plus `steps` decode steps, no
+        # timing, sampling or baselines.
+        for _ in range(args.warmup + args.steps):
+            arm.step()
+        torch.cuda.synchronize()
+        arm.check_error()
+        if rank == 0:
+            print(json.dumps({"profile_only": True, "workload": args.workload,
+                              "steps": args.steps, "warmup": args.warmup,
+                              "partitions": arm.plan.num_partitions,
+                              "partition_size": arm.plan.partition_size}), flush=True)
+        return 0
 
     if world > 1:
         torch.distributed.barrier()
@@ -433,20 +453,23 @@ def run_gpu(args):
         fl = l2_flush_buffer(torch, device)
         for name in workloads.WORKLOAD_ORDER:
             c = case if name == args.workload else workloads.workload(name)
-            a = arm if name == args.workload else GpuArm(c, device)
             b = kv_bytes(c)
-            med, kmed = time_flushed(a, args.per_workload_iters, fl)
-            a.check_error()
-            per[name] = {"us_per_step": med * 1e3, "partition_kernel_us": kmed * 1e3,
-                         "kv_bytes": b, "kv_gbs": b / (med * 1e-3) / 1e9,
-                         "frac_of_measured_hbm": b / (med * 1e-3) / 1e9 / peak,
-                         "frac_of_nominal_8tbs": b / (med * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
-                         "partitions": a.plan.num_partitions,
-                         "partition_size": a.plan.partition_size, "ctas": a.plan.ctas,
-                         "l2": "flushed before each step"}
-            if a is not arm:
+            entry = {}
+            for kname in ("mma", "simt"):
+                a = GpuArm(c, device, kernel=kname)
+                med, kmed = time_flushed(a, args.per_workload_iters, fl)
+                a.check_error()
+                entry[kname] = {"us_per_step": med * 1e3, "partition_kernel_us": kmed * 1e3,
+                                "kv_gbs": b / (med * 1e-3) / 1e9,
+                                "frac_of_measured_hbm": b / (med * 1e-3) / 1e9 / peak,
+                                "frac_of_nominal_8tbs": b / (med * 1e-3) / 1e9 / NOMINAL_HBM_GBS}
+                entry.update({"partitions": a.plan.num_partitions,
+                              "partition_size": a.plan.partition_size, "ctas": a.plan.ctas,
+                              "planner_kernel": KERNEL_NAMES[a.planner_kernel]})
                 del a
-            torch.cuda.empty_cache()
+                torch.cuda.empty_cache()
+            entry.update({"kv_bytes": b, "l2": "flushed before each step"})
+            per[name] = entry
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -471,7 +494,8 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": kern_gbs, "peak": peak, "unit": "GB/s",
                          "frac": kern_gbs / peak, "traffic": traffic,
-                         "peak_kind": peak_kind, "kernel": "attend_kernel (partition kernel)",
+                         "peak_kind": peak_kind,
+                         "kernel": f"partition kernel ({KERNEL_NAMES[arm.plan.kernel]})",
                          "kernel_us": kern_ms * 1e3, "frac_of_nominal_8tbs":
                              kern_gbs / NOMINAL_HBM_GBS, "src_sha": sha},
             "cpu_baseline": cpu,
@@ -497,6 +521,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true")
     ap.add_argument("--no-kv-upload", action="store_true")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "simt"])
+    ap.add_argument("--batch", type=int, default=None,
+                    help="keep only the workload's first sequences (profiler captures)")
+    ap.add_argument("--profile-only", action="store_true",
+                    help="run warm-up + steps untimed (for ncu captures) and exit")
     ap.add_argument("--per-workload-iters", type=int, default=50)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)

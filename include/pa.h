@@ -84,8 +84,15 @@ typedef struct pa_plan {
     int num_sms;            /* SM count the plan was made for */
     int ctas;               /* CTAs of the attention kernel */
     size_t workspace_bytes; /* bytes of device workspace pa_decode needs */
-    int reserved[8];
+    int kernel;             /* PA_KERNEL_* used for the partition kernel; pa_plan picks
+                               one, a caller may overwrite it before pa_decode */
+    int reserved[7];
 } pa_plan_t;
+
+/* Partition-kernel variants (pa_plan_t.kernel). */
+#define PA_KERNEL_SIMT 1   /* fp32 FMA on CUDA cores; pages by 1-D bulk copies */
+#define PA_KERNEL_MMA 2    /* mma.sync tensor cores (fp16 in, fp32 accumulate); pages by
+                              2-D TMA tensor copies with the 128-byte swizzle */
 
 /*
  * Choose the partitioning for a decode call (host only, no device access

@@ -1,8 +1,12 @@
 // pa_api.cu -- the C ABI (include/pa.h): host-side planning and argument
 // checks, the launch of the partition kernel, and the log-sum-exp merge kernel.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "pa_common.cuh"
 
@@ -11,6 +15,53 @@ namespace pa {
 template <int D>
 cudaError_t launch_attend_d(int G, bool split, const AttendParams& p, dim3 grid,
                             cudaStream_t stream);
+template <int D>
+cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtensorMap& tmK,
+                                const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
+
+static cudaError_t launch_attend_mma(int D, bool split, const AttendParams& p,
+                                     const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
+                                     cudaStream_t stream) {
+    switch (D) {
+        case 64: return launch_attend_mma_d<64>(split, p, tmK, tmV, grid, stream);
+        case 128: return launch_attend_mma_d<128>(split, p, tmK, tmV, grid, stream);
+        case 256: return launch_attend_mma_d<256>(split, p, tmK, tmV, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// The K (or V) cache as a 2-D fp16 tensor [rows = num_pages*Hkv*16, D]; one
+// box = 16 rows x 64 columns (one 128-byte slab of a page), 128-byte swizzle.
+static bool make_page_map(CUtensorMap* map, const void* base, long long rows, int D) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kPageSize};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
 
 int attend_ctas_per_sm(int D) {
     switch (D) {
@@ -36,10 +87,15 @@ cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 
 //   M = max_p m_p,  w_p = 2^(m_p - M) * l_p,  Lambda = sum_p w_p
 //   out = sum_p w_p * o_p / Lambda,  lse = (M + log2 Lambda) * ln 2
 // with m in the log2 domain and o_p already divided by its own exp-sum l_p.
-// One CTA per (query head, sequence); 256 threads = (1024 / D) partition
-// groups x (D / 4) float4 columns, reduced across groups in shared memory.
+// Grid (Hq, B, D / 64): a CTA serves 64 output dims of one (head, sequence)
+// with 16 float4 columns x 16 partition groups, reduced across groups in
+// shared memory.  Launched with programmatic stream serialization: its CTAs
+// may become resident while the partition kernel drains, and wait for it with
+// griddepcontrol.wait before touching the workspace.
 // ---------------------------------------------------------------------------
 constexpr int kMergeThreads = 256;
+constexpr int kMergeCols = 16;                          // float4 columns per CTA (64 dims)
+constexpr int kMergeGroups = kMergeThreads / kMergeCols;
 
 __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -56,30 +112,30 @@ __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) 
     return v;
 }
 
-template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
-    constexpr int D4 = D / 4;
-    constexpr int NGRP = kMergeThreads / D4;
     __shared__ float s_w[kMaxPartitions];
     __shared__ float s_red[32];
-    __shared__ __align__(16) float s_acc[NGRP][D];
+    __shared__ __align__(16) float s_acc[kMergeGroups][kMergeCols * 4];
 
     const int h = blockIdx.x;
     const int b = blockIdx.y;
+    const int D = p.D;
+    const int d0 = blockIdx.z * (kMergeCols * 4);
     const size_t bh = (size_t)b * p.Hq + h;
     const size_t row0 = bh * p.P;
+    wait_for_prerequisite_grid();
     const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, p.pages_per_part);
-    __half* orow = p.out + bh * D;
+    __half* orow = p.out + bh * D + d0;
     if (!sp.valid) {
-        if (threadIdx.x == 0 && h == 0) atomicOr(p.err, PA_DEVERR_BAD_LENGTH);
-        for (int d = threadIdx.x; d < D; d += kMergeThreads) orow[d] = __float2half_rn(NAN);
-        if (threadIdx.x == 0) p.lse[bh] = NAN;
+        if (threadIdx.x == 0 && h == 0 && blockIdx.z == 0) atomicOr(p.err, PA_DEVERR_BAD_LENGTH);
+        if (threadIdx.x < kMergeCols * 4) orow[threadIdx.x] = __float2half_rn(NAN);
+        if (threadIdx.x == 0 && blockIdx.z == 0) p.lse[bh] = NAN;
         return;
     }
     const int np = sp.num_parts;
     if (np == 0) {
-        for (int d = threadIdx.x; d < D; d += kMergeThreads) orow[d] = __float2half_rn(0.f);
-        if (threadIdx.x == 0) p.lse[bh] = -INFINITY;
+        if (threadIdx.x < kMergeCols * 4) orow[threadIdx.x] = __float2half_rn(0.f);
+        if (threadIdx.x == 0 && blockIdx.z == 0) p.lse[bh] = -INFINITY;
         return;
     }
     float mx = -INFINITY;
@@ -97,37 +153,47 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     const float lam = block_reduce(sum, s_red, false);  // also orders the s_w writes
     const float inv = 1.f / lam;
 
-    const int grp = threadIdx.x / D4;
-    const int d = (threadIdx.x % D4) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = grp; i < np; i += NGRP) {
-        const float w = s_w[i];
-        const float4 o = *reinterpret_cast<const float4*>(p.ws_o + (row0 + i) * D + d);
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
+    const int grp = threadIdx.x / kMergeCols;
+    const int col = (threadIdx.x % kMergeCols) * 4;
+    const float* src = p.ws_o + row0 * D + d0 + col;
+    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+    int i = grp;
+    for (; i + kMergeGroups < np; i += 2 * kMergeGroups) {
+        const float w0 = s_w[i], w1 = s_w[i + kMergeGroups];
+        const float4 o0 = *reinterpret_cast<const float4*>(src + (size_t)i * D);
+        const float4 o1 = *reinterpret_cast<const float4*>(src + (size_t)(i + kMergeGroups) * D);
+        acc0.x += w0 * o0.x; acc0.y += w0 * o0.y; acc0.z += w0 * o0.z; acc0.w += w0 * o0.w;
+        acc1.x += w1 * o1.x; acc1.y += w1 * o1.y; acc1.z += w1 * o1.z; acc1.w += w1 * o1.w;
     }
-    *reinterpret_cast<float4*>(&s_acc[grp][d]) = acc;
+    if (i < np) {
+        const float w0 = s_w[i];
+        const float4 o0 = *reinterpret_cast<const float4*>(src + (size_t)i * D);
+        acc0.x += w0 * o0.x; acc0.y += w0 * o0.y; acc0.z += w0 * o0.z; acc0.w += w0 * o0.w;
+    }
+    *reinterpret_cast<float4*>(&s_acc[grp][col]) =
+        make_float4(acc0.x + acc1.x, acc0.y + acc1.y, acc0.z + acc1.z, acc0.w + acc1.w);
     __syncthreads();
-    for (int dd = threadIdx.x; dd < D; dd += kMergeThreads) {
+    if (threadIdx.x < kMergeCols * 4) {
         float a = 0.f;
 #pragma unroll
-        for (int g = 0; g < NGRP; ++g) a += s_acc[g][dd];
-        orow[dd] = __float2half_rn(a * inv);
+        for (int g = 0; g < kMergeGroups; ++g) a += s_acc[g][threadIdx.x];
+        orow[threadIdx.x] = __float2half_rn(a * inv);
     }
-    if (threadIdx.x == 0) p.lse[bh] = (M + log2f(lam)) * 0.69314718055994531f;
+    if (threadIdx.x == 0 && blockIdx.z == 0) p.lse[bh] = (M + log2f(lam)) * 0.69314718055994531f;
 }
 
 cudaError_t launch_merge(int D, const MergeParams& p, cudaStream_t stream) {
-    const dim3 grid(p.Hq, p.B);
-    switch (D) {
-        case 64: merge_kernel<64><<<grid, kMergeThreads, 0, stream>>>(p); break;
-        case 128: merge_kernel<128><<<grid, kMergeThreads, 0, stream>>>(p); break;
-        case 256: merge_kernel<256><<<grid, kMergeThreads, 0, stream>>>(p); break;
-        default: return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.Hq, p.B, D / (kMergeCols * 4));
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_kernel, p);
 }
 
 // Workspace layout: [control block | m (B*Hq*P) | l (B*Hq*P) | o (B*Hq*P*D)],
@@ -246,6 +312,7 @@ int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page
     plan->num_sms = num_sms;
     plan->ctas = P * num_kv_heads * nchunk * batch;
     plan->workspace_bytes = ws_layout(batch, num_q_heads, head_dim, P).total;
+    plan->kernel = PA_KERNEL_MMA;
     return PA_OK;
 }
 
@@ -265,6 +332,11 @@ static int check_plan(const pa_plan_t* plan) {
     if (G < 1 || G > kMaxHeadsPerCta || g % G != 0) return PA_ERR_INVALID_ARG;
     if (plan->workspace_bytes < ws_layout(B, Hq, plan->head_dim, plan->num_partitions).total)
         return PA_ERR_INVALID_ARG;
+    if (plan->kernel != PA_KERNEL_SIMT && plan->kernel != PA_KERNEL_MMA) return PA_ERR_INVALID_ARG;
+    // TMA row coordinates are signed 32-bit.
+    if (plan->kernel == PA_KERNEL_MMA &&
+        (long long)plan->num_pages * Hkv * kPageSize > 0x7fffffffLL)
+        return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
 
@@ -312,10 +384,20 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     p.P = P;
     p.pages_per_part = plan->partition_size / kPageSize;
     p.nchunk = p.g / plan->heads_per_cta;
+    p.heads_per_cta = plan->heads_per_cta;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     const dim3 grid(P, p.Hkv * p.nchunk, p.B);
-    cudaError_t e = launch_attend(D, plan->heads_per_cta, P > 1, p, grid,
-                                  static_cast<cudaStream_t>(stream));
+    cudaError_t e;
+    if (plan->kernel == PA_KERNEL_MMA) {
+        alignas(64) CUtensorMap tmK, tmV;
+        const long long rows = (long long)plan->num_pages * p.Hkv * kPageSize;
+        if (!make_page_map(&tmK, k_cache, rows, D) || !make_page_map(&tmV, v_cache, rows, D))
+            return PA_ERR_CUDA;
+        e = launch_attend_mma(D, P > 1, p, tmK, tmV, grid, static_cast<cudaStream_t>(stream));
+    } else {
+        e = launch_attend(D, plan->heads_per_cta, P > 1, p, grid,
+                          static_cast<cudaStream_t>(stream));
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PA_ERR_CUDA;

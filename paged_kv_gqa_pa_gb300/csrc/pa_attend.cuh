@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 2);
     __shared__ int s_flag;
 
+    allow_dependent_launch();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int part = blockIdx.x;
@@ -297,10 +298,14 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
             consumed = item + 1;
         }
         const unsigned char* vpage = ring_wp + ((2 * k + 1) % NS) * PB;
+        const int vpos0 = (pg0 + warp + k * kWarps) * kPageSize;
 #pragma unroll
         for (int i = 0; i < TL; ++i) {
             const int t = rg * TL + i;
-            const uint4 raw = *reinterpret_cast<const uint4*>(vpage + t * (D * 2) + r * 16);
+            uint4 raw = *reinterpret_cast<const uint4*>(vpage + t * (D * 2) + r * 16);
+            // Slots outside [start, L) carry weight 0; zero their V too so that
+            // whatever an unwritten slot holds (NaN included) cannot leak in.
+            if (vpos0 + t < sp.start || vpos0 + t >= sp.L) raw = make_uint4(0, 0, 0, 0);
             float vf[8];
             half8_to_float(raw, vf);
             float pr[GP];

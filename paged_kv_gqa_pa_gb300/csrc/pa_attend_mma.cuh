@@ -1,0 +1,459 @@
+// pa_attend_mma.cuh -- tensor-core variant of the partition kernel.
+//
+// Same work split, result and epilogue as attend_kernel (pa_attend.cuh): one
+// CTA per (partition, KV head, head chunk, sequence), four warps with their own
+// page pipelines, online softmax per page, warp states merged at the end.
+// What differs is how a page is staged and contracted:
+//
+//  * Staging.  K and V pages arrive through 2-D TMA tensor copies
+//    (cp.async.bulk.tensor) of the cache viewed as a [num_pages*Hkv*16, D]
+//    fp16 matrix, one 16-row x 64-column box per 128-byte slab of the row, with
+//    the 128-byte swizzle: the 16-byte chunk c of row r lands at chunk
+//    c ^ (r & 7) of that row, so the ldmatrix reads below are free of bank
+//    conflicts.
+//  * q.K (the commit note's Phase 1 QK^T).  S^T[16 tokens x 8 heads] =
+//    K_page[16 x D] . Q^T[D x 8] with mma.sync m16n8k16 (fp16 in, fp32
+//    accumulate): K fragments via ldmatrix from the swizzled page, the q
+//    fragments sit in registers for the whole CTA.  The group's G <= 8 query
+//    heads fill the n = 8 columns (unused columns are zero and never stored).
+//  * softmax.  Each lane owns 2 tokens x 2 heads of S^T; page maxima come from
+//    three xor-shuffles, exp2 in fp32, and P is rounded to fp16 (the exp-sum
+//    adds the rounded values so numerator and denominator agree).
+//  * P.V.  O^T[D x 8] += V^T[D x 16 tokens] . P^T[16 x 8]: V^T fragments via
+//    ldmatrix.trans of the same swizzled page, P^T from S^T by movmatrix.trans.
+//    The accumulator of a lane holds two heads, so the online rescale needs
+//    no data exchange.
+#pragma once
+
+#include <cuda.h>
+#include <math.h>
+
+#include <atomic>
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+template <int D>
+struct MmaCfg {
+    static constexpr int kSlabs = D / 64;           // 128-byte slabs per K/V row
+    static constexpr int kSlabBytes = kPageSize * 128;
+    static constexpr int kPageBytes = kPageSize * D * 2;
+    static constexpr int kStages = D == 256 ? 3 : (D == 128 ? 4 : 6);
+    static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
+    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes +
+                                      kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 2 * 4 +
+                                      kWarps * kStages * 8 + 16;
+    static constexpr int kMinBlocks = D == 256 ? 2 : 3;
+    static_assert(kPageBytes == kSlabs * kSlabBytes, "slab layout");
+};
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2,
+                                        uint32_t& a3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& a0, uint32_t& a1,
+                                          uint32_t& a2, uint32_t& a3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+// c += A(16x16, row) . B(16x8, col), fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+        " {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi, float& lo_r, float& hi_r) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    const float2 back = __half22float2(h);
+    lo_r = back.x;
+    hi_r = back.y;
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Byte offset inside a swizzled page of the 16-byte chunk `chunk` (0..D/8-1)
+// of token row `row`.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    return (uint32_t)((chunk >> 3) * (kPageSize * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+template <int D, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
+    attend_mma_kernel(const AttendParams p, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV) {
+    using Cfg = MmaCfg<D>;
+    constexpr int NS = Cfg::kStages;
+    constexpr int PB = Cfg::kPageBytes;
+    constexpr int KT = D / 16;  // k-steps of q.K, m-tiles of P.V
+
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;  // 128-byte swizzle needs 1 KiB alignment
+    unsigned char* base = smem_raw + (base_u32 - raw_u32);
+    unsigned char* ring = base;
+    int* s_pid = reinterpret_cast<int*>(base + Cfg::kRingBytes);
+    float* s_ml = reinterpret_cast<float*>(s_pid + kMaxPagesPerPart);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 2);
+    __shared__ int s_flag;
+
+    allow_dependent_launch();
+    const int G = p.heads_per_cta;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int part = blockIdx.x;
+    const int kvh = blockIdx.y / p.nchunk;
+    const int h0 = kvh * p.g + (blockIdx.y % p.nchunk) * G;
+    const int b = blockIdx.z;
+
+    const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, p.pages_per_part);
+    auto fill_rows = [&](float o_val, float m_val, float l_val, float lse_val) {
+        for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+            const int h = idx / D, d = idx % D;
+            const size_t bh = (size_t)b * p.Hq + h0 + h;
+            if constexpr (SPLIT) {
+                const size_t row = bh * p.P + part;
+                p.ws_o[row * D + d] = o_val;
+                if (d == 0) {
+                    p.ws_m[row] = m_val;
+                    p.ws_l[row] = l_val;
+                }
+            } else {
+                p.out[bh * D + d] = __float2half_rn(o_val);
+                if (d == 0) p.lse[bh] = lse_val;
+            }
+        }
+    };
+    if (!sp.valid) {
+        if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0) atomicOr(p.err, PA_DEVERR_BAD_LENGTH);
+        if constexpr (!SPLIT) fill_rows(NAN, NAN, NAN, NAN);
+        return;
+    }
+    if (part >= sp.num_parts) {
+        if constexpr (!SPLIT) fill_rows(0.f, 0.f, 0.f, -INFINITY);
+        return;
+    }
+    const int pg0 = sp.first_page + part * p.pages_per_part;
+    const int npg = min(p.pages_per_part, sp.end_page - pg0);
+
+    if (threadIdx.x == 0) {
+        s_flag = 0;
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
+    }
+    const uint32_t bar_w = smem_u32(bars) + warp * NS * 8;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < NS; ++s) mbar_init(bar_w + s * 8, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < npg; j += kThreads) {
+        int id = p.block_tables[(size_t)b * p.maxp + pg0 + j];
+        if (id < 0 || id >= p.num_pages) {
+            s_flag = 1;
+            id = 0;
+        }
+        s_pid[j] = id;
+    }
+    __syncthreads();
+    if (s_flag) {
+        if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+        fill_rows(NAN, NAN, NAN, NAN);
+        return;
+    }
+
+    const int nk = npg > warp ? (npg - warp + kWarps - 1) / kWarps : 0;
+    const int n_items = 2 * nk;
+    const uint32_t ring_w = smem_u32(ring) + warp * NS * PB;
+
+    auto issue = [&](int item) {
+        const int slot = item % NS;
+        const int jj = warp + (item >> 1) * kWarps;
+        const CUtensorMap* map = (item & 1) ? &tmV : &tmK;
+        const int y = (s_pid[jj] * p.Hkv + kvh) * kPageSize;
+        const uint32_t bar = bar_w + slot * 8;
+        mbar_arrive_expect_tx(bar, PB);
+#pragma unroll
+        for (int s = 0; s < Cfg::kSlabs; ++s)
+            tma_load_2d(ring_w + slot * PB + s * Cfg::kSlabBytes, map, s * 64, y, bar);
+    };
+    if (lane == 0) {
+        for (int i = 0; i < NS && i < n_items; ++i) issue(i);
+    }
+    int issued = min(NS, n_items);
+
+    // q as the B operand of q.K: lane holds q[head = lane/4][dims kk*16 + (lane%4)*2 + {0,1}, +8]
+    const int qh = lane >> 2;
+    const bool q_ok = qh < G;
+    uint32_t qb[KT][2];
+    {
+        const __half* qrow = p.q + ((size_t)b * p.Hq + h0 + (q_ok ? qh : 0)) * D + (lane & 3) * 2;
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+            qb[kk][0] = q_ok ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16) : 0u;
+            qb[kk][1] = q_ok ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8) : 0u;
+        }
+    }
+
+    float o[KT][4];
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    const int tok0 = lane >> 2;  // this lane's tokens of a page: tok0 and tok0 + 8
+    // ldmatrix row/chunk roles of this lane
+    const int ld_j = lane >> 3;
+    const int ld_i = lane & 7;
+    const int k_row = ld_i + (ld_j & 1) * 8;  // q.K: matrices (rows 0-7|8-15) x (chunk +0|+1)
+    const int k_chk = ld_j >> 1;
+    const int v_row = ld_i + (ld_j >> 1) * 8; // P.V (trans): (chunk +0|+1) x (tokens 0-7|8-15)
+    const int v_chk = ld_j & 1;
+    bool ok = true;
+    int consumed = 0;
+
+    for (int k = 0; k < nk; ++k) {
+        const int page_pos = (pg0 + warp + k * kWarps) * kPageSize;
+        // ---------------- K page: S^T = K . Q^T
+        {
+            const int item = 2 * k;
+            const bool got = mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            consumed = item + 1;
+        }
+        const uint32_t kaddr = ring_w + ((2 * k) % NS) * PB;
+        float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(kaddr + swz(k_row, kk * 2 + k_chk), a0, a1, a2, a3);
+            if (kk & 1)
+                mma_16816(cb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+            else
+                mma_16816(ca, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        }
+        __syncwarp();
+        if (lane == 0 && 2 * k + NS < n_items) {
+            fence_proxy_async_smem();
+            issue(2 * k + NS);
+        }
+        if (2 * k + NS < n_items) issued = 2 * k + NS + 1;
+
+        // ---------------- online softmax (log2 domain); lane: tokens tok0, tok0+8; heads hA, hA+1
+        const bool v0 = page_pos + tok0 >= sp.start && page_pos + tok0 < sp.L;
+        const bool v1 = page_pos + tok0 + 8 >= sp.start && page_pos + tok0 + 8 < sp.L;
+        float s00 = v0 ? (ca[0] + cb[0]) * p.scale_log2 : -INFINITY;  // token0, head A
+        float s01 = v0 ? (ca[1] + cb[1]) * p.scale_log2 : -INFINITY;  // token0, head B
+        float s10 = v1 ? (ca[2] + cb[2]) * p.scale_log2 : -INFINITY;  // token1, head A
+        float s11 = v1 ? (ca[3] + cb[3]) * p.scale_log2 : -INFINITY;  // token1, head B
+        float mA = fmaxf(s00, s10), mB = fmaxf(s01, s11);
+#pragma unroll
+        for (int mask = 4; mask < 32; mask <<= 1) {
+            mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, mask));
+            mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, mask));
+        }
+        if (__any_sync(0xffffffffu, mA > m_run[0] || mB > m_run[1])) {
+            const float nA = fmaxf(m_run[0], mA), nB = fmaxf(m_run[1], mB);
+            const float aA = (nA == -INFINITY) ? 1.f : ex2(m_run[0] - nA);
+            const float aB = (nB == -INFINITY) ? 1.f : ex2(m_run[1] - nB);
+            m_run[0] = nA;
+            m_run[1] = nB;
+            l_run[0] *= aA;
+            l_run[1] *= aB;
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+                o[mt][0] *= aA;
+                o[mt][2] *= aA;
+                o[mt][1] *= aB;
+                o[mt][3] *= aB;
+            }
+        }
+        const float p00 = (s00 == -INFINITY) ? 0.f : ex2(s00 - m_run[0]);
+        const float p01 = (s01 == -INFINITY) ? 0.f : ex2(s01 - m_run[1]);
+        const float p10 = (s10 == -INFINITY) ? 0.f : ex2(s10 - m_run[0]);
+        const float p11 = (s11 == -INFINITY) ? 0.f : ex2(s11 - m_run[1]);
+        float r00, r01, r10, r11;
+        const uint32_t top = pack_half2(p00, p01, r00, r01);  // P[tok0][hA, hB]
+        const uint32_t bot = pack_half2(p10, p11, r10, r11);  // P[tok0 + 8][hA, hB]
+        l_run[0] += r00 + r10;
+        l_run[1] += r01 + r11;
+        // P^T fragments: lane gets P[tokens (lane%4)*2 + {0,1} (+8)][head lane/4]
+        const uint32_t pb0 = movmatrix_trans(top);
+        const uint32_t pb1 = movmatrix_trans(bot);
+
+        // ---------------- V page: O^T += V^T . P^T
+        {
+            const int item = 2 * k + 1;
+            const bool got = mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            consumed = item + 1;
+        }
+        const uint32_t vaddr = ring_w + ((2 * k + 1) % NS) * PB;
+        if (page_pos < sp.start || page_pos + kPageSize > sp.L) {
+            // Boundary page: zero the V rows of tokens outside [start, L) so
+            // that whatever those slots hold (never-written cache slots may
+            // hold NaN) cannot reach the output through a zero weight.
+            unsigned char* vgen = ring + warp * NS * PB + ((2 * k + 1) % NS) * PB;
+            for (int idx = lane; idx < kPageSize * (D / 8); idx += 32) {
+                const int row = idx / (D / 8);
+                const int pos = page_pos + row;
+                if (pos < sp.start || pos >= sp.L)
+                    *reinterpret_cast<uint4*>(vgen + swz(row, idx % (D / 8))) = make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+        }
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vaddr + swz(v_row, mt * 2 + v_chk), a0, a1, a2, a3);
+            mma_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+        }
+        __syncwarp();
+        if (lane == 0 && 2 * k + 1 + NS < n_items) {
+            fence_proxy_async_smem();
+            issue(2 * k + 1 + NS);
+        }
+        if (2 * k + 1 + NS < n_items) issued = 2 * k + 1 + NS + 1;
+    }
+
+    if (!ok) {
+        if (lane == 0) atomicOr(p.err, PA_DEVERR_TIMEOUT);
+        for (int item = consumed; item < issued; ++item)
+            (void)mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
+        s_flag = 1;
+    }
+
+    // ---- warp state -> shared memory.  Exp-sums: lanes with equal lane%4
+    // hold the same heads over different tokens.
+#pragma unroll
+    for (int mask = 4; mask < 32; mask <<= 1) {
+        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], mask);
+        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], mask);
+    }
+    __syncthreads();  // rings idle: reuse them for the warp states
+    float* s_o = reinterpret_cast<float*>(ring);  // [warps][G][D]
+    const int hA = (lane & 3) * 2;
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) {
+        const int d = mt * 16 + (lane >> 2);
+        if (hA < G) {
+            s_o[(warp * G + hA) * D + d] = o[mt][0];
+            s_o[(warp * G + hA) * D + d + 8] = o[mt][2];
+        }
+        if (hA + 1 < G) {
+            s_o[(warp * G + hA + 1) * D + d] = o[mt][1];
+            s_o[(warp * G + hA + 1) * D + d + 8] = o[mt][3];
+        }
+    }
+    if (lane < 4) {
+        if (hA < G) {
+            s_ml[warp * 2 * kMaxHeadsPerCta + hA] = m_run[0];
+            s_ml[warp * 2 * kMaxHeadsPerCta + kMaxHeadsPerCta + hA] = l_run[0];
+        }
+        if (hA + 1 < G) {
+            s_ml[warp * 2 * kMaxHeadsPerCta + hA + 1] = m_run[1];
+            s_ml[warp * 2 * kMaxHeadsPerCta + kMaxHeadsPerCta + hA + 1] = l_run[1];
+        }
+    }
+    __syncthreads();
+    if (s_flag) {
+        fill_rows(NAN, NAN, NAN, NAN);
+        return;
+    }
+
+    constexpr int D4 = D / 4;
+    for (int idx = threadIdx.x; idx < G * D4; idx += kThreads) {
+        const int h = idx / D4;
+        const int d = (idx % D4) * 4;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w * 2 * kMaxHeadsPerCta + h]);
+        float Ls = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float mw = s_ml[w * 2 * kMaxHeadsPerCta + h];
+            const float c = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+            Ls += c * s_ml[w * 2 * kMaxHeadsPerCta + kMaxHeadsPerCta + h];
+            const float4 ow = *reinterpret_cast<const float4*>(s_o + (w * G + h) * D + d);
+            acc.x += c * ow.x;
+            acc.y += c * ow.y;
+            acc.z += c * ow.z;
+            acc.w += c * ow.w;
+        }
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        const size_t bh = (size_t)b * p.Hq + h0 + h;
+        if constexpr (SPLIT) {
+            const size_t row = bh * p.P + part;
+            *reinterpret_cast<float4*>(p.ws_o + row * D + d) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            if (d == 0) {
+                p.ws_m[row] = M;
+                p.ws_l[row] = Ls;
+            }
+        } else {
+            __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
+            __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
+            uint2 packed;
+            packed.x = *reinterpret_cast<uint32_t*>(&lo);
+            packed.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(p.out + bh * D + d) = packed;
+            if (d == 0) p.lse[bh] = Ls > 0.f ? M * 0.69314718055994531f + logf(Ls) : -INFINITY;
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtensorMap& tmK,
+                                const CUtensorMap& tmV, dim3 grid, cudaStream_t stream) {
+    const void* fn = split ? reinterpret_cast<const void*>(&attend_mma_kernel<D, true>)
+                           : reinterpret_cast<const void*>(&attend_mma_kernel<D, false>);
+    constexpr int kMaxDevices = 64;
+    static std::atomic<uint32_t> configured[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint32_t bit = split ? 2u : 1u;
+    if (dev < 0 || dev >= kMaxDevices || !(configured[dev].load() & bit)) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 MmaCfg<D>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) configured[dev].fetch_or(bit);
+    }
+    void* args[] = {const_cast<AttendParams*>(&p), const_cast<CUtensorMap*>(&tmK),
+                    const_cast<CUtensorMap*>(&tmV)};
+    return cudaLaunchKernel(fn, grid, dim3(kThreads), args, MmaCfg<D>::kSmemBytes, stream);
+}
+
+}  // namespace pa

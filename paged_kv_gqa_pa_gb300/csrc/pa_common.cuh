@@ -39,6 +39,7 @@ struct AttendParams {
     int P;                  // partitions (grid.x)
     int pages_per_part;     // partition size in pages
     int nchunk;             // head chunks per KV head (grid.y = Hkv * nchunk)
+    int heads_per_cta;      // G: query heads one CTA serves
     float scale_log2;       // scale * log2(e)
 };
 
@@ -156,9 +157,22 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Let a dependent grid launched with programmatic stream serialization (the
+// merge) get scheduled while this grid's last CTAs still run; the dependent
+// grid waits for this grid's completion before it reads anything.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grid this one depends on has completed and its writes are
+// visible (no-op for a normal launch).
+__device__ __forceinline__ void wait_for_prerequisite_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 }  // namespace pa
 
-// Launchers implemented per head dim (pa_attend_d*.cu).
+// Launchers (pa_attend_d*.cu, pa_attend_mma.cu).
 namespace pa {
 cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 grid,
                           cudaStream_t stream);

@@ -165,12 +165,17 @@ WORKLOADS = {
 WORKLOAD_ORDER = list(WORKLOADS)
 
 
-def workload(name: str) -> Case:
+def workload(name: str, batch: int | None = None) -> Case:
+    """One of the measured workloads; `batch` keeps only its first sequences
+    (a smaller case of the same shapes, e.g. for profiler captures)."""
     spec = dict(WORKLOADS[name])
     lens = spec.pop("lens")
     seed = spec["seed"]
     if lens == "ragged":
         lens = _ragged_lengths(spec["B"], 1, 4096, seed, 512)
         spec["max_pages_per_seq"] = 4096 // PAGE_SIZE
+    if batch is not None:
+        spec["B"] = batch
+        lens = list(lens)[:batch]
     return make_case(name=name, B=spec.pop("B"), Hq=spec.pop("Hq"), Hkv=spec.pop("Hkv"),
                      D=spec.pop("D"), context_lens=lens, seed=spec.pop("seed"), **spec)

@@ -15,6 +15,11 @@ LSE_TOL = 1e-4
 
 _built = False
 
+# Partition-kernel variant the GPU tests run (set per test by a fixture);
+# None keeps the planner's choice.
+KERNEL = None
+KERNELS = {"mma": 2, "simt": 1}
+
 
 def ensure_built():
     global _built
@@ -52,6 +57,8 @@ def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=N
         num_sms = torch.cuda.get_device_properties(0).multi_processor_count
     plan = pa.pa_plan(B, Hq, case.Hkv, D, case.page_size, case.num_pages, case.max_pages_per_seq,
                       max_context_len, case.window, partition_size, num_sms)
+    if KERNEL is not None:
+        plan.kernel = KERNELS[KERNEL]
     n_out = B * Hq * D
     out_buf = torch.full((n_out + 2 * guard,), float("nan"), dtype=torch.float16, device="cuda")
     lse_buf = torch.full((B * Hq + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")

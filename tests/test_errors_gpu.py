@@ -6,12 +6,21 @@ values are rejected by the kernel's own bounds checks before any access."""
 import numpy as np
 import pytest
 
+import gpu_helpers
 import oracle
 import paged_kv_gqa_pa_gb300 as pa
 from gpu_helpers import assert_matches_oracle, run_gpu
 from paged_kv_gqa_pa_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=["mma", "simt"], autouse=True)
+def kernel_variant(request):
+    """Run every test on both partition kernels (tensor-core and CUDA-core)."""
+    gpu_helpers.KERNEL = request.param
+    yield request.param
+    gpu_helpers.KERNEL = None
 
 
 def _ref_rows(case, rows):

@@ -10,11 +10,20 @@ import numpy as np
 import pytest
 import torch
 
+import gpu_helpers
 import oracle
 from gpu_helpers import assert_matches_oracle, run_gpu, to_device
 from paged_kv_gqa_pa_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=["mma", "simt"], autouse=True)
+def kernel_variant(request):
+    """Run every test on both partition kernels (tensor-core and CUDA-core)."""
+    gpu_helpers.KERNEL = request.param
+    yield request.param
+    gpu_helpers.KERNEL = None
 
 
 # ---- the five measured workloads, at full size, in the plan the bench uses
@@ -186,3 +195,25 @@ def test_max_shapes():
         out, lse, err, _ = run_gpu(case)
         assert err == 0
         assert_matches_oracle(case, out, lse, what=f"max S{S}")
+
+
+def test_unwritten_slots_never_leak():
+    """Cache slots outside the attended range (the tail of the last page, the
+    head of the first page under a window) may hold anything, NaN included:
+    they get weight 0 and must not reach the output."""
+    lens = [37, 1000, 16, 3001]
+    case = workloads.make_case("tail", len(lens), 8, 2, 128, lens, seed=508, window=700)
+    ps = case.page_size
+    for b, L in enumerate(lens):
+        start = L - case.window if 0 < case.window < L else 0
+        first, last = start // ps, (L - 1) // ps
+        pf, pl = case.block_tables[b, first], case.block_tables[b, last]
+        case.k_cache[pf, :, :start % ps] = np.float16(np.nan)
+        case.v_cache[pf, :, :start % ps] = np.float16(np.nan)
+        case.k_cache[pl, :, (L - 1) % ps + 1:] = np.float16(np.nan)
+        case.v_cache[pl, :, (L - 1) % ps + 1:] = np.float16(np.inf)
+    for S in (0, 64, 4096):
+        case.partition_size = S
+        out, lse, err, _ = run_gpu(case)
+        assert err == 0
+        assert_matches_oracle(case, out, lse, what=f"tail S{S}")
