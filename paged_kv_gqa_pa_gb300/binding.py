@@ -23,6 +23,8 @@ PA_ERR_WORKSPACE = 4
 PA_DEVERR_BAD_PAGE = 1
 PA_DEVERR_BAD_LENGTH = 2
 PA_DEVERR_TIMEOUT = 4
+PA_KERNEL_SIMT = 1
+PA_KERNEL_MMA = 2
 
 EXPORTED = ("pa_plan", "pa_decode", "pa_decode_partitions", "pa_merge", "pa_get_error",
             "pa_status_string", "pa_version")
@@ -45,7 +47,8 @@ class pa_plan_t(ctypes.Structure):
         ("num_sms", ctypes.c_int),
         ("ctas", ctypes.c_int),
         ("workspace_bytes", ctypes.c_size_t),
-        ("reserved", ctypes.c_int * 8),
+        ("kernel", ctypes.c_int),
+        ("reserved", ctypes.c_int * 7),
     ]
 
     def as_dict(self):

@@ -17,8 +17,10 @@
 //    fragments sit in registers for the whole CTA.  The group's G <= 8 query
 //    heads fill the n = 8 columns (unused columns are zero and never stored).
 //  * softmax.  Each lane owns 2 tokens x 2 heads of S^T; page maxima come from
-//    three xor-shuffles, exp2 in fp32, and P is rounded to fp16 (the exp-sum
-//    adds the rounded values so numerator and denominator agree).
+//    three xor-shuffles, exp2 in fp32, and P is rounded to fp16 for the mma.
+//    Two exp-sums are kept: of the rounded weights, which normalises the
+//    output (so the weights applied to V sum to one), and of the fp32
+//    weights, which gives the LSE and the partition's weight in the merge.
 //  * P.V.  O^T[D x 8] += V^T[D x 16 tokens] . P^T[16 x 8]: V^T fragments via
 //    ldmatrix.trans of the same swizzled page, P^T from S^T by movmatrix.trans.
 //    The accumulator of a lane holds two heads, so the online rescale needs
@@ -42,7 +44,7 @@ struct MmaCfg {
     static constexpr int kStages = D == 256 ? 3 : (D == 128 ? 4 : 6);
     static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes +
-                                      kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 2 * 4 +
+                                      kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 3 * 4 +
                                       kWarps * kStages * 8 + 16;
     static constexpr int kMinBlocks = D == 256 ? 2 : 3;
     static_assert(kPageBytes == kSlabs * kSlabBytes, "slab layout");
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     unsigned char* ring = base;
     int* s_pid = reinterpret_cast<int*>(base + Cfg::kRingBytes);
     float* s_ml = reinterpret_cast<float*>(s_pid + kMaxPagesPerPart);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 2);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 3);
     __shared__ int s_flag;
 
     allow_dependent_launch();
@@ -225,7 +227,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
 #pragma unroll
     for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY};
-    float l_run[2] = {0.f, 0.f};
+    float l_run[2] = {0.f, 0.f};   // exp-sum of the fp32 weights
+    float n_run[2] = {0.f, 0.f};   // exp-sum of the fp16-rounded weights
     const int tok0 = lane >> 2;  // this lane's tokens of a page: tok0 and tok0 + 8
     // ldmatrix row/chunk roles of this lane
     const int ld_j = lane >> 3;
@@ -288,6 +291,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
             m_run[1] = nB;
             l_run[0] *= aA;
             l_run[1] *= aB;
+            n_run[0] *= aA;
+            n_run[1] *= aB;
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt) {
                 o[mt][0] *= aA;
@@ -303,8 +308,10 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         float r00, r01, r10, r11;
         const uint32_t top = pack_half2(p00, p01, r00, r01);  // P[tok0][hA, hB]
         const uint32_t bot = pack_half2(p10, p11, r10, r11);  // P[tok0 + 8][hA, hB]
-        l_run[0] += r00 + r10;
-        l_run[1] += r01 + r11;
+        l_run[0] += p00 + p10;
+        l_run[1] += p01 + p11;
+        n_run[0] += r00 + r10;
+        n_run[1] += r01 + r11;
         // P^T fragments: lane gets P[tokens (lane%4)*2 + {0,1} (+8)][head lane/4]
         const uint32_t pb0 = movmatrix_trans(top);
         const uint32_t pb1 = movmatrix_trans(bot);
@@ -360,6 +367,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     for (int mask = 4; mask < 32; mask <<= 1) {
         l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], mask);
         l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], mask);
+        n_run[0] += __shfl_xor_sync(0xffffffffu, n_run[0], mask);
+        n_run[1] += __shfl_xor_sync(0xffffffffu, n_run[1], mask);
     }
     __syncthreads();  // rings idle: reuse them for the warp states
     float* s_o = reinterpret_cast<float*>(ring);  // [warps][G][D]
@@ -376,14 +385,17 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
             s_o[(warp * G + hA + 1) * D + d + 8] = o[mt][3];
         }
     }
-    if (lane < 4) {
+    if (lane < 4) {  // s_ml: [warps][m | l | n][8]
+        float* ml = s_ml + warp * 3 * kMaxHeadsPerCta;
         if (hA < G) {
-            s_ml[warp * 2 * kMaxHeadsPerCta + hA] = m_run[0];
-            s_ml[warp * 2 * kMaxHeadsPerCta + kMaxHeadsPerCta + hA] = l_run[0];
+            ml[hA] = m_run[0];
+            ml[kMaxHeadsPerCta + hA] = l_run[0];
+            ml[2 * kMaxHeadsPerCta + hA] = n_run[0];
         }
         if (hA + 1 < G) {
-            s_ml[warp * 2 * kMaxHeadsPerCta + hA + 1] = m_run[1];
-            s_ml[warp * 2 * kMaxHeadsPerCta + kMaxHeadsPerCta + hA + 1] = l_run[1];
+            ml[hA + 1] = m_run[1];
+            ml[kMaxHeadsPerCta + hA + 1] = l_run[1];
+            ml[2 * kMaxHeadsPerCta + hA + 1] = n_run[1];
         }
     }
     __syncthreads();
@@ -398,21 +410,23 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         const int d = (idx % D4) * 4;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w * 2 * kMaxHeadsPerCta + h]);
-        float Ls = 0.f;
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w * 3 * kMaxHeadsPerCta + h]);
+        float Ls = 0.f, Ns = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float mw = s_ml[w * 2 * kMaxHeadsPerCta + h];
+            const float* ml = s_ml + w * 3 * kMaxHeadsPerCta;
+            const float mw = ml[h];
             const float c = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-            Ls += c * s_ml[w * 2 * kMaxHeadsPerCta + kMaxHeadsPerCta + h];
+            Ls += c * ml[kMaxHeadsPerCta + h];
+            Ns += c * ml[2 * kMaxHeadsPerCta + h];
             const float4 ow = *reinterpret_cast<const float4*>(s_o + (w * G + h) * D + d);
             acc.x += c * ow.x;
             acc.y += c * ow.y;
             acc.z += c * ow.z;
             acc.w += c * ow.w;
         }
-        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        const float inv = Ns > 0.f ? 1.f / Ns : 0.f;
         const size_t bh = (size_t)b * p.Hq + h0 + h;
         if constexpr (SPLIT) {
             const size_t row = bh * p.P + part;

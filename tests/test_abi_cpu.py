@@ -47,9 +47,16 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_plan_struct_layout_matches_header():
-    # 14 ints, then a size_t, then 8 reserved ints.
+    # Field names and order of the ctypes mirror equal the C struct's.
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    body = re.search(r"typedef struct pa_plan \{(.*?)\} pa_plan_t;", text, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"\b(?:int|size_t)\s+([a-z_]+)(?:\[\d+\])?\s*;", body)
+    assert fields == [f for f, _ in binding.pa_plan_t._fields_]
+    # 14 ints, a size_t, the kernel id, 7 reserved ints.
     assert binding.pa_plan_t.workspace_bytes.offset == 56
-    assert ctypes.sizeof(binding.pa_plan_t) == 56 + 8 + 32
+    assert binding.pa_plan_t.kernel.offset == 64
+    assert ctypes.sizeof(binding.pa_plan_t) == 96
 
 
 def test_status_strings_and_version():
