@@ -138,6 +138,35 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
              void* workspace, void* stream);
 
 /*
+ * pa_decode for callers that cannot allocate device memory when they decode
+ * (inside a CUDA graph capture, inside an engine or plugin that only hands
+ * over its input and output buffers, or in a loop that must never enter the
+ * allocator).  The pages have no counterpart: this is a convenience of the
+ * library, not a step of the method.
+ *
+ * Same arguments, layouts and result as pa_decode, minus the workspace: the
+ * partition partials go to a scratch array of PA_STATIC_WORKSPACE_BYTES
+ * compiled into the library (a __device__ array, so every GPU that loads the
+ * library keeps that much memory until the process exits).  Nothing is
+ * allocated or freed by this call.
+ *   - A plan with workspace_bytes > PA_STATIC_WORKSPACE_BYTES is rejected with
+ *     PA_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture on that device.
+ *   - All calls on a device share the one array, which keeps the previous
+ *     call's contents: calls whose kernels overlap on the GPU (different
+ *     streams, no ordering between them) race on it and must not be issued.
+ *   - Data-dependent faults still produce NaN rows in out/lse; the device
+ *     error word lives in the shared array and is not reported by this call.
+ */
+#define PA_STATIC_WORKSPACE_BYTES (32u << 20)
+int pa_decode_static(const pa_plan_t* plan, const void* q, const void* k_cache,
+                     const void* v_cache, const int32_t* block_tables,
+                     const int32_t* context_lens, float scale, int window, void* out,
+                     float* lse, void* stream);
+
+/*
  * Synchronise `stream`, read the device error word kept in `workspace`
  * (PA_DEVERR_* bits, 0 = none) into *device_error, and reset it to 0 when
  * `clear` is non-zero.

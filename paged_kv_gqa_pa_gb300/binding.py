@@ -27,7 +27,7 @@ PA_KERNEL_SIMT = 1
 PA_KERNEL_MMA = 2
 
 EXPORTED = ("pa_plan", "pa_decode", "pa_decode_partitions", "pa_merge", "pa_get_error",
-            "pa_status_string", "pa_version")
+            "pa_status_string", "pa_version", "pa_decode_static")
 
 
 class pa_plan_t(ctypes.Structure):
@@ -99,6 +99,8 @@ def load():
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_version.argtypes = []
         lib.pa_version.restype = i
+        lib.pa_decode_static.argtypes = dec[:10] + [P]
+        lib.pa_decode_static.restype = i
         _lib = lib
         return lib
 
@@ -180,6 +182,17 @@ def pa_merge(plan, context_lens, out, lse, workspace, stream=None) -> None:
                          _dev_ptr(workspace, "workspace"), _stream_ptr(stream))
     if st != PA_OK:
         raise PAError("pa_merge", st)
+
+
+def pa_decode_static(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window, out,
+                     lse, stream=None) -> None:
+    """pa_decode with the library's built-in scratch instead of a workspace,
+    for callers that must not allocate device memory (see include/pa.h)."""
+    args = _decode_args(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window,
+                        out, lse, None, stream)
+    st = load().pa_decode_static(*args[:10], args[11])
+    if st != PA_OK:
+        raise PAError("pa_decode_static", st)
 
 
 def pa_get_error(workspace, stream=None, clear=True) -> int:
