@@ -112,8 +112,15 @@ __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) 
     return v;
 }
 
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
-    __shared__ float s_w[kMaxPartitions];
+__global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergeParams p) {
+    // Partitions are taken in chunks of kChunk; within a chunk every load (the
+    // chunk's m and l, and each thread's kPer float4 slices of o) is issued
+    // before any is used, so a chunk costs one memory round trip.  Chunks are
+    // combined with a running maximum (the same log-sum-exp algebra).
+    constexpr int kPer = 16;
+    constexpr int kChunk = kMergeGroups * kPer;  // 256 partitions
+    static_assert(kChunk == kMergeThreads, "one (m, l) per thread per chunk");
+    __shared__ float s_w[kChunk];
     __shared__ float s_red[32];
     __shared__ __align__(16) float s_acc[kMergeGroups][kMergeCols * 4];
 
@@ -138,41 +145,52 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
         if (threadIdx.x == 0 && blockIdx.z == 0) p.lse[bh] = -INFINITY;
         return;
     }
-    float mx = -INFINITY;
-    for (int i = threadIdx.x; i < np; i += kMergeThreads) mx = fmaxf(mx, p.ws_m[row0 + i]);
-    const float M = block_reduce(mx, s_red, true);
-    float sum = 0.f;
-    for (int i = threadIdx.x; i < np; i += kMergeThreads) {
-        const float l = p.ws_l[row0 + i];
-        // l == 0 marks a partition with nothing attended; a NaN l (a partition
-        // that found a bad page) is kept so the NaN reaches the output.
-        const float w = (l == 0.f) ? 0.f : ex2(p.ws_m[row0 + i] - M) * l;
-        s_w[i] = w;
-        sum += w;
-    }
-    const float lam = block_reduce(sum, s_red, false);  // also orders the s_w writes
-    const float inv = 1.f / lam;
-
     const int grp = threadIdx.x / kMergeCols;
     const int col = (threadIdx.x % kMergeCols) * 4;
     const float* src = p.ws_o + row0 * D + d0 + col;
-    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-    int i = grp;
-    for (; i + kMergeGroups < np; i += 2 * kMergeGroups) {
-        const float w0 = s_w[i], w1 = s_w[i + kMergeGroups];
-        const float4 o0 = *reinterpret_cast<const float4*>(src + (size_t)i * D);
-        const float4 o1 = *reinterpret_cast<const float4*>(src + (size_t)(i + kMergeGroups) * D);
-        acc0.x += w0 * o0.x; acc0.y += w0 * o0.y; acc0.z += w0 * o0.z; acc0.w += w0 * o0.w;
-        acc1.x += w1 * o1.x; acc1.y += w1 * o1.y; acc1.z += w1 * o1.z; acc1.w += w1 * o1.w;
+
+    float M = -INFINITY;   // running max (log2 domain)
+    float lam = 0.f;       // running sum of partition weights
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < np; c0 += kChunk) {
+        const int i_ml = c0 + threadIdx.x;
+        const float m_i = i_ml < np ? p.ws_m[row0 + i_ml] : -INFINITY;
+        const float l_i = i_ml < np ? p.ws_l[row0 + i_ml] : 0.f;
+        float4 o[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = c0 + grp + k * kMergeGroups;
+            o[k] = i < np ? *reinterpret_cast<const float4*>(src + (size_t)i * D)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const float Mc = block_reduce(m_i, s_red, true);
+        const float Mn = fmaxf(M, Mc);
+        const float rescale = (M == -INFINITY) ? 0.f : ex2(M - Mn);
+        // l == 0 marks a partition with nothing attended; a NaN (a partition
+        // that met a bad page) is kept so that it reaches the output.
+        const float w = (l_i == 0.f) ? 0.f : ex2(m_i - Mn) * l_i;
+        s_w[threadIdx.x] = w;
+        const float wsum = block_reduce(w, s_red, false);  // also orders the s_w writes
+        lam = lam * rescale + wsum;
+        acc.x *= rescale;
+        acc.y *= rescale;
+        acc.z *= rescale;
+        acc.w *= rescale;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = grp + k * kMergeGroups;
+            const float wk = (c0 + i < np) ? s_w[i] : 0.f;
+            acc.x += wk * o[k].x;
+            acc.y += wk * o[k].y;
+            acc.z += wk * o[k].z;
+            acc.w += wk * o[k].w;
+        }
+        M = Mn;
+        __syncthreads();  // s_w is rewritten by the next chunk
     }
-    if (i < np) {
-        const float w0 = s_w[i];
-        const float4 o0 = *reinterpret_cast<const float4*>(src + (size_t)i * D);
-        acc0.x += w0 * o0.x; acc0.y += w0 * o0.y; acc0.z += w0 * o0.z; acc0.w += w0 * o0.w;
-    }
-    *reinterpret_cast<float4*>(&s_acc[grp][col]) =
-        make_float4(acc0.x + acc1.x, acc0.y + acc1.y, acc0.z + acc1.z, acc0.w + acc1.w);
+    *reinterpret_cast<float4*>(&s_acc[grp][col]) = acc;
     __syncthreads();
+    const float inv = 1.f / lam;
     if (threadIdx.x < kMergeCols * 4) {
         float a = 0.f;
 #pragma unroll
@@ -283,14 +301,30 @@ int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page
     if (partition_size > 0) {
         pp = partition_size / page_size;
     } else {
-        // Enough CTAs for two waves of the kernel's resident CTAs, with at
-        // least one page per warp; no split when one pass already fills it.
-        const long long per_part = (long long)batch * num_kv_heads * nchunk;
-        const long long want = 2LL * num_sms * attend_ctas_per_sm(head_dim);
-        int parts = per_part > 0 ? (int)((want + per_part - 1) / per_part) : 1;
-        if (parts < 1) parts = 1;
-        pp = (span + parts - 1) / parts;
-        if (pp < kWarps) pp = kWarps;
+        // Automatic: split only when it pays.  A group's whole context of at
+        // most kNoSplitBytes streams through one CTA faster than a second
+        // launch (the merge) costs, and when the unsplit grid already fills
+        // the GPU a split only adds merge traffic.  Otherwise cut each group's
+        // span so that the grid is a whole number of waves of resident CTAs
+        // (the fewest waves whose partitions fit kMaxPagesPerPart), with at
+        // least kMinPagesPerPart pages per partition.
+        constexpr long long kNoSplitBytes = 128 << 10;
+        constexpr int kMinPagesPerPart = 2 * kWarps;
+        const long long groups = (long long)batch * num_kv_heads * nchunk;
+        const long long slots = (long long)num_sms * attend_ctas_per_sm(head_dim);
+        const long long span_bytes = (long long)span * 2 * page_size * head_dim * 2;
+        if (groups == 0 || groups >= slots || span_bytes <= kNoSplitBytes) {
+            pp = span;
+        } else {
+            pp = span;
+            for (long long waves = 1; waves <= 64; ++waves) {
+                long long parts = waves * slots / groups;
+                if (parts < 1) parts = 1;
+                pp = (int)((span + parts - 1) / parts);
+                if (pp <= kMaxPagesPerPart) break;
+            }
+            if (pp < kMinPagesPerPart) pp = kMinPagesPerPart;
+        }
         if (pp > kMaxPagesPerPart) pp = kMaxPagesPerPart;
     }
     if (pp > kMaxPagesPerPart) return PA_ERR_UNSUPPORTED;
