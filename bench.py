@@ -43,14 +43,27 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the partition kernel, from one ncu
 # capture, keyed by workload; valid only while the kernel sources hash to
 # `src_sha` (otherwise the bench reports traffic = null).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/attend_mma_gqa6_ctx100k_b1.md: one capture of the B = 1 case,
+    # (409.73 + 6.41) MB read + written, scaled by tokens to the B = 4 launch.
+    ("gqa6_ctx100k", "mma"): {"src_sha": "5e600045fe794112", "partition_size": 512,
+                              "bytes_per_launch": 4 * (409.731072e6 + 6.412544e6)},
+}
 
 
-def kernel_src_sha() -> str:
+KERNEL_SOURCES = {
+    "mma": ("pa_attend_mma.cuh", "pa_attend_mma.cu", "pa_common.cuh"),
+    "simt": ("pa_attend.cuh", "pa_attend_d64.cu", "pa_attend_d128.cu", "pa_attend_d256.cu",
+             "pa_common.cuh"),
+}
+
+
+def kernel_src_sha(kernel: str) -> str:
+    """Hash of the sources that define one partition-kernel variant."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "paged_kv_gqa_pa_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "paged_kv_gqa_pa_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -484,9 +497,13 @@ def run_gpu(args):
 
     peak, peak_kind = measured_peaks()
     kern_gbs = byts / (kern_ms * 1e-3) / 1e9
-    sha = kernel_src_sha()
-    tr = NCU_TRAFFIC.get(args.workload)
-    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == sha else None
+    kname = KERNEL_NAMES[arm.plan.kernel]
+    sha = kernel_src_sha(kname)
+    tr = NCU_TRAFFIC.get((args.workload, kname))
+    traffic = None
+    if tr and tr["src_sha"] == sha and tr["partition_size"] == arm.plan.partition_size \
+            and args.batch is None:
+        traffic = tr["bytes_per_launch"]
 
     e2e_ms, h2d, d2h = e2e_steps(arm, max(10, min(args.steps, 200)), 3)
     e2e = {"value": byts / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
