@@ -86,7 +86,10 @@ typedef struct pa_plan {
     size_t workspace_bytes; /* bytes of device workspace pa_decode needs */
     int kernel;             /* PA_KERNEL_* used for the partition kernel; pa_plan picks
                                one, a caller may overwrite it before pa_decode */
-    int reserved[7];
+    int parts_per_cta;      /* consecutive partitions one CTA of the tensor-core kernel
+                               streams (one partial per partition all the same); the
+                               CUDA-core kernel always serves one */
+    int reserved[6];
 } pa_plan_t;
 
 /* Partition-kernel variants (pa_plan_t.kernel). */

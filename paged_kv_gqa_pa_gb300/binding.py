@@ -48,7 +48,8 @@ class pa_plan_t(ctypes.Structure):
         ("ctas", ctypes.c_int),
         ("workspace_bytes", ctypes.c_size_t),
         ("kernel", ctypes.c_int),
-        ("reserved", ctypes.c_int * 7),
+        ("parts_per_cta", ctypes.c_int),
+        ("reserved", ctypes.c_int * 6),
     ]
 
     def as_dict(self):

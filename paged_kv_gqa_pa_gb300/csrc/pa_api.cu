@@ -88,14 +88,15 @@ cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 
 //   out = sum_p w_p * o_p / Lambda,  lse = (M + log2 Lambda) * ln 2
 // with m in the log2 domain and o_p already divided by its own exp-sum l_p.
 // Grid (Hq, B, D / 64): a CTA serves 64 output dims of one (head, sequence)
-// with 16 float4 columns x 16 partition groups, reduced across groups in
-// shared memory.  Launched with programmatic stream serialization: its CTAs
+// with 16 float4 columns x 8 partition groups, reduced across groups in
+// shared memory; small CTAs with many loads each keep three CTAs per SM, so
+// the grid of a long-context step fits in one wave.  Launched with programmatic stream serialization: its CTAs
 // may become resident while the partition kernel drains, and wait for it with
 // griddepcontrol.wait before touching the workspace.
 // ---------------------------------------------------------------------------
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 128;
 constexpr int kMergeCols = 16;                          // float4 columns per CTA (64 dims)
-constexpr int kMergeGroups = kMergeThreads / kMergeCols;
+constexpr int kMergeGroups = kMergeThreads / kMergeCols;  // partition groups (8)
 
 __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -112,14 +113,14 @@ __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) 
     return v;
 }
 
-__global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeParams p) {
     // Partitions are taken in chunks of kChunk; within a chunk every load (the
     // chunk's m and l, and each thread's kPer float4 slices of o) is issued
     // before any is used, so a chunk costs one memory round trip.  Chunks are
     // combined with a running maximum (the same log-sum-exp algebra).
-    constexpr int kPer = 16;
+    constexpr int kPer = 32;
     constexpr int kChunk = kMergeGroups * kPer;  // 256 partitions
-    static_assert(kChunk == kMergeThreads, "one (m, l) per thread per chunk");
+    constexpr int kMlPer = kChunk / kMergeThreads;  // (m, l) pairs per thread per chunk
     __shared__ float s_w[kChunk];
     __shared__ float s_red[32];
     __shared__ __align__(16) float s_acc[kMergeGroups][kMergeCols * 4];
@@ -153,9 +154,13 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergePara
     float lam = 0.f;       // running sum of partition weights
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c0 = 0; c0 < np; c0 += kChunk) {
-        const int i_ml = c0 + threadIdx.x;
-        const float m_i = i_ml < np ? p.ws_m[row0 + i_ml] : -INFINITY;
-        const float l_i = i_ml < np ? p.ws_l[row0 + i_ml] : 0.f;
+        float m_i[kMlPer], l_i[kMlPer];
+#pragma unroll
+        for (int u = 0; u < kMlPer; ++u) {
+            const int i_ml = c0 + threadIdx.x + u * kMergeThreads;
+            m_i[u] = i_ml < np ? p.ws_m[row0 + i_ml] : -INFINITY;
+            l_i[u] = i_ml < np ? p.ws_l[row0 + i_ml] : 0.f;
+        }
         float4 o[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
@@ -163,14 +168,23 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergePara
             o[k] = i < np ? *reinterpret_cast<const float4*>(src + (size_t)i * D)
                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const float Mc = block_reduce(m_i, s_red, true);
+        float mloc = m_i[0];
+#pragma unroll
+        for (int u = 1; u < kMlPer; ++u) mloc = fmaxf(mloc, m_i[u]);
+        const float Mc = block_reduce(mloc, s_red, true);
         const float Mn = fmaxf(M, Mc);
         const float rescale = (M == -INFINITY) ? 0.f : ex2(M - Mn);
-        // l == 0 marks a partition with nothing attended; a NaN (a partition
-        // that met a bad page) is kept so that it reaches the output.
-        const float w = (l_i == 0.f) ? 0.f : ex2(m_i - Mn) * l_i;
-        s_w[threadIdx.x] = w;
-        const float wsum = block_reduce(w, s_red, false);  // also orders the s_w writes
+        float wloc = 0.f;
+#pragma unroll
+        for (int u = 0; u < kMlPer; ++u) {
+            // l == 0 marks a partition with nothing attended; a NaN (a
+            // partition that met a bad page) is kept so that it reaches the
+            // output.
+            const float w = (l_i[u] == 0.f) ? 0.f : ex2(m_i[u] - Mn) * l_i[u];
+            s_w[threadIdx.x + u * kMergeThreads] = w;
+            wloc += w;
+        }
+        const float wsum = block_reduce(wloc, s_red, false);  // also orders the s_w writes
         lam = lam * rescale + wsum;
         acc.x *= rescale;
         acc.y *= rescale;
@@ -347,6 +361,19 @@ int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page
     plan->ctas = P * num_kv_heads * nchunk * batch;
     plan->workspace_bytes = ws_layout(batch, num_q_heads, head_dim, P).total;
     plan->kernel = PA_KERNEL_MMA;
+    // Partitions per CTA (tensor-core kernel): when the one-partition grid
+    // runs many waves of resident CTAs (more than four), let each CTA stream
+    // two consecutive partitions.  That halves the CTA prologues and
+    // epilogues while the grid keeps enough waves that the last, partial one
+    // stays short; longer CTAs (more partitions each) measured slower.
+    {
+        const long long groups = (long long)batch * num_kv_heads * nchunk;
+        const long long slots = (long long)num_sms * attend_ctas_per_sm(head_dim);
+        const bool many_waves = slots > 0 && groups * P > 4 * slots;
+        plan->parts_per_cta = (many_waves && P >= 2 && 2 * pp <= kMaxPagesPerPart) ? 2 : 1;
+    }
+    plan->ctas = (int)(((P + plan->parts_per_cta - 1) / plan->parts_per_cta) * num_kv_heads *
+                       nchunk * (long long)batch);
     return PA_OK;
 }
 
@@ -367,6 +394,9 @@ static int check_plan(const pa_plan_t* plan) {
     if (plan->workspace_bytes < ws_layout(B, Hq, plan->head_dim, plan->num_partitions).total)
         return PA_ERR_INVALID_ARG;
     if (plan->kernel != PA_KERNEL_SIMT && plan->kernel != PA_KERNEL_MMA) return PA_ERR_INVALID_ARG;
+    if (plan->parts_per_cta < 1 ||
+        (long long)plan->parts_per_cta * (plan->partition_size / kPageSize) > kMaxPagesPerPart)
+        return PA_ERR_INVALID_ARG;
     // TMA row coordinates are signed 32-bit.
     if (plan->kernel == PA_KERNEL_MMA &&
         (long long)plan->num_pages * Hkv * kPageSize > 0x7fffffffLL)
@@ -420,15 +450,18 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     p.nchunk = p.g / plan->heads_per_cta;
     p.heads_per_cta = plan->heads_per_cta;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    const dim3 grid(P, p.Hkv * p.nchunk, p.B);
     cudaError_t e;
     if (plan->kernel == PA_KERNEL_MMA) {
         alignas(64) CUtensorMap tmK, tmV;
         const long long rows = (long long)plan->num_pages * p.Hkv * kPageSize;
         if (!make_page_map(&tmK, k_cache, rows, D) || !make_page_map(&tmV, v_cache, rows, D))
             return PA_ERR_CUDA;
+        p.parts_per_cta = plan->parts_per_cta;
+        const dim3 grid((P + p.parts_per_cta - 1) / p.parts_per_cta, p.Hkv * p.nchunk, p.B);
         e = launch_attend_mma(D, P > 1, p, tmK, tmV, grid, static_cast<cudaStream_t>(stream));
     } else {
+        p.parts_per_cta = 1;
+        const dim3 grid(P, p.Hkv * p.nchunk, p.B);
         e = launch_attend(D, plan->heads_per_cta, P > 1, p, grid,
                           static_cast<cudaStream_t>(stream));
     }

@@ -25,6 +25,12 @@
 //    ldmatrix.trans of the same swizzled page, P^T from S^T by movmatrix.trans.
 //    The accumulator of a lane holds two heads, so the online rescale needs
 //    no data exchange.
+//  * Several partitions per CTA.  A CTA may stream parts_per_cta consecutive
+//    partitions of its (sequence, KV head); the warps' page pipelines run on
+//    across partition edges, and at each edge the four warp states are
+//    combined through a small shared buffer (64 output dims per round) into
+//    that partition's partial.  Fewer, longer CTAs spend less time in
+//    prologues and epilogues; the partials stay one per partition.
 #pragma once
 
 #include <cuda.h>
@@ -43,7 +49,9 @@ struct MmaCfg {
     static constexpr int kPageBytes = kPageSize * D * 2;
     static constexpr int kStages = D == 256 ? 3 : (D == 128 ? 4 : 6);
     static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
-    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes +
+    static constexpr int kXDims = 64;  // output dims combined per round at a partition edge
+    static constexpr int kXBytes = kWarps * kMaxHeadsPerCta * kXDims * 4;
+    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes + kXBytes +
                                       kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 3 * 4 +
                                       kWarps * kStages * 8 + 16;
     static constexpr int kMinBlocks = D == 256 ? 2 : 3;
@@ -113,14 +121,17 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     constexpr int NS = Cfg::kStages;
     constexpr int PB = Cfg::kPageBytes;
     constexpr int KT = D / 16;  // k-steps of q.K, m-tiles of P.V
+    constexpr int XD = Cfg::kXDims;
+    constexpr int ROUNDS = D / XD;
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;  // 128-byte swizzle needs 1 KiB alignment
     unsigned char* base = smem_raw + (base_u32 - raw_u32);
     unsigned char* ring = base;
-    int* s_pid = reinterpret_cast<int*>(base + Cfg::kRingBytes);
-    float* s_ml = reinterpret_cast<float*>(s_pid + kMaxPagesPerPart);
+    float* xbuf = reinterpret_cast<float*>(base + Cfg::kRingBytes);  // [warps][G][XD]
+    int* s_pid = reinterpret_cast<int*>(base + Cfg::kRingBytes + Cfg::kXBytes);
+    float* s_ml = reinterpret_cast<float*>(s_pid + kMaxPagesPerPart);  // [warps][m|l|n][8]
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 3);
     __shared__ int s_flag;
 
@@ -128,13 +139,15 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     const int G = p.heads_per_cta;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int part = blockIdx.x;
+    const int ppc = p.parts_per_cta;
+    const int part0 = blockIdx.x * ppc;
     const int kvh = blockIdx.y / p.nchunk;
     const int h0 = kvh * p.g + (blockIdx.y % p.nchunk) * G;
     const int b = blockIdx.z;
+    const int pp = p.pages_per_part;
 
-    const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, p.pages_per_part);
-    auto fill_rows = [&](float o_val, float m_val, float l_val, float lse_val) {
+    const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, pp);
+    auto fill_rows = [&](int part, float o_val, float m_val, float l_val, float lse_val) {
         for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
             const int h = idx / D, d = idx % D;
             const size_t bh = (size_t)b * p.Hq + h0 + h;
@@ -152,16 +165,19 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         }
     };
     if (!sp.valid) {
-        if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0) atomicOr(p.err, PA_DEVERR_BAD_LENGTH);
-        if constexpr (!SPLIT) fill_rows(NAN, NAN, NAN, NAN);
+        if (threadIdx.x == 0 && part0 == 0 && blockIdx.y == 0) atomicOr(p.err, PA_DEVERR_BAD_LENGTH);
+        if constexpr (!SPLIT) fill_rows(0, NAN, NAN, NAN, NAN);
+        return;  // with a split, the merge writes the NaN rows
+    }
+    if (part0 >= sp.num_parts) {
+        // Nothing attended here.  Without a split this only happens for an
+        // empty context: out = 0, lse = -inf.
+        if constexpr (!SPLIT) fill_rows(0, 0.f, 0.f, 0.f, -INFINITY);
         return;
     }
-    if (part >= sp.num_parts) {
-        if constexpr (!SPLIT) fill_rows(0.f, 0.f, 0.f, -INFINITY);
-        return;
-    }
-    const int pg0 = sp.first_page + part * p.pages_per_part;
-    const int npg = min(p.pages_per_part, sp.end_page - pg0);
+    const int nparts = min(ppc, sp.num_parts - part0);
+    const int pgA = sp.first_page + part0 * pp;           // first page of this CTA
+    const int n_range = min(nparts * pp, sp.end_page - pgA);  // pages of this CTA
 
     if (threadIdx.x == 0) {
         s_flag = 0;
@@ -175,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         fence_mbar_init();
     }
     __syncthreads();
-    for (int j = threadIdx.x; j < npg; j += kThreads) {
-        int id = p.block_tables[(size_t)b * p.maxp + pg0 + j];
+    for (int j = threadIdx.x; j < n_range; j += kThreads) {
+        int id = p.block_tables[(size_t)b * p.maxp + pgA + j];
         if (id < 0 || id >= p.num_pages) {
             s_flag = 1;
             id = 0;
@@ -186,11 +202,13 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     __syncthreads();
     if (s_flag) {
         if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
-        fill_rows(NAN, NAN, NAN, NAN);
+        for (int q = 0; q < nparts; ++q) fill_rows(part0 + q, NAN, NAN, NAN, NAN);
         return;
     }
 
-    const int nk = npg > warp ? (npg - warp + kWarps - 1) / kWarps : 0;
+    // ---- this warp's pages over the whole range: j = warp, warp + 4, ...;
+    // items K0, V0, K1, V1, ...
+    const int nk = n_range > warp ? (n_range - warp + kWarps - 1) / kWarps : 0;
     const int n_items = 2 * nk;
     const uint32_t ring_w = smem_u32(ring) + warp * NS * PB;
 
@@ -223,13 +241,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         }
     }
 
-    float o[KT][4];
-#pragma unroll
-    for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY};
-    float l_run[2] = {0.f, 0.f};   // exp-sum of the fp32 weights
-    float n_run[2] = {0.f, 0.f};   // exp-sum of the fp16-rounded weights
     const int tok0 = lane >> 2;  // this lane's tokens of a page: tok0 and tok0 + 8
+    const int hA = (lane & 3) * 2;  // and its heads hA, hA + 1
     // ldmatrix row/chunk roles of this lane
     const int ld_j = lane >> 3;
     const int ld_i = lane & 7;
@@ -239,212 +252,235 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     const int v_chk = ld_j & 1;
     bool ok = true;
     int consumed = 0;
+    int k = 0;  // this warp's next page (index into its stream)
 
-    for (int k = 0; k < nk; ++k) {
-        const int page_pos = (pg0 + warp + k * kWarps) * kPageSize;
-        // ---------------- K page: S^T = K . Q^T
-        {
-            const int item = 2 * k;
-            const bool got = mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
-            if (!__all_sync(0xffffffffu, got)) {
-                ok = false;
-                break;
-            }
-            consumed = item + 1;
-        }
-        const uint32_t kaddr = ring_w + ((2 * k) % NS) * PB;
-        float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int qp = 0; qp < nparts; ++qp) {
+        const int qend = min((qp + 1) * pp, n_range);  // end of partition qp, relative page
+        float o[KT][4];
 #pragma unroll
-        for (int kk = 0; kk < KT; ++kk) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(kaddr + swz(k_row, kk * 2 + k_chk), a0, a1, a2, a3);
-            if (kk & 1)
-                mma_16816(cb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
-            else
-                mma_16816(ca, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
-        }
-        __syncwarp();
-        if (lane == 0 && 2 * k + NS < n_items) {
-            fence_proxy_async_smem();
-            issue(2 * k + NS);
-        }
-        if (2 * k + NS < n_items) issued = 2 * k + NS + 1;
+        for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        float m_run[2] = {-INFINITY, -INFINITY};
+        float l_run[2] = {0.f, 0.f};   // exp-sum of the fp32 weights
+        float n_run[2] = {0.f, 0.f};   // exp-sum of the fp16-rounded weights
 
-        // ---------------- online softmax (log2 domain); lane: tokens tok0, tok0+8; heads hA, hA+1
-        const bool v0 = page_pos + tok0 >= sp.start && page_pos + tok0 < sp.L;
-        const bool v1 = page_pos + tok0 + 8 >= sp.start && page_pos + tok0 + 8 < sp.L;
-        float s00 = v0 ? (ca[0] + cb[0]) * p.scale_log2 : -INFINITY;  // token0, head A
-        float s01 = v0 ? (ca[1] + cb[1]) * p.scale_log2 : -INFINITY;  // token0, head B
-        float s10 = v1 ? (ca[2] + cb[2]) * p.scale_log2 : -INFINITY;  // token1, head A
-        float s11 = v1 ? (ca[3] + cb[3]) * p.scale_log2 : -INFINITY;  // token1, head B
-        float mA = fmaxf(s00, s10), mB = fmaxf(s01, s11);
-#pragma unroll
-        for (int mask = 4; mask < 32; mask <<= 1) {
-            mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, mask));
-            mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, mask));
-        }
-        if (__any_sync(0xffffffffu, mA > m_run[0] || mB > m_run[1])) {
-            const float nA = fmaxf(m_run[0], mA), nB = fmaxf(m_run[1], mB);
-            const float aA = (nA == -INFINITY) ? 1.f : ex2(m_run[0] - nA);
-            const float aB = (nB == -INFINITY) ? 1.f : ex2(m_run[1] - nB);
-            m_run[0] = nA;
-            m_run[1] = nB;
-            l_run[0] *= aA;
-            l_run[1] *= aB;
-            n_run[0] *= aA;
-            n_run[1] *= aB;
-#pragma unroll
-            for (int mt = 0; mt < KT; ++mt) {
-                o[mt][0] *= aA;
-                o[mt][2] *= aA;
-                o[mt][1] *= aB;
-                o[mt][3] *= aB;
+        for (; ok && k < nk && warp + k * kWarps < qend; ++k) {
+            const int page_pos = (pgA + warp + k * kWarps) * kPageSize;
+            // ---------------- K page: S^T = K . Q^T
+            {
+                const int item = 2 * k;
+                const bool got = mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                consumed = item + 1;
             }
-        }
-        const float p00 = (s00 == -INFINITY) ? 0.f : ex2(s00 - m_run[0]);
-        const float p01 = (s01 == -INFINITY) ? 0.f : ex2(s01 - m_run[1]);
-        const float p10 = (s10 == -INFINITY) ? 0.f : ex2(s10 - m_run[0]);
-        const float p11 = (s11 == -INFINITY) ? 0.f : ex2(s11 - m_run[1]);
-        float r00, r01, r10, r11;
-        const uint32_t top = pack_half2(p00, p01, r00, r01);  // P[tok0][hA, hB]
-        const uint32_t bot = pack_half2(p10, p11, r10, r11);  // P[tok0 + 8][hA, hB]
-        l_run[0] += p00 + p10;
-        l_run[1] += p01 + p11;
-        n_run[0] += r00 + r10;
-        n_run[1] += r01 + r11;
-        // P^T fragments: lane gets P[tokens (lane%4)*2 + {0,1} (+8)][head lane/4]
-        const uint32_t pb0 = movmatrix_trans(top);
-        const uint32_t pb1 = movmatrix_trans(bot);
-
-        // ---------------- V page: O^T += V^T . P^T
-        {
-            const int item = 2 * k + 1;
-            const bool got = mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
-            if (!__all_sync(0xffffffffu, got)) {
-                ok = false;
-                break;
-            }
-            consumed = item + 1;
-        }
-        const uint32_t vaddr = ring_w + ((2 * k + 1) % NS) * PB;
-        if (page_pos < sp.start || page_pos + kPageSize > sp.L) {
-            // Boundary page: zero the V rows of tokens outside [start, L) so
-            // that whatever those slots hold (never-written cache slots may
-            // hold NaN) cannot reach the output through a zero weight.
-            unsigned char* vgen = ring + warp * NS * PB + ((2 * k + 1) % NS) * PB;
-            for (int idx = lane; idx < kPageSize * (D / 8); idx += 32) {
-                const int row = idx / (D / 8);
-                const int pos = page_pos + row;
-                if (pos < sp.start || pos >= sp.L)
-                    *reinterpret_cast<uint4*>(vgen + swz(row, idx % (D / 8))) = make_uint4(0, 0, 0, 0);
+            const uint32_t kaddr = ring_w + ((2 * k) % NS) * PB;
+            float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kaddr + swz(k_row, kk * 2 + k_chk), a0, a1, a2, a3);
+                if (kk & 1)
+                    mma_16816(cb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+                else
+                    mma_16816(ca, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
             }
             __syncwarp();
-        }
+            if (lane == 0 && 2 * k + NS < n_items) {
+                fence_proxy_async_smem();
+                issue(2 * k + NS);
+            }
+            if (2 * k + NS < n_items) issued = 2 * k + NS + 1;
+
+            // ---------------- online softmax (log2 domain); lane: tokens tok0, tok0+8; heads hA, hA+1
+            const bool v0 = page_pos + tok0 >= sp.start && page_pos + tok0 < sp.L;
+            const bool v1 = page_pos + tok0 + 8 >= sp.start && page_pos + tok0 + 8 < sp.L;
+            float s00 = v0 ? (ca[0] + cb[0]) * p.scale_log2 : -INFINITY;  // token0, head A
+            float s01 = v0 ? (ca[1] + cb[1]) * p.scale_log2 : -INFINITY;  // token0, head B
+            float s10 = v1 ? (ca[2] + cb[2]) * p.scale_log2 : -INFINITY;  // token1, head A
+            float s11 = v1 ? (ca[3] + cb[3]) * p.scale_log2 : -INFINITY;  // token1, head B
+            float mA = fmaxf(s00, s10), mB = fmaxf(s01, s11);
 #pragma unroll
-        for (int mt = 0; mt < KT; ++mt) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(vaddr + swz(v_row, mt * 2 + v_chk), a0, a1, a2, a3);
-            mma_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+            for (int mask = 4; mask < 32; mask <<= 1) {
+                mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, mask));
+                mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, mask));
+            }
+            if (__any_sync(0xffffffffu, mA > m_run[0] || mB > m_run[1])) {
+                const float nA = fmaxf(m_run[0], mA), nB = fmaxf(m_run[1], mB);
+                const float aA = (nA == -INFINITY) ? 1.f : ex2(m_run[0] - nA);
+                const float aB = (nB == -INFINITY) ? 1.f : ex2(m_run[1] - nB);
+                m_run[0] = nA;
+                m_run[1] = nB;
+                l_run[0] *= aA;
+                l_run[1] *= aB;
+                n_run[0] *= aA;
+                n_run[1] *= aB;
+#pragma unroll
+                for (int mt = 0; mt < KT; ++mt) {
+                    o[mt][0] *= aA;
+                    o[mt][2] *= aA;
+                    o[mt][1] *= aB;
+                    o[mt][3] *= aB;
+                }
+            }
+            const float p00 = (s00 == -INFINITY) ? 0.f : ex2(s00 - m_run[0]);
+            const float p01 = (s01 == -INFINITY) ? 0.f : ex2(s01 - m_run[1]);
+            const float p10 = (s10 == -INFINITY) ? 0.f : ex2(s10 - m_run[0]);
+            const float p11 = (s11 == -INFINITY) ? 0.f : ex2(s11 - m_run[1]);
+            float r00, r01, r10, r11;
+            const uint32_t top = pack_half2(p00, p01, r00, r01);  // P[tok0][hA, hB]
+            const uint32_t bot = pack_half2(p10, p11, r10, r11);  // P[tok0 + 8][hA, hB]
+            l_run[0] += p00 + p10;
+            l_run[1] += p01 + p11;
+            n_run[0] += r00 + r10;
+            n_run[1] += r01 + r11;
+            // P^T fragments: lane gets P[tokens (lane%4)*2 + {0,1} (+8)][head lane/4]
+            const uint32_t pb0 = movmatrix_trans(top);
+            const uint32_t pb1 = movmatrix_trans(bot);
+
+            // ---------------- V page: O^T += V^T . P^T
+            {
+                const int item = 2 * k + 1;
+                const bool got = mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                consumed = item + 1;
+            }
+            const uint32_t vaddr = ring_w + ((2 * k + 1) % NS) * PB;
+            if (page_pos < sp.start || page_pos + kPageSize > sp.L) {
+                // Boundary page: zero the V rows of tokens outside [start, L) so
+                // that whatever those slots hold (never-written cache slots may
+                // hold NaN) cannot reach the output through a zero weight.
+                unsigned char* vgen = ring + warp * NS * PB + ((2 * k + 1) % NS) * PB;
+                for (int idx = lane; idx < kPageSize * (D / 8); idx += 32) {
+                    const int row = idx / (D / 8);
+                    const int pos = page_pos + row;
+                    if (pos < sp.start || pos >= sp.L)
+                        *reinterpret_cast<uint4*>(vgen + swz(row, idx % (D / 8))) =
+                            make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(vaddr + swz(v_row, mt * 2 + v_chk), a0, a1, a2, a3);
+                mma_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+            }
+            __syncwarp();
+            if (lane == 0 && 2 * k + 1 + NS < n_items) {
+                fence_proxy_async_smem();
+                issue(2 * k + 1 + NS);
+            }
+            if (2 * k + 1 + NS < n_items) issued = 2 * k + 1 + NS + 1;
         }
-        __syncwarp();
-        if (lane == 0 && 2 * k + 1 + NS < n_items) {
-            fence_proxy_async_smem();
-            issue(2 * k + 1 + NS);
+        if (!ok && lane == 0) {
+            atomicOr(p.err, PA_DEVERR_TIMEOUT);
+            s_flag = 1;
         }
-        if (2 * k + 1 + NS < n_items) issued = 2 * k + 1 + NS + 1;
+
+        // ---- partition qp: combine the four warp states.  Exp-sums: lanes
+        // with equal lane%4 hold the same heads over different tokens.
+#pragma unroll
+        for (int mask = 4; mask < 32; mask <<= 1) {
+            l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], mask);
+            l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], mask);
+            n_run[0] += __shfl_xor_sync(0xffffffffu, n_run[0], mask);
+            n_run[1] += __shfl_xor_sync(0xffffffffu, n_run[1], mask);
+        }
+        if (lane < 4) {
+            float* ml = s_ml + warp * 3 * kMaxHeadsPerCta;
+            if (hA < G) {
+                ml[hA] = m_run[0];
+                ml[kMaxHeadsPerCta + hA] = l_run[0];
+                ml[2 * kMaxHeadsPerCta + hA] = n_run[0];
+            }
+            if (hA + 1 < G) {
+                ml[hA + 1] = m_run[1];
+                ml[kMaxHeadsPerCta + hA + 1] = l_run[1];
+                ml[2 * kMaxHeadsPerCta + hA + 1] = n_run[1];
+            }
+        }
+        const int part = part0 + qp;
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) {
+#pragma unroll
+            for (int mi = 0; mi < XD / 16; ++mi) {
+                const int mt = r * (XD / 16) + mi;
+                const int d = mi * 16 + (lane >> 2);
+                if (hA < G) {
+                    xbuf[(warp * G + hA) * XD + d] = o[mt][0];
+                    xbuf[(warp * G + hA) * XD + d + 8] = o[mt][2];
+                }
+                if (hA + 1 < G) {
+                    xbuf[(warp * G + hA + 1) * XD + d] = o[mt][1];
+                    xbuf[(warp * G + hA + 1) * XD + d + 8] = o[mt][3];
+                }
+            }
+            __syncthreads();
+            const bool failed = s_flag != 0;
+            for (int idx = threadIdx.x; idx < G * (XD / 4); idx += kThreads) {
+                const int h = idx / (XD / 4);
+                const int dl = (idx % (XD / 4)) * 4;
+                const int d = r * XD + dl;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w * 3 * kMaxHeadsPerCta + h]);
+                float Ls = 0.f, Ns = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    const float* ml = s_ml + w * 3 * kMaxHeadsPerCta;
+                    const float mw = ml[h];
+                    const float c = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+                    Ls += c * ml[kMaxHeadsPerCta + h];
+                    Ns += c * ml[2 * kMaxHeadsPerCta + h];
+                    const float4 ow = *reinterpret_cast<const float4*>(xbuf + (w * G + h) * XD + dl);
+                    acc.x += c * ow.x;
+                    acc.y += c * ow.y;
+                    acc.z += c * ow.z;
+                    acc.w += c * ow.w;
+                }
+                float inv = Ns > 0.f ? 1.f / Ns : 0.f;
+                if (failed) {
+                    inv = NAN;
+                    M = NAN;
+                    Ls = NAN;
+                }
+                const size_t bh = (size_t)b * p.Hq + h0 + h;
+                if constexpr (SPLIT) {
+                    const size_t row = bh * p.P + part;
+                    *reinterpret_cast<float4*>(p.ws_o + row * D + d) =
+                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                    if (d == 0) {
+                        p.ws_m[row] = M;
+                        p.ws_l[row] = Ls;
+                    }
+                } else {
+                    __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
+                    __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
+                    uint2 packed;
+                    packed.x = *reinterpret_cast<uint32_t*>(&lo);
+                    packed.y = *reinterpret_cast<uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(p.out + bh * D + d) = packed;
+                    if (d == 0)
+                        p.lse[bh] = failed ? NAN
+                                           : (Ls > 0.f ? M * 0.69314718055994531f + logf(Ls)
+                                                       : -INFINITY);
+                }
+            }
+            __syncthreads();  // xbuf and s_ml are rewritten next
+        }
     }
 
     if (!ok) {
-        if (lane == 0) atomicOr(p.err, PA_DEVERR_TIMEOUT);
+        // Give every copy this warp issued a bounded chance to land, so that
+        // none writes into shared memory after the CTA exits.
         for (int item = consumed; item < issued; ++item)
             (void)mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
-        s_flag = 1;
-    }
-
-    // ---- warp state -> shared memory.  Exp-sums: lanes with equal lane%4
-    // hold the same heads over different tokens.
-#pragma unroll
-    for (int mask = 4; mask < 32; mask <<= 1) {
-        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], mask);
-        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], mask);
-        n_run[0] += __shfl_xor_sync(0xffffffffu, n_run[0], mask);
-        n_run[1] += __shfl_xor_sync(0xffffffffu, n_run[1], mask);
-    }
-    __syncthreads();  // rings idle: reuse them for the warp states
-    float* s_o = reinterpret_cast<float*>(ring);  // [warps][G][D]
-    const int hA = (lane & 3) * 2;
-#pragma unroll
-    for (int mt = 0; mt < KT; ++mt) {
-        const int d = mt * 16 + (lane >> 2);
-        if (hA < G) {
-            s_o[(warp * G + hA) * D + d] = o[mt][0];
-            s_o[(warp * G + hA) * D + d + 8] = o[mt][2];
-        }
-        if (hA + 1 < G) {
-            s_o[(warp * G + hA + 1) * D + d] = o[mt][1];
-            s_o[(warp * G + hA + 1) * D + d + 8] = o[mt][3];
-        }
-    }
-    if (lane < 4) {  // s_ml: [warps][m | l | n][8]
-        float* ml = s_ml + warp * 3 * kMaxHeadsPerCta;
-        if (hA < G) {
-            ml[hA] = m_run[0];
-            ml[kMaxHeadsPerCta + hA] = l_run[0];
-            ml[2 * kMaxHeadsPerCta + hA] = n_run[0];
-        }
-        if (hA + 1 < G) {
-            ml[hA + 1] = m_run[1];
-            ml[kMaxHeadsPerCta + hA + 1] = l_run[1];
-            ml[2 * kMaxHeadsPerCta + hA + 1] = n_run[1];
-        }
-    }
-    __syncthreads();
-    if (s_flag) {
-        fill_rows(NAN, NAN, NAN, NAN);
-        return;
-    }
-
-    constexpr int D4 = D / 4;
-    for (int idx = threadIdx.x; idx < G * D4; idx += kThreads) {
-        const int h = idx / D4;
-        const int d = (idx % D4) * 4;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w * 3 * kMaxHeadsPerCta + h]);
-        float Ls = 0.f, Ns = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float* ml = s_ml + w * 3 * kMaxHeadsPerCta;
-            const float mw = ml[h];
-            const float c = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-            Ls += c * ml[kMaxHeadsPerCta + h];
-            Ns += c * ml[2 * kMaxHeadsPerCta + h];
-            const float4 ow = *reinterpret_cast<const float4*>(s_o + (w * G + h) * D + d);
-            acc.x += c * ow.x;
-            acc.y += c * ow.y;
-            acc.z += c * ow.z;
-            acc.w += c * ow.w;
-        }
-        const float inv = Ns > 0.f ? 1.f / Ns : 0.f;
-        const size_t bh = (size_t)b * p.Hq + h0 + h;
-        if constexpr (SPLIT) {
-            const size_t row = bh * p.P + part;
-            *reinterpret_cast<float4*>(p.ws_o + row * D + d) =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-            if (d == 0) {
-                p.ws_m[row] = M;
-                p.ws_l[row] = Ls;
-            }
-        } else {
-            __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
-            __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
-            uint2 packed;
-            packed.x = *reinterpret_cast<uint32_t*>(&lo);
-            packed.y = *reinterpret_cast<uint32_t*>(&hi);
-            *reinterpret_cast<uint2*>(p.out + bh * D + d) = packed;
-            if (d == 0) p.lse[bh] = Ls > 0.f ? M * 0.69314718055994531f + logf(Ls) : -INFINITY;
-        }
     }
 }
 

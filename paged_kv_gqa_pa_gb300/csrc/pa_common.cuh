@@ -40,6 +40,7 @@ struct AttendParams {
     int pages_per_part;     // partition size in pages
     int nchunk;             // head chunks per KV head (grid.y = Hkv * nchunk)
     int heads_per_cta;      // G: query heads one CTA serves
+    int parts_per_cta;      // consecutive partitions one CTA streams (tensor-core kernel)
     float scale_log2;       // scale * log2(e)
 };
 

@@ -41,7 +41,7 @@ def to_device(case, device="cuda"):
 
 
 def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=None,
-            guard=0):
+            guard=0, parts_per_cta=None):
     """Plan + pa_decode through the C ABI.  Returns (out fp64 numpy, lse fp64
     numpy, device error word, plan).  With guard > 0 the outputs and the
     workspace sit inside larger NaN/0xA5-filled buffers whose guard regions are
@@ -59,6 +59,8 @@ def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=N
                       max_context_len, case.window, partition_size, num_sms)
     if KERNEL is not None:
         plan.kernel = KERNELS[KERNEL]
+    if parts_per_cta is not None:
+        plan.parts_per_cta = parts_per_cta
     n_out = B * Hq * D
     out_buf = torch.full((n_out + 2 * guard,), float("nan"), dtype=torch.float16, device="cuda")
     lse_buf = torch.full((B * Hq + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")

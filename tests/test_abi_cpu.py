@@ -53,9 +53,10 @@ def test_plan_struct_layout_matches_header():
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     fields = re.findall(r"\b(?:int|size_t)\s+([a-z_]+)(?:\[\d+\])?\s*;", body)
     assert fields == [f for f, _ in binding.pa_plan_t._fields_]
-    # 14 ints, a size_t, the kernel id, 7 reserved ints.
+    # 14 ints, a size_t, the kernel id, partitions per CTA, 6 reserved ints.
     assert binding.pa_plan_t.workspace_bytes.offset == 56
     assert binding.pa_plan_t.kernel.offset == 64
+    assert binding.pa_plan_t.parts_per_cta.offset == 68
     assert ctypes.sizeof(binding.pa_plan_t) == 96
 
 
@@ -80,7 +81,9 @@ def test_plan_matches_the_pages_partition_counts():
 def test_plan_long_context_workload():
     plan = pa.pa_plan(4, 24, 4, 256, 16, 31250, 6250, 100000, 0, 512, 152)
     assert plan.num_partitions == 196 and plan.heads_per_cta == 6
-    assert plan.ctas == 196 * 4 * 4
+    # 3136 one-partition CTAs would be ~10 waves of 304 resident CTAs; each
+    # CTA streams 2 consecutive partitions instead (98 per group, 1568 CTAs).
+    assert plan.parts_per_cta == 2 and plan.ctas == 98 * 4 * 4
     rows = 4 * 24 * 196
     assert plan.workspace_bytes >= 256 + rows * 4 * 2 + rows * 256 * 4
 

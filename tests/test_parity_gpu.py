@@ -217,3 +217,22 @@ def test_unwritten_slots_never_leak():
         out, lse, err, _ = run_gpu(case)
         assert err == 0
         assert_matches_oracle(case, out, lse, what=f"tail S{S}")
+
+
+@pytest.mark.parametrize("ppc", [1, 2, 3, 8])
+def test_several_partitions_per_cta(ppc):
+    """A CTA streaming several consecutive partitions writes the same partials
+    as one CTA per partition (the CUDA-core kernel ignores the setting)."""
+    case = workloads.make_case("ppc", 3, 12, 2, 256, [20000, 7777, 1], seed=509, window=0)
+    ref = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                        case.context_lens, case.scale)
+    for S in (64, 512):
+        case.partition_size = S
+        out, lse, err, plan = run_gpu(case, guard=64, parts_per_cta=ppc)
+        assert err == 0
+        assert_matches_oracle(case, out, lse, ref=ref, what=f"ppc{ppc} S{S}")
+    wcase = workloads.make_case("ppcw", 2, 8, 4, 128, [9000, 3001], seed=510, window=2500)
+    wcase.partition_size = 128
+    out, lse, err, _ = run_gpu(wcase, parts_per_cta=ppc)
+    assert err == 0
+    assert_matches_oracle(wcase, out, lse, what=f"ppc{ppc} window")
