@@ -89,7 +89,14 @@ typedef struct pa_plan {
     int parts_per_cta;      /* consecutive partitions one CTA of the tensor-core kernel
                                streams (one partial per partition all the same); the
                                CUDA-core kernel always serves one */
-    int reserved[6];
+    int merge_in_kernel;    /* 1: with the tensor-core kernel, the last CTA of each
+                               (sequence, KV head) merges that group's partials and
+                               pa_merge has nothing to do; 0: pa_merge launches the
+                               merge kernel */
+    int ctrl_bytes;         /* leading workspace bytes that must be zero before the
+                               first call (error word, per-group arrival counters); the
+                               library leaves them zero after every call */
+    int reserved[4];
 } pa_plan_t;
 
 /* Partition-kernel variants (pa_plan_t.kernel). */
@@ -117,10 +124,11 @@ int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page
  * Full decode step: the partition kernel (gather pages, q.K, per-partition
  * softmax statistics, P.V) and, when plan->num_partitions > 1, the
  * log-sum-exp merge.  `window` must equal plan->window.
- * workspace: >= plan->workspace_bytes of device memory, zero-filled once when
- * allocated (its first word is the device error word); it holds the
- * partition partials between the two kernels, so concurrent calls must not
- * share one workspace.
+ * workspace: >= plan->workspace_bytes of device memory whose first
+ * plan->ctrl_bytes are zero before the first call (zero-fill it once when
+ * allocated; every call leaves those bytes zero again).  They hold the device
+ * error word and per-group arrival counters; the rest holds the partition
+ * partials between the kernels.  Concurrent calls must not share a workspace.
  */
 int pa_decode(const pa_plan_t* plan, const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, const int32_t* context_lens, float scale, int window,

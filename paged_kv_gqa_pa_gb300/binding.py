@@ -49,7 +49,9 @@ class pa_plan_t(ctypes.Structure):
         ("workspace_bytes", ctypes.c_size_t),
         ("kernel", ctypes.c_int),
         ("parts_per_cta", ctypes.c_int),
-        ("reserved", ctypes.c_int * 6),
+        ("merge_in_kernel", ctypes.c_int),
+        ("ctrl_bytes", ctypes.c_int),
+        ("reserved", ctypes.c_int * 4),
     ]
 
     def as_dict(self):

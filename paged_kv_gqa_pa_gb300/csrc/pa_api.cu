@@ -228,24 +228,28 @@ cudaError_t launch_merge(int D, const MergeParams& p, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, merge_kernel, p);
 }
 
-// Workspace layout: [control block | m (B*Hq*P) | l (B*Hq*P) | o (B*Hq*P*D)],
-// each region 256-byte aligned.  The control block's first word is the device
-// error word.
+// Workspace layout: [control block | arrival counters (one per group) |
+// m (B*Hq*P) | l (B*Hq*P) | o (B*Hq*P*D)], each region 256-byte aligned.  The
+// control block's first word is the device error word; it and the counters
+// (ctrl_bytes in all) must start at zero and are left at zero by every call.
 struct WsLayout {
-    size_t m_off, l_off, o_off, total;
+    size_t ctr_off, ctrl_bytes, m_off, l_off, o_off, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-static WsLayout ws_layout(int B, int Hq, int D, int P) {
+// groups = B * Hkv * head chunks (one arrival counter each).
+static WsLayout ws_layout(int B, int Hq, int D, int P, long long groups) {
     WsLayout w;
+    w.ctr_off = kCtrlBytes;
     if (P <= 1) {
-        w.m_off = w.l_off = w.o_off = kCtrlBytes;
+        w.ctrl_bytes = w.m_off = w.l_off = w.o_off = kCtrlBytes;
         w.total = kCtrlBytes;
         return w;
     }
     const size_t rows = (size_t)B * Hq * P;
-    w.m_off = kCtrlBytes;
+    w.ctrl_bytes = kCtrlBytes + align256((size_t)groups * 4);
+    w.m_off = w.ctrl_bytes;
     w.l_off = w.m_off + align256(rows * 4);
     w.o_off = w.l_off + align256(rows * 4);
     w.total = w.o_off + align256(rows * D * 4);
@@ -359,8 +363,15 @@ int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page
     plan->heads_per_cta = G;
     plan->num_sms = num_sms;
     plan->ctas = P * num_kv_heads * nchunk * batch;
-    plan->workspace_bytes = ws_layout(batch, num_q_heads, head_dim, P).total;
+    const long long groups_all = (long long)batch * num_kv_heads * nchunk;
+    const WsLayout wl = ws_layout(batch, num_q_heads, head_dim, P, groups_all);
+    plan->workspace_bytes = wl.total;
+    plan->ctrl_bytes = (int)wl.ctrl_bytes;
     plan->kernel = PA_KERNEL_MMA;
+    // Merge inside the partition kernel when a group's partials are small
+    // (its last CTA merges them, no second launch); the merge kernel when they
+    // are many (the one-CTA merge would then trail the grid).
+    plan->merge_in_kernel = (P > 1 && kFusedMergeFits(G, head_dim, P)) ? 1 : 0;
     // Partitions per CTA (tensor-core kernel): when the one-partition grid
     // runs many waves of resident CTAs (more than four), let each CTA stream
     // two consecutive partitions.  That halves the CTA prologues and
@@ -391,7 +402,11 @@ static int check_plan(const pa_plan_t* plan) {
     const int g = Hq / Hkv;
     const int G = plan->heads_per_cta;
     if (G < 1 || G > kMaxHeadsPerCta || g % G != 0) return PA_ERR_INVALID_ARG;
-    if (plan->workspace_bytes < ws_layout(B, Hq, plan->head_dim, plan->num_partitions).total)
+    const WsLayout wl = ws_layout(B, Hq, plan->head_dim, plan->num_partitions,
+                                  (long long)B * Hkv * (Hq / Hkv / plan->heads_per_cta));
+    if (plan->workspace_bytes < wl.total) return PA_ERR_INVALID_ARG;
+    if (plan->merge_in_kernel &&
+        !kFusedMergeFits(plan->heads_per_cta, plan->head_dim, plan->num_partitions))
         return PA_ERR_INVALID_ARG;
     if (plan->kernel != PA_KERNEL_SIMT && plan->kernel != PA_KERNEL_MMA) return PA_ERR_INVALID_ARG;
     if (plan->parts_per_cta < 1 ||
@@ -423,7 +438,9 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
 
     const int D = plan->head_dim;
     const int P = plan->num_partitions;
-    const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, D, P);
+    const int nchunk = plan->num_q_heads / plan->num_kv_heads / plan->heads_per_cta;
+    const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, D, P,
+                                  (long long)plan->batch * plan->num_kv_heads * nchunk);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     AttendParams p;
     p.q = static_cast<const __half*>(q);
@@ -437,6 +454,8 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     p.ws_l = reinterpret_cast<float*>(ws + wl.l_off);
     p.ws_o = reinterpret_cast<float*>(ws + wl.o_off);
     p.err = reinterpret_cast<unsigned*>(ws);
+    p.counters = reinterpret_cast<unsigned*>(ws + wl.ctr_off);
+    p.merge_in_kernel = (plan->kernel == PA_KERNEL_MMA && P > 1 && plan->merge_in_kernel) ? 1 : 0;
     p.B = plan->batch;
     p.Hq = plan->num_q_heads;
     p.Hkv = plan->num_kv_heads;
@@ -479,9 +498,13 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
     if (!workspace) return PA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return PA_ERR_INVALID_ARG;
     if (plan->batch == 0 || plan->num_partitions == 1) return PA_OK;
+    // The partition kernel already merged in its last CTAs.
+    if (plan->kernel == PA_KERNEL_MMA && plan->merge_in_kernel) return PA_OK;
     if (!context_lens || !out || !lse || !aligned16(out)) return PA_ERR_INVALID_ARG;
     const int D = plan->head_dim;
-    const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, D, plan->num_partitions);
+    const int nchunk = plan->num_q_heads / plan->num_kv_heads / plan->heads_per_cta;
+    const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, D, plan->num_partitions,
+                                  (long long)plan->batch * plan->num_kv_heads * nchunk);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     MergeParams p;
     p.context_lens = context_lens;

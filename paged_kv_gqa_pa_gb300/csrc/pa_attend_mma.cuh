@@ -113,6 +113,123 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return (uint32_t)((chunk >> 3) * (kPageSize * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
+// In-kernel log-sum-exp merge (the commit note's Phase 2) for plans whose
+// partials are small: every CTA of a (sequence, KV head, head chunk) group
+// that wrote partials arrives on the group's counter once it is done; the
+// last one to arrive resets the counter to zero for the next call and merges
+// the group's partials (read through L2) into the final fp16 rows and the LSE.
+// Nobody waits: a CTA that is not last simply exits.
+//
+// The merge issues all of its loads at once, so it costs one memory round
+// trip: the (m, l) pairs of the G x P partials, and for each (head, 4-dim
+// column) item the partials' o values, spread over kThreads / items threads
+// of kFusedLoads loads each.  The planner enables it only where that covers
+// the group (kFusedMergeFits).  xbuf holds the G x P (m, weight) pairs, the
+// idle page ring the per-thread partial sums.
+template <int D>
+__device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, const SeqSpan& sp,
+                                                       int b, int h0, int G, float* xbuf,
+                                                       float* s_small, float* scratch) {
+    __shared__ int s_last;
+    __threadfence();  // this CTA's partials, before the arrival below
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int target = (sp.num_parts + p.parts_per_cta - 1) / p.parts_per_cta;
+        unsigned* ctr = p.counters + ((size_t)b * gridDim.y + blockIdx.y);
+        const unsigned prev = atomicAdd(ctr, 1u);
+        const int last = (int)(prev + 1u) == target;
+        if (last) atomicExch(ctr, 0u);
+        s_last = last;
+        __threadfence();
+    }
+    __syncthreads();
+    if (!s_last) return;
+
+    constexpr int D4 = D / 4;
+    const int np = sp.num_parts;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int items = G * D4;               // (head, float4 column) pairs, <= kThreads
+    const int tpi = kThreads / items;        // threads per item, each a stride-tpi slice of partitions
+    const int item = threadIdx.x % items;
+    const int sub = threadIdx.x / items;     // < tpi for active threads
+    const bool active = sub < tpi;
+    const int ih = item / D4;
+    const int id = (item % D4) * 4;
+    const size_t row0 = ((size_t)b * p.Hq + h0) * p.P;
+    float* s_m = xbuf;           // [G][np]
+    float* s_w = xbuf + G * np;  // [G][np]: exp-sums, then merge weights
+    float* s_M = s_small;        // [G]
+    float* s_L = s_small + kMaxHeadsPerCta;
+
+    // One round trip: the (m, l) pairs and this thread's o slices together.
+    for (int idx = threadIdx.x; idx < G * np; idx += kThreads) {
+        const int h = idx / np, i = idx % np;
+        s_m[idx] = __ldcg(p.ws_m + row0 + (size_t)h * p.P + i);
+        s_w[idx] = __ldcg(p.ws_l + row0 + (size_t)h * p.P + i);
+    }
+    float4 ov[kFusedLoads];
+    const float* src = p.ws_o + (row0 + (size_t)ih * p.P) * D + id;
+#pragma unroll
+    for (int u = 0; u < kFusedLoads; ++u) {
+        const int i = sub + u * tpi;
+        ov[u] = (active && i < np) ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)i * D))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+    for (int h = warp; h < G; h += kWarps) {
+        float mx = -INFINITY;
+        for (int i = lane; i < np; i += 32) mx = fmaxf(mx, s_m[h * np + i]);
+#pragma unroll
+        for (int mask = 16; mask > 0; mask >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, mask));
+        float sum = 0.f;
+        for (int i = lane; i < np; i += 32) {
+            const float l = s_w[h * np + i];
+            // l == 0: nothing attended; a NaN (bad page) is kept so it reaches the output.
+            const float w = (l == 0.f) ? 0.f : ex2(s_m[h * np + i] - mx) * l;
+            s_w[h * np + i] = w;
+            sum += w;
+        }
+#pragma unroll
+        for (int mask = 16; mask > 0; mask >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, mask);
+        if (lane == 0) {
+            s_M[h] = mx;
+            s_L[h] = sum;
+        }
+    }
+    __syncthreads();
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < kFusedLoads; ++u) {
+        const int i = sub + u * tpi;
+        const float w = (active && i < np) ? s_w[ih * np + i] : 0.f;
+        acc.x += w * ov[u].x;
+        acc.y += w * ov[u].y;
+        acc.z += w * ov[u].z;
+        acc.w += w * ov[u].w;
+    }
+    if (active) reinterpret_cast<float4*>(scratch)[sub * items + item] = acc;
+    __syncthreads();
+    if (sub == 0) {
+        for (int t = 1; t < tpi; ++t) {
+            const float4 a = reinterpret_cast<const float4*>(scratch)[t * items + item];
+            acc.x += a.x;
+            acc.y += a.y;
+            acc.z += a.z;
+            acc.w += a.w;
+        }
+        const float lam = s_L[ih];
+        const float inv = 1.f / lam;
+        const size_t bh = (size_t)b * p.Hq + h0 + ih;
+        __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
+        __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t*>(&lo);
+        packed.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(p.out + bh * D + id) = packed;
+        if (id == 0) p.lse[bh] = (s_M[ih] + log2f(lam)) * 0.69314718055994531f;
+    }
+}
+
 template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     attend_mma_kernel(const AttendParams p, const __grid_constant__ CUtensorMap tmK,
@@ -164,15 +281,25 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
             }
         }
     };
+    const bool fused = SPLIT && p.merge_in_kernel;
+    // Final rows written without any partial (used when nothing is merged).
+    auto final_rows = [&](float o_val, float lse_val) {
+        for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+            const int h = idx / D, d = idx % D;
+            const size_t bh = (size_t)b * p.Hq + h0 + h;
+            p.out[bh * D + d] = __float2half_rn(o_val);
+            if (d == 0) p.lse[bh] = lse_val;
+        }
+    };
     if (!sp.valid) {
         if (threadIdx.x == 0 && part0 == 0 && blockIdx.y == 0) atomicOr(p.err, PA_DEVERR_BAD_LENGTH);
-        if constexpr (!SPLIT) fill_rows(0, NAN, NAN, NAN, NAN);
-        return;  // with a split, the merge writes the NaN rows
+        if (!SPLIT || (fused && blockIdx.x == 0)) final_rows(NAN, NAN);
+        return;  // with a separate merge, the merge writes the NaN rows
     }
     if (part0 >= sp.num_parts) {
-        // Nothing attended here.  Without a split this only happens for an
-        // empty context: out = 0, lse = -inf.
-        if constexpr (!SPLIT) fill_rows(0, 0.f, 0.f, 0.f, -INFINITY);
+        // Nothing attended here.  The group's rows are written here only for
+        // an empty context (out = 0, lse = -inf) when no merge kernel runs.
+        if (!SPLIT || (fused && sp.num_parts == 0 && blockIdx.x == 0)) final_rows(0.f, -INFINITY);
         return;
     }
     const int nparts = min(ppc, sp.num_parts - part0);
@@ -203,6 +330,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     if (s_flag) {
         if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
         for (int q = 0; q < nparts; ++q) fill_rows(part0 + q, NAN, NAN, NAN, NAN);
+        if (fused) group_arrive_and_merge<D>(p, sp, b, h0, G, xbuf, s_ml,
+                                             reinterpret_cast<float*>(ring));
         return;
     }
 
@@ -482,6 +611,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         for (int item = consumed; item < issued; ++item)
             (void)mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
     }
+    if (fused) group_arrive_and_merge<D>(p, sp, b, h0, G, xbuf, s_ml,
+                                         reinterpret_cast<float*>(ring));
 }
 
 template <int D>

@@ -35,6 +35,8 @@ struct AttendParams {
     float* ws_m;   // [B, Hq, P] partition max, log2 domain
     float* ws_l;   // [B, Hq, P] partition exp-sum
     unsigned* err; // device error word
+    unsigned* counters;  // per-(sequence, KV head, head chunk) arrival counters (fused merge)
+    int merge_in_kernel; // 1: the last CTA of each group merges its partials
     int B, Hq, Hkv, g, num_pages, maxp, max_ctx, window;
     int P;                  // partitions (grid.x)
     int pages_per_part;     // partition size in pages
@@ -68,6 +70,22 @@ struct AttendCfg {
                                       kWarps * kStages * 8 + 16;
     static constexpr int kMinBlocks = D == 256 ? 2 : 3;
 };
+
+// The in-kernel merge of the tensor-core kernel issues all of its loads at
+// once: kFusedLoads float4 partial slices per thread, plus the (m, l) pairs
+// staged in the 8 KiB combine buffer.  It is used only where that covers a
+// whole group (G heads x D dims x P partitions) and P is small: measured on
+// GB300 it beats the merge kernel for P = 7 and loses to it for P = 19..24,
+// where every CTA's fence and arrival lengthen the grid more than the second
+// launch costs.
+constexpr int kFusedLoads = 24;
+constexpr int kFusedMaxParts = 8;
+
+__host__ __device__ constexpr bool kFusedMergeFits(int G, int D, int P) {
+    return P <= kFusedMaxParts && G * (D / 4) <= kThreads &&
+           (P + (kThreads / (G * (D / 4))) - 1) / (kThreads / (G * (D / 4))) <= kFusedLoads &&
+           2 * G * P * 4 <= kWarps * kMaxHeadsPerCta * 64 * 4;
+}
 
 // Span of pages a sequence attends, shared by the partition and merge kernels
 // so both agree on the partition count of every sequence.

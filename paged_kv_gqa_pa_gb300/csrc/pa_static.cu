@@ -57,9 +57,11 @@ extern "C" int pa_decode_static(const pa_plan_t* plan, const void* q, const void
     if (plan->workspace_bytes > (size_t)PA_STATIC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE;
     void* ws = static_workspace_ptr();
     if (!ws) return PA_ERR_CUDA;
-    // Nothing in the scratch has to start at zero: every partition partial is
-    // written before the merge reads it, and the device error word it holds
-    // is only ever OR-ed into (no caller reads it through this entry point).
+    // The scratch's control bytes (error word, per-group arrival counters)
+    // start at zero because a __device__ array is zero-initialised when the
+    // library loads, and every call leaves them at zero.  The partials need
+    // no clearing: each is written before it is read.  The error word is only
+    // ever OR-ed into; no caller reads it through this entry point.
     return pa_decode(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window, out,
                      lse, ws, stream);
 }

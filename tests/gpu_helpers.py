@@ -41,7 +41,7 @@ def to_device(case, device="cuda"):
 
 
 def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=None,
-            guard=0, parts_per_cta=None):
+            guard=0, parts_per_cta=None, merge_in_kernel=None, ws=None):
     """Plan + pa_decode through the C ABI.  Returns (out fp64 numpy, lse fp64
     numpy, device error word, plan).  With guard > 0 the outputs and the
     workspace sit inside larger NaN/0xA5-filled buffers whose guard regions are
@@ -61,20 +61,30 @@ def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=N
         plan.kernel = KERNELS[KERNEL]
     if parts_per_cta is not None:
         plan.parts_per_cta = parts_per_cta
+    if merge_in_kernel is not None:
+        plan.merge_in_kernel = merge_in_kernel
     n_out = B * Hq * D
     out_buf = torch.full((n_out + 2 * guard,), float("nan"), dtype=torch.float16, device="cuda")
     lse_buf = torch.full((B * Hq + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")
     ws_bytes = int(plan.workspace_bytes)
-    ws_buf = torch.full((ws_bytes + 2 * guard * 16,), 0xA5, dtype=torch.uint8, device="cuda")
     out = out_buf[guard:guard + n_out].view(B, Hq, D)
     lse = lse_buf[guard:guard + B * Hq].view(B, Hq)
-    ws = ws_buf[guard * 16:guard * 16 + ws_bytes]
-    ws[:256].zero_()
+    if ws is None:
+        # Only the control bytes start at zero; the partials area holds junk
+        # (0xA5), so nothing may rely on it being cleared.
+        ws_buf = torch.full((ws_bytes + 2 * guard * 16,), 0xA5, dtype=torch.uint8, device="cuda")
+        ws = ws_buf[guard * 16:guard * 16 + ws_bytes]
+        ws[:plan.ctrl_bytes].zero_()
+    else:
+        ws_buf = None
+        assert ws.numel() >= ws_bytes
     pa.pa_decode(plan, dev["q"], dev["k"], dev["v"], dev["bt"], dev["cl"], case.scale,
                  case.window, out, lse, ws)
     err = pa.pa_get_error(ws)
     torch.cuda.synchronize()
-    if guard:
+    # Every call leaves the control bytes (error word, arrival counters) zero.
+    assert int(ws[:plan.ctrl_bytes].count_nonzero()) == 0, "control bytes not left zero"
+    if guard and ws_buf is not None:
         ob = out_buf.cpu()
         lb = lse_buf.cpu()
         wb = ws_buf.cpu()

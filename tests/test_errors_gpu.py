@@ -29,13 +29,15 @@ def _ref_rows(case, rows):
     return ref_out[rows], ref_lse[rows]
 
 
+@pytest.mark.parametrize("fused", [0, 1])
 @pytest.mark.parametrize("S", [0, 64, 4096])
 @pytest.mark.parametrize("bad", ["past_pool", "minus_one"])
-def test_bad_page_id_sets_error_and_nan_rows(S, bad):
+def test_bad_page_id_sets_error_and_nan_rows(S, bad, fused):
     case = workloads.make_case("bad", 3, 8, 2, 128, [700, 1200, 90], seed=600, partition_size=S)
     good_ref = _ref_rows(case, [0, 2])
     case.block_tables[1, 5] = case.num_pages if bad == "past_pool" else -1
-    out, lse, err, _ = run_gpu(case, guard=64, parts_per_cta=3 if S == 64 else None)
+    out, lse, err, _ = run_gpu(case, guard=64, parts_per_cta=3 if S == 64 else None,
+                               merge_in_kernel=fused)
     assert err & pa.binding.PA_DEVERR_BAD_PAGE
     assert np.isnan(out[1]).all() and np.isnan(lse[1]).all()
     sub = workloads.Case(**{**case.__dict__, "q": case.q[[0, 2]],
@@ -44,12 +46,13 @@ def test_bad_page_id_sets_error_and_nan_rows(S, bad):
     assert_matches_oracle(sub, out[[0, 2]], lse[[0, 2]], ref=good_ref, what="good rows")
 
 
+@pytest.mark.parametrize("fused", [0, 1])
 @pytest.mark.parametrize("S", [0, 64, 4096])
-def test_context_longer_than_plan_bound(S):
+def test_context_longer_than_plan_bound(S, fused):
     case = workloads.make_case("long", 2, 4, 1, 64, [300, 1000], seed=601, partition_size=S)
     good_ref = _ref_rows(case, [0])
     # Plan for at most 512 tokens: sequence 1 (1000 tokens) breaks the bound.
-    out, lse, err, _ = run_gpu(case, max_context_len=512)
+    out, lse, err, _ = run_gpu(case, max_context_len=512, merge_in_kernel=fused)
     assert err & pa.binding.PA_DEVERR_BAD_LENGTH
     assert np.isnan(out[1]).all() and np.isnan(lse[1]).all()
     assert np.abs(lse[0] - good_ref[1][0]).max() <= 1e-4

@@ -236,3 +236,36 @@ def test_several_partitions_per_cta(ppc):
     out, lse, err, _ = run_gpu(wcase, parts_per_cta=ppc)
     assert err == 0
     assert_matches_oracle(wcase, out, lse, what=f"ppc{ppc} window")
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+def test_merge_in_kernel_and_merge_kernel_agree(fused):
+    """The last-CTA merge inside the partition kernel and the separate merge
+    kernel give the same result, with ragged, empty, unit and windowed
+    sequences (the CUDA-core kernel always uses the merge kernel)."""
+    lens = [0, 1, 4096, 17, 1000, 2, 3333]
+    case = workloads.make_case("fm", len(lens), 16, 4, 128, lens, seed=511, window=1500)
+    ref = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                        case.context_lens, case.scale, case.window)
+    for S in (64, 256):
+        case.partition_size = S
+        out, lse, err, plan = run_gpu(case, guard=64, merge_in_kernel=fused)
+        assert err == 0 and plan.num_partitions > 1
+        assert_matches_oracle(case, out, lse, ref=ref, what=f"fused{fused} S{S}")
+
+
+def test_workspace_reused_across_calls_and_shapes():
+    """One workspace, several calls in a row with different inputs: the
+    arrival counters and the error word come back to zero after each call."""
+    a = workloads.make_case("wa", 3, 8, 2, 128, [900, 3000, 1], seed=512)
+    b = workloads.make_case("wb", 3, 8, 2, 128, [2500, 40, 1700], seed=513)
+    for c in (a, b):
+        c.partition_size = 128
+        c.block_tables = np.pad(c.block_tables, ((0, 0), (0, 200 - c.block_tables.shape[1])),
+                                constant_values=-1)
+    plan_probe = run_gpu(a, max_context_len=3200)[3]
+    ws = torch.zeros(int(plan_probe.workspace_bytes), dtype=torch.uint8, device="cuda")
+    for c in (a, b, a, b):
+        out, lse, err, _ = run_gpu(c, max_context_len=3200, ws=ws)
+        assert err == 0
+        assert_matches_oracle(c, out, lse, what=c.name)
