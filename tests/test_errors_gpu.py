@@ -33,6 +33,8 @@ def _ref_rows(case, rows):
 @pytest.mark.parametrize("S", [0, 64, 4096])
 @pytest.mark.parametrize("bad", ["past_pool", "minus_one"])
 def test_bad_page_id_sets_error_and_nan_rows(S, bad, fused):
+    if fused:  # partition sizes whose partition count the in-kernel merge takes (<= 8)
+        S = {0: 512, 64: 256}.get(S, S)
     case = workloads.make_case("bad", 3, 8, 2, 128, [700, 1200, 90], seed=600, partition_size=S)
     good_ref = _ref_rows(case, [0, 2])
     case.block_tables[1, 5] = case.num_pages if bad == "past_pool" else -1
