@@ -56,13 +56,15 @@ def bind(path: str):
     P = ctypes.c_void_p
     i = ctypes.c_int
     lib.pa_oracle_decode.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P,
-                                     ctypes.c_double, i, P, P, i]
+                                     ctypes.c_double, i, P, P, i, i]
     lib.pa_oracle_decode.restype = i
     lib.pa_oracle_scores.argtypes = [i, i, i, i, i, i, P, P, P, P,
-                                     ctypes.c_double, i, i, i, P, i]
+                                     ctypes.c_double, i, i, i, P, i, i]
     lib.pa_oracle_scores.restype = i
     lib.pa_oracle_half_to_double.argtypes = [ctypes.c_uint16]
     lib.pa_oracle_half_to_double.restype = ctypes.c_double
+    lib.pa_oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.pa_oracle_bf16_to_double.restype = ctypes.c_double
     return lib
 
 
@@ -72,6 +74,9 @@ def _load():
         if _lib is None:
             _lib = bind(build())
     return _lib
+
+
+DTYPES = {"f16": 0, "bf16": 1}
 
 
 def _as_bits(a: np.ndarray) -> np.ndarray:
@@ -92,11 +97,11 @@ class OracleError(RuntimeError):
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
-           window: int = 0, num_threads: int = 0):
+           window: int = 0, num_threads: int = 0, dtype: str = "f16"):
     """fp64 decode attention over a paged KV cache.
 
-    q            float16 [B, Hq, D]
-    k_cache      float16 [num_pages, Hkv, page_size, D]; v_cache the same
+    q            float16 [B, Hq, D] (or the uint16 bits of bf16 when dtype="bf16")
+    k_cache      [num_pages, Hkv, page_size, D] of the same type; v_cache the same
     block_tables int32   [B, max_pages_per_seq]
     context_lens int32   [B]
     Returns (out float64 [B, Hq, D], lse float64 [B, Hq]).
@@ -116,14 +121,14 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
     rc = lib.pa_oracle_decode(B, Hq, Hkv, D, page_size, num_pages, bt.shape[1],
                               _ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(cl),
                               float(scale), int(window), _ptr(out), _ptr(lse),
-                              int(num_threads))
+                              int(num_threads), DTYPES[dtype])
     if rc != 0:
         raise OracleError(f"pa_oracle_decode returned {rc}")
     return out, lse
 
 
 def scores(q, k_cache, block_tables, context_lens, scale: float, window: int,
-           b: int, h: int) -> np.ndarray:
+           b: int, h: int, dtype: str = "f16") -> np.ndarray:
     """The attended scores scale*q.K_t of one (sequence, head), in fp64."""
     lib = _load()
     q = _as_bits(q)
@@ -136,7 +141,7 @@ def scores(q, k_cache, block_tables, context_lens, scale: float, window: int,
     s = np.empty(max(cap, 1), dtype=np.float64)
     n = lib.pa_oracle_scores(Hq, Hkv, D, page_size, num_pages, bt.shape[1], _ptr(q),
                              _ptr(k), _ptr(bt), _ptr(cl), float(scale), int(window),
-                             int(b), int(h), _ptr(s), cap)
+                             int(b), int(h), _ptr(s), cap, DTYPES[dtype])
     if n < 0:
         raise OracleError("pa_oracle_scores failed")
     return s[:n].copy()
@@ -144,3 +149,7 @@ def scores(q, k_cache, block_tables, context_lens, scale: float, window: int,
 
 def half_to_double(bits: int) -> float:
     return _load().pa_oracle_half_to_double(int(bits) & 0xFFFF)
+
+
+def bf16_to_double(bits: int) -> float:
+    return _load().pa_oracle_bf16_to_double(int(bits) & 0xFFFF)

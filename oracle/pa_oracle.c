@@ -33,9 +33,10 @@
  *                                           exactly this value)
  *   L == 0 (nothing attended): out = 0, lse = -inf.
  *
- * Arithmetic: every fp16 value is converted exactly to double (binary16 ->
- * binary64 is exact), all sums and exponentials are in double.  `scale` is
- * taken as a double.  No blocking, reordering or fusion beyond the definition.
+ * Arithmetic: every fp16 (or bf16) value is converted exactly to double (both
+ * binary16 -> binary64 and bfloat16 -> binary64 are exact), all sums and
+ * exponentials are in double.  `scale` is taken as a double.  No blocking,
+ * reordering or fusion beyond the definition.
  *
  * Parity status: pinned (dense textbook attention, closed forms, invariants;
  * see tests/test_oracle_pins.py).
@@ -72,15 +73,38 @@ static double half_bits_to_double(uint16_t h) {
 
 double pa_oracle_half_to_double(uint16_t h) { return half_bits_to_double(h); }
 
+/* bfloat16 -> binary64, exact: a bfloat16 is the upper 16 bits of a binary32
+ * (sign, 8-bit exponent, 7-bit fraction), so value = (-1)^s * 2^(e-127) *
+ * (1 + m/128) for 0 < e < 255, (-1)^s * 2^-126 * (m/128) for e == 0. */
+static double bf16_bits_to_double(uint16_t h) {
+    const int sign = (h >> 15) & 1;
+    const int e = (h >> 7) & 0xff;
+    const int m = h & 0x7f;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -133);             /* 2^-126 * m / 2^7 */
+    } else if (e == 255) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(128 + m), e - 134);  /* 2^(e-127) * (128+m) / 2^7 */
+    }
+    return sign ? -v : v;
+}
+
+double pa_oracle_bf16_to_double(uint16_t h) { return bf16_bits_to_double(h); }
+
+typedef double (*to_double_fn)(uint16_t);
+
 /*
- * q            [B, Hq, D]                    binary16 bits
- * k_cache      [num_pages, Hkv, page_size, D] binary16 bits
+ * q            [B, Hq, D]                    binary16 (or bfloat16) bits
+ * k_cache      [num_pages, Hkv, page_size, D] same element type
  * v_cache      same as k_cache
  * block_tables [B, max_pages_per_seq]         int32 physical page ids
  * context_lens [B]                            int32
  * out          [B, Hq, D]  double (written)
  * lse          [B, Hq]     double (written)
  * num_threads  OpenMP threads over (b, h); <= 0 means the runtime default.
+ * dtype        element type of q, k_cache, v_cache: 0 = fp16, 1 = bf16.
  * Returns 0, or a PA_ORACLE_* code (a page id outside [0, num_pages) or a
  * context longer than the table are reported, never read).
  */
@@ -88,10 +112,11 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
                      int max_pages_per_seq, const uint16_t* q, const uint16_t* k_cache,
                      const uint16_t* v_cache, const int32_t* block_tables,
                      const int32_t* context_lens, double scale, int window, double* out,
-                     double* lse, int num_threads) {
+                     double* lse, int num_threads, int dtype) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || page_size <= 0 ||
-        num_pages < 0 || max_pages_per_seq < 0)
+        num_pages < 0 || max_pages_per_seq < 0 || (dtype != 0 && dtype != 1))
         return PA_ORACLE_BAD_ARG;
+    const to_double_fn cvt = dtype ? bf16_bits_to_double : half_bits_to_double;
     const int g = Hq / Hkv;
     int status = PA_ORACLE_OK;
 
@@ -131,7 +156,7 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
             continue;
         }
         const uint16_t* qrow = q + ((size_t)b * Hq + h) * D;
-        for (int d = 0; d < D; ++d) qd[d] = half_bits_to_double(qrow[d]);
+        for (int d = 0; d < D; ++d) qd[d] = cvt(qrow[d]);
 
         int bad = 0;
         /* Step 1-2: gather K_t through the table, score it. */
@@ -144,7 +169,7 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
             const uint16_t* krow =
                 k_cache + (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
             double dot = 0.0;
-            for (int d = 0; d < D; ++d) dot += qd[d] * half_bits_to_double(krow[d]);
+            for (int d = 0; d < D; ++d) dot += qd[d] * cvt(krow[d]);
             s[t - start] = scale * dot;
         }
         if (bad) {
@@ -169,7 +194,7 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
             const uint16_t* vrow =
                 v_cache + (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
             const double w = exp(s[t - start] - l);
-            for (int d = 0; d < D; ++d) o[d] += w * half_bits_to_double(vrow[d]);
+            for (int d = 0; d < D; ++d) o[d] += w * cvt(vrow[d]);
         }
         free(s);
         free(qd);
@@ -184,8 +209,9 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
 int pa_oracle_scores(int Hq, int Hkv, int D, int page_size, int num_pages, int max_pages_per_seq,
                      const uint16_t* q, const uint16_t* k_cache, const int32_t* block_tables,
                      const int32_t* context_lens, double scale, int window, int b, int h,
-                     double* s_out, int cap) {
-    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return -1;
+                     double* s_out, int cap, int dtype) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (dtype != 0 && dtype != 1)) return -1;
+    const to_double_fn cvt = dtype ? bf16_bits_to_double : half_bits_to_double;
     const int kvh = h / (Hq / Hkv);
     const int L = context_lens[b];
     if (L < 0 || (long)L > (long)max_pages_per_seq * page_size) return -1;
@@ -198,7 +224,7 @@ int pa_oracle_scores(int Hq, int Hkv, int D, int page_size, int num_pages, int m
         const uint16_t* krow =
             k_cache + (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
         double dot = 0.0;
-        for (int d = 0; d < D; ++d) dot += half_bits_to_double(qrow[d]) * half_bits_to_double(krow[d]);
+        for (int d = 0; d < D; ++d) dot += cvt(qrow[d]) * cvt(krow[d]);
         s_out[t - start] = scale * dot;
     }
     return L - start;

@@ -31,6 +31,8 @@ PAGE_SIZE = 16
 
 @dataclasses.dataclass
 class Case:
+    """One decode problem.  With dtype "bf16", q/k_cache/v_cache hold the
+    uint16 bit patterns of bfloat16 values (numpy has no bfloat16)."""
     name: str
     q: np.ndarray
     k_cache: np.ndarray
@@ -41,6 +43,7 @@ class Case:
     window: int
     partition_size: int  # 0 = let the planner choose
     seed: int
+    dtype: str = "f16"
 
     @property
     def B(self):
@@ -75,11 +78,21 @@ class Case:
         return int(self.context_lens.max()) if self.context_lens.size else 0
 
 
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return ((u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
+
+
+BF16_NAN = np.uint16(0x7FC0)
+
+
 def _fill_normal(out16: np.ndarray, seed_seq: np.random.SeedSequence, std: float,
                  chunk: int = 1 << 24, workers: int | None = None) -> None:
-    """Fill a flat float16 array with std*N(0,1), drawn in fixed-size chunks, each
+    """Fill a flat 16-bit array with std*N(0,1), drawn in fixed-size chunks, each
     chunk from its own child generator (deterministic for a given seed and size,
-    independent of the number of worker threads)."""
+    independent of the number of worker threads).  A float16 array gets the
+    values rounded to fp16; a uint16 array gets bfloat16 bit patterns."""
     flat = out16.reshape(-1)
     n = flat.size
     nchunks = max(1, math.ceil(n / chunk))
@@ -92,7 +105,7 @@ def _fill_normal(out16: np.ndarray, seed_seq: np.random.SeedSequence, std: float
         x = g.standard_normal(hi - lo, dtype=np.float32)
         if std != 1.0:
             x *= np.float32(std)
-        flat[lo:hi] = x.astype(np.float16)
+        flat[lo:hi] = x.astype(np.float16) if flat.dtype == np.float16 else to_bf16_bits(x)
 
     if nchunks == 1:
         work(0)
@@ -106,7 +119,8 @@ def make_case(name: str, B: int, Hq: int, Hkv: int, D: int, context_lens, seed: 
               scale: float | None = None, window: int = 0, q_std: float = 1.0,
               partition_size: int = 0, page_size: int = PAGE_SIZE,
               pool_pages: int | None = None, slack: float = 0.25,
-              max_pages_per_seq: int | None = None, nan_slack: bool = True) -> Case:
+              max_pages_per_seq: int | None = None, nan_slack: bool = True,
+              dtype: str = "f16") -> Case:
     lens = np.asarray(context_lens, dtype=np.int64).reshape(B)
     need = [math.ceil(int(L) / page_size) for L in lens]
     total = int(sum(need))
@@ -118,9 +132,10 @@ def make_case(name: str, B: int, Hq: int, Hkv: int, D: int, context_lens, seed: 
     ss = np.random.SeedSequence(seed)
     s_q, s_k, s_v, s_perm = ss.spawn(4)
 
-    q = np.empty((B, Hq, D), dtype=np.float16)
+    et = np.float16 if dtype == "f16" else np.uint16
+    q = np.empty((B, Hq, D), dtype=et)
     _fill_normal(q, s_q, q_std)
-    k = np.empty((pool_pages, Hkv, page_size, D), dtype=np.float16)
+    k = np.empty((pool_pages, Hkv, page_size, D), dtype=et)
     v = np.empty_like(k)
     _fill_normal(k, s_k, 1.0)
     _fill_normal(v, s_v, 1.0)
@@ -133,13 +148,14 @@ def make_case(name: str, B: int, Hq: int, Hkv: int, D: int, context_lens, seed: 
         off += need[b]
     if nan_slack and off < pool_pages:
         slack_ids = perm[off:]
-        k[slack_ids] = np.float16(np.nan)
-        v[slack_ids] = np.float16(np.nan)
+        nan = np.float16(np.nan) if dtype == "f16" else BF16_NAN
+        k[slack_ids] = nan
+        v[slack_ids] = nan
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     return Case(name=name, q=q, k_cache=k, v_cache=v, block_tables=bt,
                 context_lens=lens.astype(np.int32), scale=float(scale), window=int(window),
-                partition_size=int(partition_size), seed=int(seed))
+                partition_size=int(partition_size), seed=int(seed), dtype=dtype)
 
 
 def _ragged_lengths(B: int, lo: int, hi: int, seed: int, not_multiple_of: int) -> np.ndarray:

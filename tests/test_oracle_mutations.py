@@ -26,6 +26,7 @@ MUTATIONS = {
                              "const double w = exp(s[t - start] - M);"),
     "k_in_place_of_v": ("v_cache + (((size_t)page", "k_cache + (((size_t)page"),
     "half_exponent_bias": ("ldexp((double)(1024 + m), e - 25)", "ldexp((double)(1024 + m), e - 24)"),
+    "bf16_exponent_bias": ("ldexp((double)(128 + m), e - 134)", "ldexp((double)(128 + m), e - 133)"),
 }
 
 
@@ -34,6 +35,7 @@ def _checks():
     yield lambda: pins.test_matches_dense_textbook_attention(*pins.SMALL[2])
     yield pins.test_closed_form_golden_cases
     yield lambda: pins.test_window_equals_truncated_context(17)
+    yield lambda: pins.test_bf16_inputs_match_dense_textbook_attention(*pins.SMALL[2])
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))

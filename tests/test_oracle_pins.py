@@ -21,13 +21,21 @@ from paged_kv_gqa_pa_gb300 import workloads
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-def _contiguous_kv(case_k, case_v, bt_row, L, ps):
+def values(a, dtype="f16"):
+    """Element values as float64, independently of the oracle: fp16 through
+    numpy, bf16 bit patterns as the upper half of a float32."""
+    if dtype == "bf16":
+        return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def _contiguous_kv(case_k, case_v, bt_row, L, ps, dtype="f16"):
     """Gather one sequence's K/V into contiguous [Hkv, L, D] arrays (numpy fancy
     indexing; no code shared with the oracle)."""
     npg = math.ceil(L / ps)
     pages = bt_row[:npg]
-    k = case_k[pages].astype(np.float64)  # [npg, Hkv, ps, D]
-    v = case_v[pages].astype(np.float64)
+    k = values(case_k[pages], dtype)  # [npg, Hkv, ps, D]
+    v = values(case_v[pages], dtype)
     Hkv, D = k.shape[1], k.shape[3]
     k = k.transpose(1, 0, 2, 3).reshape(Hkv, npg * ps, D)[:, :L]
     v = v.transpose(1, 0, 2, 3).reshape(Hkv, npg * ps, D)[:, :L]
@@ -51,10 +59,10 @@ def _dense_reference(case, window):
             lse[b] = -np.inf
             continue
         k, v = _contiguous_kv(case.k_cache, case.v_cache, case.block_tables[b], L,
-                              case.page_size)
+                              case.page_size, case.dtype)
         k = torch.from_numpy(k[:, start:L]).repeat_interleave(g, dim=0)  # [Hq, n, D]
         v = torch.from_numpy(v[:, start:L]).repeat_interleave(g, dim=0)
-        q = torch.from_numpy(case.q[b].astype(np.float64)).unsqueeze(1)  # [Hq, 1, D]
+        q = torch.from_numpy(values(case.q[b], case.dtype)).unsqueeze(1)  # [Hq, 1, D]
         o = torch.nn.functional.scaled_dot_product_attention(
             q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0), scale=case.scale)
         out[b] = o[0, :, 0, :].numpy()
@@ -72,6 +80,7 @@ SMALL = [
     (2, 8, 4, 64, [70, 129], 20),
     (1, 4, 4, 128, [48], 48),
     (2, 2, 1, 256, [31, 1], 7),
+    (2, 6, 2, 96, [77, 160], 0),
 ]
 
 
@@ -84,6 +93,27 @@ def test_matches_dense_textbook_attention(B, Hq, Hkv, D, lens, window):
     ref_out, ref_lse = _dense_reference(case, window)
     np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(lse, ref_lse, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,lens,window", [SMALL[2], SMALL[4], SMALL[7]])
+def test_bf16_inputs_match_dense_textbook_attention(B, Hq, Hkv, D, lens, window):
+    case = workloads.make_case("t", B, Hq, Hkv, D, lens, seed=77 + D, window=window,
+                               q_std=2.0, dtype="bf16")
+    out, lse = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                             case.context_lens, case.scale, window, dtype="bf16")
+    ref_out, ref_lse = _dense_reference(case, window)
+    np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-13, atol=1e-13)
+
+
+def test_bf16_conversion_is_exact_for_every_bit_pattern():
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):  # signalling-NaN patterns
+        ref = (bits << np.uint32(16)).view(np.float32).astype(np.float64)
+    got = np.array([oracle.bf16_to_double(int(x)) for x in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
 
 
 def test_gqa_mapping_is_contiguous_groups():
