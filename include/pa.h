@@ -21,15 +21,16 @@
  * L_b == 0 (or an empty attended range) gives out = 0, lse = -inf.
  *
  * Layouts (row-major, element strides implied by the shapes):
- *   q            fp16  [B, Hq, D]
- *   k_cache      fp16  [num_pages, Hkv, page_size, D]   (v_cache the same)
+ *   q            T     [B, Hq, D]      T = fp16, or bf16 (plan.dtype)
+ *   k_cache      T     [num_pages, Hkv, page_size, D]   (v_cache the same)
  *   block_tables int32 [B, max_pages_per_seq]   entry j = physical page of the
  *                                               sequence's logical page j
  *   context_lens int32 [B]
- *   out          fp16  [B, Hq, D]   (round to nearest even)
+ *   out          T     [B, Hq, D]   (round to nearest even)
  *   lse          fp32  [B, Hq]
- * Supported: head_dim in {64, 128, 256}; page_size 16; Hq % Hkv == 0 with
- * g = Hq / Hkv split into at most ceil(g / 8) equal head chunks per CTA.
+ * Supported: head_dim in {64, 96, 128, 256} (96 and bf16 with the tensor-core
+ * kernel only); page_size 16; Hq % Hkv == 0 with g = Hq / Hkv split into at
+ * most ceil(g / 8) equal head chunks per CTA.
  * q, k_cache, v_cache, out and workspace must be 16-byte aligned.
  *
  * Ownership: every pointer is caller-owned device memory (the library
@@ -96,8 +97,14 @@ typedef struct pa_plan {
     int ctrl_bytes;         /* leading workspace bytes that must be zero before the
                                first call (error word, per-group arrival counters); the
                                library leaves them zero after every call */
-    int reserved[4];
+    int dtype;              /* PA_DTYPE_*: element type of q, k_cache, v_cache and out
+                               (pa_plan sets fp16; a caller may set bf16) */
+    int reserved[3];
 } pa_plan_t;
+
+/* Element types (pa_plan_t.dtype).  bf16 needs the tensor-core kernel. */
+#define PA_DTYPE_F16 0
+#define PA_DTYPE_BF16 1
 
 /* Partition-kernel variants (pa_plan_t.kernel). */
 #define PA_KERNEL_SIMT 1   /* fp32 FMA on CUDA cores; pages by 1-D bulk copies */

@@ -25,6 +25,9 @@ PA_DEVERR_BAD_LENGTH = 2
 PA_DEVERR_TIMEOUT = 4
 PA_KERNEL_SIMT = 1
 PA_KERNEL_MMA = 2
+PA_DTYPE_F16 = 0
+PA_DTYPE_BF16 = 1
+_TORCH_DTYPE = {PA_DTYPE_F16: torch.float16, PA_DTYPE_BF16: torch.bfloat16}
 
 EXPORTED = ("pa_plan", "pa_decode", "pa_decode_partitions", "pa_merge", "pa_get_error",
             "pa_status_string", "pa_version", "pa_decode_static")
@@ -51,7 +54,8 @@ class pa_plan_t(ctypes.Structure):
         ("parts_per_cta", ctypes.c_int),
         ("merge_in_kernel", ctypes.c_int),
         ("ctrl_bytes", ctypes.c_int),
-        ("reserved", ctypes.c_int * 4),
+        ("dtype", ctypes.c_int),
+        ("reserved", ctypes.c_int * 3),
     ]
 
     def as_dict(self):
@@ -153,12 +157,13 @@ def _stream_ptr(stream):
 
 def _decode_args(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window, out, lse,
                  workspace, stream):
-    return (ctypes.byref(plan), _dev_ptr(q, "q", torch.float16),
-            _dev_ptr(k_cache, "k_cache", torch.float16),
-            _dev_ptr(v_cache, "v_cache", torch.float16),
+    et = _TORCH_DTYPE.get(plan.dtype, torch.float16)
+    return (ctypes.byref(plan), _dev_ptr(q, "q", et),
+            _dev_ptr(k_cache, "k_cache", et),
+            _dev_ptr(v_cache, "v_cache", et),
             _dev_ptr(block_tables, "block_tables", torch.int32),
             _dev_ptr(context_lens, "context_lens", torch.int32), ctypes.c_float(scale),
-            int(window), _dev_ptr(out, "out", torch.float16), _dev_ptr(lse, "lse", torch.float32),
+            int(window), _dev_ptr(out, "out", et), _dev_ptr(lse, "lse", torch.float32),
             _dev_ptr(workspace, "workspace"), _stream_ptr(stream))
 
 
@@ -180,8 +185,9 @@ def pa_decode_partitions(plan, q, k_cache, v_cache, block_tables, context_lens, 
 
 
 def pa_merge(plan, context_lens, out, lse, workspace, stream=None) -> None:
+    et = _TORCH_DTYPE.get(plan.dtype, torch.float16)
     st = load().pa_merge(ctypes.byref(plan), _dev_ptr(context_lens, "context_lens", torch.int32),
-                         _dev_ptr(out, "out", torch.float16), _dev_ptr(lse, "lse", torch.float32),
+                         _dev_ptr(out, "out", et), _dev_ptr(lse, "lse", torch.float32),
                          _dev_ptr(workspace, "workspace"), _stream_ptr(stream))
     if st != PA_OK:
         raise PAError("pa_merge", st)

@@ -1,6 +1,7 @@
 // pa_api.cu -- the C ABI (include/pa.h): host-side planning and argument
 // checks, the launch of the partition kernel, and the log-sum-exp merge kernel.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdint.h>
@@ -15,19 +16,27 @@ namespace pa {
 template <int D>
 cudaError_t launch_attend_d(int G, bool split, const AttendParams& p, dim3 grid,
                             cudaStream_t stream);
-template <int D>
-cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtensorMap& tmK,
-                                const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
+template <int D, typename T>
+cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtensorMap* maps,
+                                dim3 grid, cudaStream_t stream);
 
-static cudaError_t launch_attend_mma(int D, bool split, const AttendParams& p,
-                                     const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
-                                     cudaStream_t stream) {
+template <typename T>
+static cudaError_t launch_attend_mma_t(int D, bool split, const AttendParams& p,
+                                       const CUtensorMap* maps, dim3 grid, cudaStream_t stream) {
     switch (D) {
-        case 64: return launch_attend_mma_d<64>(split, p, tmK, tmV, grid, stream);
-        case 128: return launch_attend_mma_d<128>(split, p, tmK, tmV, grid, stream);
-        case 256: return launch_attend_mma_d<256>(split, p, tmK, tmV, grid, stream);
+        case 64: return launch_attend_mma_d<64, T>(split, p, maps, grid, stream);
+        case 96: return launch_attend_mma_d<96, T>(split, p, maps, grid, stream);
+        case 128: return launch_attend_mma_d<128, T>(split, p, maps, grid, stream);
+        case 256: return launch_attend_mma_d<256, T>(split, p, maps, grid, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+static cudaError_t launch_attend_mma(int D, int dtype, bool split, const AttendParams& p,
+                                     const CUtensorMap* maps, dim3 grid, cudaStream_t stream) {
+    return dtype == PA_DTYPE_BF16
+               ? launch_attend_mma_t<__nv_bfloat16>(D, split, p, maps, grid, stream)
+               : launch_attend_mma_t<__half>(D, split, p, maps, grid, stream);
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
@@ -48,17 +57,24 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// The K (or V) cache as a 2-D fp16 tensor [rows = num_pages*Hkv*16, D]; one
-// box = 16 rows x 64 columns (one 128-byte slab of a page), 128-byte swizzle.
-static bool make_page_map(CUtensorMap* map, const void* base, long long rows, int D) {
+// The K (or V) cache as a 2-D tensor [rows = num_pages*Hkv*16, D] of 16-bit
+// elements.  The main map's box is 16 rows x 64 columns (one 128-byte slab of
+// a page, 128-byte swizzle); the tail map's box, used when D is not a
+// multiple of 64, is 16 rows x 32 columns (64-byte swizzle).
+static bool make_page_map(CUtensorMap* map, const void* base, long long rows, int D, int dtype,
+                          bool tail) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)kPageSize};
+    const cuuint32_t box[2] = {tail ? 32u : 64u, (cuuint32_t)kPageSize};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return enc(map,
+               dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+               2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE,
+               tail ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
@@ -66,6 +82,7 @@ static bool make_page_map(CUtensorMap* map, const void* base, long long rows, in
 int attend_ctas_per_sm(int D) {
     switch (D) {
         case 64: return AttendCfg<64>::kMinBlocks;
+        case 96: return 3;
         case 128: return AttendCfg<128>::kMinBlocks;
         default: return AttendCfg<256>::kMinBlocks;
     }
@@ -113,6 +130,16 @@ __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) 
     return v;
 }
 
+template <typename T>
+__device__ __forceinline__ T to_elem(float v);
+template <>
+__device__ __forceinline__ __half to_elem<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_elem<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+template <typename T>
 __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeParams p) {
     // Partitions are taken in chunks of kChunk; within a chunk every load (the
     // chunk's m and l, and each thread's kPer float4 slices of o) is issued
@@ -133,22 +160,24 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergePara
     const size_t row0 = bh * p.P;
     wait_for_prerequisite_grid();
     const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, p.pages_per_part);
-    __half* orow = p.out + bh * D + d0;
+    T* orow = reinterpret_cast<T*>(p.out) + bh * D + d0;
+    const int ncols = min(kMergeCols * 4, D - d0);  // a 96-dim head ends in a half chunk
     if (!sp.valid) {
         if (threadIdx.x == 0 && h == 0 && blockIdx.z == 0) atomicOr(p.err, PA_DEVERR_BAD_LENGTH);
-        if (threadIdx.x < kMergeCols * 4) orow[threadIdx.x] = __float2half_rn(NAN);
+        if (threadIdx.x < ncols) orow[threadIdx.x] = to_elem<T>(NAN);
         if (threadIdx.x == 0 && blockIdx.z == 0) p.lse[bh] = NAN;
         return;
     }
     const int np = sp.num_parts;
     if (np == 0) {
-        if (threadIdx.x < kMergeCols * 4) orow[threadIdx.x] = __float2half_rn(0.f);
+        if (threadIdx.x < ncols) orow[threadIdx.x] = to_elem<T>(0.f);
         if (threadIdx.x == 0 && blockIdx.z == 0) p.lse[bh] = -INFINITY;
         return;
     }
     const int grp = threadIdx.x / kMergeCols;
     const int col = (threadIdx.x % kMergeCols) * 4;
-    const float* src = p.ws_o + row0 * D + d0 + col;
+    const bool col_ok = col < ncols;
+    const float* src = p.ws_o + row0 * D + d0 + (col_ok ? col : 0);
 
     float M = -INFINITY;   // running max (log2 domain)
     float lam = 0.f;       // running sum of partition weights
@@ -165,8 +194,8 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergePara
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
             const int i = c0 + grp + k * kMergeGroups;
-            o[k] = i < np ? *reinterpret_cast<const float4*>(src + (size_t)i * D)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            o[k] = (col_ok && i < np) ? *reinterpret_cast<const float4*>(src + (size_t)i * D)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float mloc = m_i[0];
 #pragma unroll
@@ -205,18 +234,18 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergePara
     *reinterpret_cast<float4*>(&s_acc[grp][col]) = acc;
     __syncthreads();
     const float inv = 1.f / lam;
-    if (threadIdx.x < kMergeCols * 4) {
+    if (threadIdx.x < ncols) {
         float a = 0.f;
 #pragma unroll
         for (int g = 0; g < kMergeGroups; ++g) a += s_acc[g][threadIdx.x];
-        orow[threadIdx.x] = __float2half_rn(a * inv);
+        orow[threadIdx.x] = to_elem<T>(a * inv);
     }
     if (threadIdx.x == 0 && blockIdx.z == 0) p.lse[bh] = (M + log2f(lam)) * 0.69314718055994531f;
 }
 
 cudaError_t launch_merge(int D, const MergeParams& p, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.Hq, p.B, D / (kMergeCols * 4));
+    cfg.gridDim = dim3(p.Hq, p.B, (D + kMergeCols * 4 - 1) / (kMergeCols * 4));
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -225,7 +254,8 @@ cudaError_t launch_merge(int D, const MergeParams& p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, merge_kernel, p);
+    return p.dtype == PA_DTYPE_BF16 ? cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16>, p)
+                                    : cudaLaunchKernelEx(&cfg, merge_kernel<__half>, p);
 }
 
 // Workspace layout: [control block | arrival counters (one per group) |
@@ -287,7 +317,8 @@ int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page
         return PA_ERR_INVALID_ARG;
     if ((long long)max_context_len > (long long)max_pages_per_seq * page_size)
         return PA_ERR_INVALID_ARG;
-    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 96 && head_dim != 128 && head_dim != 256)
+        return PA_ERR_UNSUPPORTED;
     if (page_size != kPageSize) return PA_ERR_UNSUPPORTED;
     if (partition_size % page_size != 0) return PA_ERR_INVALID_ARG;
 
@@ -368,6 +399,7 @@ int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page
     plan->workspace_bytes = wl.total;
     plan->ctrl_bytes = (int)wl.ctrl_bytes;
     plan->kernel = PA_KERNEL_MMA;
+    plan->dtype = PA_DTYPE_F16;
     // Merge inside the partition kernel when a group's partials are small
     // (its last CTA merges them, no second launch); the merge kernel when they
     // are many (the one-CTA merge would then trail the grid).
@@ -397,7 +429,12 @@ static int check_plan(const pa_plan_t* plan) {
         plan->partition_size / kPageSize > kMaxPagesPerPart || plan->num_pages <= 0 ||
         plan->max_pages_per_seq <= 0 || plan->max_context_len < 0 || plan->window < 0)
         return PA_ERR_INVALID_ARG;
-    if (plan->head_dim != 64 && plan->head_dim != 128 && plan->head_dim != 256)
+    if (plan->head_dim != 64 && plan->head_dim != 96 && plan->head_dim != 128 &&
+        plan->head_dim != 256)
+        return PA_ERR_UNSUPPORTED;
+    if (plan->dtype != PA_DTYPE_F16 && plan->dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+    // The CUDA-core kernel is built for fp16 and head dims 64/128/256.
+    if (plan->kernel == PA_KERNEL_SIMT && (plan->dtype != PA_DTYPE_F16 || plan->head_dim == 96))
         return PA_ERR_UNSUPPORTED;
     const int g = Hq / Hkv;
     const int G = plan->heads_per_cta;
@@ -471,13 +508,25 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     cudaError_t e;
     if (plan->kernel == PA_KERNEL_MMA) {
-        alignas(64) CUtensorMap tmK, tmV;
+        // K, V (64-column boxes), then K, V tails (32-column boxes, D = 96).
+        alignas(64) CUtensorMap maps[4];
         const long long rows = (long long)plan->num_pages * p.Hkv * kPageSize;
-        if (!make_page_map(&tmK, k_cache, rows, D) || !make_page_map(&tmV, v_cache, rows, D))
+        const bool tail = (D % 64) != 0;
+        if (!make_page_map(&maps[0], k_cache, rows, D, plan->dtype, false) ||
+            !make_page_map(&maps[1], v_cache, rows, D, plan->dtype, false))
             return PA_ERR_CUDA;
+        if (tail) {
+            if (!make_page_map(&maps[2], k_cache, rows, D, plan->dtype, true) ||
+                !make_page_map(&maps[3], v_cache, rows, D, plan->dtype, true))
+                return PA_ERR_CUDA;
+        } else {
+            maps[2] = maps[0];
+            maps[3] = maps[1];
+        }
         p.parts_per_cta = plan->parts_per_cta;
         const dim3 grid((P + p.parts_per_cta - 1) / p.parts_per_cta, p.Hkv * p.nchunk, p.B);
-        e = launch_attend_mma(D, P > 1, p, tmK, tmV, grid, static_cast<cudaStream_t>(stream));
+        e = launch_attend_mma(D, plan->dtype, P > 1, p, maps, grid,
+                              static_cast<cudaStream_t>(stream));
     } else {
         p.parts_per_cta = 1;
         const dim3 grid(P, p.Hkv * p.nchunk, p.B);
@@ -511,7 +560,7 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
     p.ws_m = reinterpret_cast<const float*>(ws + wl.m_off);
     p.ws_l = reinterpret_cast<const float*>(ws + wl.l_off);
     p.ws_o = reinterpret_cast<const float*>(ws + wl.o_off);
-    p.out = static_cast<__half*>(out);
+    p.out = out;
     p.lse = lse;
     p.err = reinterpret_cast<unsigned*>(ws);
     p.B = plan->batch;
@@ -522,6 +571,7 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
     p.maxp = plan->max_pages_per_seq;
     p.max_ctx = plan->max_context_len;
     p.window = plan->window;
+    p.dtype = plan->dtype;
     if (launch_merge(D, p, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return PA_ERR_CUDA;

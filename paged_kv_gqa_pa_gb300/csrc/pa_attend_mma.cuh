@@ -7,13 +7,16 @@
 //
 //  * Staging.  K and V pages arrive through 2-D TMA tensor copies
 //    (cp.async.bulk.tensor) of the cache viewed as a [num_pages*Hkv*16, D]
-//    fp16 matrix, one 16-row x 64-column box per 128-byte slab of the row, with
-//    the 128-byte swizzle: the 16-byte chunk c of row r lands at chunk
-//    c ^ (r & 7) of that row, so the ldmatrix reads below are free of bank
-//    conflicts.
+//    matrix, one 16-row x 64-column box per 128-byte slab of the row, with the
+//    128-byte swizzle: the 16-byte chunk c of row r lands at chunk c ^ (r & 7)
+//    of that row, so the ldmatrix reads below are free of bank conflicts.
+//    A head dim that is not a multiple of 64 (96) ends in a 32-column slab,
+//    copied with the 64-byte swizzle (chunk c of row r at c ^ ((r >> 1) & 3)),
+//    which keeps those reads conflict-free too.
+//  * Element type T: fp16, or bf16 (then q and out are bf16 as well).
 //  * q.K (the commit note's Phase 1 QK^T).  S^T[16 tokens x 8 heads] =
 //    K_page[16 x D] . Q^T[D x 8] with mma.sync m16n8k16 (fp16 in, fp32
-//    accumulate): K fragments via ldmatrix from the swizzled page, the q
+//    accumulate; bf16 in for bf16 caches): K fragments via ldmatrix from the swizzled page, the q
 //    fragments sit in registers for the whole CTA.  The group's G <= 8 query
 //    heads fill the n = 8 columns (unused columns are zero and never stored).
 //  * softmax.  Each lane owns 2 tokens x 2 heads of S^T; page maxima come from
@@ -21,6 +24,9 @@
 //    Two exp-sums are kept: of the rounded weights, which normalises the
 //    output (so the weights applied to V sum to one), and of the fp32
 //    weights, which gives the LSE and the partition's weight in the merge.
+//    With bf16 (8 significant bits) P is split into a bf16 head and a bf16
+//    remainder, and P.V takes both (two mma per tile), so the weights keep
+//    about 16 significant bits.
 //  * P.V.  O^T[D x 8] += V^T[D x 16 tokens] . P^T[16 x 8]: V^T fragments via
 //    ldmatrix.trans of the same swizzled page, P^T from S^T by movmatrix.trans.
 //    The accumulator of a lane holds two heads, so the online rescale needs
@@ -34,9 +40,11 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <math.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "pa_common.cuh"
 
@@ -44,19 +52,82 @@ namespace pa {
 
 template <int D>
 struct MmaCfg {
-    static constexpr int kSlabs = D / 64;           // 128-byte slabs per K/V row
+    static_assert(D % 64 == 0 || D % 64 == 32, "head dim: 64-column slabs plus at most one 32-column slab");
+    static constexpr int kFullSlabs = D / 64;       // 128-byte slabs per K/V row (128-byte swizzle)
+    static constexpr bool kTail = (D % 64) != 0;    // a trailing 64-byte slab (64-byte swizzle)
     static constexpr int kSlabBytes = kPageSize * 128;
+    static constexpr int kTailBytes = kPageSize * 64;
     static constexpr int kPageBytes = kPageSize * D * 2;
     static constexpr int kStages = D == 256 ? 3 : (D == 128 ? 4 : 6);
     static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
-    static constexpr int kXDims = 64;  // output dims combined per round at a partition edge
-    static constexpr int kXBytes = kWarps * kMaxHeadsPerCta * kXDims * 4;
+    // output dims combined per round at a partition edge
+    static constexpr int kXDims = (D % 64 == 0) ? 64 : 32;
+    static constexpr int kXBytes = kWarps * kMaxHeadsPerCta * 64 * 4;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes + kXBytes +
                                       kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 3 * 4 +
                                       kWarps * kStages * 8 + 16;
     static constexpr int kMinBlocks = D == 256 ? 2 : 3;
-    static_assert(kPageBytes == kSlabs * kSlabBytes, "slab layout");
+    static_assert(kPageBytes == kFullSlabs * kSlabBytes + (kTail ? kTailBytes : 0), "slab layout");
+    static_assert(kPageBytes % 1024 == 0, "page slots keep the 1 KiB swizzle alignment");
 };
+
+// Element-type specifics: the mma flavour and the packing of fp32 pairs.
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<__half> {
+    __device__ static __forceinline__ void mma(float (&c)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+            " {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+    // (lo, hi) rounded to nearest; the rounded values come back in lo_r, hi_r.
+    __device__ static __forceinline__ uint32_t pack2(float lo, float hi, float& lo_r, float& hi_r) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        const float2 back = __half22float2(h);
+        lo_r = back.x;
+        hi_r = back.y;
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __device__ static __forceinline__ __half from_float(float v) { return __float2half_rn(v); }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    __device__ static __forceinline__ void mma(float (&c)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+            " {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+    __device__ static __forceinline__ uint32_t pack2(float lo, float hi, float& lo_r, float& hi_r) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        const float2 back = __bfloat1622float2(h);
+        lo_r = back.x;
+        hi_r = back.y;
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __device__ static __forceinline__ __nv_bfloat16 from_float(float v) {
+        return __float2bfloat16_rn(v);
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, float a, float b, float c, float d) {
+    float ra, rb, rc, rd;
+    uint2 packed;
+    packed.x = Elem<T>::pack2(a, b, ra, rb);
+    packed.y = Elem<T>::pack2(c, d, rc, rd);
+    *reinterpret_cast<uint2*>(dst) = packed;
+}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
@@ -83,34 +154,22 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& a0, uint32_t&
                  : "memory");
 }
 
-// c += A(16x16, row) . B(16x8, col), fp16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
-        " {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
     return y;
 }
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi, float& lo_r, float& hi_r) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    const float2 back = __half22float2(h);
-    lo_r = back.x;
-    hi_r = back.y;
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
 // Byte offset inside a swizzled page of the 16-byte chunk `chunk` (0..D/8-1)
-// of token row `row`.
+// of token row `row`: 128-byte slabs first, then the optional 64-byte slab.
+template <int D>
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    return (uint32_t)((chunk >> 3) * (kPageSize * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+    constexpr int kFull = (D / 64) * 8;  // chunks in the 128-byte slabs
+    if (D % 64 == 0 || chunk < kFull)
+        return (uint32_t)((chunk >> 3) * (kPageSize * 128) + row * 128 +
+                          (((chunk & 7) ^ (row & 7)) << 4));
+    const int c = chunk - kFull;  // 0..3 in a 64-byte row
+    return (uint32_t)((D / 64) * (kPageSize * 128) + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
 }
 
 // In-kernel log-sum-exp merge (the commit note's Phase 2) for plans whose
@@ -126,7 +185,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // of kFusedLoads loads each.  The planner enables it only where that covers
 // the group (kFusedMergeFits).  xbuf holds the G x P (m, weight) pairs, the
 // idle page ring the per-thread partial sums.
-template <int D>
+template <int D, typename T>
 __device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, const SeqSpan& sp,
                                                        int b, int h0, int G, float* xbuf,
                                                        float* s_small, float* scratch) {
@@ -220,20 +279,18 @@ __device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, co
         const float lam = s_L[ih];
         const float inv = 1.f / lam;
         const size_t bh = (size_t)b * p.Hq + h0 + ih;
-        __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
-        __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
-        uint2 packed;
-        packed.x = *reinterpret_cast<uint32_t*>(&lo);
-        packed.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(p.out + bh * D + id) = packed;
+        store4<T>(reinterpret_cast<T*>(p.out) + bh * D + id, acc.x * inv, acc.y * inv,
+                  acc.z * inv, acc.w * inv);
         if (id == 0) p.lse[bh] = (s_M[ih] + log2f(lam)) * 0.69314718055994531f;
     }
 }
 
-template <int D, bool SPLIT>
+template <int D, typename T, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     attend_mma_kernel(const AttendParams p, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV) {
+                      const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmKt,
+                      const __grid_constant__ CUtensorMap tmVt) {
     using Cfg = MmaCfg<D>;
     constexpr int NS = Cfg::kStages;
     constexpr int PB = Cfg::kPageBytes;
@@ -264,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     const int pp = p.pages_per_part;
 
     const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, pp);
+    T* const out = reinterpret_cast<T*>(p.out);
     auto fill_rows = [&](int part, float o_val, float m_val, float l_val, float lse_val) {
         for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
             const int h = idx / D, d = idx % D;
@@ -276,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
                     p.ws_l[row] = l_val;
                 }
             } else {
-                p.out[bh * D + d] = __float2half_rn(o_val);
+                out[bh * D + d] = Elem<T>::from_float(o_val);
                 if (d == 0) p.lse[bh] = lse_val;
             }
         }
@@ -287,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
             const int h = idx / D, d = idx % D;
             const size_t bh = (size_t)b * p.Hq + h0 + h;
-            p.out[bh * D + d] = __float2half_rn(o_val);
+            out[bh * D + d] = Elem<T>::from_float(o_val);
             if (d == 0) p.lse[bh] = lse_val;
         }
     };
@@ -310,6 +368,10 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         s_flag = 0;
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
+        if (Cfg::kTail) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmKt)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmVt)) : "memory");
+        }
     }
     const uint32_t bar_w = smem_u32(bars) + warp * NS * 8;
     if (lane == 0) {
@@ -330,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     if (s_flag) {
         if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
         for (int q = 0; q < nparts; ++q) fill_rows(part0 + q, NAN, NAN, NAN, NAN);
-        if (fused) group_arrive_and_merge<D>(p, sp, b, h0, G, xbuf, s_ml,
-                                             reinterpret_cast<float*>(ring));
+        if (fused) group_arrive_and_merge<D, T>(p, sp, b, h0, G, xbuf, s_ml,
+                                                reinterpret_cast<float*>(ring));
         return;
     }
 
@@ -349,8 +411,11 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         const uint32_t bar = bar_w + slot * 8;
         mbar_arrive_expect_tx(bar, PB);
 #pragma unroll
-        for (int s = 0; s < Cfg::kSlabs; ++s)
+        for (int s = 0; s < Cfg::kFullSlabs; ++s)
             tma_load_2d(ring_w + slot * PB + s * Cfg::kSlabBytes, map, s * 64, y, bar);
+        if (Cfg::kTail)
+            tma_load_2d(ring_w + slot * PB + Cfg::kFullSlabs * Cfg::kSlabBytes,
+                        (item & 1) ? &tmVt : &tmKt, Cfg::kFullSlabs * 64, y, bar);
     };
     if (lane == 0) {
         for (int i = 0; i < NS && i < n_items; ++i) issue(i);
@@ -409,11 +474,11 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4(kaddr + swz(k_row, kk * 2 + k_chk), a0, a1, a2, a3);
+                ldsm_x4(kaddr + swz<D>(k_row, kk * 2 + k_chk), a0, a1, a2, a3);
                 if (kk & 1)
-                    mma_16816(cb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+                    Elem<T>::mma(cb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
                 else
-                    mma_16816(ca, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+                    Elem<T>::mma(ca, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
             }
             __syncwarp();
             if (lane == 0 && 2 * k + NS < n_items) {
@@ -458,15 +523,27 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
             const float p10 = (s10 == -INFINITY) ? 0.f : ex2(s10 - m_run[0]);
             const float p11 = (s11 == -INFINITY) ? 0.f : ex2(s11 - m_run[1]);
             float r00, r01, r10, r11;
-            const uint32_t top = pack_half2(p00, p01, r00, r01);  // P[tok0][hA, hB]
-            const uint32_t bot = pack_half2(p10, p11, r10, r11);  // P[tok0 + 8][hA, hB]
+            const uint32_t top = Elem<T>::pack2(p00, p01, r00, r01);  // P[tok0][hA, hB]
+            const uint32_t bot = Elem<T>::pack2(p10, p11, r10, r11);  // P[tok0 + 8][hA, hB]
             l_run[0] += p00 + p10;
             l_run[1] += p01 + p11;
-            n_run[0] += r00 + r10;
-            n_run[1] += r01 + r11;
             // P^T fragments: lane gets P[tokens (lane%4)*2 + {0,1} (+8)][head lane/4]
             const uint32_t pb0 = movmatrix_trans(top);
             const uint32_t pb1 = movmatrix_trans(bot);
+            uint32_t pc0 = 0u, pc1 = 0u;  // bf16 only: the remainders P - head
+            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                float e00, e01, e10, e11;
+                const uint32_t ltop = Elem<T>::pack2(p00 - r00, p01 - r01, e00, e01);
+                const uint32_t lbot = Elem<T>::pack2(p10 - r10, p11 - r11, e10, e11);
+                r00 += e00;
+                r01 += e01;
+                r10 += e10;
+                r11 += e11;
+                pc0 = movmatrix_trans(ltop);
+                pc1 = movmatrix_trans(lbot);
+            }
+            n_run[0] += r00 + r10;
+            n_run[1] += r01 + r11;
 
             // ---------------- V page: O^T += V^T . P^T
             {
@@ -488,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
                     const int row = idx / (D / 8);
                     const int pos = page_pos + row;
                     if (pos < sp.start || pos >= sp.L)
-                        *reinterpret_cast<uint4*>(vgen + swz(row, idx % (D / 8))) =
+                        *reinterpret_cast<uint4*>(vgen + swz<D>(row, idx % (D / 8))) =
                             make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();
@@ -496,8 +573,10 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt) {
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(vaddr + swz(v_row, mt * 2 + v_chk), a0, a1, a2, a3);
-                mma_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+                ldsm_x4_t(vaddr + swz<D>(v_row, mt * 2 + v_chk), a0, a1, a2, a3);
+                Elem<T>::mma(o[mt], a0, a1, a2, a3, pb0, pb1);
+                if constexpr (std::is_same<T, __nv_bfloat16>::value)
+                    Elem<T>::mma(o[mt], a0, a1, a2, a3, pc0, pc1);
             }
             __syncwarp();
             if (lane == 0 && 2 * k + 1 + NS < n_items) {
@@ -589,12 +668,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
                         p.ws_l[row] = Ls;
                     }
                 } else {
-                    __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
-                    __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
-                    uint2 packed;
-                    packed.x = *reinterpret_cast<uint32_t*>(&lo);
-                    packed.y = *reinterpret_cast<uint32_t*>(&hi);
-                    *reinterpret_cast<uint2*>(p.out + bh * D + d) = packed;
+                    store4<T>(out + bh * D + d, acc.x * inv, acc.y * inv, acc.z * inv,
+                              acc.w * inv);
                     if (d == 0)
                         p.lse[bh] = failed ? NAN
                                            : (Ls > 0.f ? M * 0.69314718055994531f + logf(Ls)
@@ -611,15 +686,15 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         for (int item = consumed; item < issued; ++item)
             (void)mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
     }
-    if (fused) group_arrive_and_merge<D>(p, sp, b, h0, G, xbuf, s_ml,
-                                         reinterpret_cast<float*>(ring));
+    if (fused) group_arrive_and_merge<D, T>(p, sp, b, h0, G, xbuf, s_ml,
+                                            reinterpret_cast<float*>(ring));
 }
 
-template <int D>
-cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtensorMap& tmK,
-                                const CUtensorMap& tmV, dim3 grid, cudaStream_t stream) {
-    const void* fn = split ? reinterpret_cast<const void*>(&attend_mma_kernel<D, true>)
-                           : reinterpret_cast<const void*>(&attend_mma_kernel<D, false>);
+template <int D, typename T>
+cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtensorMap* maps,
+                                dim3 grid, cudaStream_t stream) {
+    const void* fn = split ? reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true>)
+                           : reinterpret_cast<const void*>(&attend_mma_kernel<D, T, false>);
     constexpr int kMaxDevices = 64;
     static std::atomic<uint32_t> configured[kMaxDevices];
     int dev = 0;
@@ -632,8 +707,9 @@ cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtenso
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDevices) configured[dev].fetch_or(bit);
     }
-    void* args[] = {const_cast<AttendParams*>(&p), const_cast<CUtensorMap*>(&tmK),
-                    const_cast<CUtensorMap*>(&tmV)};
+    void* args[] = {const_cast<AttendParams*>(&p), const_cast<CUtensorMap*>(&maps[0]),
+                    const_cast<CUtensorMap*>(&maps[1]), const_cast<CUtensorMap*>(&maps[2]),
+                    const_cast<CUtensorMap*>(&maps[3])};
     return cudaLaunchKernel(fn, grid, dim3(kThreads), args, MmaCfg<D>::kSmemBytes, stream);
 }
 

@@ -51,10 +51,11 @@ struct MergeParams {
     const float* ws_o;
     const float* ws_m;
     const float* ws_l;
-    __half* out;
+    void* out;               // fp16 or bf16 (dtype)
     float* lse;
     unsigned* err;
     int B, Hq, D, P, pages_per_part, maxp, max_ctx, window;
+    int dtype;               // PA_DTYPE_*
 };
 
 // Pipeline depth (pages of K or V in flight per warp) for each head dim; the

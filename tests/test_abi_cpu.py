@@ -107,7 +107,7 @@ def test_auto_plan_is_consistent(num_sms, B, Hkv, L, W):
 
 @pytest.mark.parametrize("args,status", [
     ((1, 8, 3, 128, 16, 10, 10, 100, 0, 0, 152), binding.PA_ERR_INVALID_ARG),   # Hq % Hkv
-    ((1, 8, 8, 96, 16, 10, 10, 100, 0, 0, 152), binding.PA_ERR_UNSUPPORTED),    # head_dim
+    ((1, 8, 8, 80, 16, 10, 10, 100, 0, 0, 152), binding.PA_ERR_UNSUPPORTED),    # head_dim
     ((1, 8, 8, 128, 32, 10, 10, 100, 0, 0, 152), binding.PA_ERR_UNSUPPORTED),   # page_size
     ((1, 8, 8, 128, 16, 10, 10, 100, 0, 24, 152), binding.PA_ERR_INVALID_ARG),  # S % 16
     ((1, 8, 8, 128, 16, 10, 10, 161, 0, 0, 152), binding.PA_ERR_INVALID_ARG),   # Lmax > table
@@ -148,6 +148,18 @@ def test_decode_argument_checks_return_before_launch():
     bad = binding.pa_plan_t.from_buffer_copy(plan)
     bad.heads_per_cta = 3
     assert _call_decode(bad) == binding.PA_ERR_INVALID_ARG
+    # The CUDA-core kernel has no bf16 or head_dim-96 build.
+    simt_bf16 = binding.pa_plan_t.from_buffer_copy(plan)
+    simt_bf16.kernel = binding.PA_KERNEL_SIMT
+    simt_bf16.dtype = binding.PA_DTYPE_BF16
+    assert _call_decode(simt_bf16) == binding.PA_ERR_UNSUPPORTED
+    p96 = pa.pa_plan(2, 8, 2, 96, 16, 100, 50, 800, 0, 64, 152)
+    assert p96.kernel == binding.PA_KERNEL_MMA
+    p96.kernel = binding.PA_KERNEL_SIMT
+    assert _call_decode(p96) == binding.PA_ERR_UNSUPPORTED
+    bad_dtype = binding.pa_plan_t.from_buffer_copy(plan)
+    bad_dtype.dtype = 7
+    assert _call_decode(bad_dtype) == binding.PA_ERR_INVALID_ARG
     empty = pa.pa_plan(0, 8, 2, 128, 16, 100, 50, 800, 0, 64, 152)
     assert _call_decode(empty) == binding.PA_OK   # nothing to do, nothing launched
     lib = pa.load()

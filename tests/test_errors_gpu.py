@@ -25,7 +25,7 @@ def kernel_variant(request):
 
 def _ref_rows(case, rows):
     ref_out, ref_lse = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
-                                     case.context_lens, case.scale, case.window)
+                                     case.context_lens, case.scale, case.window, dtype=case.dtype)
     return ref_out[rows], ref_lse[rows]
 
 
@@ -70,3 +70,20 @@ def test_negative_context_length():
     assert err & pa.binding.PA_DEVERR_BAD_LENGTH
     assert np.isnan(out[1]).all()
     assert not np.isnan(out[0]).any()
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f16", 96)])
+def test_bad_page_on_wider_paths(dtype, D):
+    if gpu_helpers.KERNEL == "simt":
+        pytest.skip("the CUDA-core kernel is built for fp16 and head dims 64/128/256")
+    case = workloads.make_case("badw", 3, 8, 2, D, [700, 1200, 90], seed=610, partition_size=256,
+                               dtype=dtype)
+    good_ref = _ref_rows(case, [0, 2])
+    case.block_tables[1, 7] = -1
+    out, lse, err, _ = run_gpu(case, guard=64)
+    assert err & pa.binding.PA_DEVERR_BAD_PAGE
+    assert np.isnan(out[1]).all() and np.isnan(lse[1]).all()
+    sub = workloads.Case(**{**case.__dict__, "q": case.q[[0, 2]],
+                            "block_tables": case.block_tables[[0, 2]],
+                            "context_lens": case.context_lens[[0, 2]]})
+    assert_matches_oracle(sub, out[[0, 2]], lse[[0, 2]], ref=good_ref, what="good rows")

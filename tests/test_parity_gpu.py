@@ -269,3 +269,53 @@ def test_workspace_reused_across_calls_and_shapes():
         out, lse, err, _ = run_gpu(c, max_context_len=3200, ws=ws)
         assert err == 0
         assert_matches_oracle(c, out, lse, what=c.name)
+
+
+def _mma_only():
+    if gpu_helpers.KERNEL == "simt":
+        pytest.skip("the CUDA-core kernel is built for fp16 and head dims 64/128/256")
+
+
+@pytest.mark.parametrize("partition_size", [0, 16, 64, 512, 4096])
+def test_head_dim_96(partition_size):
+    _mma_only()
+    case = workloads.make_case("d96", len(LENS), 12, 2, 96, LENS, seed=700,
+                               partition_size=partition_size, q_std=2.0)
+    out, lse, err, plan = run_gpu(case, guard=64)
+    assert err == 0
+    assert_matches_oracle(case, out, lse, what=f"D96 S{partition_size}")
+
+
+@pytest.mark.parametrize("D", [64, 96, 128, 256])
+@pytest.mark.parametrize("partition_size", [0, 64, 4096])
+def test_bf16_cache(D, partition_size):
+    _mma_only()
+    case = workloads.make_case("bf16", len(LENS), 16, 4, D, LENS, seed=710 + D,
+                               partition_size=partition_size, q_std=2.0, dtype="bf16")
+    out, lse, err, plan = run_gpu(case, guard=64)
+    assert err == 0
+    rel = assert_matches_oracle(case, out, lse, what=f"bf16 D{D} S{partition_size}")
+    print(f"bf16 D{D} S{partition_size}: rel L2 {rel:.2e}")
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 256), ("bf16", 96), ("f16", 96)])
+def test_wider_paths_window_ragged_and_invariants(dtype, D):
+    _mma_only()
+    lens = [0, 1, 3001, 17, 5000]
+    case = workloads.make_case("wide", len(lens), 8, 2, D, lens, seed=720 + D, window=1000,
+                               q_std=3.0, dtype=dtype)
+    # The in-kernel merge covers G x D/4 <= 128 items: not D = 256 with G = 4.
+    for S, fused, ppc in ((0, None, None), (256, 1 if D < 256 else 0, None), (64, 0, 3)):
+        case.partition_size = S
+        out, lse, err, _ = run_gpu(case, guard=64, merge_in_kernel=fused, parts_per_cta=ppc)
+        assert err == 0
+        assert_matches_oracle(case, out, lse, what=f"{dtype} D{D} S{S}")
+    # A single-token context returns that V row bit for bit.
+    one = workloads.make_case("one", 3, 8, 2, D, [1, 1, 1], seed=721, dtype=dtype)
+    out, lse, err, _ = run_gpu(one, max_context_len=16)
+    for b in range(3):
+        page = one.block_tables[b, 0]
+        for h in range(8):
+            row = one.v_cache[page, h // 4, 0]
+            vals = (row.astype(np.uint32) << 16).view(np.float32) if dtype == "bf16" else row
+            assert np.array_equal(out[b, h], vals.astype(np.float64))
