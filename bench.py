@@ -52,7 +52,7 @@ NCU_TRAFFIC = {
 
 
 KERNEL_SOURCES = {
-    "mma": ("pa_attend_mma.cuh", "pa_attend_mma.cu", "pa_common.cuh"),
+    "mma": ("pa_attend_mma.cuh", "pa_attend_mma_f16.cu", "pa_attend_mma_bf16.cu", "pa_common.cuh"),
     "simt": ("pa_attend.cuh", "pa_attend_d64.cu", "pa_attend_d128.cu", "pa_attend_d256.cu",
              "pa_common.cuh"),
 }
@@ -170,9 +170,12 @@ class GpuArm:
         self.pa = pa
         self.case = case
         self.device = device
-        self.q = torch.from_numpy(case.q).to(device)
-        self.k = torch.from_numpy(case.k_cache).to(device)
-        self.v = torch.from_numpy(case.v_cache).to(device)
+        def elems(a):
+            t = torch.from_numpy(a)
+            return t.view(torch.bfloat16) if case.dtype == "bf16" else t
+        self.q = elems(case.q).to(device)
+        self.k = elems(case.k_cache).to(device)
+        self.v = elems(case.v_cache).to(device)
         self.bt = torch.from_numpy(case.block_tables).to(device)
         self.cl = torch.from_numpy(case.context_lens).to(device)
         B, Hq, D = case.q.shape
@@ -180,10 +183,11 @@ class GpuArm:
         ps = case.partition_size if partition_size is None else partition_size
         self.plan = pa.pa_plan(B, Hq, case.Hkv, D, case.page_size, case.num_pages,
                                case.max_pages_per_seq, case.max_context_len, case.window, ps, sms)
+        self.plan.dtype = 1 if case.dtype == "bf16" else 0
         self.planner_kernel = self.plan.kernel
         if kernel:
             self.plan.kernel = KERNEL_IDS[kernel]
-        self.out = torch.empty((B, Hq, D), dtype=torch.float16, device=device)
+        self.out = torch.empty((B, Hq, D), dtype=self.q.dtype, device=device)
         self.lse = torch.empty((B, Hq), dtype=torch.float32, device=device)
         self.ws = pa.new_workspace(self.plan, device)
         self.stream = torch.cuda.current_stream(device)
@@ -325,15 +329,19 @@ def e2e_steps(arm, steps, warmup, upload_kv=False):
     from pinned host memory, decode, read out + LSE back to pinned host."""
     torch = arm.torch
     c = arm.case
-    hq = torch.from_numpy(c.q).pin_memory()
+    def host(a):
+        t = torch.from_numpy(a)
+        return (t.view(torch.bfloat16) if c.dtype == "bf16" else t).pin_memory()
+
+    hq = host(c.q)
     hbt = torch.from_numpy(c.block_tables).pin_memory()
     hcl = torch.from_numpy(c.context_lens).pin_memory()
     hout = torch.empty(arm.out.shape, dtype=arm.out.dtype).pin_memory()
     hlse = torch.empty(arm.lse.shape, dtype=arm.lse.dtype).pin_memory()
     hk = hv = None
     if upload_kv:
-        hk = torch.from_numpy(c.k_cache).pin_memory()
-        hv = torch.from_numpy(c.v_cache).pin_memory()
+        hk = host(c.k_cache)
+        hv = host(c.v_cache)
     h2d = hq.numel() * 2 + hbt.numel() * 4 + hcl.numel() * 4
     if upload_kv:
         h2d += hk.numel() * 2 + hv.numel() * 2
@@ -387,12 +395,12 @@ class OracleSampler:
                               k_cache=c.k_cache, v_cache=c.v_cache,
                               block_tables=c.block_tables[:1],
                               context_lens=c.context_lens[:1].copy(), scale=c.scale, window=L,
-                              partition_size=0, seed=c.seed)
+                              partition_size=0, seed=c.seed, dtype=c.dtype)
 
     def _run(self, L, threads):
         s = self._sub(L)
         self.oracle.decode(s.q, s.k_cache, s.v_cache, s.block_tables, s.context_lens, s.scale,
-                           s.window, num_threads=threads)
+                           s.window, num_threads=threads, dtype=s.dtype)
 
     def tokens_for(self, budget_s):
         par = min(self.threads, self.case.Hq)
@@ -521,11 +529,12 @@ def run_gpu(args):
     per = None
     if not args.no_per_workload and rank == 0:
         per = {}
-        for name in workloads.WORKLOAD_ORDER:
+        for name in workloads.WORKLOAD_ORDER + workloads.EXTRA_ORDER:
             c = case if name == args.workload else workloads.workload(name)
             b = kv_bytes(c)
-            entry = {}
-            for kname in ("mma", "simt"):
+            entry = {"dtype": c.dtype, "head_dim": c.D}
+            simt_ok = c.dtype == "f16" and c.D in (64, 128, 256)
+            for kname in (("mma", "simt") if simt_ok else ("mma",)):
                 us, kus, copies, l2state, plan = time_graph_rotating(c, device, kname)
                 entry[kname] = {"us_per_step": us, "partition_kernel_us": kus,
                                 "kv_gbs": b / (us * 1e-6) / 1e9,
@@ -584,7 +593,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.WORKLOAD_ORDER)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=workloads.WORKLOAD_ORDER + workloads.EXTRA_ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true")
     ap.add_argument("--no-kv-upload", action="store_true")

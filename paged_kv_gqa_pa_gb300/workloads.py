@@ -180,11 +180,22 @@ WORKLOADS = {
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
+# Further measured workloads for the widened paths: a bf16 cache at the
+# long-context shapes, and head_dim 96 (GQA-4, 32K tokens).  Only the
+# tensor-core kernel serves them.
+EXTRA_WORKLOADS = {
+    "gqa6_ctx100k_bf16": dict(B=4, Hq=24, Hkv=4, D=256, lens=[100000] * 4, seed=1006,
+                              partition_size=512, dtype="bf16"),
+    "gqa4_d96_ctx32k": dict(B=4, Hq=32, Hkv=8, D=96, lens=[32768] * 4, seed=1007),
+}
+EXTRA_ORDER = list(EXTRA_WORKLOADS)
+ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}
+
 
 def workload(name: str, batch: int | None = None) -> Case:
     """One of the measured workloads; `batch` keeps only its first sequences
     (a smaller case of the same shapes, e.g. for profiler captures)."""
-    spec = dict(WORKLOADS[name])
+    spec = dict(ALL_WORKLOADS[name])
     lens = spec.pop("lens")
     seed = spec["seed"]
     if lens == "ragged":

@@ -176,3 +176,13 @@ def test_binding_rejects_host_tensors():
     t = torch.zeros(4, dtype=torch.float16)
     with pytest.raises(ValueError):
         pa.pa_decode(plan, t, t, t, t, t, 0.1, 0, t, t, t)
+
+
+def test_bench_kernel_source_lists_exist():
+    import bench
+    for kernel in bench.KERNEL_SOURCES:
+        assert len(bench.kernel_src_sha(kernel)) == 16
+    csrc = os.path.join(ROOT, "paged_kv_gqa_pa_gb300", "csrc")
+    listed = {f for files in bench.KERNEL_SOURCES.values() for f in files}
+    kernels = {f for f in os.listdir(csrc) if f.startswith("pa_attend")}
+    assert kernels <= listed

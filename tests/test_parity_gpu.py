@@ -27,13 +27,15 @@ def kernel_variant(request):
 
 
 # ---- the five measured workloads, at full size, in the plan the bench uses
-@pytest.mark.parametrize("name", workloads.WORKLOAD_ORDER)
+@pytest.mark.parametrize("name", workloads.WORKLOAD_ORDER + workloads.EXTRA_ORDER)
 def test_workload_full_size(name):
     case = workloads.workload(name)
+    if gpu_helpers.KERNEL == "simt" and (case.dtype != "f16" or case.D == 96):
+        pytest.skip("the CUDA-core kernel is built for fp16 and head dims 64/128/256")
     out, lse, err, plan = run_gpu(case)
     assert err == 0
     rel = assert_matches_oracle(case, out, lse, what=name)
-    if name == "gqa6_ctx100k":
+    if name.startswith("gqa6_ctx100k"):
         # 100000 tokens in 512-token partitions: 196 partitions, the last one
         # holding 160 tokens.
         assert plan.num_partitions == 196
