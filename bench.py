@@ -45,9 +45,9 @@ FALLBACK_HBM_GBS = 6800.0
 # `src_sha` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     # profiles/attend_mma_gqa6_ctx100k_b1.md: one capture of the B = 1 case,
-    # (409.73 + 6.41) MB read + written, scaled by tokens to the B = 4 launch.
-    ("gqa6_ctx100k", "mma"): {"src_sha": "5e600045fe794112", "partition_size": 512,
-                              "bytes_per_launch": 4 * (409.731072e6 + 6.412544e6)},
+    # (409.77 + 6.52) MB read + written, scaled by tokens to the B = 4 launch.
+    ("gqa6_ctx100k", "mma"): {"src_sha": "0564c1f71219c348", "partition_size": 512,
+                              "bytes_per_launch": 4 * (409.766656e6 + 6.522112e6)},
 }
 
 
