@@ -151,6 +151,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(ms: float, device, world: int) -> float:
+    """The slowest rank's time per step (every rank runs its own replica)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput_gbs(kv_bytes_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job KV-read GB/s: every rank reads its own replica's bytes each
+    step, and the step takes as long as the slowest rank."""
+    return kv_bytes_per_rank * world / (ms_per_step * 1e-3) / 1e9
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -497,11 +514,8 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.barrier()
     arm.check_error()
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = byts * world / (ms_max * 1e-3) / 1e9
+    ms_max = max_over_ranks(ms, device, world)
+    value = job_throughput_gbs(byts, world, ms_max)
 
     peak, peak_kind = measured_peaks()
     kern_gbs = byts / (kern_ms * 1e-3) / 1e9
