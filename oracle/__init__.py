@@ -56,10 +56,10 @@ def bind(path: str):
     P = ctypes.c_void_p
     i = ctypes.c_int
     lib.pa_oracle_decode.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P,
-                                     ctypes.c_double, i, P, P, i, i]
+                                     ctypes.c_double, i, P, P, i, i, ctypes.c_double]
     lib.pa_oracle_decode.restype = i
     lib.pa_oracle_scores.argtypes = [i, i, i, i, i, i, P, P, P, P,
-                                     ctypes.c_double, i, i, i, P, i, i]
+                                     ctypes.c_double, i, i, i, P, i, i, ctypes.c_double]
     lib.pa_oracle_scores.restype = i
     lib.pa_oracle_half_to_double.argtypes = [ctypes.c_uint16]
     lib.pa_oracle_half_to_double.restype = ctypes.c_double
@@ -97,13 +97,14 @@ class OracleError(RuntimeError):
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
-           window: int = 0, num_threads: int = 0, dtype: str = "f16"):
+           window: int = 0, num_threads: int = 0, dtype: str = "f16", rope_theta: float = 0.0):
     """fp64 decode attention over a paged KV cache.
 
     q            float16 [B, Hq, D] (or the uint16 bits of bf16 when dtype="bf16")
     k_cache      [num_pages, Hkv, page_size, D] of the same type; v_cache the same
     block_tables int32   [B, max_pages_per_seq]
     context_lens int32   [B]
+    rope_theta   > 0: rotate q (position L-1) and K_t (position t) first
     Returns (out float64 [B, Hq, D], lse float64 [B, Hq]).
     """
     lib = _load()
@@ -121,14 +122,14 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
     rc = lib.pa_oracle_decode(B, Hq, Hkv, D, page_size, num_pages, bt.shape[1],
                               _ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(cl),
                               float(scale), int(window), _ptr(out), _ptr(lse),
-                              int(num_threads), DTYPES[dtype])
+                              int(num_threads), DTYPES[dtype], float(rope_theta))
     if rc != 0:
         raise OracleError(f"pa_oracle_decode returned {rc}")
     return out, lse
 
 
 def scores(q, k_cache, block_tables, context_lens, scale: float, window: int,
-           b: int, h: int, dtype: str = "f16") -> np.ndarray:
+           b: int, h: int, dtype: str = "f16", rope_theta: float = 0.0) -> np.ndarray:
     """The attended scores scale*q.K_t of one (sequence, head), in fp64."""
     lib = _load()
     q = _as_bits(q)
@@ -141,7 +142,7 @@ def scores(q, k_cache, block_tables, context_lens, scale: float, window: int,
     s = np.empty(max(cap, 1), dtype=np.float64)
     n = lib.pa_oracle_scores(Hq, Hkv, D, page_size, num_pages, bt.shape[1], _ptr(q),
                              _ptr(k), _ptr(bt), _ptr(cl), float(scale), int(window),
-                             int(b), int(h), _ptr(s), cap, DTYPES[dtype])
+                             int(b), int(h), _ptr(s), cap, DTYPES[dtype], float(rope_theta))
     if n < 0:
         raise OracleError("pa_oracle_scores failed")
     return s[:n].copy()

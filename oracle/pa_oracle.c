@@ -33,6 +33,15 @@
  *                                           exactly this value)
  *   L == 0 (nothing attended): out = 0, lse = -inf.
  *
+ * Rotary embedding inside the kernel (rotary_mode = 1 of apache/tvm PR #20426,
+ * section Correctness), when rope_theta > 0: before the scores, q is rotated
+ * to position L - 1 (the new token) and every gathered K_t to position t, with
+ * the rotate-half pairing of dimension i and i + D/2 and frequency
+ * theta_i = rope_theta^(-2i/D):
+ *     x'_i       = x_i cos(pos theta_i) - x_{i+D/2} sin(pos theta_i)
+ *     x'_{i+D/2} = x_{i+D/2} cos(pos theta_i) + x_i sin(pos theta_i)
+ * V is not rotated.
+ *
  * Arithmetic: every fp16 (or bf16) value is converted exactly to double (both
  * binary16 -> binary64 and bfloat16 -> binary64 are exact), all sums and
  * exponentials are in double.  `scale` is taken as a double.  No blocking,
@@ -95,6 +104,18 @@ double pa_oracle_bf16_to_double(uint16_t h) { return bf16_bits_to_double(h); }
 
 typedef double (*to_double_fn)(uint16_t);
 
+/* Rotate x[0..D) in place to position pos (rotate-half pairing). */
+static void rope_rotate(double* x, int D, double theta, double pos) {
+    const int half = D / 2;
+    for (int i = 0; i < half; ++i) {
+        const double freq = pow(theta, -2.0 * i / D);
+        const double c = cos(pos * freq), sn = sin(pos * freq);
+        const double a = x[i], b = x[i + half];
+        x[i] = a * c - b * sn;
+        x[i + half] = b * c + a * sn;
+    }
+}
+
 /*
  * q            [B, Hq, D]                    binary16 (or bfloat16) bits
  * k_cache      [num_pages, Hkv, page_size, D] same element type
@@ -105,6 +126,7 @@ typedef double (*to_double_fn)(uint16_t);
  * lse          [B, Hq]     double (written)
  * num_threads  OpenMP threads over (b, h); <= 0 means the runtime default.
  * dtype        element type of q, k_cache, v_cache: 0 = fp16, 1 = bf16.
+ * rope_theta   > 0: rotary embedding of q and K as above; 0: none.
  * Returns 0, or a PA_ORACLE_* code (a page id outside [0, num_pages) or a
  * context longer than the table are reported, never read).
  */
@@ -112,9 +134,10 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
                      int max_pages_per_seq, const uint16_t* q, const uint16_t* k_cache,
                      const uint16_t* v_cache, const int32_t* block_tables,
                      const int32_t* context_lens, double scale, int window, double* out,
-                     double* lse, int num_threads, int dtype) {
+                     double* lse, int num_threads, int dtype, double rope_theta) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || page_size <= 0 ||
-        num_pages < 0 || max_pages_per_seq < 0 || (dtype != 0 && dtype != 1))
+        num_pages < 0 || max_pages_per_seq < 0 || (dtype != 0 && dtype != 1) ||
+        (rope_theta > 0 && D % 2 != 0))
         return PA_ORACLE_BAD_ARG;
     const to_double_fn cvt = dtype ? bf16_bits_to_double : half_bits_to_double;
     const int g = Hq / Hkv;
@@ -148,15 +171,18 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
         }
         double* s = (double*)malloc(sizeof(double) * (size_t)n);
         double* qd = (double*)malloc(sizeof(double) * (size_t)D);
-        if (!s || !qd) {
+        double* kd = (double*)malloc(sizeof(double) * (size_t)D);
+        if (!s || !qd || !kd) {
             free(s);
             free(qd);
+            free(kd);
 #pragma omp atomic write
             status = PA_ORACLE_NO_MEM;
             continue;
         }
         const uint16_t* qrow = q + ((size_t)b * Hq + h) * D;
         for (int d = 0; d < D; ++d) qd[d] = cvt(qrow[d]);
+        if (rope_theta > 0) rope_rotate(qd, D, rope_theta, (double)(L - 1));
 
         int bad = 0;
         /* Step 1-2: gather K_t through the table, score it. */
@@ -168,13 +194,16 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
             }
             const uint16_t* krow =
                 k_cache + (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
+            for (int d = 0; d < D; ++d) kd[d] = cvt(krow[d]);
+            if (rope_theta > 0) rope_rotate(kd, D, rope_theta, (double)t);
             double dot = 0.0;
-            for (int d = 0; d < D; ++d) dot += qd[d] * cvt(krow[d]);
+            for (int d = 0; d < D; ++d) dot += qd[d] * kd[d];
             s[t - start] = scale * dot;
         }
         if (bad) {
             free(s);
             free(qd);
+            free(kd);
 #pragma omp atomic write
             status = PA_ORACLE_BAD_PAGE;
             lse[(size_t)b * Hq + h] = NAN;
@@ -198,6 +227,7 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
         }
         free(s);
         free(qd);
+        free(kd);
     }
     return status;
 }
@@ -209,8 +239,8 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
 int pa_oracle_scores(int Hq, int Hkv, int D, int page_size, int num_pages, int max_pages_per_seq,
                      const uint16_t* q, const uint16_t* k_cache, const int32_t* block_tables,
                      const int32_t* context_lens, double scale, int window, int b, int h,
-                     double* s_out, int cap, int dtype) {
-    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (dtype != 0 && dtype != 1)) return -1;
+                     double* s_out, int cap, int dtype, double rope_theta) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (dtype != 0 && dtype != 1) || D > 1024) return -1;
     const to_double_fn cvt = dtype ? bf16_bits_to_double : half_bits_to_double;
     const int kvh = h / (Hq / Hkv);
     const int L = context_lens[b];
@@ -218,13 +248,18 @@ int pa_oracle_scores(int Hq, int Hkv, int D, int page_size, int num_pages, int m
     const int start = (window > 0 && window < L) ? L - window : 0;
     if (L - start > cap) return -1;
     const uint16_t* qrow = q + ((size_t)b * Hq + h) * D;
+    double qd[1024], kd[1024];
+    for (int d = 0; d < D; ++d) qd[d] = cvt(qrow[d]);
+    if (rope_theta > 0) rope_rotate(qd, D, rope_theta, (double)(L - 1));
     for (int t = start; t < L; ++t) {
         const int page = block_tables[(size_t)b * max_pages_per_seq + t / page_size];
         if (page < 0 || page >= num_pages) return -1;
         const uint16_t* krow =
             k_cache + (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
+        for (int d = 0; d < D; ++d) kd[d] = cvt(krow[d]);
+        if (rope_theta > 0) rope_rotate(kd, D, rope_theta, (double)t);
         double dot = 0.0;
-        for (int d = 0; d < D; ++d) dot += cvt(qrow[d]) * cvt(krow[d]);
+        for (int d = 0; d < D; ++d) dot += qd[d] * kd[d];
         s_out[t - start] = scale * dot;
     }
     return L - start;

@@ -15,8 +15,8 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "pa_oracle.c")
 MUTATIONS = {
     "kv_head_modulo": ("const int kvh = h / g;", "const int kvh = h % Hkv;"),
     "dropped_scale": ("s[t - start] = scale * dot;", "s[t - start] = dot;"),
-    "wrong_slot": ("+ (t % page_size)) * D;\n            double dot",
-                   "+ ((t + 1) % page_size)) * D;\n            double dot"),
+    "wrong_slot": ("+ (t % page_size)) * D;\n            for (int d = 0; d < D; ++d) kd[d]",
+                   "+ ((t + 1) % page_size)) * D;\n            for (int d = 0; d < D; ++d) kd[d]"),
     "window_off_by_one": ("const int start = (window > 0 && window < L) ? L - window : 0;\n"
                           "        const int n",
                           "const int start = (window > 0 && window < L) ? L - window + 1 : 0;\n"
@@ -27,6 +27,10 @@ MUTATIONS = {
     "k_in_place_of_v": ("v_cache + (((size_t)page", "k_cache + (((size_t)page"),
     "half_exponent_bias": ("ldexp((double)(1024 + m), e - 25)", "ldexp((double)(1024 + m), e - 24)"),
     "bf16_exponent_bias": ("ldexp((double)(128 + m), e - 134)", "ldexp((double)(128 + m), e - 133)"),
+    "rope_sign": ("x[i] = a * c - b * sn;", "x[i] = a * c + b * sn;"),
+    "rope_query_position": ("rope_rotate(qd, D, rope_theta, (double)(L - 1));\n\n",
+                            "rope_rotate(qd, D, rope_theta, (double)L);\n\n"),
+    "rope_frequency": ("pow(theta, -2.0 * i / D)", "pow(theta, -1.0 * i / D)"),
 }
 
 
@@ -36,6 +40,7 @@ def _checks():
     yield pins.test_closed_form_golden_cases
     yield lambda: pins.test_window_equals_truncated_context(17)
     yield lambda: pins.test_bf16_inputs_match_dense_textbook_attention(*pins.SMALL[2])
+    yield lambda: pins.test_rope_matches_complex_rotation_reference(64, 10000.0)
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))

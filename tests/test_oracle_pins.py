@@ -326,3 +326,57 @@ def test_workload_recipe_shapes():
     c3 = workloads.workload("batch8_ragged_d128")
     assert c3.context_lens[0] == 1 and c3.block_tables.shape == (8, 256)
     assert np.any(c3.context_lens % 512 != 0) and c3.context_lens.max() <= 4096
+
+
+def _rope_complex(x, pos, theta):
+    """Rotary embedding written with complex numbers (independent of the
+    oracle's pairwise form): the pair (x_i, x_{i+D/2}) is the complex number
+    x_i + i x_{i+D/2}, multiplied by exp(i * pos * theta^(-2i/D))."""
+    half = x.shape[-1] // 2
+    z = x[..., :half] + 1j * x[..., half:]
+    freq = theta ** (-2.0 * np.arange(half) / x.shape[-1])
+    z = z * np.exp(1j * np.multiply.outer(pos, freq))
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+@pytest.mark.parametrize("D,theta", [(64, 10000.0), (128, 500000.0), (256, 10000.0)])
+def test_rope_matches_complex_rotation_reference(D, theta):
+    lens = [1, 37, 300]
+    case = workloads.make_case("r", 3, 4, 2, D, lens, seed=91 + D, window=100)
+    out, lse = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                             case.context_lens, case.scale, case.window, rope_theta=theta)
+    for b, L in enumerate(lens):
+        start = L - case.window if 0 < case.window < L else 0
+        k, v = _contiguous_kv(case.k_cache, case.v_cache, case.block_tables[b], L, 16)
+        pos = np.arange(L)
+        kr = _rope_complex(k, pos, theta)                                 # [Hkv, L, D]
+        qr = _rope_complex(case.q[b].astype(np.float64), np.full(4, L - 1.0), theta)
+        for h in range(4):
+            s = case.scale * (kr[h // 2, start:] @ qr[h])
+            w = np.exp(s - s.max())
+            np.testing.assert_allclose(out[b, h], (w / w.sum()) @ v[h // 2, start:],
+                                       rtol=1e-11, atol=1e-12)
+            assert lse[b, h] == pytest.approx(s.max() + np.log(w.sum()), abs=1e-11)
+
+
+def test_rope_depends_only_on_relative_position():
+    """Shifting every position by the same amount leaves the scores unchanged:
+    move a context of 40 tokens so that it starts at token 1000 (fresh pages,
+    the first 1000 tokens outside a window of 40)."""
+    D, theta = 64, 10000.0
+    case = workloads.make_case("r", 1, 2, 1, D, [40], seed=95)
+    a = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                      case.context_lens, case.scale, 0, rope_theta=theta)
+    k, v = _contiguous_kv(case.k_cache, case.v_cache, case.block_tables[0], 40, 16)
+    L2 = 1040
+    npg = math.ceil(L2 / 16)
+    k2 = np.zeros((npg, 1, 16, D), dtype=np.float16)
+    v2 = np.zeros_like(k2)
+    for t in range(40):
+        k2[(1000 + t) // 16, 0, (1000 + t) % 16] = k[0, t].astype(np.float16)
+        v2[(1000 + t) // 16, 0, (1000 + t) % 16] = v[0, t].astype(np.float16)
+    bt2 = np.arange(npg, dtype=np.int32)[None, :]
+    b = oracle.decode(case.q, k2, v2, bt2, np.array([L2], np.int32), case.scale, 40,
+                      rope_theta=theta)
+    np.testing.assert_allclose(b[0], a[0], rtol=1e-9, atol=1e-10)
+    np.testing.assert_allclose(b[1], a[1], rtol=1e-10, atol=1e-10)
