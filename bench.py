@@ -201,7 +201,10 @@ class GpuArm:
         self.plan = pa.pa_plan(B, Hq, case.Hkv, D, case.page_size, case.num_pages,
                                case.max_pages_per_seq, case.max_context_len, case.window, ps, sms)
         self.plan.dtype = 1 if case.dtype == "bf16" else 0
+        self.plan.rope_theta = case.rope_theta
         self.planner_kernel = self.plan.kernel
+        if kernel is None and case.rope_theta > 0:
+            kernel = "simt"  # rotary embedding runs on the CUDA-core kernel
         if kernel:
             self.plan.kernel = KERNEL_IDS[kernel]
         self.out = torch.empty((B, Hq, D), dtype=self.q.dtype, device=device)
@@ -412,12 +415,14 @@ class OracleSampler:
                               k_cache=c.k_cache, v_cache=c.v_cache,
                               block_tables=c.block_tables[:1],
                               context_lens=c.context_lens[:1].copy(), scale=c.scale, window=L,
-                              partition_size=0, seed=c.seed, dtype=c.dtype)
+                              partition_size=0, seed=c.seed, dtype=c.dtype,
+                              rope_theta=c.rope_theta)
 
     def _run(self, L, threads):
         s = self._sub(L)
         self.oracle.decode(s.q, s.k_cache, s.v_cache, s.block_tables, s.context_lens, s.scale,
-                           s.window, num_threads=threads, dtype=s.dtype)
+                           s.window, num_threads=threads, dtype=s.dtype,
+                           rope_theta=s.rope_theta)
 
     def tokens_for(self, budget_s):
         par = min(self.threads, self.case.Hq)
@@ -546,9 +551,12 @@ def run_gpu(args):
         for name in workloads.WORKLOAD_ORDER + workloads.EXTRA_ORDER:
             c = case if name == args.workload else workloads.workload(name)
             b = kv_bytes(c)
-            entry = {"dtype": c.dtype, "head_dim": c.D}
+            entry = {"dtype": c.dtype, "head_dim": c.D, "rope_theta": c.rope_theta}
             simt_ok = c.dtype == "f16" and c.D in (64, 128, 256)
-            for kname in (("mma", "simt") if simt_ok else ("mma",)):
+            kernels = ("mma", "simt") if simt_ok else ("mma",)
+            if c.rope_theta > 0:
+                kernels = ("simt",)
+            for kname in kernels:
                 us, kus, copies, l2state, plan = time_graph_rotating(c, device, kname)
                 entry[kname] = {"us_per_step": us, "partition_kernel_us": kus,
                                 "kv_gbs": b / (us * 1e-6) / 1e9,

@@ -99,7 +99,11 @@ typedef struct pa_plan {
                                library leaves them zero after every call */
     int dtype;              /* PA_DTYPE_*: element type of q, k_cache, v_cache and out
                                (pa_plan sets fp16; a caller may set bf16) */
-    int reserved[3];
+    float rope_theta;       /* > 0: rotary embedding inside the kernel (rotate-half
+                               pairing of dim i and i + D/2, frequency
+                               rope_theta^(-2i/D); q at position L - 1, K_t at t, V
+                               untouched), CUDA-core kernel and fp16 only; 0 = none */
+    int reserved[2];
 } pa_plan_t;
 
 /* Element types (pa_plan_t.dtype).  bf16 needs the tensor-core kernel. */

@@ -55,7 +55,8 @@ class pa_plan_t(ctypes.Structure):
         ("merge_in_kernel", ctypes.c_int),
         ("ctrl_bytes", ctypes.c_int),
         ("dtype", ctypes.c_int),
-        ("reserved", ctypes.c_int * 3),
+        ("rope_theta", ctypes.c_float),
+        ("reserved", ctypes.c_int * 2),
     ]
 
     def as_dict(self):

@@ -433,6 +433,11 @@ static int check_plan(const pa_plan_t* plan) {
         plan->head_dim != 256)
         return PA_ERR_UNSUPPORTED;
     if (plan->dtype != PA_DTYPE_F16 && plan->dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+    if (!(plan->rope_theta >= 0.f) || plan->rope_theta == INFINITY) return PA_ERR_INVALID_ARG;
+    // Rotary embedding runs on the CUDA-core kernel, which keeps the rotated
+    // q and K in fp32 (rounding them to fp16/bf16 for the tensor cores would
+    // cost more than the LSE tolerance allows).
+    if (plan->rope_theta > 0.f && plan->kernel != PA_KERNEL_SIMT) return PA_ERR_UNSUPPORTED;
     // The CUDA-core kernel is built for fp16 and head dims 64/128/256.
     if (plan->kernel == PA_KERNEL_SIMT && (plan->dtype != PA_DTYPE_F16 || plan->head_dim == 96))
         return PA_ERR_UNSUPPORTED;
@@ -506,6 +511,16 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     p.nchunk = p.g / plan->heads_per_cta;
     p.heads_per_cta = plan->heads_per_cta;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.rope = plan->rope_theta > 0.f ? 1 : 0;
+    if (p.rope) {
+        // theta_i / (2 pi) in double, split into two floats.
+        for (int i = 0; i < D / 2; ++i) {
+            const double turn = pow((double)plan->rope_theta, -2.0 * i / D) / (2.0 * M_PI);
+            const float hi = (float)turn;
+            p.rope_phi[0][i] = hi;
+            p.rope_phi[1][i] = (float)(turn - (double)hi);
+        }
+    }
     cudaError_t e;
     if (plan->kernel == PA_KERNEL_MMA) {
         // K, V (64-column boxes), then K, V tails (32-column boxes, D = 96).

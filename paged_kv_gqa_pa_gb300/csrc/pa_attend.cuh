@@ -57,17 +57,53 @@ __device__ __forceinline__ void half8_to_float(const uint4 raw, float (&f)[8]) {
     }
 }
 
+// Rotary state of a lane: cos/sin of its 8 frequencies at the position of
+// the next token it scores, and the one-token step.  The lane's dims are
+// [8r, 8r + 8) of the row; the lane r ^ (R/2) holds the partner dims
+// (i <-> i + D/2 of the rotate-half pairing).
+struct RopeLane {
+    float c[8], s[8], c1[8], s1[8];
+};
+
+// Rotate this lane's 8 K values (kf) with its partner's (pf) and advance the
+// rotary state by one position.
+__device__ __forceinline__ void rope_apply_and_step(float (&kf)[8], const float (&pf)[8],
+                                                    bool low, RopeLane& rl) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float c = rl.c[j], s = rl.s[j];
+        kf[j] = low ? fmaf(kf[j], c, -pf[j] * s) : fmaf(kf[j], c, pf[j] * s);
+        const float cn = fmaf(c, rl.c1[j], -s * rl.s1[j]);
+        const float sn = fmaf(s, rl.c1[j], c * rl.s1[j]);
+        rl.c[j] = cn;
+        rl.s[j] = sn;
+    }
+}
+
 // Partial dot products of the G heads with token `tok` of the K page (this
 // lane's 8 dims), combined across the 2^LEVEL tokens tok .. tok + 2^LEVEL - 1
 // by a shuffle reduce-scatter: the exchange over lane mask (1 << LEVEL) pairs
 // token bit LEVEL-1, and a lane keeps the token whose bit equals its lane bit.
+// Tokens are visited in increasing order, which the rotary recurrence relies on.
 template <int D, int G, int LEVEL>
 __device__ __forceinline__ void qk_tree(float (&res)[G], const unsigned char* kpage, int tok,
-                                        int r, int lane, const float (&qf)[G][8]) {
+                                        int r, int lane, const float (&qf)[G][8], bool rope,
+                                        RopeLane& rl) {
     if constexpr (LEVEL == 0) {
         const uint4 raw = *reinterpret_cast<const uint4*>(kpage + tok * (D * 2) + r * 16);
         float kf[8];
         half8_to_float(raw, kf);
+        if (rope) {  // warp-uniform
+            constexpr int kHalf = D / 16;  // lanes per half row
+            uint4 praw;
+            praw.x = __shfl_xor_sync(0xffffffffu, raw.x, kHalf);
+            praw.y = __shfl_xor_sync(0xffffffffu, raw.y, kHalf);
+            praw.z = __shfl_xor_sync(0xffffffffu, raw.z, kHalf);
+            praw.w = __shfl_xor_sync(0xffffffffu, raw.w, kHalf);
+            float pf[8];
+            half8_to_float(praw, pf);
+            rope_apply_and_step(kf, pf, (r & kHalf) == 0, rl);
+        }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             float a = qf[h][0] * kf[0];
@@ -77,8 +113,8 @@ __device__ __forceinline__ void qk_tree(float (&res)[G], const unsigned char* kp
         }
     } else {
         float lo[G], hi[G];
-        qk_tree<D, G, LEVEL - 1>(lo, kpage, tok, r, lane, qf);
-        qk_tree<D, G, LEVEL - 1>(hi, kpage, tok + (1 << (LEVEL - 1)), r, lane, qf);
+        qk_tree<D, G, LEVEL - 1>(lo, kpage, tok, r, lane, qf, rope, rl);
+        qk_tree<D, G, LEVEL - 1>(hi, kpage, tok + (1 << (LEVEL - 1)), r, lane, qf, rope, rl);
         constexpr int kMask = 1 << LEVEL;
         const bool up = (lane & kMask) != 0;
 #pragma unroll
@@ -208,6 +244,30 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
             *reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.Hq + h0 + h) * D + r * 8);
         half8_to_float(raw, qf[h]);
     }
+    // Rotary embedding: q to position L - 1; the K rows follow per token.
+    const bool rope = p.rope != 0;
+    const bool rope_low = (r & (D / 16)) == 0;
+    const int rope_f0 = (r & (D / 16 - 1)) * 8;  // this lane's first frequency
+    RopeLane rl;
+    if (rope) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            rope_twiddle(1, p.rope_phi[0][rope_f0 + j], p.rope_phi[1][rope_f0 + j], rl.c1[j],
+                         rl.s1[j]);
+            rope_twiddle(sp.L - 1, p.rope_phi[0][rope_f0 + j], p.rope_phi[1][rope_f0 + j],
+                         rl.c[j], rl.s[j]);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float pq[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) pq[j] = __shfl_xor_sync(0xffffffffu, qf[h][j], D / 16);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                qf[h][j] = rope_low ? fmaf(qf[h][j], rl.c[j], -pq[j] * rl.s[j])
+                                    : fmaf(qf[h][j], rl.c[j], pq[j] * rl.s[j]);
+        }
+    }
 
     float o[G][8];
     float m[G], lsum[G];
@@ -235,8 +295,18 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
             }
             consumed = item + 1;
         }
+        if (rope) {
+            // Rotary state at this lane's first token of the page, computed
+            // afresh each page; the tokens after it step by recurrence.
+            const int pos0 = (pg0 + warp + k * kWarps) * kPageSize + rg * TL;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                rope_twiddle(pos0, p.rope_phi[0][rope_f0 + j], p.rope_phi[1][rope_f0 + j],
+                             rl.c[j], rl.s[j]);
+        }
         float s[G];
-        qk_tree<D, G, LN::LOG_TL>(s, ring_wp + ((2 * k) % NS) * PB, rg * TL, r, lane, qf);
+        qk_tree<D, G, LN::LOG_TL>(s, ring_wp + ((2 * k) % NS) * PB, rg * TL, r, lane, qf, rope,
+                                  rl);
 #pragma unroll
         for (int h = 0; h < G; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], 1);
         __syncwarp();

@@ -18,6 +18,7 @@ constexpr int kMaxPagesPerPart = 256;  // page ids a CTA stages in shared memory
 constexpr int kMaxPartitions = 4096;   // partitions the merge kernel reduces
 constexpr int kMaxHeadsPerCta = 8;
 constexpr int kCtrlBytes = 256;        // workspace control block (device error word)
+constexpr int kMaxRopePairs = 128;     // head_dim / 2 of the widest rotary head
 
 // Bounded waits: a bulk copy that has not landed after this long is reported
 // as PA_DEVERR_TIMEOUT instead of hanging the GPU.
@@ -44,6 +45,11 @@ struct AttendParams {
     int heads_per_cta;      // G: query heads one CTA serves
     int parts_per_cta;      // consecutive partitions one CTA streams (tensor-core kernel)
     float scale_log2;       // scale * log2(e)
+    int rope;               // 1: rotary embedding of q and K (CUDA-core kernel)
+    // Rotary frequency i as a fraction of a turn, theta_i / (2 pi), split into
+    // two floats (rope_phi[0][i] + rope_phi[1][i]) so that pos * theta_i
+    // reduces modulo one turn with fp32 accuracy for any position below 2^24.
+    float rope_phi[2][kMaxRopePairs];
 };
 
 struct MergeParams {
@@ -168,6 +174,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
         if (mbar_try_wait(bar, parity)) return true;
         if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
+}
+
+// cos and sin of pos * theta_i for a rotary frequency given as a fraction of a
+// turn split into phi1 + phi2: the product is reduced modulo one turn exactly
+// (fma recovers the rounding error of pos * phi1), then sincospif evaluates
+// the reduced angle.  Accurate to a few fp32 ulps for pos < 2^24.
+__device__ __forceinline__ void rope_twiddle(int pos, float phi1, float phi2, float& c,
+                                             float& s) {
+    const float pf = (float)pos;
+    const float hi = pf * phi1;
+    const float err = fmaf(pf, phi1, -hi);
+    float fr = hi - floorf(hi);
+    fr += err + pf * phi2;
+    fr -= floorf(fr);
+    sincospif(2.f * fr, &s, &c);
 }
 
 // 2^x with the MUFU approximation (relative error ~2^-22); -inf -> +0.

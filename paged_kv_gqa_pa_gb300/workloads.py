@@ -44,6 +44,7 @@ class Case:
     partition_size: int  # 0 = let the planner choose
     seed: int
     dtype: str = "f16"
+    rope_theta: float = 0.0  # > 0: rotary embedding inside the kernel
 
     @property
     def B(self):
@@ -120,7 +121,7 @@ def make_case(name: str, B: int, Hq: int, Hkv: int, D: int, context_lens, seed: 
               partition_size: int = 0, page_size: int = PAGE_SIZE,
               pool_pages: int | None = None, slack: float = 0.25,
               max_pages_per_seq: int | None = None, nan_slack: bool = True,
-              dtype: str = "f16") -> Case:
+              dtype: str = "f16", rope_theta: float = 0.0) -> Case:
     lens = np.asarray(context_lens, dtype=np.int64).reshape(B)
     need = [math.ceil(int(L) / page_size) for L in lens]
     total = int(sum(need))
@@ -155,7 +156,8 @@ def make_case(name: str, B: int, Hq: int, Hkv: int, D: int, context_lens, seed: 
         scale = 1.0 / math.sqrt(D)
     return Case(name=name, q=q, k_cache=k, v_cache=v, block_tables=bt,
                 context_lens=lens.astype(np.int32), scale=float(scale), window=int(window),
-                partition_size=int(partition_size), seed=int(seed), dtype=dtype)
+                partition_size=int(partition_size), seed=int(seed), dtype=dtype,
+                rope_theta=float(rope_theta))
 
 
 def _ragged_lengths(B: int, lo: int, hi: int, seed: int, not_multiple_of: int) -> np.ndarray:
@@ -181,12 +183,15 @@ WORKLOADS = {
 WORKLOAD_ORDER = list(WORKLOADS)
 
 # Further measured workloads for the widened paths: a bf16 cache at the
-# long-context shapes, and head_dim 96 (GQA-4, 32K tokens).  Only the
-# tensor-core kernel serves them.
+# long-context shapes and head_dim 96 (tensor-core kernel only), and a rotary
+# embedding applied inside the kernel (CUDA-core kernel only).
 EXTRA_WORKLOADS = {
     "gqa6_ctx100k_bf16": dict(B=4, Hq=24, Hkv=4, D=256, lens=[100000] * 4, seed=1006,
                               partition_size=512, dtype="bf16"),
     "gqa4_d96_ctx32k": dict(B=4, Hq=32, Hkv=8, D=96, lens=[32768] * 4, seed=1007),
+    # Rotary embedding inside the kernel (Llama-3 frequency base), fp16, D 128.
+    "gqa4_rope_ctx32k": dict(B=4, Hq=32, Hkv=8, D=128, lens=[32768] * 4, seed=1008,
+                             rope_theta=500000.0),
 }
 EXTRA_ORDER = list(EXTRA_WORKLOADS)
 ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}

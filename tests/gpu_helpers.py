@@ -68,6 +68,7 @@ def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=N
     if KERNEL is not None:
         plan.kernel = KERNELS[KERNEL]
     plan.dtype = 1 if case.dtype == "bf16" else 0
+    plan.rope_theta = case.rope_theta
     if parts_per_cta is not None:
         plan.parts_per_cta = parts_per_cta
     if merge_in_kernel is not None:
@@ -114,7 +115,8 @@ def rel_l2(a, b):
 def assert_matches_oracle(case, out, lse, ref=None, what=""):
     if ref is None:
         ref = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
-                            case.context_lens, case.scale, case.window, dtype=case.dtype)
+                            case.context_lens, case.scale, case.window, dtype=case.dtype,
+                            rope_theta=case.rope_theta)
     ref_out, ref_lse = ref
     assert not np.isnan(out).any(), f"{what}: NaN in output"
     err = rel_l2(out, ref_out)

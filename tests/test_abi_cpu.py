@@ -51,7 +51,7 @@ def test_plan_struct_layout_matches_header():
     text = open(os.path.join(ROOT, "include", "pa.h")).read()
     body = re.search(r"typedef struct pa_plan \{(.*?)\} pa_plan_t;", text, flags=re.S).group(1)
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
-    fields = re.findall(r"\b(?:int|size_t)\s+([a-z_]+)(?:\[\d+\])?\s*;", body)
+    fields = re.findall(r"\b(?:int|size_t|float)\s+([a-z_]+)(?:\[\d+\])?\s*;", body)
     assert fields == [f for f, _ in binding.pa_plan_t._fields_]
     # 14 ints, a size_t, the kernel id, partitions per CTA, 6 reserved ints.
     assert binding.pa_plan_t.workspace_bytes.offset == 56
@@ -157,6 +157,13 @@ def test_decode_argument_checks_return_before_launch():
     assert p96.kernel == binding.PA_KERNEL_MMA
     p96.kernel = binding.PA_KERNEL_SIMT
     assert _call_decode(p96) == binding.PA_ERR_UNSUPPORTED
+    # Rotary embedding needs the CUDA-core kernel; a negative base is invalid.
+    rope_mma = binding.pa_plan_t.from_buffer_copy(plan)
+    rope_mma.rope_theta = 10000.0
+    assert _call_decode(rope_mma) == binding.PA_ERR_UNSUPPORTED
+    rope_neg = binding.pa_plan_t.from_buffer_copy(plan)
+    rope_neg.rope_theta = -1.0
+    assert _call_decode(rope_neg) == binding.PA_ERR_INVALID_ARG
     bad_dtype = binding.pa_plan_t.from_buffer_copy(plan)
     bad_dtype.dtype = 7
     assert _call_decode(bad_dtype) == binding.PA_ERR_INVALID_ARG

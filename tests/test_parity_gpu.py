@@ -32,6 +32,8 @@ def test_workload_full_size(name):
     case = workloads.workload(name)
     if gpu_helpers.KERNEL == "simt" and (case.dtype != "f16" or case.D == 96):
         pytest.skip("the CUDA-core kernel is built for fp16 and head dims 64/128/256")
+    if gpu_helpers.KERNEL == "mma" and case.rope_theta > 0:
+        pytest.skip("rotary embedding runs on the CUDA-core kernel")
     out, lse, err, plan = run_gpu(case)
     assert err == 0
     rel = assert_matches_oracle(case, out, lse, what=name)
@@ -321,3 +323,23 @@ def test_wider_paths_window_ragged_and_invariants(dtype, D):
             row = one.v_cache[page, h // 4, 0]
             vals = (row.astype(np.uint32) << 16).view(np.float32) if dtype == "bf16" else row
             assert np.array_equal(out[b, h], vals.astype(np.float64))
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("theta", [10000.0, 500000.0])
+def test_rotary_embedding_in_kernel(D, theta):
+    if gpu_helpers.KERNEL == "mma":
+        pytest.skip("rotary embedding runs on the CUDA-core kernel")
+    case = workloads.make_case("rope", len(LENS), 8, 2, D, LENS, seed=800 + D, q_std=2.0,
+                               rope_theta=theta)
+    for S in (0, 64, 4096):
+        case.partition_size = S
+        out, lse, err, _ = run_gpu(case, guard=64)
+        assert err == 0
+        assert_matches_oracle(case, out, lse, what=f"rope D{D} S{S}")
+    # with a window, and positions past 2^16
+    wcase = workloads.make_case("ropew", 2, 6, 2, D, [70000, 999], seed=801 + D, window=3000,
+                                rope_theta=theta)
+    out, lse, err, _ = run_gpu(wcase)
+    assert err == 0
+    assert_matches_oracle(wcase, out, lse, what=f"rope window D{D}")
