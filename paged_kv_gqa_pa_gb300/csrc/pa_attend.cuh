@@ -147,7 +147,7 @@ __device__ __forceinline__ void write_rows(const AttendParams& p, int b, int h0,
     }
 }
 
-template <int D, int G, bool SPLIT>
+template <int D, int G, bool SPLIT, bool ROPE>
 __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBlocks))
     attend_kernel(const AttendParams p) {
     using Cfg = AttendCfg<D>;
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
         half8_to_float(raw, qf[h]);
     }
     // Rotary embedding: q to position L - 1; the K rows follow per token.
-    const bool rope = p.rope != 0;
+    constexpr bool rope = ROPE;  // rotary instances are separate, so the plain ones pay nothing
     const bool rope_low = (r & (D / 16)) == 0;
     const int rope_f0 = (r & (D / 16 - 1)) * 8;  // this lane's first frequency
     RopeLane rl;
@@ -498,11 +498,13 @@ template <int D>
 cudaError_t launch_attend_d(int G, bool split, const AttendParams& p, dim3 grid,
                             cudaStream_t stream) {
     const void* fn = nullptr;
+    const bool rope = p.rope != 0;
     switch (G) {
-#define PA_ATTEND_CASE(GG)                                                    \
-    case GG:                                                                  \
-        fn = split ? reinterpret_cast<const void*>(&attend_kernel<D, GG, true>) \
-                   : reinterpret_cast<const void*>(&attend_kernel<D, GG, false>); \
+#define PA_ATTEND_PICK(GG, S, R) reinterpret_cast<const void*>(&attend_kernel<D, GG, S, R>)
+#define PA_ATTEND_CASE(GG)                                                                   \
+    case GG:                                                                                 \
+        fn = split ? (rope ? PA_ATTEND_PICK(GG, true, true) : PA_ATTEND_PICK(GG, true, false)) \
+                   : (rope ? PA_ATTEND_PICK(GG, false, true) : PA_ATTEND_PICK(GG, false, false)); \
         break;
         PA_ATTEND_CASE(1)
         PA_ATTEND_CASE(2)
@@ -513,6 +515,7 @@ cudaError_t launch_attend_d(int G, bool split, const AttendParams& p, dim3 grid,
         PA_ATTEND_CASE(7)
         PA_ATTEND_CASE(8)
 #undef PA_ATTEND_CASE
+#undef PA_ATTEND_PICK
         default:
             return cudaErrorInvalidValue;
     }
@@ -521,7 +524,7 @@ cudaError_t launch_attend_d(int G, bool split, const AttendParams& p, dim3 grid,
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const uint32_t bit = 1u << ((G - 1) * 2 + (split ? 1 : 0));
+    const uint32_t bit = 1u << ((G - 1) * 4 + (split ? 2 : 0) + (rope ? 1 : 0));
     if (dev < 0 || dev >= kMaxDevices || !(configured[dev].load() & bit)) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  AttendCfg<D>::kSmemBytes);
