@@ -76,16 +76,16 @@ def _load():
     return _lib
 
 
-DTYPES = {"f16": 0, "bf16": 1}
+DTYPES = {"f16": 0, "bf16": 1, "f32": 2}
 
 
 def _as_bits(a: np.ndarray) -> np.ndarray:
     a = np.ascontiguousarray(a)
     if a.dtype == np.float16:
         return a.view(np.uint16)
-    if a.dtype == np.uint16:
+    if a.dtype in (np.uint16, np.float32):
         return a
-    raise TypeError(f"expected float16 (or its uint16 bits), got {a.dtype}")
+    raise TypeError(f"expected float16, bf16 bits (uint16) or float32, got {a.dtype}")
 
 
 def _ptr(a: np.ndarray):
@@ -100,7 +100,7 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
            window: int = 0, num_threads: int = 0, dtype: str = "f16", rope_theta: float = 0.0):
     """fp64 decode attention over a paged KV cache.
 
-    q            float16 [B, Hq, D] (or the uint16 bits of bf16 when dtype="bf16")
+    q            float16 [B, Hq, D] (uint16 bf16 bits when dtype="bf16", float32 for "f32")
     k_cache      [num_pages, Hkv, page_size, D] of the same type; v_cache the same
     block_tables int32   [B, max_pages_per_seq]
     context_lens int32   [B]

@@ -42,8 +42,8 @@
  *     x'_{i+D/2} = x_{i+D/2} cos(pos theta_i) + x_i sin(pos theta_i)
  * V is not rotated.
  *
- * Arithmetic: every fp16 (or bf16) value is converted exactly to double (both
- * binary16 -> binary64 and bfloat16 -> binary64 are exact), all sums and
+ * Arithmetic: every fp16, bf16 or fp32 value is converted exactly to double
+ * (binary16, bfloat16 and binary32 all embed exactly in binary64), all sums and
  * exponentials are in double.  `scale` is taken as a double.  No blocking,
  * reordering or fusion beyond the definition.
  *
@@ -104,6 +104,13 @@ double pa_oracle_bf16_to_double(uint16_t h) { return bf16_bits_to_double(h); }
 
 typedef double (*to_double_fn)(uint16_t);
 
+/* Element e of an array of the given type, exactly as a double. */
+static double elem(const void* base, size_t e, int dtype) {
+    if (dtype == 2) return (double)((const float*)base)[e];
+    const uint16_t bits = ((const uint16_t*)base)[e];
+    return dtype == 1 ? bf16_bits_to_double(bits) : half_bits_to_double(bits);
+}
+
 /* Rotate x[0..D) in place to position pos (rotate-half pairing). */
 static void rope_rotate(double* x, int D, double theta, double pos) {
     const int half = D / 2;
@@ -117,7 +124,7 @@ static void rope_rotate(double* x, int D, double theta, double pos) {
 }
 
 /*
- * q            [B, Hq, D]                    binary16 (or bfloat16) bits
+ * q            [B, Hq, D]                    binary16, bfloat16 or binary32
  * k_cache      [num_pages, Hkv, page_size, D] same element type
  * v_cache      same as k_cache
  * block_tables [B, max_pages_per_seq]         int32 physical page ids
@@ -125,21 +132,20 @@ static void rope_rotate(double* x, int D, double theta, double pos) {
  * out          [B, Hq, D]  double (written)
  * lse          [B, Hq]     double (written)
  * num_threads  OpenMP threads over (b, h); <= 0 means the runtime default.
- * dtype        element type of q, k_cache, v_cache: 0 = fp16, 1 = bf16.
+ * dtype        element type of q, k_cache, v_cache: 0 = fp16, 1 = bf16, 2 = fp32.
  * rope_theta   > 0: rotary embedding of q and K as above; 0: none.
  * Returns 0, or a PA_ORACLE_* code (a page id outside [0, num_pages) or a
  * context longer than the table are reported, never read).
  */
 int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages,
-                     int max_pages_per_seq, const uint16_t* q, const uint16_t* k_cache,
-                     const uint16_t* v_cache, const int32_t* block_tables,
+                     int max_pages_per_seq, const void* q, const void* k_cache,
+                     const void* v_cache, const int32_t* block_tables,
                      const int32_t* context_lens, double scale, int window, double* out,
                      double* lse, int num_threads, int dtype, double rope_theta) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || page_size <= 0 ||
-        num_pages < 0 || max_pages_per_seq < 0 || (dtype != 0 && dtype != 1) ||
+        num_pages < 0 || max_pages_per_seq < 0 || dtype < 0 || dtype > 2 ||
         (rope_theta > 0 && D % 2 != 0))
         return PA_ORACLE_BAD_ARG;
-    const to_double_fn cvt = dtype ? bf16_bits_to_double : half_bits_to_double;
     const int g = Hq / Hkv;
     int status = PA_ORACLE_OK;
 
@@ -180,8 +186,8 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
             status = PA_ORACLE_NO_MEM;
             continue;
         }
-        const uint16_t* qrow = q + ((size_t)b * Hq + h) * D;
-        for (int d = 0; d < D; ++d) qd[d] = cvt(qrow[d]);
+        const size_t qrow = ((size_t)b * Hq + h) * D;
+        for (int d = 0; d < D; ++d) qd[d] = elem(q, qrow + d, dtype);
         if (rope_theta > 0) rope_rotate(qd, D, rope_theta, (double)(L - 1));
 
         int bad = 0;
@@ -192,9 +198,8 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
                 bad = 1;
                 break;
             }
-            const uint16_t* krow =
-                k_cache + (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
-            for (int d = 0; d < D; ++d) kd[d] = cvt(krow[d]);
+            const size_t krow = (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
+            for (int d = 0; d < D; ++d) kd[d] = elem(k_cache, krow + d, dtype);
             if (rope_theta > 0) rope_rotate(kd, D, rope_theta, (double)t);
             double dot = 0.0;
             for (int d = 0; d < D; ++d) dot += qd[d] * kd[d];
@@ -220,10 +225,9 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
         /* Step 4: softmax-weighted sum of the gathered V rows. */
         for (int t = start; t < L; ++t) {
             const int page = block_tables[(size_t)b * max_pages_per_seq + t / page_size];
-            const uint16_t* vrow =
-                v_cache + (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
+            const size_t vrow = (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
             const double w = exp(s[t - start] - l);
-            for (int d = 0; d < D; ++d) o[d] += w * cvt(vrow[d]);
+            for (int d = 0; d < D; ++d) o[d] += w * elem(v_cache, vrow + d, dtype);
         }
         free(s);
         free(qd);
@@ -237,26 +241,24 @@ int pa_oracle_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages
  * identity against an independent library routine.  Returns the number of
  * scores written to s_out (capacity cap), or -1 on a bad page / argument. */
 int pa_oracle_scores(int Hq, int Hkv, int D, int page_size, int num_pages, int max_pages_per_seq,
-                     const uint16_t* q, const uint16_t* k_cache, const int32_t* block_tables,
+                     const void* q, const void* k_cache, const int32_t* block_tables,
                      const int32_t* context_lens, double scale, int window, int b, int h,
                      double* s_out, int cap, int dtype, double rope_theta) {
-    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (dtype != 0 && dtype != 1) || D > 1024) return -1;
-    const to_double_fn cvt = dtype ? bf16_bits_to_double : half_bits_to_double;
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || dtype < 0 || dtype > 2 || D > 1024) return -1;
     const int kvh = h / (Hq / Hkv);
     const int L = context_lens[b];
     if (L < 0 || (long)L > (long)max_pages_per_seq * page_size) return -1;
     const int start = (window > 0 && window < L) ? L - window : 0;
     if (L - start > cap) return -1;
-    const uint16_t* qrow = q + ((size_t)b * Hq + h) * D;
+    const size_t qrow = ((size_t)b * Hq + h) * D;
     double qd[1024], kd[1024];
-    for (int d = 0; d < D; ++d) qd[d] = cvt(qrow[d]);
+    for (int d = 0; d < D; ++d) qd[d] = elem(q, qrow + d, dtype);
     if (rope_theta > 0) rope_rotate(qd, D, rope_theta, (double)(L - 1));
     for (int t = start; t < L; ++t) {
         const int page = block_tables[(size_t)b * max_pages_per_seq + t / page_size];
         if (page < 0 || page >= num_pages) return -1;
-        const uint16_t* krow =
-            k_cache + (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
-        for (int d = 0; d < D; ++d) kd[d] = cvt(krow[d]);
+        const size_t krow = (((size_t)page * Hkv + kvh) * page_size + (t % page_size)) * D;
+        for (int d = 0; d < D; ++d) kd[d] = elem(k_cache, krow + d, dtype);
         if (rope_theta > 0) rope_rotate(kd, D, rope_theta, (double)t);
         double dot = 0.0;
         for (int d = 0; d < D; ++d) dot += qd[d] * kd[d];

@@ -31,8 +31,9 @@ PAGE_SIZE = 16
 
 @dataclasses.dataclass
 class Case:
-    """One decode problem.  With dtype "bf16", q/k_cache/v_cache hold the
-    uint16 bit patterns of bfloat16 values (numpy has no bfloat16)."""
+    """One decode problem.  dtype "f16" and "f32" arrays hold the values;
+    with "bf16", q/k_cache/v_cache hold the uint16 bit patterns of bfloat16
+    values (numpy has no bfloat16)."""
     name: str
     q: np.ndarray
     k_cache: np.ndarray
@@ -93,7 +94,8 @@ def _fill_normal(out16: np.ndarray, seed_seq: np.random.SeedSequence, std: float
     """Fill a flat 16-bit array with std*N(0,1), drawn in fixed-size chunks, each
     chunk from its own child generator (deterministic for a given seed and size,
     independent of the number of worker threads).  A float16 array gets the
-    values rounded to fp16; a uint16 array gets bfloat16 bit patterns."""
+    values rounded to fp16, a float32 array the draws themselves, a uint16
+    array bfloat16 bit patterns."""
     flat = out16.reshape(-1)
     n = flat.size
     nchunks = max(1, math.ceil(n / chunk))
@@ -106,7 +108,12 @@ def _fill_normal(out16: np.ndarray, seed_seq: np.random.SeedSequence, std: float
         x = g.standard_normal(hi - lo, dtype=np.float32)
         if std != 1.0:
             x *= np.float32(std)
-        flat[lo:hi] = x.astype(np.float16) if flat.dtype == np.float16 else to_bf16_bits(x)
+        if flat.dtype == np.float16:
+            flat[lo:hi] = x.astype(np.float16)
+        elif flat.dtype == np.float32:
+            flat[lo:hi] = x
+        else:
+            flat[lo:hi] = to_bf16_bits(x)
 
     if nchunks == 1:
         work(0)
@@ -133,7 +140,7 @@ def make_case(name: str, B: int, Hq: int, Hkv: int, D: int, context_lens, seed: 
     ss = np.random.SeedSequence(seed)
     s_q, s_k, s_v, s_perm = ss.spawn(4)
 
-    et = np.float16 if dtype == "f16" else np.uint16
+    et = {"f16": np.float16, "bf16": np.uint16, "f32": np.float32}[dtype]
     q = np.empty((B, Hq, D), dtype=et)
     _fill_normal(q, s_q, q_std)
     k = np.empty((pool_pages, Hkv, page_size, D), dtype=et)
@@ -149,7 +156,7 @@ def make_case(name: str, B: int, Hq: int, Hkv: int, D: int, context_lens, seed: 
         off += need[b]
     if nan_slack and off < pool_pages:
         slack_ids = perm[off:]
-        nan = np.float16(np.nan) if dtype == "f16" else BF16_NAN
+        nan = {"f16": np.float16(np.nan), "bf16": BF16_NAN, "f32": np.float32(np.nan)}[dtype]
         k[slack_ids] = nan
         v[slack_ids] = nan
     if scale is None:

@@ -17,6 +17,8 @@ MUTATIONS = {
     "dropped_scale": ("s[t - start] = scale * dot;", "s[t - start] = dot;"),
     "wrong_slot": ("+ (t % page_size)) * D;\n            for (int d = 0; d < D; ++d) kd[d]",
                    "+ ((t + 1) % page_size)) * D;\n            for (int d = 0; d < D; ++d) kd[d]"),
+    "f32_as_bf16": ("if (dtype == 2) return (double)((const float*)base)[e];",
+                    "if (dtype == 2) return bf16_bits_to_double(((const uint16_t*)base)[e]);"),
     "window_off_by_one": ("const int start = (window > 0 && window < L) ? L - window : 0;\n"
                           "        const int n",
                           "const int start = (window > 0 && window < L) ? L - window + 1 : 0;\n"
@@ -24,7 +26,8 @@ MUTATIONS = {
     "base2_lse": ("const double l = M + log(Z);", "const double l = M + log2(Z);"),
     "unnormalised_weights": ("const double w = exp(s[t - start] - l);",
                              "const double w = exp(s[t - start] - M);"),
-    "k_in_place_of_v": ("v_cache + (((size_t)page", "k_cache + (((size_t)page"),
+    "k_in_place_of_v": ("o[d] += w * elem(v_cache, vrow + d, dtype);",
+                        "o[d] += w * elem(k_cache, vrow + d, dtype);"),
     "half_exponent_bias": ("ldexp((double)(1024 + m), e - 25)", "ldexp((double)(1024 + m), e - 24)"),
     "bf16_exponent_bias": ("ldexp((double)(128 + m), e - 134)", "ldexp((double)(128 + m), e - 133)"),
     "rope_sign": ("x[i] = a * c - b * sn;", "x[i] = a * c + b * sn;"),
@@ -41,6 +44,7 @@ def _checks():
     yield lambda: pins.test_window_equals_truncated_context(17)
     yield lambda: pins.test_bf16_inputs_match_dense_textbook_attention(*pins.SMALL[2])
     yield lambda: pins.test_rope_matches_complex_rotation_reference(64, 10000.0)
+    yield lambda: pins.test_fp32_inputs_match_dense_textbook_attention(*pins.SMALL[2])
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))

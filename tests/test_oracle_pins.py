@@ -22,8 +22,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 def values(a, dtype="f16"):
-    """Element values as float64, independently of the oracle: fp16 through
-    numpy, bf16 bit patterns as the upper half of a float32."""
+    """Element values as float64, independently of the oracle: fp16 and fp32
+    through numpy, bf16 bit patterns as the upper half of a float32."""
     if dtype == "bf16":
         return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
     return a.astype(np.float64)
@@ -101,6 +101,18 @@ def test_bf16_inputs_match_dense_textbook_attention(B, Hq, Hkv, D, lens, window)
                                q_std=2.0, dtype="bf16")
     out, lse = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
                              case.context_lens, case.scale, window, dtype="bf16")
+    ref_out, ref_lse = _dense_reference(case, window)
+    np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,lens,window", [SMALL[2], SMALL[4], SMALL[6]])
+def test_fp32_inputs_match_dense_textbook_attention(B, Hq, Hkv, D, lens, window):
+    case = workloads.make_case("t", B, Hq, Hkv, D, lens, seed=99 + D, window=window,
+                               q_std=2.0, dtype="f32")
+    assert case.q.dtype == np.float32
+    out, lse = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                             case.context_lens, case.scale, window, dtype="f32")
     ref_out, ref_lse = _dense_reference(case, window)
     np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(lse, ref_lse, rtol=1e-13, atol=1e-13)
