@@ -54,6 +54,7 @@ NCU_TRAFFIC = {
 KERNEL_SOURCES = {
     "mma": ("pa_attend_mma.cuh", "pa_attend_mma_f16.cu", "pa_attend_mma_bf16.cu", "pa_common.cuh"),
     "simt": ("pa_attend.cuh", "pa_attend_d64.cu", "pa_attend_d128.cu", "pa_attend_d256.cu",
+             "pa_attend_f32_d64.cu", "pa_attend_f32_d128.cu", "pa_attend_f32_d256.cu",
              "pa_common.cuh"),
 }
 
@@ -189,7 +190,7 @@ class GpuArm:
         self.device = device
         def elems(a):
             t = torch.from_numpy(a)
-            return t.view(torch.bfloat16) if case.dtype == "bf16" else t
+            return t.view(torch.bfloat16) if case.dtype == "bf16" else t  # f16/f32 as is
         self.q = elems(case.q).to(device)
         self.k = elems(case.k_cache).to(device)
         self.v = elems(case.v_cache).to(device)
@@ -200,11 +201,11 @@ class GpuArm:
         ps = case.partition_size if partition_size is None else partition_size
         self.plan = pa.pa_plan(B, Hq, case.Hkv, D, case.page_size, case.num_pages,
                                case.max_pages_per_seq, case.max_context_len, case.window, ps, sms)
-        self.plan.dtype = 1 if case.dtype == "bf16" else 0
+        self.plan.dtype = {"f16": 0, "bf16": 1, "f32": 2}[case.dtype]
         self.plan.rope_theta = case.rope_theta
         self.planner_kernel = self.plan.kernel
-        if kernel is None and case.rope_theta > 0:
-            kernel = "simt"  # rotary embedding runs on the CUDA-core kernel
+        if kernel is None and (case.rope_theta > 0 or case.dtype == "f32"):
+            kernel = "simt"  # rotary embedding and fp32 caches run on the CUDA-core kernel
         if kernel:
             self.plan.kernel = KERNEL_IDS[kernel]
         self.out = torch.empty((B, Hq, D), dtype=self.q.dtype, device=device)
@@ -552,9 +553,9 @@ def run_gpu(args):
             c = case if name == args.workload else workloads.workload(name)
             b = kv_bytes(c)
             entry = {"dtype": c.dtype, "head_dim": c.D, "rope_theta": c.rope_theta}
-            simt_ok = c.dtype == "f16" and c.D in (64, 128, 256)
+            simt_ok = c.dtype in ("f16", "f32") and c.D in (64, 128, 256)
             kernels = ("mma", "simt") if simt_ok else ("mma",)
-            if c.rope_theta > 0:
+            if c.rope_theta > 0 or c.dtype == "f32":
                 kernels = ("simt",)
             for kname in kernels:
                 us, kus, copies, l2state, plan = time_graph_rotating(c, device, kname)

@@ -21,7 +21,7 @@
  * L_b == 0 (or an empty attended range) gives out = 0, lse = -inf.
  *
  * Layouts (row-major, element strides implied by the shapes):
- *   q            T     [B, Hq, D]      T = fp16, or bf16 (plan.dtype)
+ *   q            T     [B, Hq, D]      T = fp16, bf16 or fp32 (plan.dtype)
  *   k_cache      T     [num_pages, Hkv, page_size, D]   (v_cache the same)
  *   block_tables int32 [B, max_pages_per_seq]   entry j = physical page of the
  *                                               sequence's logical page j
@@ -29,8 +29,9 @@
  *   out          T     [B, Hq, D]   (round to nearest even)
  *   lse          fp32  [B, Hq]
  * Supported: head_dim in {64, 96, 128, 256} (96 and bf16 with the tensor-core
- * kernel only); page_size 16; Hq % Hkv == 0 with g = Hq / Hkv split into at
- * most ceil(g / 8) equal head chunks per CTA.
+ * kernel only, fp32 with the CUDA-core kernel only); page_size 16;
+ * Hq % Hkv == 0 with g = Hq / Hkv split into at most ceil(g / 8) equal head
+ * chunks per CTA.
  * q, k_cache, v_cache, out and workspace must be 16-byte aligned.
  *
  * Ownership: every pointer is caller-owned device memory (the library
@@ -98,17 +99,19 @@ typedef struct pa_plan {
                                first call (error word, per-group arrival counters); the
                                library leaves them zero after every call */
     int dtype;              /* PA_DTYPE_*: element type of q, k_cache, v_cache and out
-                               (pa_plan sets fp16; a caller may set bf16) */
+                               (pa_plan sets fp16; a caller may set bf16 or fp32) */
     float rope_theta;       /* > 0: rotary embedding inside the kernel (rotate-half
                                pairing of dim i and i + D/2, frequency
                                rope_theta^(-2i/D); q at position L - 1, K_t at t, V
-                               untouched), CUDA-core kernel and fp16 only; 0 = none */
+                               untouched), CUDA-core kernel (fp16, fp32); 0 = none */
     int reserved[2];
 } pa_plan_t;
 
-/* Element types (pa_plan_t.dtype).  bf16 needs the tensor-core kernel. */
+/* Element types (pa_plan_t.dtype).  bf16 needs the tensor-core kernel, fp32
+ * the CUDA-core kernel (fp32 FMA throughout; head_dim 64/128/256). */
 #define PA_DTYPE_F16 0
 #define PA_DTYPE_BF16 1
+#define PA_DTYPE_F32 2
 
 /* Partition-kernel variants (pa_plan_t.kernel). */
 #define PA_KERNEL_SIMT 1   /* fp32 FMA on CUDA cores; pages by 1-D bulk copies */

@@ -27,7 +27,9 @@ PA_KERNEL_SIMT = 1
 PA_KERNEL_MMA = 2
 PA_DTYPE_F16 = 0
 PA_DTYPE_BF16 = 1
-_TORCH_DTYPE = {PA_DTYPE_F16: torch.float16, PA_DTYPE_BF16: torch.bfloat16}
+PA_DTYPE_F32 = 2
+_TORCH_DTYPE = {PA_DTYPE_F16: torch.float16, PA_DTYPE_BF16: torch.bfloat16,
+                PA_DTYPE_F32: torch.float32}
 
 EXPORTED = ("pa_plan", "pa_decode", "pa_decode_partitions", "pa_merge", "pa_get_error",
             "pa_status_string", "pa_version", "pa_decode_static")

@@ -13,7 +13,7 @@
 
 namespace pa {
 
-template <int D>
+template <int D, typename E>
 cudaError_t launch_attend_d(int G, bool split, const AttendParams& p, dim3 grid,
                             cudaStream_t stream);
 template <int D, typename T>
@@ -88,14 +88,21 @@ int attend_ctas_per_sm(int D) {
     }
 }
 
-cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 grid,
-                          cudaStream_t stream) {
+template <typename E>
+static cudaError_t launch_attend_e(int D, int G, bool split, const AttendParams& p, dim3 grid,
+                                   cudaStream_t stream) {
     switch (D) {
-        case 64: return launch_attend_d<64>(G, split, p, grid, stream);
-        case 128: return launch_attend_d<128>(G, split, p, grid, stream);
-        case 256: return launch_attend_d<256>(G, split, p, grid, stream);
+        case 64: return launch_attend_d<64, E>(G, split, p, grid, stream);
+        case 128: return launch_attend_d<128, E>(G, split, p, grid, stream);
+        case 256: return launch_attend_d<256, E>(G, split, p, grid, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 grid,
+                          cudaStream_t stream) {
+    return p.elem_fp32 ? launch_attend_e<float>(D, G, split, p, grid, stream)
+                       : launch_attend_e<__half>(D, G, split, p, grid, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -138,6 +145,8 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 to_elem<__nv_bfloat16>(float v) {
     return __float2bfloat16_rn(v);
 }
+template <>
+__device__ __forceinline__ float to_elem<float>(float v) { return v; }
 
 template <typename T>
 __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeParams p) {
@@ -254,8 +263,11 @@ cudaError_t launch_merge(int D, const MergeParams& p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return p.dtype == PA_DTYPE_BF16 ? cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16>, p)
-                                    : cudaLaunchKernelEx(&cfg, merge_kernel<__half>, p);
+    switch (p.dtype) {
+        case PA_DTYPE_BF16: return cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16>, p);
+        case PA_DTYPE_F32: return cudaLaunchKernelEx(&cfg, merge_kernel<float>, p);
+        default: return cudaLaunchKernelEx(&cfg, merge_kernel<__half>, p);
+    }
 }
 
 // Workspace layout: [control block | arrival counters (one per group) |
@@ -432,15 +444,19 @@ static int check_plan(const pa_plan_t* plan) {
     if (plan->head_dim != 64 && plan->head_dim != 96 && plan->head_dim != 128 &&
         plan->head_dim != 256)
         return PA_ERR_UNSUPPORTED;
-    if (plan->dtype != PA_DTYPE_F16 && plan->dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+    if (plan->dtype != PA_DTYPE_F16 && plan->dtype != PA_DTYPE_BF16 &&
+        plan->dtype != PA_DTYPE_F32)
+        return PA_ERR_INVALID_ARG;
     if (!(plan->rope_theta >= 0.f) || plan->rope_theta == INFINITY) return PA_ERR_INVALID_ARG;
     // Rotary embedding runs on the CUDA-core kernel, which keeps the rotated
     // q and K in fp32 (rounding them to fp16/bf16 for the tensor cores would
     // cost more than the LSE tolerance allows).
     if (plan->rope_theta > 0.f && plan->kernel != PA_KERNEL_SIMT) return PA_ERR_UNSUPPORTED;
-    // The CUDA-core kernel is built for fp16 and head dims 64/128/256.
-    if (plan->kernel == PA_KERNEL_SIMT && (plan->dtype != PA_DTYPE_F16 || plan->head_dim == 96))
+    // The CUDA-core kernel is built for fp16/fp32 and head dims 64/128/256;
+    // the tensor-core kernel for fp16/bf16.
+    if (plan->kernel == PA_KERNEL_SIMT && (plan->dtype == PA_DTYPE_BF16 || plan->head_dim == 96))
         return PA_ERR_UNSUPPORTED;
+    if (plan->kernel == PA_KERNEL_MMA && plan->dtype == PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
     const int g = Hq / Hkv;
     const int G = plan->heads_per_cta;
     if (G < 1 || G > kMaxHeadsPerCta || g % G != 0) return PA_ERR_INVALID_ARG;
@@ -512,6 +528,7 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     p.heads_per_cta = plan->heads_per_cta;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.rope = plan->rope_theta > 0.f ? 1 : 0;
+    p.elem_fp32 = plan->dtype == PA_DTYPE_F32 ? 1 : 0;
     if (p.rope) {
         // theta_i / (2 pi) in double, split into two floats.
         for (int i = 0; i < D / 2; ++i) {

@@ -47,6 +47,48 @@ struct Lanes {
     static_assert(R * kPageSize / 2 == D, "lane layout");
 };
 
+// This lane's 8 consecutive elements starting at `src` (16 bytes of fp16 or
+// 32 bytes of fp32), as floats.
+template <typename E>
+__device__ __forceinline__ void load8(const unsigned char* src, float (&f)[8]);
+
+__device__ __forceinline__ void half8_to_float(const uint4 raw, float (&f)[8]);
+
+template <>
+__device__ __forceinline__ void load8<__half>(const unsigned char* src, float (&f)[8]) {
+    half8_to_float(*reinterpret_cast<const uint4*>(src), f);
+}
+
+template <>
+__device__ __forceinline__ void load8<float>(const unsigned char* src, float (&f)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(src)[0];
+    const float4 b = reinterpret_cast<const float4*>(src)[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+template <typename E>
+__device__ __forceinline__ E from_float_e(float v);
+template <>
+__device__ __forceinline__ __half from_float_e<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ float from_float_e<float>(float v) { return v; }
+
+// Four consecutive outputs of type E (8-byte aligned fp16, 16-byte fp32).
+template <typename E>
+__device__ __forceinline__ void store4e(E* dst, float a, float b, float c, float d) {
+    if constexpr (sizeof(E) == 2) {
+        __half2 lo = __floats2half2_rn(a, b);
+        __half2 hi = __floats2half2_rn(c, d);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t*>(&lo);
+        packed.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(dst) = packed;
+    } else {
+        *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
+    }
+}
+
 __device__ __forceinline__ void half8_to_float(const uint4 raw, float (&f)[8]) {
     const __half2* h = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
@@ -85,23 +127,18 @@ __device__ __forceinline__ void rope_apply_and_step(float (&kf)[8], const float 
 // by a shuffle reduce-scatter: the exchange over lane mask (1 << LEVEL) pairs
 // token bit LEVEL-1, and a lane keeps the token whose bit equals its lane bit.
 // Tokens are visited in increasing order, which the rotary recurrence relies on.
-template <int D, int G, int LEVEL>
+template <int D, int G, int LEVEL, typename E>
 __device__ __forceinline__ void qk_tree(float (&res)[G], const unsigned char* kpage, int tok,
                                         int r, int lane, const float (&qf)[G][8], bool rope,
                                         RopeLane& rl) {
     if constexpr (LEVEL == 0) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(kpage + tok * (D * 2) + r * 16);
         float kf[8];
-        half8_to_float(raw, kf);
+        load8<E>(kpage + tok * (D * (int)sizeof(E)) + r * (8 * (int)sizeof(E)), kf);
         if (rope) {  // warp-uniform
             constexpr int kHalf = D / 16;  // lanes per half row
-            uint4 praw;
-            praw.x = __shfl_xor_sync(0xffffffffu, raw.x, kHalf);
-            praw.y = __shfl_xor_sync(0xffffffffu, raw.y, kHalf);
-            praw.z = __shfl_xor_sync(0xffffffffu, raw.z, kHalf);
-            praw.w = __shfl_xor_sync(0xffffffffu, raw.w, kHalf);
             float pf[8];
-            half8_to_float(praw, pf);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) pf[j] = __shfl_xor_sync(0xffffffffu, kf[j], kHalf);
             rope_apply_and_step(kf, pf, (r & kHalf) == 0, rl);
         }
 #pragma unroll
@@ -113,8 +150,8 @@ __device__ __forceinline__ void qk_tree(float (&res)[G], const unsigned char* kp
         }
     } else {
         float lo[G], hi[G];
-        qk_tree<D, G, LEVEL - 1>(lo, kpage, tok, r, lane, qf, rope, rl);
-        qk_tree<D, G, LEVEL - 1>(hi, kpage, tok + (1 << (LEVEL - 1)), r, lane, qf, rope, rl);
+        qk_tree<D, G, LEVEL - 1, E>(lo, kpage, tok, r, lane, qf, rope, rl);
+        qk_tree<D, G, LEVEL - 1, E>(hi, kpage, tok + (1 << (LEVEL - 1)), r, lane, qf, rope, rl);
         constexpr int kMask = 1 << LEVEL;
         const bool up = (lane & kMask) != 0;
 #pragma unroll
@@ -126,7 +163,7 @@ __device__ __forceinline__ void qk_tree(float (&res)[G], const unsigned char* kp
     }
 }
 
-template <int D, int G, bool SPLIT>
+template <int D, int G, bool SPLIT, typename E>
 __device__ __forceinline__ void write_rows(const AttendParams& p, int b, int h0, int part,
                                            float o_val, float m_val, float l_val,
                                            float lse_val) {
@@ -141,16 +178,20 @@ __device__ __forceinline__ void write_rows(const AttendParams& p, int b, int h0,
                 p.ws_l[row] = l_val;
             }
         } else {
-            p.out[bh * D + d] = __float2half_rn(o_val);
+            reinterpret_cast<E*>(p.out)[bh * D + d] = from_float_e<E>(o_val);
             if (d == 0) p.lse[bh] = lse_val;
         }
     }
 }
 
-template <int D, int G, bool SPLIT, bool ROPE>
-__global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBlocks))
+template <int D, int G, bool SPLIT, bool ROPE, typename E>
+__global__ void __launch_bounds__(kThreads,
+                                  (G >= 7 && AttendCfg<D, sizeof(E)>::kMinBlocks > 2
+                                       ? 2
+                                       : AttendCfg<D, sizeof(E)>::kMinBlocks))
     attend_kernel(const AttendParams p) {
-    using Cfg = AttendCfg<D>;
+    using Cfg = AttendCfg<D, sizeof(E)>;
+    constexpr int ES = sizeof(E);
     using LN = Lanes<D, G>;
     constexpr int R = LN::R;
     constexpr int TL = LN::TL;
@@ -177,13 +218,13 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
     const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, p.pages_per_part);
     if (!sp.valid) {
         if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0) atomicOr(p.err, PA_DEVERR_BAD_LENGTH);
-        if constexpr (!SPLIT) write_rows<D, G, SPLIT>(p, b, h0, part, NAN, NAN, NAN, NAN);
+        if constexpr (!SPLIT) write_rows<D, G, SPLIT, E>(p, b, h0, part, NAN, NAN, NAN, NAN);
         return;  // with a split, the merge writes the NaN rows
     }
     if (part >= sp.num_parts) {
         // Nothing attended in this partition.  Without a split this only
         // happens for an empty context: out = 0, lse = -inf.
-        if constexpr (!SPLIT) write_rows<D, G, SPLIT>(p, b, h0, part, 0.f, 0.f, 0.f, -INFINITY);
+        if constexpr (!SPLIT) write_rows<D, G, SPLIT, E>(p, b, h0, part, 0.f, 0.f, 0.f, -INFINITY);
         return;
     }
     const int pg0 = sp.first_page + part * p.pages_per_part;
@@ -208,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
     __syncthreads();
     if (s_flag) {
         if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
-        write_rows<D, G, SPLIT>(p, b, h0, part, NAN, NAN, NAN, NAN);
+        write_rows<D, G, SPLIT, E>(p, b, h0, part, NAN, NAN, NAN, NAN);
         return;
     }
 
@@ -222,8 +263,9 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
     auto issue = [&](int item) {
         const int slot = item % NS;
         const int jj = warp + (item >> 1) * kWarps;
-        const __half* base = (item & 1) ? p.v : p.k;
-        const __half* src = base + ((size_t)s_pid[jj] * p.Hkv + kvh) * kv_stride;
+        const unsigned char* base =
+            reinterpret_cast<const unsigned char*>((item & 1) ? p.v : p.k);
+        const unsigned char* src = base + ((size_t)s_pid[jj] * p.Hkv + kvh) * kv_stride * ES;
         const uint32_t bar = bar_w + slot * 8;
         mbar_arrive_expect_tx(bar, PB);
         bulk_g2s(ring_w + slot * PB, src, PB, bar);
@@ -240,9 +282,9 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
     float qf[G][8];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        const uint4 raw =
-            *reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.Hq + h0 + h) * D + r * 8);
-        half8_to_float(raw, qf[h]);
+        load8<E>(reinterpret_cast<const unsigned char*>(p.q) +
+                     (((size_t)b * p.Hq + h0 + h) * D + r * 8) * ES,
+                 qf[h]);
     }
     // Rotary embedding: q to position L - 1; the K rows follow per token.
     constexpr bool rope = ROPE;  // rotary instances are separate, so the plain ones pay nothing
@@ -305,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
                              rl.c[j], rl.s[j]);
         }
         float s[G];
-        qk_tree<D, G, LN::LOG_TL>(s, ring_wp + ((2 * k) % NS) * PB, rg * TL, r, lane, qf, rope,
-                                  rl);
+        qk_tree<D, G, LN::LOG_TL, E>(s, ring_wp + ((2 * k) % NS) * PB, rg * TL, r, lane, qf, rope,
+                                     rl);
 #pragma unroll
         for (int h = 0; h < G; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], 1);
         __syncwarp();
@@ -372,12 +414,14 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
 #pragma unroll
         for (int i = 0; i < TL; ++i) {
             const int t = rg * TL + i;
-            uint4 raw = *reinterpret_cast<const uint4*>(vpage + t * (D * 2) + r * 16);
+            float vf[8];
+            load8<E>(vpage + t * (D * ES) + r * (8 * ES), vf);
             // Slots outside [start, L) carry weight 0; zero their V too so that
             // whatever an unwritten slot holds (NaN included) cannot leak in.
-            if (vpos0 + t < sp.start || vpos0 + t >= sp.L) raw = make_uint4(0, 0, 0, 0);
-            float vf[8];
-            half8_to_float(raw, vf);
+            if (vpos0 + t < sp.start || vpos0 + t >= sp.L) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) vf[j] = 0.f;
+            }
             float pr[GP];
 #pragma unroll
             for (int h4 = 0; h4 < GP; h4 += 4) {
@@ -445,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
     }
     __syncthreads();
     if (s_flag) {
-        write_rows<D, G, SPLIT>(p, b, h0, part, NAN, NAN, NAN, NAN);
+        write_rows<D, G, SPLIT, E>(p, b, h0, part, NAN, NAN, NAN, NAN);
         return;
     }
 
@@ -481,26 +525,24 @@ __global__ void __launch_bounds__(kThreads, (G >= 7 ? 2 : AttendCfg<D>::kMinBloc
                 p.ws_l[row] = Ls;
             }
         } else {
-            __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
-            __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
-            uint2 packed;
-            packed.x = *reinterpret_cast<uint32_t*>(&lo);
-            packed.y = *reinterpret_cast<uint32_t*>(&hi);
-            *reinterpret_cast<uint2*>(p.out + bh * D + d) = packed;
+            store4e<E>(reinterpret_cast<E*>(p.out) + bh * D + d, acc.x * inv, acc.y * inv,
+                       acc.z * inv, acc.w * inv);
             if (d == 0) p.lse[bh] = Ls > 0.f ? M * 0.69314718055994531f + logf(Ls) : -INFINITY;
         }
     }
 }
 
-// Launcher for one head dim: picks the <G, SPLIT> instance, raises its
-// dynamic shared-memory limit once per device, launches on `stream`.
-template <int D>
+// Launcher for one head dim and element type: picks the <G, SPLIT, ROPE>
+// instance, raises its dynamic shared-memory limit once per device, launches
+// on `stream`.
+template <int D, typename E>
 cudaError_t launch_attend_d(int G, bool split, const AttendParams& p, dim3 grid,
                             cudaStream_t stream) {
+    using Cfg = AttendCfg<D, sizeof(E)>;
     const void* fn = nullptr;
     const bool rope = p.rope != 0;
     switch (G) {
-#define PA_ATTEND_PICK(GG, S, R) reinterpret_cast<const void*>(&attend_kernel<D, GG, S, R>)
+#define PA_ATTEND_PICK(GG, S, R) reinterpret_cast<const void*>(&attend_kernel<D, GG, S, R, E>)
 #define PA_ATTEND_CASE(GG)                                                                   \
     case GG:                                                                                 \
         fn = split ? (rope ? PA_ATTEND_PICK(GG, true, true) : PA_ATTEND_PICK(GG, true, false)) \
@@ -526,13 +568,12 @@ cudaError_t launch_attend_d(int G, bool split, const AttendParams& p, dim3 grid,
     if (e != cudaSuccess) return e;
     const uint32_t bit = 1u << ((G - 1) * 4 + (split ? 2 : 0) + (rope ? 1 : 0));
     if (dev < 0 || dev >= kMaxDevices || !(configured[dev].load() & bit)) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 AttendCfg<D>::kSmemBytes);
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDevices) configured[dev].fetch_or(bit);
     }
     void* args[] = {const_cast<AttendParams*>(&p)};
-    return cudaLaunchKernel(fn, grid, dim3(kThreads), args, AttendCfg<D>::kSmemBytes, stream);
+    return cudaLaunchKernel(fn, grid, dim3(kThreads), args, Cfg::kSmemBytes, stream);
 }
 
 }  // namespace pa

@@ -1,7 +1,8 @@
-// Partition-kernel instances for head_dim 128 (one translation unit per head dim
-// so the build compiles them in parallel).
+// CUDA-core partition-kernel instances for head_dim 128, fp16 (one translation
+// unit per head dim and element type so the build compiles them in parallel).
 #include "pa_attend.cuh"
 
 namespace pa {
-template cudaError_t launch_attend_d<128>(int, bool, const AttendParams&, dim3, cudaStream_t);
+template cudaError_t launch_attend_d<128, __half>(int, bool, const AttendParams&, dim3,
+                                                 cudaStream_t);
 }  // namespace pa

@@ -46,6 +46,7 @@ struct AttendParams {
     int parts_per_cta;      // consecutive partitions one CTA streams (tensor-core kernel)
     float scale_log2;       // scale * log2(e)
     int rope;               // 1: rotary embedding of q and K (CUDA-core kernel)
+    int elem_fp32;          // 1: q, K, V and out are fp32 (CUDA-core kernel)
     // Rotary frequency i as a fraction of a turn, theta_i / (2 pi), split into
     // two floats (rope_phi[0][i] + rope_phi[1][i]) so that pos * theta_i
     // reduces modulo one turn with fp32 accuracy for any position below 2^24.
@@ -66,16 +67,19 @@ struct MergeParams {
 
 // Pipeline depth (pages of K or V in flight per warp) for each head dim; the
 // resulting shared-memory footprint sets the CTAs per SM.
-template <int D>
+// (CUDA-core kernel; ES = element bytes: 2 for fp16, 4 for fp32.)
+template <int D, int ES = 2>
 struct AttendCfg {
-    static constexpr int kPageBytes = kPageSize * D * 2;
-    static constexpr int kStages = D == 256 ? 3 : (D == 128 ? 4 : 6);
+    static constexpr int kPageBytes = kPageSize * D * ES;
+    static constexpr int kStages =
+        ES == 2 ? (D == 256 ? 3 : (D == 128 ? 4 : 6)) : (D == 64 ? 4 : 3);
     static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
     static constexpr int kPBufFloats = kPageSize * kMaxHeadsPerCta;  // per warp
     static constexpr int kSmemBytes = kRingBytes + kWarps * kPBufFloats * 4 +
                                       kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 2 * 4 +
                                       kWarps * kStages * 8 + 16;
-    static constexpr int kMinBlocks = D == 256 ? 2 : 3;
+    static constexpr int kMinBlocks =
+        ES == 2 ? (D == 256 ? 2 : 3) : (D == 256 ? 1 : (D == 128 ? 2 : 3));
 };
 
 // The in-kernel merge of the tensor-core kernel issues all of its loads at

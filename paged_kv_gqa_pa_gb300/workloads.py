@@ -190,8 +190,9 @@ WORKLOADS = {
 WORKLOAD_ORDER = list(WORKLOADS)
 
 # Further measured workloads for the widened paths: a bf16 cache at the
-# long-context shapes and head_dim 96 (tensor-core kernel only), and a rotary
-# embedding applied inside the kernel (CUDA-core kernel only).
+# long-context shapes and head_dim 96 (tensor-core kernel only), a rotary
+# embedding applied inside the kernel and an fp32 cache (CUDA-core kernel
+# only).
 EXTRA_WORKLOADS = {
     "gqa6_ctx100k_bf16": dict(B=4, Hq=24, Hkv=4, D=256, lens=[100000] * 4, seed=1006,
                               partition_size=512, dtype="bf16"),
@@ -199,6 +200,9 @@ EXTRA_WORKLOADS = {
     # Rotary embedding inside the kernel (Llama-3 frequency base), fp16, D 128.
     "gqa4_rope_ctx32k": dict(B=4, Hq=32, Hkv=8, D=128, lens=[32768] * 4, seed=1008,
                              rope_theta=500000.0),
+    # An fp32 cache (the dtype the PagedAttention-V2 commit note sizes), D 128.
+    "gqa4_f32_ctx32k": dict(B=4, Hq=32, Hkv=8, D=128, lens=[32768] * 4, seed=1009,
+                            dtype="f32"),
 }
 EXTRA_ORDER = list(EXTRA_WORKLOADS)
 ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}

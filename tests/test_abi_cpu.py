@@ -164,6 +164,9 @@ def test_decode_argument_checks_return_before_launch():
     rope_neg = binding.pa_plan_t.from_buffer_copy(plan)
     rope_neg.rope_theta = -1.0
     assert _call_decode(rope_neg) == binding.PA_ERR_INVALID_ARG
+    f32_mma = binding.pa_plan_t.from_buffer_copy(plan)
+    f32_mma.dtype = binding.PA_DTYPE_F32
+    assert _call_decode(f32_mma) == binding.PA_ERR_UNSUPPORTED
     bad_dtype = binding.pa_plan_t.from_buffer_copy(plan)
     bad_dtype.dtype = 7
     assert _call_decode(bad_dtype) == binding.PA_ERR_INVALID_ARG

@@ -30,10 +30,10 @@ def kernel_variant(request):
 @pytest.mark.parametrize("name", workloads.WORKLOAD_ORDER + workloads.EXTRA_ORDER)
 def test_workload_full_size(name):
     case = workloads.workload(name)
-    if gpu_helpers.KERNEL == "simt" and (case.dtype != "f16" or case.D == 96):
-        pytest.skip("the CUDA-core kernel is built for fp16 and head dims 64/128/256")
-    if gpu_helpers.KERNEL == "mma" and case.rope_theta > 0:
-        pytest.skip("rotary embedding runs on the CUDA-core kernel")
+    if gpu_helpers.KERNEL == "simt" and (case.dtype == "bf16" or case.D == 96):
+        pytest.skip("the CUDA-core kernel is built for fp16/fp32 and head dims 64/128/256")
+    if gpu_helpers.KERNEL == "mma" and (case.rope_theta > 0 or case.dtype == "f32"):
+        pytest.skip("rotary embedding and fp32 caches run on the CUDA-core kernel")
     out, lse, err, plan = run_gpu(case)
     assert err == 0
     rel = assert_matches_oracle(case, out, lse, what=name)
@@ -343,3 +343,24 @@ def test_rotary_embedding_in_kernel(D, theta):
     out, lse, err, _ = run_gpu(wcase)
     assert err == 0
     assert_matches_oracle(wcase, out, lse, what=f"rope window D{D}")
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_fp32_cache(D):
+    if gpu_helpers.KERNEL == "mma":
+        pytest.skip("fp32 caches run on the CUDA-core kernel")
+    case = workloads.make_case("f32", len(LENS), 12, 4, D, LENS, seed=900 + D, q_std=2.0,
+                               dtype="f32")
+    for S in (0, 64, 4096):
+        case.partition_size = S
+        out, lse, err, _ = run_gpu(case, guard=64)
+        assert err == 0
+        rel = assert_matches_oracle(case, out, lse, what=f"f32 D{D} S{S}")
+        print(f"f32 D{D} S{S}: rel L2 {rel:.2e}")
+    wcase = workloads.make_case("f32w", 3, 8, 2, D, [0, 5000, 333], seed=901 + D, window=700,
+                                dtype="f32", rope_theta=10000.0)
+    for S in (128, 4096):
+        wcase.partition_size = S
+        out, lse, err, _ = run_gpu(wcase, guard=64)
+        assert err == 0
+        assert_matches_oracle(wcase, out, lse, what=f"f32 rope window D{D} S{S}")
