@@ -5,8 +5,9 @@
 
 One step = one full decode call (partition kernel + log-sum-exp merge) over
 one batch of the workload, inputs resident in HBM.  Rank 0 prints ONE JSON
-line.  The metric is KV-read bandwidth: algorithmic bytes = 4 * Hkv * D bytes
-(fp16 K and V rows) per attended token, divided by the time per step.
+line.  The metric is KV-read bandwidth: algorithmic bytes = 2 * Hkv * D *
+element bytes (one K and one V row) per attended token, divided by the time
+per step.
 
 --impl reference times the fp64 CPU oracle on the host cores instead (the only
 other path that runs the oracle), on bounded samples of the same workload.
@@ -76,8 +77,12 @@ def attended_tokens(case) -> int:
     return n
 
 
+ELEM_BYTES = {"f16": 2, "bf16": 2, "f32": 4}
+
+
 def kv_bytes(case) -> int:
-    return 4 * case.Hkv * case.D * attended_tokens(case)
+    """Algorithmic bytes: one K row and one V row per attended token."""
+    return 2 * ELEM_BYTES[case.dtype] * case.Hkv * case.D * attended_tokens(case)
 
 
 def measured_peaks():
@@ -435,7 +440,7 @@ class OracleSampler:
         self._run(L, self.threads)
         dt = time.perf_counter() - t0
         c = self.case
-        byts = 4 * c.Hkv * c.D * L
+        byts = 2 * ELEM_BYTES[c.dtype] * c.Hkv * c.D * L
         used = min(self.threads, c.Hq)
         desc = (f"sequence 0 of {c.B}, all {c.Hq} query heads, last {L} of {self.att} attended "
                 f"tokens; fp64 C oracle, OpenMP over heads")

@@ -196,3 +196,11 @@ def test_bench_kernel_source_lists_exist():
     listed = {f for files in bench.KERNEL_SOURCES.values() for f in files}
     kernels = {f for f in os.listdir(csrc) if f.startswith("pa_attend")}
     assert kernels <= listed
+
+
+def test_bench_counts_algorithmic_bytes_per_element_type():
+    import bench
+    from paged_kv_gqa_pa_gb300 import workloads
+    for dtype, eb in (("f16", 2), ("bf16", 2), ("f32", 4)):
+        c = workloads.make_case("b", 2, 4, 2, 64, [100, 40], seed=1, window=64, dtype=dtype)
+        assert bench.kv_bytes(c) == 2 * eb * 2 * 64 * (64 + 40)
