@@ -204,15 +204,15 @@ class GpuArm:
         B, Hq, D = case.q.shape
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         ps = case.partition_size if partition_size is None else partition_size
-        self.plan = pa.pa_plan(B, Hq, case.Hkv, D, case.page_size, case.num_pages,
-                               case.max_pages_per_seq, case.max_context_len, case.window, ps, sms)
-        self.plan.dtype = {"f16": 0, "bf16": 1, "f32": 2}[case.dtype]
-        self.plan.rope_theta = case.rope_theta
-        self.planner_kernel = self.plan.kernel
-        if kernel is None and (case.rope_theta > 0 or case.dtype == "f32"):
-            kernel = "simt"  # rotary embedding and fp32 caches run on the CUDA-core kernel
-        if kernel:
-            self.plan.kernel = KERNEL_IDS[kernel]
+        dtype = {"f16": 0, "bf16": 1, "f32": 2}[case.dtype]
+        self.planner_kernel = pa.pa_plan_ex(
+            B, Hq, case.Hkv, D, case.page_size, case.num_pages, case.max_pages_per_seq,
+            case.max_context_len, case.window, ps, sms, dtype=dtype, kernel=0,
+            rope_theta=case.rope_theta).kernel
+        self.plan = pa.pa_plan_ex(B, Hq, case.Hkv, D, case.page_size, case.num_pages,
+                                  case.max_pages_per_seq, case.max_context_len, case.window, ps,
+                                  sms, dtype=dtype, kernel=KERNEL_IDS[kernel] if kernel else 0,
+                                  rope_theta=case.rope_theta)
         self.out = torch.empty((B, Hq, D), dtype=self.q.dtype, device=device)
         self.lse = torch.empty((B, Hq), dtype=torch.float32, device=device)
         self.ws = pa.new_workspace(self.plan, device)

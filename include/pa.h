@@ -135,6 +135,21 @@ int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page
             int partition_size, int num_sms, pa_plan_t* plan);
 
 /*
+ * pa_plan for a given element type, kernel and rotary base: the automatic
+ * partitioning then sizes the grid for that kernel's residency.
+ *   dtype       PA_DTYPE_F16 / PA_DTYPE_BF16 / PA_DTYPE_F32
+ *   kernel      0 = automatic (the tensor-core kernel, or the CUDA-core kernel
+ *               for fp32 or a rotary embedding), else PA_KERNEL_*
+ *   rope_theta  0 = no rotary embedding, else its frequency base
+ * pa_plan(...) is pa_plan_ex(..., PA_DTYPE_F16, 0, 0, plan).  Returns
+ * PA_ERR_UNSUPPORTED for combinations no kernel is built for.
+ */
+int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+               int num_pages, int max_pages_per_seq, int max_context_len, int window,
+               int partition_size, int num_sms, int dtype, int kernel, float rope_theta,
+               pa_plan_t* plan);
+
+/*
  * Full decode step: the partition kernel (gather pages, q.K, per-partition
  * softmax statistics, P.V) and, when plan->num_partitions > 1, the
  * log-sum-exp merge.  `window` must equal plan->window.

@@ -31,8 +31,8 @@ PA_DTYPE_F32 = 2
 _TORCH_DTYPE = {PA_DTYPE_F16: torch.float16, PA_DTYPE_BF16: torch.bfloat16,
                 PA_DTYPE_F32: torch.float32}
 
-EXPORTED = ("pa_plan", "pa_decode", "pa_decode_partitions", "pa_merge", "pa_get_error",
-            "pa_status_string", "pa_version", "pa_decode_static")
+EXPORTED = ("pa_plan", "pa_plan_ex", "pa_decode", "pa_decode_partitions", "pa_merge",
+            "pa_get_error", "pa_status_string", "pa_version", "pa_decode_static")
 
 
 class pa_plan_t(ctypes.Structure):
@@ -96,6 +96,8 @@ def load():
         pp = ctypes.POINTER(pa_plan_t)
         lib.pa_plan.argtypes = [i] * 11 + [pp]
         lib.pa_plan.restype = i
+        lib.pa_plan_ex.argtypes = [i] * 13 + [ctypes.c_float, pp]
+        lib.pa_plan_ex.restype = i
         dec = [pp, P, P, P, P, P, ctypes.c_float, i, P, P, P, P]
         lib.pa_decode.argtypes = dec
         lib.pa_decode.restype = i
@@ -133,6 +135,20 @@ def pa_plan(batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
                         ctypes.byref(plan))
     if st != PA_OK:
         raise PAError("pa_plan", st)
+    return plan
+
+
+def pa_plan_ex(batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+               max_pages_per_seq, max_context_len, window=0, partition_size=0, num_sms=0,
+               dtype=PA_DTYPE_F16, kernel=0, rope_theta=0.0) -> pa_plan_t:
+    plan = pa_plan_t()
+    st = load().pa_plan_ex(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim),
+                           int(page_size), int(num_pages), int(max_pages_per_seq),
+                           int(max_context_len), int(window), int(partition_size), int(num_sms),
+                           int(dtype), int(kernel), ctypes.c_float(rope_theta),
+                           ctypes.byref(plan))
+    if st != PA_OK:
+        raise PAError("pa_plan_ex", st)
     return plan
 
 

@@ -57,34 +57,53 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// The K (or V) cache as a 2-D tensor [rows = num_pages*Hkv*16, D] of 16-bit
-// elements.  The main map's box is 16 rows x 64 columns (one 128-byte slab of
-// a page, 128-byte swizzle); the tail map's box, used when D is not a
-// multiple of 64, is 16 rows x 32 columns (64-byte swizzle).
-static bool make_page_map(CUtensorMap* map, const void* base, long long rows, int D, int dtype,
-                          bool tail) {
+// The K (or V) cache as a tensor of 16-bit elements for the tensor-core
+// kernel's page copies.  D a multiple of 64: 2-D [rows = num_pages*Hkv*16, D],
+// box 16 rows x 64 columns (one 128-byte slab of a page), 128-byte swizzle.
+// D = 96: 3-D [rows][D/32][32], box 16 x D/32 x 32 (a whole page), 64-byte
+// swizzle.
+static bool make_page_map(CUtensorMap* map, const void* base, long long rows, int D,
+                          int dtype) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    const cuuint32_t box[2] = {tail ? 32u : 64u, (cuuint32_t)kPageSize};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map,
-               dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-               2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE,
-               tail ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+    const CUtensorMapDataType et =
+        dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (D % 64 == 0) {
+        const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+        const cuuint32_t box[2] = {64u, (cuuint32_t)kPageSize};
+        const cuuint32_t estr[2] = {1, 1};
+        return enc(map, et, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+               CUDA_SUCCESS;
+    }
+    const cuuint64_t dims[3] = {32u, (cuuint64_t)(D / 32), (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {64u, (cuuint64_t)D * 2};
+    const cuuint32_t box[3] = {32u, (cuuint32_t)(D / 32), (cuuint32_t)kPageSize};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, et, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
 
-int attend_ctas_per_sm(int D) {
+// CTAs of the partition kernel resident per SM (the launch bound, which the
+// configurations' static checks also guarantee in shared memory).
+int attend_ctas_per_sm(int kernel, int dtype, int D) {
+    if (kernel == PA_KERNEL_MMA) {
+        switch (D) {
+            case 64: return MmaCfg<64>::kMinBlocks;
+            case 96: return MmaCfg<96>::kMinBlocks;
+            case 128: return MmaCfg<128>::kMinBlocks;
+            default: return MmaCfg<256>::kMinBlocks;
+        }
+    }
+    const bool f32 = dtype == PA_DTYPE_F32;
     switch (D) {
-        case 64: return AttendCfg<64>::kMinBlocks;
-        case 96: return 3;
-        case 128: return AttendCfg<128>::kMinBlocks;
-        default: return AttendCfg<256>::kMinBlocks;
+        case 64: return f32 ? AttendCfg<64, 4>::kMinBlocks : AttendCfg<64>::kMinBlocks;
+        case 128: return f32 ? AttendCfg<128, 4>::kMinBlocks : AttendCfg<128>::kMinBlocks;
+        default: return f32 ? AttendCfg<256, 4>::kMinBlocks : AttendCfg<256>::kMinBlocks;
     }
 }
 
@@ -320,8 +339,27 @@ const char* pa_status_string(int status) {
 int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
             int num_pages, int max_pages_per_seq, int max_context_len, int window,
             int partition_size, int num_sms, pa_plan_t* plan) {
+    return pa_plan_ex(batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                      max_pages_per_seq, max_context_len, window, partition_size, num_sms,
+                      PA_DTYPE_F16, 0, 0.f, plan);
+}
+
+int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+               int num_pages, int max_pages_per_seq, int max_context_len, int window,
+               int partition_size, int num_sms, int dtype, int kernel, float rope_theta,
+               pa_plan_t* plan) {
     if (!plan) return PA_ERR_INVALID_ARG;
     memset(plan, 0, sizeof(*plan));
+    if (dtype != PA_DTYPE_F16 && dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F32)
+        return PA_ERR_INVALID_ARG;
+    if (!(rope_theta >= 0.f) || rope_theta == INFINITY) return PA_ERR_INVALID_ARG;
+    if (kernel == 0)  // automatic: rotary embedding and fp32 need the CUDA-core kernel
+        kernel = (rope_theta > 0.f || dtype == PA_DTYPE_F32) ? PA_KERNEL_SIMT : PA_KERNEL_MMA;
+    if (kernel != PA_KERNEL_SIMT && kernel != PA_KERNEL_MMA) return PA_ERR_INVALID_ARG;
+    if (kernel == PA_KERNEL_MMA && (dtype == PA_DTYPE_F32 || rope_theta > 0.f))
+        return PA_ERR_UNSUPPORTED;
+    if (kernel == PA_KERNEL_SIMT && (dtype == PA_DTYPE_BF16 || head_dim == 96))
+        return PA_ERR_UNSUPPORTED;
     if (batch < 0 || batch > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         num_q_heads % num_kv_heads != 0 || head_dim <= 0 || page_size <= 0 || num_pages <= 0 ||
         max_pages_per_seq <= 0 || max_context_len < 0 || window < 0 || partition_size < 0 ||
@@ -372,7 +410,7 @@ int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page
         constexpr long long kNoSplitBytes = 128 << 10;
         constexpr int kMinPagesPerPart = 2 * kWarps;
         const long long groups = (long long)batch * num_kv_heads * nchunk;
-        const long long slots = (long long)num_sms * attend_ctas_per_sm(head_dim);
+        const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim);
         const long long span_bytes = (long long)span * 2 * page_size * head_dim * 2;
         if (groups == 0 || groups >= slots || span_bytes <= kNoSplitBytes) {
             pp = span;
@@ -410,12 +448,14 @@ int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page
     const WsLayout wl = ws_layout(batch, num_q_heads, head_dim, P, groups_all);
     plan->workspace_bytes = wl.total;
     plan->ctrl_bytes = (int)wl.ctrl_bytes;
-    plan->kernel = PA_KERNEL_MMA;
-    plan->dtype = PA_DTYPE_F16;
+    plan->kernel = kernel;
+    plan->dtype = dtype;
+    plan->rope_theta = rope_theta;
     // Merge inside the partition kernel when a group's partials are small
     // (its last CTA merges them, no second launch); the merge kernel when they
     // are many (the one-CTA merge would then trail the grid).
-    plan->merge_in_kernel = (P > 1 && kFusedMergeFits(G, head_dim, P)) ? 1 : 0;
+    plan->merge_in_kernel =
+        (kernel == PA_KERNEL_MMA && P > 1 && kFusedMergeFits(G, head_dim, P)) ? 1 : 0;
     // Partitions per CTA (tensor-core kernel): when the one-partition grid
     // runs many waves of resident CTAs (more than four), let each CTA stream
     // two consecutive partitions.  That halves the CTA prologues and
@@ -423,7 +463,7 @@ int pa_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page
     // stays short; longer CTAs (more partitions each) measured slower.
     {
         const long long groups = (long long)batch * num_kv_heads * nchunk;
-        const long long slots = (long long)num_sms * attend_ctas_per_sm(head_dim);
+        const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim);
         const bool many_waves = slots > 0 && groups * P > 4 * slots;
         plan->parts_per_cta = (many_waves && P >= 2 && 2 * pp <= kMaxPagesPerPart) ? 2 : 1;
     }
@@ -540,21 +580,11 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     }
     cudaError_t e;
     if (plan->kernel == PA_KERNEL_MMA) {
-        // K, V (64-column boxes), then K, V tails (32-column boxes, D = 96).
-        alignas(64) CUtensorMap maps[4];
+        alignas(64) CUtensorMap maps[2];  // K, V
         const long long rows = (long long)plan->num_pages * p.Hkv * kPageSize;
-        const bool tail = (D % 64) != 0;
-        if (!make_page_map(&maps[0], k_cache, rows, D, plan->dtype, false) ||
-            !make_page_map(&maps[1], v_cache, rows, D, plan->dtype, false))
+        if (!make_page_map(&maps[0], k_cache, rows, D, plan->dtype) ||
+            !make_page_map(&maps[1], v_cache, rows, D, plan->dtype))
             return PA_ERR_CUDA;
-        if (tail) {
-            if (!make_page_map(&maps[2], k_cache, rows, D, plan->dtype, true) ||
-                !make_page_map(&maps[3], v_cache, rows, D, plan->dtype, true))
-                return PA_ERR_CUDA;
-        } else {
-            maps[2] = maps[0];
-            maps[3] = maps[1];
-        }
         p.parts_per_cta = plan->parts_per_cta;
         const dim3 grid((P + p.parts_per_cta - 1) / p.parts_per_cta, p.Hkv * p.nchunk, p.B);
         e = launch_attend_mma(D, plan->dtype, P > 1, p, maps, grid,

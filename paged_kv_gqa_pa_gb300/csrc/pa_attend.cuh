@@ -132,14 +132,29 @@ __device__ __forceinline__ void qk_tree(float (&res)[G], const unsigned char* kp
                                         int r, int lane, const float (&qf)[G][8], bool rope,
                                         RopeLane& rl) {
     if constexpr (LEVEL == 0) {
+        const unsigned char* src = kpage + tok * (D * (int)sizeof(E)) + r * (8 * (int)sizeof(E));
         float kf[8];
-        load8<E>(kpage + tok * (D * (int)sizeof(E)) + r * (8 * (int)sizeof(E)), kf);
         if (rope) {  // warp-uniform
             constexpr int kHalf = D / 16;  // lanes per half row
             float pf[8];
+            if constexpr (sizeof(E) == 2) {
+                // exchange the packed fp16 words (4 shuffles), then widen
+                const uint4 raw = *reinterpret_cast<const uint4*>(src);
+                uint4 praw;
+                praw.x = __shfl_xor_sync(0xffffffffu, raw.x, kHalf);
+                praw.y = __shfl_xor_sync(0xffffffffu, raw.y, kHalf);
+                praw.z = __shfl_xor_sync(0xffffffffu, raw.z, kHalf);
+                praw.w = __shfl_xor_sync(0xffffffffu, raw.w, kHalf);
+                half8_to_float(raw, kf);
+                half8_to_float(praw, pf);
+            } else {
+                load8<E>(src, kf);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) pf[j] = __shfl_xor_sync(0xffffffffu, kf[j], kHalf);
+                for (int j = 0; j < 8; ++j) pf[j] = __shfl_xor_sync(0xffffffffu, kf[j], kHalf);
+            }
             rope_apply_and_step(kf, pf, (r & kHalf) == 0, rl);
+        } else {
+            load8<E>(src, kf);
         }
 #pragma unroll
         for (int h = 0; h < G; ++h) {

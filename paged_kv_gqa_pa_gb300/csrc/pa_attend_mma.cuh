@@ -10,9 +10,11 @@
 //    matrix, one 16-row x 64-column box per 128-byte slab of the row, with the
 //    128-byte swizzle: the 16-byte chunk c of row r lands at chunk c ^ (r & 7)
 //    of that row, so the ldmatrix reads below are free of bank conflicts.
-//    A head dim that is not a multiple of 64 (96) ends in a 32-column slab,
-//    copied with the 64-byte swizzle (chunk c of row r at c ^ ((r >> 1) & 3)),
-//    which keeps those reads conflict-free too.
+//    A head dim that is not a multiple of 64 (96) is copied instead as one
+//    3-D box per page, [16 rows][D/32 units of 64 bytes], with the 64-byte
+//    swizzle: chunk c of 64-byte unit u (u = row * D/32 + slab) lands at
+//    c ^ ((u >> 1) & 3).  D/32 = 3 is odd, so the 8 rows an ldmatrix reads
+//    still fall in 8 distinct bank groups.
 //  * Element type T: fp16, or bf16 (then q and out are bf16 as well).
 //  * q.K (the commit note's Phase 1 QK^T).  S^T[16 tokens x 8 heads] =
 //    K_page[16 x D] . Q^T[D x 8] with mma.sync m16n8k16 (fp16 in, fp32
@@ -49,27 +51,6 @@
 #include "pa_common.cuh"
 
 namespace pa {
-
-template <int D>
-struct MmaCfg {
-    static_assert(D % 64 == 0 || D % 64 == 32, "head dim: 64-column slabs plus at most one 32-column slab");
-    static constexpr int kFullSlabs = D / 64;       // 128-byte slabs per K/V row (128-byte swizzle)
-    static constexpr bool kTail = (D % 64) != 0;    // a trailing 64-byte slab (64-byte swizzle)
-    static constexpr int kSlabBytes = kPageSize * 128;
-    static constexpr int kTailBytes = kPageSize * 64;
-    static constexpr int kPageBytes = kPageSize * D * 2;
-    static constexpr int kStages = D == 256 ? 3 : (D == 128 ? 4 : 6);
-    static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
-    // output dims combined per round at a partition edge
-    static constexpr int kXDims = (D % 64 == 0) ? 64 : 32;
-    static constexpr int kXBytes = kWarps * kMaxHeadsPerCta * 64 * 4;
-    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes + kXBytes +
-                                      kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 3 * 4 +
-                                      kWarps * kStages * 8 + 16;
-    static constexpr int kMinBlocks = D == 256 ? 2 : 3;
-    static_assert(kPageBytes == kFullSlabs * kSlabBytes + (kTail ? kTailBytes : 0), "slab layout");
-    static_assert(kPageBytes % 1024 == 0, "page slots keep the 1 KiB swizzle alignment");
-};
 
 // Element-type specifics: the mma flavour and the packing of fp32 pairs.
 template <typename T>
@@ -161,15 +142,25 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 }
 
 // Byte offset inside a swizzled page of the 16-byte chunk `chunk` (0..D/8-1)
-// of token row `row`: 128-byte slabs first, then the optional 64-byte slab.
+// of token row `row`.
 template <int D>
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    constexpr int kFull = (D / 64) * 8;  // chunks in the 128-byte slabs
-    if (D % 64 == 0 || chunk < kFull)
+    if constexpr (D % 64 == 0) {  // [slab][16 rows][128 bytes], 128-byte swizzle
         return (uint32_t)((chunk >> 3) * (kPageSize * 128) + row * 128 +
                           (((chunk & 7) ^ (row & 7)) << 4));
-    const int c = chunk - kFull;  // 0..3 in a 64-byte row
-    return (uint32_t)((D / 64) * (kPageSize * 128) + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+    } else {  // [16 rows][D/32 units][64 bytes], 64-byte swizzle
+        const int unit = row * (D / 32) + (chunk >> 2);
+        return (uint32_t)(unit * 64 + (((chunk & 3) ^ ((unit >> 1) & 3)) << 4));
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
 }
 
 // In-kernel log-sum-exp merge (the commit note's Phase 2) for plans whose
@@ -288,9 +279,7 @@ __device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, co
 template <int D, typename T, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     attend_mma_kernel(const AttendParams p, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV,
-                      const __grid_constant__ CUtensorMap tmKt,
-                      const __grid_constant__ CUtensorMap tmVt) {
+                      const __grid_constant__ CUtensorMap tmV) {
     using Cfg = MmaCfg<D>;
     constexpr int NS = Cfg::kStages;
     constexpr int PB = Cfg::kPageBytes;
@@ -368,10 +357,6 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         s_flag = 0;
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
-        if (Cfg::kTail) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmKt)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmVt)) : "memory");
-        }
     }
     const uint32_t bar_w = smem_u32(bars) + warp * NS * 8;
     if (lane == 0) {
@@ -410,12 +395,13 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         const int y = (s_pid[jj] * p.Hkv + kvh) * kPageSize;
         const uint32_t bar = bar_w + slot * 8;
         mbar_arrive_expect_tx(bar, PB);
+        if constexpr (Cfg::kRows64) {
+            tma_load_3d(ring_w + slot * PB, map, 0, 0, y, bar);
+        } else {
 #pragma unroll
-        for (int s = 0; s < Cfg::kFullSlabs; ++s)
-            tma_load_2d(ring_w + slot * PB + s * Cfg::kSlabBytes, map, s * 64, y, bar);
-        if (Cfg::kTail)
-            tma_load_2d(ring_w + slot * PB + Cfg::kFullSlabs * Cfg::kSlabBytes,
-                        (item & 1) ? &tmVt : &tmKt, Cfg::kFullSlabs * 64, y, bar);
+            for (int s = 0; s < Cfg::kFullSlabs; ++s)
+                tma_load_2d(ring_w + slot * PB + s * Cfg::kSlabBytes, map, s * 64, y, bar);
+        }
     };
     if (lane == 0) {
         for (int i = 0; i < NS && i < n_items; ++i) issue(i);
@@ -708,8 +694,7 @@ cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtenso
         if (dev >= 0 && dev < kMaxDevices) configured[dev].fetch_or(bit);
     }
     void* args[] = {const_cast<AttendParams*>(&p), const_cast<CUtensorMap*>(&maps[0]),
-                    const_cast<CUtensorMap*>(&maps[1]), const_cast<CUtensorMap*>(&maps[2]),
-                    const_cast<CUtensorMap*>(&maps[3])};
+                    const_cast<CUtensorMap*>(&maps[1])};
     return cudaLaunchKernel(fn, grid, dim3(kThreads), args, MmaCfg<D>::kSmemBytes, stream);
 }
 

@@ -72,14 +72,39 @@ template <int D, int ES = 2>
 struct AttendCfg {
     static constexpr int kPageBytes = kPageSize * D * ES;
     static constexpr int kStages =
-        ES == 2 ? (D == 256 ? 3 : (D == 128 ? 4 : 6)) : (D == 64 ? 4 : 3);
+        ES == 2 ? (D == 256 ? 3 : (D == 128 ? 4 : 6)) : (D == 64 ? 4 : 2);
     static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
     static constexpr int kPBufFloats = kPageSize * kMaxHeadsPerCta;  // per warp
     static constexpr int kSmemBytes = kRingBytes + kWarps * kPBufFloats * 4 +
                                       kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 2 * 4 +
                                       kWarps * kStages * 8 + 16;
-    static constexpr int kMinBlocks =
-        ES == 2 ? (D == 256 ? 2 : 3) : (D == 256 ? 1 : (D == 128 ? 2 : 3));
+    static constexpr int kMinBlocks = ES == 2 ? (D == 256 ? 2 : 3) : (D == 256 ? 1 : 3);
+    static_assert(kMinBlocks * (kSmemBytes + 1024) <= 228 * 1024, "CTAs per SM by shared memory");
+};
+
+// Tensor-core kernel configuration per head dim (see pa_attend_mma.cuh).
+template <int D>
+struct MmaCfg {
+    static_assert(D % 64 == 0 || (D % 64 == 32 && (D / 32) % 2 == 1),
+                  "head dim: 64-column slabs, or an odd number of 32-column units");
+    static constexpr bool kRows64 = (D % 64) != 0;  // one 3-D box, 64-byte units, 64-byte swizzle
+    static constexpr int kFullSlabs = D / 64;       // else: 128-byte slabs (128-byte swizzle)
+    static constexpr int kSlabBytes = kPageSize * 128;
+    static constexpr int kPageBytes = kPageSize * D * 2;
+    // pages in flight per warp; with the fixed buffers below this keeps
+    // kMinBlocks CTAs per SM within 228 KiB of shared memory
+    static constexpr int kStages = D == 256 ? 3 : (D == 128 ? 4 : (D == 96 ? 5 : 6));
+    static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
+    // output dims combined per round at a partition edge
+    static constexpr int kXDims = (D % 64 == 0) ? 64 : 32;
+    static constexpr int kXBytes = kWarps * kMaxHeadsPerCta * 64 * 4;
+    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes + kXBytes +
+                                      kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 3 * 4 +
+                                      kWarps * kStages * 8 + 16;
+    static constexpr int kMinBlocks = D == 256 ? 2 : 3;
+    static_assert(kMinBlocks * (kSmemBytes + 1024) <= 228 * 1024, "CTAs per SM by shared memory");
+    static_assert(kRows64 || kPageBytes == kFullSlabs * kSlabBytes, "slab layout");
+    static_assert(kPageBytes % 1024 == 0, "page slots keep the 1 KiB swizzle alignment");
 };
 
 // The in-kernel merge of the tensor-core kernel issues all of its loads at
@@ -221,5 +246,5 @@ __device__ __forceinline__ void wait_for_prerequisite_grid() {
 namespace pa {
 cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 grid,
                           cudaStream_t stream);
-int attend_ctas_per_sm(int D);
+int attend_ctas_per_sm(int kernel, int dtype, int D);
 }  // namespace pa

@@ -65,12 +65,11 @@ def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=N
         max_context_len = max(case.max_context_len, 0)
     if num_sms is None:
         num_sms = torch.cuda.get_device_properties(0).multi_processor_count
-    plan = pa.pa_plan(B, Hq, case.Hkv, D, case.page_size, case.num_pages, case.max_pages_per_seq,
-                      max_context_len, case.window, partition_size, num_sms)
-    if KERNEL is not None:
-        plan.kernel = KERNELS[KERNEL]
-    plan.dtype = {"f16": 0, "bf16": 1, "f32": 2}[case.dtype]
-    plan.rope_theta = case.rope_theta
+    plan = pa.pa_plan_ex(B, Hq, case.Hkv, D, case.page_size, case.num_pages,
+                         case.max_pages_per_seq, max_context_len, case.window, partition_size,
+                         num_sms, dtype={"f16": 0, "bf16": 1, "f32": 2}[case.dtype],
+                         kernel=KERNELS[KERNEL] if KERNEL is not None else 0,
+                         rope_theta=case.rope_theta)
     if parts_per_cta is not None:
         plan.parts_per_cta = parts_per_cta
     if merge_in_kernel is not None:

@@ -204,3 +204,33 @@ def test_bench_counts_algorithmic_bytes_per_element_type():
     for dtype, eb in (("f16", 2), ("bf16", 2), ("f32", 4)):
         c = workloads.make_case("b", 2, 4, 2, 64, [100, 40], seed=1, window=64, dtype=dtype)
         assert bench.kv_bytes(c) == 2 * eb * 2 * 64 * (64 + 40)
+
+
+def test_plan_ex_picks_the_kernel_and_sizes_for_its_residency():
+    args = (4, 32, 8, 128, 16, 10000, 2048, 32768, 0, 0, 152)
+    f16 = pa.pa_plan_ex(*args)
+    assert f16.kernel == binding.PA_KERNEL_MMA and f16.dtype == binding.PA_DTYPE_F16
+    bf16 = pa.pa_plan_ex(*args, dtype=binding.PA_DTYPE_BF16)
+    assert bf16.kernel == binding.PA_KERNEL_MMA and bf16.dtype == binding.PA_DTYPE_BF16
+    f32 = pa.pa_plan_ex(*args, dtype=binding.PA_DTYPE_F32)
+    assert f32.kernel == binding.PA_KERNEL_SIMT and f32.merge_in_kernel == 0
+    rope = pa.pa_plan_ex(*args, rope_theta=10000.0)
+    assert rope.kernel == binding.PA_KERNEL_SIMT and rope.rope_theta == 10000.0
+    # fp32 at D = 256 keeps one CTA per SM, so its automatic grid is smaller
+    wide = (4, 24, 4, 256, 16, 10000, 2048, 32768, 0, 0, 152)
+    assert (pa.pa_plan_ex(*wide, dtype=binding.PA_DTYPE_F32).ctas <
+            pa.pa_plan_ex(*wide).ctas)
+    for kw, st in ((dict(dtype=binding.PA_DTYPE_F32, kernel=binding.PA_KERNEL_MMA),
+                    binding.PA_ERR_UNSUPPORTED),
+                   (dict(rope_theta=1e4, kernel=binding.PA_KERNEL_MMA), binding.PA_ERR_UNSUPPORTED),
+                   (dict(dtype=binding.PA_DTYPE_BF16, kernel=binding.PA_KERNEL_SIMT),
+                    binding.PA_ERR_UNSUPPORTED),
+                   (dict(dtype=9), binding.PA_ERR_INVALID_ARG),
+                   (dict(kernel=7), binding.PA_ERR_INVALID_ARG),
+                   (dict(rope_theta=-2.0), binding.PA_ERR_INVALID_ARG)):
+        with pytest.raises(pa.PAError) as e:
+            pa.pa_plan_ex(*args, **kw)
+        assert e.value.status == st
+    with pytest.raises(pa.PAError):
+        pa.pa_plan_ex(4, 32, 8, 96, 16, 10000, 2048, 32768, 0, 0, 152,
+                      kernel=binding.PA_KERNEL_SIMT)
