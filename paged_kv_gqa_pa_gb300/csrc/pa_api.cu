@@ -89,8 +89,9 @@ static bool make_page_map(CUtensorMap* map, const void* base, long long rows, in
 }
 
 // CTAs of the partition kernel resident per SM (the launch bound, which the
-// configurations' static checks also guarantee in shared memory).
-int attend_ctas_per_sm(int kernel, int dtype, int D) {
+// configurations' static checks also guarantee in shared memory), for G query
+// heads per CTA.
+int attend_ctas_per_sm(int kernel, int dtype, int D, int G) {
     if (kernel == PA_KERNEL_MMA) {
         switch (D) {
             case 64: return MmaCfg<64>::kMinBlocks;
@@ -101,9 +102,9 @@ int attend_ctas_per_sm(int kernel, int dtype, int D) {
     }
     const bool f32 = dtype == PA_DTYPE_F32;
     switch (D) {
-        case 64: return f32 ? AttendCfg<64, 4>::kMinBlocks : AttendCfg<64>::kMinBlocks;
-        case 128: return f32 ? AttendCfg<128, 4>::kMinBlocks : AttendCfg<128>::kMinBlocks;
-        default: return f32 ? AttendCfg<256, 4>::kMinBlocks : AttendCfg<256>::kMinBlocks;
+        case 64: return f32 ? AttendCfg<64, 4>::blocks_for(G) : AttendCfg<64>::blocks_for(G);
+        case 128: return f32 ? AttendCfg<128, 4>::blocks_for(G) : AttendCfg<128>::blocks_for(G);
+        default: return f32 ? AttendCfg<256, 4>::blocks_for(G) : AttendCfg<256>::blocks_for(G);
     }
 }
 
@@ -410,8 +411,9 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         constexpr long long kNoSplitBytes = 128 << 10;
         constexpr int kMinPagesPerPart = 2 * kWarps;
         const long long groups = (long long)batch * num_kv_heads * nchunk;
-        const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim);
-        const long long span_bytes = (long long)span * 2 * page_size * head_dim * 2;
+        const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim, G);
+        const long long span_bytes =
+            (long long)span * 2 * page_size * head_dim * (dtype == PA_DTYPE_F32 ? 4 : 2);
         if (groups == 0 || groups >= slots || span_bytes <= kNoSplitBytes) {
             pp = span;
         } else {
@@ -463,7 +465,7 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     // stays short; longer CTAs (more partitions each) measured slower.
     {
         const long long groups = (long long)batch * num_kv_heads * nchunk;
-        const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim);
+        const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim, G);
         const bool many_waves = slots > 0 && groups * P > 4 * slots;
         plan->parts_per_cta = (many_waves && P >= 2 && 2 * pp <= kMaxPagesPerPart) ? 2 : 1;
     }

@@ -105,6 +105,7 @@ __device__ __forceinline__ void half8_to_float(const uint4 raw, float (&f)[8]) {
 // (i <-> i + D/2 of the rotate-half pairing).
 struct RopeLane {
     float c[8], s[8], c1[8], s1[8];
+    float cp[8], sp[8];  // step from past this lane's tokens of one page to its next page
 };
 
 // Rotate this lane's 8 K values (kf) with its partner's (pf) and advance the
@@ -200,10 +201,7 @@ __device__ __forceinline__ void write_rows(const AttendParams& p, int b, int h0,
 }
 
 template <int D, int G, bool SPLIT, bool ROPE, typename E>
-__global__ void __launch_bounds__(kThreads,
-                                  (G >= 7 && AttendCfg<D, sizeof(E)>::kMinBlocks > 2
-                                       ? 2
-                                       : AttendCfg<D, sizeof(E)>::kMinBlocks))
+__global__ void __launch_bounds__(kThreads, AttendCfg<D, sizeof(E)>::blocks_for(G))
     attend_kernel(const AttendParams p) {
     using Cfg = AttendCfg<D, sizeof(E)>;
     constexpr int ES = sizeof(E);
@@ -311,6 +309,8 @@ __global__ void __launch_bounds__(kThreads,
         for (int j = 0; j < 8; ++j) {
             rope_twiddle(1, p.rope_phi[0][rope_f0 + j], p.rope_phi[1][rope_f0 + j], rl.c1[j],
                          rl.s1[j]);
+            rope_twiddle(kWarps * kPageSize - TL, p.rope_phi[0][rope_f0 + j],
+                         p.rope_phi[1][rope_f0 + j], rl.cp[j], rl.sp[j]);
             rope_twiddle(sp.L - 1, p.rope_phi[0][rope_f0 + j], p.rope_phi[1][rope_f0 + j],
                          rl.c[j], rl.s[j]);
         }
@@ -353,13 +353,26 @@ __global__ void __launch_bounds__(kThreads,
             consumed = item + 1;
         }
         if (rope) {
-            // Rotary state at this lane's first token of the page, computed
-            // afresh each page; the tokens after it step by recurrence.
-            const int pos0 = (pg0 + warp + k * kWarps) * kPageSize + rg * TL;
+            // Rotary state at this lane's first token of the page: evaluated
+            // exactly every kRopeResync pages of this warp; in between, the
+            // state the previous page's token recurrence left (TL tokens on)
+            // is turned on to this page by one fixed rotation.
+            constexpr int kRopeResync = 8;
+            if (k % kRopeResync == 0) {
+                const int pos0 = (pg0 + warp + k * kWarps) * kPageSize + rg * TL;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                rope_twiddle(pos0, p.rope_phi[0][rope_f0 + j], p.rope_phi[1][rope_f0 + j],
-                             rl.c[j], rl.s[j]);
+                for (int j = 0; j < 8; ++j)
+                    rope_twiddle(pos0, p.rope_phi[0][rope_f0 + j], p.rope_phi[1][rope_f0 + j],
+                                 rl.c[j], rl.s[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float cn = fmaf(rl.c[j], rl.cp[j], -rl.s[j] * rl.sp[j]);
+                    const float sn = fmaf(rl.s[j], rl.cp[j], rl.c[j] * rl.sp[j]);
+                    rl.c[j] = cn;
+                    rl.s[j] = sn;
+                }
+            }
         }
         float s[G];
         qk_tree<D, G, LN::LOG_TL, E>(s, ring_wp + ((2 * k) % NS) * PB, rg * TL, r, lane, qf, rope,

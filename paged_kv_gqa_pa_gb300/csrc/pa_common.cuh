@@ -80,6 +80,9 @@ struct AttendCfg {
                                       kWarps * kStages * 8 + 16;
     static constexpr int kMinBlocks = ES == 2 ? (D == 256 ? 2 : 3) : (D == 256 ? 1 : 3);
     static_assert(kMinBlocks * (kSmemBytes + 1024) <= 228 * 1024, "CTAs per SM by shared memory");
+    // The launch bound of the G-head instance: seven or eight heads per CTA
+    // keep their q, scores and accumulators in registers only at two CTAs.
+    static constexpr int blocks_for(int G) { return (G >= 7 && kMinBlocks > 2) ? 2 : kMinBlocks; }
 };
 
 // Tensor-core kernel configuration per head dim (see pa_attend_mma.cuh).
@@ -246,5 +249,5 @@ __device__ __forceinline__ void wait_for_prerequisite_grid() {
 namespace pa {
 cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 grid,
                           cudaStream_t stream);
-int attend_ctas_per_sm(int kernel, int dtype, int D);
+int attend_ctas_per_sm(int kernel, int dtype, int D, int G);
 }  // namespace pa
