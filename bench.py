@@ -46,9 +46,9 @@ FALLBACK_HBM_GBS = 6800.0
 # `src_sha` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     # profiles/attend_mma_gqa6_ctx100k_b1.md: one capture of the B = 1 case,
-    # (409.77 + 6.52) MB read + written, scaled by tokens to the B = 4 launch.
-    ("gqa6_ctx100k", "mma"): {"src_sha": "0564c1f71219c348", "partition_size": 512,
-                              "bytes_per_launch": 4 * (409.766656e6 + 6.522112e6)},
+    # (409.76 + 6.25) MB read + written, scaled by tokens to the B = 4 launch.
+    ("gqa6_ctx100k", "mma"): {"src_sha": "61be43378f5b6cf0", "partition_size": 512,
+                              "bytes_per_launch": 4 * (409.764096e6 + 6.251008e6)},
 }
 
 
