@@ -217,7 +217,9 @@ class GpuArm:
         self.lse = torch.empty((B, Hq), dtype=torch.float32, device=device)
         self.ws = pa.new_workspace(self.plan, device)
         self.stream = torch.cuda.current_stream(device)
-        self.launches_per_step = 1 if self.plan.num_partitions == 1 else 2
+        merged_inside = self.plan.cluster > 1 or (
+            self.plan.kernel == KERNEL_IDS["mma"] and self.plan.merge_in_kernel)
+        self.launches_per_step = 1 if (self.plan.num_partitions == 1 or merged_inside) else 2
 
     def partitions(self):
         self.pa.pa_decode_partitions(self.plan, self.q, self.k, self.v, self.bt, self.cl,

@@ -104,7 +104,14 @@ typedef struct pa_plan {
                                pairing of dim i and i + D/2, frequency
                                rope_theta^(-2i/D); q at position L - 1, K_t at t, V
                                untouched), CUDA-core kernel (fp16, fp32); 0 = none */
-    int reserved[2];
+    int cluster;            /* > 1: with the tensor-core kernel, the num_partitions
+                               (== cluster, at most 16) CTAs of each (sequence, KV head,
+                               head chunk) run as one thread-block cluster and merge the
+                               group's partials through distributed shared memory, so
+                               pa_decode_partitions writes out and lse itself and
+                               pa_merge has nothing to do (parts_per_cta must be 1 and
+                               merge_in_kernel 0); 0 or 1: no cluster */
+    int reserved;
 } pa_plan_t;
 
 /* Element types (pa_plan_t.dtype).  bf16 needs the tensor-core kernel, fp32

@@ -58,7 +58,8 @@ class pa_plan_t(ctypes.Structure):
         ("ctrl_bytes", ctypes.c_int),
         ("dtype", ctypes.c_int),
         ("rope_theta", ctypes.c_float),
-        ("reserved", ctypes.c_int * 2),
+        ("cluster", ctypes.c_int),
+        ("reserved", ctypes.c_int),
     ]
 
     def as_dict(self):

@@ -7,6 +7,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -86,6 +87,15 @@ static bool make_page_map(CUtensorMap* map, const void* base, long long rows, in
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
+}
+
+// Clusters of c CTAs that one wave of `slots` resident CTAs holds.  A cluster
+// must fit inside one GPC, so part of the slots stay unused; the fractions
+// are lower bounds of cudaOccupancyMaxActiveClusters measured on GB300 (152
+// SMs, 2 and 3 CTAs per SM) for clusters of up to 8, 9..12 and 13..16 CTAs.
+static long long clusters_per_wave(long long slots, int c) {
+    const long long pct = c <= 8 ? 85 : (c <= 12 ? 80 : 60);
+    return slots * pct / 100 / c;
 }
 
 // CTAs of the partition kernel resident per SM (the launch bound, which the
@@ -187,6 +197,7 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergePara
     const int d0 = blockIdx.z * (kMergeCols * 4);
     const size_t bh = (size_t)b * p.Hq + h;
     const size_t row0 = bh * p.P;
+    allow_dependent_launch();  // the next call's partition grid may be scheduled now
     wait_for_prerequisite_grid();
     const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, p.pages_per_part);
     T* orow = reinterpret_cast<T*>(p.out) + bh * D + d0;
@@ -398,6 +409,7 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     if (span < 1) span = 1;
 
     int pp;  // pages per partition
+    bool use_cluster = false;
     if (partition_size > 0) {
         pp = partition_size / page_size;
     } else {
@@ -414,8 +426,29 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim, G);
         const long long span_bytes =
             (long long)span * 2 * page_size * head_dim * (dtype == PA_DTYPE_F32 ? 4 : 2);
+        // Cluster merge (tensor-core kernel): the largest cluster C (2 ..
+        // kMaxClusterParts) of which one wave holds one per group, when the
+        // span cut C ways gives short partitions (at most
+        // kClusterMaxPagesPerPart pages).  The grid is then that single wave
+        // and the merge stays on chip.  Longer partitions keep the
+        // whole-wave split below: a cluster wave leaves slots empty and some
+        // SMs with more CTAs than others, which costs more there than the
+        // merge launch saves (measured on GB300).
+        constexpr int kClusterMaxPagesPerPart = 64;
+        long long cpar = 0;
+        for (int c = kMaxClusterParts; c >= 2 && groups > 0; --c) {
+            if (clusters_per_wave(slots, c) >= groups) {
+                cpar = c;
+                break;
+            }
+        }
+        const int cpp = cpar >= 2 ? std::max<int>((int)((span + cpar - 1) / cpar), kMinPagesPerPart) : 0;
         if (groups == 0 || groups >= slots || span_bytes <= kNoSplitBytes) {
             pp = span;
+        } else if (kernel == PA_KERNEL_MMA && cpar >= 2 && cpp <= kClusterMaxPagesPerPart &&
+                   (span + cpp - 1) / cpp >= 2) {
+            pp = cpp;
+            use_cluster = true;
         } else {
             pp = span;
             for (long long waves = 1; waves <= 64; ++waves) {
@@ -456,8 +489,11 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     // Merge inside the partition kernel when a group's partials are small
     // (its last CTA merges them, no second launch); the merge kernel when they
     // are many (the one-CTA merge would then trail the grid).
+    plan->cluster = (use_cluster && P >= 2 && P <= kMaxClusterParts) ? P : 0;
     plan->merge_in_kernel =
-        (kernel == PA_KERNEL_MMA && P > 1 && kFusedMergeFits(G, head_dim, P)) ? 1 : 0;
+        (kernel == PA_KERNEL_MMA && P > 1 && plan->cluster == 0 && kFusedMergeFits(G, head_dim, P))
+            ? 1
+            : 0;
     // Partitions per CTA (tensor-core kernel): when the one-partition grid
     // runs many waves of resident CTAs (more than four), let each CTA stream
     // two consecutive partitions.  That halves the CTA prologues and
@@ -467,7 +503,8 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         const long long groups = (long long)batch * num_kv_heads * nchunk;
         const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim, G);
         const bool many_waves = slots > 0 && groups * P > 4 * slots;
-        plan->parts_per_cta = (many_waves && P >= 2 && 2 * pp <= kMaxPagesPerPart) ? 2 : 1;
+        plan->parts_per_cta =
+            (plan->cluster == 0 && many_waves && P >= 2 && 2 * pp <= kMaxPagesPerPart) ? 2 : 1;
     }
     plan->ctas = (int)(((P + plan->parts_per_cta - 1) / plan->parts_per_cta) * num_kv_heads *
                        nchunk * (long long)batch);
@@ -509,6 +546,12 @@ static int check_plan(const pa_plan_t* plan) {
         !kFusedMergeFits(plan->heads_per_cta, plan->head_dim, plan->num_partitions))
         return PA_ERR_INVALID_ARG;
     if (plan->kernel != PA_KERNEL_SIMT && plan->kernel != PA_KERNEL_MMA) return PA_ERR_INVALID_ARG;
+    if (plan->cluster < 0) return PA_ERR_INVALID_ARG;
+    if (plan->cluster > 1 &&
+        (plan->kernel != PA_KERNEL_MMA || plan->cluster > kMaxClusterParts ||
+         plan->num_partitions != plan->cluster || plan->parts_per_cta != 1 ||
+         plan->merge_in_kernel))
+        return PA_ERR_INVALID_ARG;
     if (plan->parts_per_cta < 1 ||
         (long long)plan->parts_per_cta * (plan->partition_size / kPageSize) > kMaxPagesPerPart)
         return PA_ERR_INVALID_ARG;
@@ -556,6 +599,7 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     p.err = reinterpret_cast<unsigned*>(ws);
     p.counters = reinterpret_cast<unsigned*>(ws + wl.ctr_off);
     p.merge_in_kernel = (plan->kernel == PA_KERNEL_MMA && P > 1 && plan->merge_in_kernel) ? 1 : 0;
+    p.cluster = (plan->kernel == PA_KERNEL_MMA && P > 1 && plan->cluster > 1) ? plan->cluster : 0;
     p.B = plan->batch;
     p.Hq = plan->num_q_heads;
     p.Hkv = plan->num_kv_heads;
@@ -611,8 +655,8 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
     if (!workspace) return PA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return PA_ERR_INVALID_ARG;
     if (plan->batch == 0 || plan->num_partitions == 1) return PA_OK;
-    // The partition kernel already merged in its last CTAs.
-    if (plan->kernel == PA_KERNEL_MMA && plan->merge_in_kernel) return PA_OK;
+    // The partition kernel already merged (in its last CTAs, or in each cluster).
+    if (plan->kernel == PA_KERNEL_MMA && (plan->merge_in_kernel || plan->cluster > 1)) return PA_OK;
     if (!context_lens || !out || !lse || !aligned16(out)) return PA_ERR_INVALID_ARG;
     const int D = plan->head_dim;
     const int nchunk = plan->num_q_heads / plan->num_kv_heads / plan->heads_per_cta;

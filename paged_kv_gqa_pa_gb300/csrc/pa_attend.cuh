@@ -32,6 +32,7 @@
 #include <math.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "pa_common.cuh"
 
@@ -47,24 +48,32 @@ struct Lanes {
     static_assert(R * kPageSize / 2 == D, "lane layout");
 };
 
-// This lane's 8 consecutive elements starting at `src` (16 bytes of fp16 or
-// 32 bytes of fp32), as floats.
-template <typename E>
-__device__ __forceinline__ void load8(const unsigned char* src, float (&f)[8]);
+// Packed fp32 pair arithmetic: one fma.rn.f32x2 / mul.rn.f32x2 instruction
+// (sm_100 and later) does the operation on both halves, which halves the
+// issue slots of the lane-local rotations, dot products and P.V updates.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
-__device__ __forceinline__ void half8_to_float(const uint4 raw, float (&f)[8]);
+// This lane's 8 consecutive elements starting at `src` (16 bytes of fp16 or
+// 32 bytes of fp32), as 4 float pairs (dims 2j, 2j + 1 in f[j]).
+template <typename E>
+__device__ __forceinline__ void load8(const unsigned char* src, float2 (&f)[4]);
+
+__device__ __forceinline__ void half8_to_float(const uint4 raw, float2 (&f)[4]);
 
 template <>
-__device__ __forceinline__ void load8<__half>(const unsigned char* src, float (&f)[8]) {
+__device__ __forceinline__ void load8<__half>(const unsigned char* src, float2 (&f)[4]) {
     half8_to_float(*reinterpret_cast<const uint4*>(src), f);
 }
 
 template <>
-__device__ __forceinline__ void load8<float>(const unsigned char* src, float (&f)[8]) {
+__device__ __forceinline__ void load8<float>(const unsigned char* src, float2 (&f)[4]) {
     const float4 a = reinterpret_cast<const float4*>(src)[0];
     const float4 b = reinterpret_cast<const float4*>(src)[1];
-    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    f[0] = make_float2(a.x, a.y);
+    f[1] = make_float2(a.z, a.w);
+    f[2] = make_float2(b.x, b.y);
+    f[3] = make_float2(b.z, b.w);
 }
 
 template <typename E>
@@ -89,37 +98,41 @@ __device__ __forceinline__ void store4e(E* dst, float a, float b, float c, float
     }
 }
 
-__device__ __forceinline__ void half8_to_float(const uint4 raw, float (&f)[8]) {
+__device__ __forceinline__ void half8_to_float(const uint4 raw, float2 (&f)[4]) {
     const __half2* h = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float2 t = __half22float2(h[j]);
-        f[2 * j] = t.x;
-        f[2 * j + 1] = t.y;
-    }
+    for (int j = 0; j < 4; ++j) f[j] = __half22float2(h[j]);
 }
 
-// Rotary state of a lane: cos/sin of its 8 frequencies at the position of
-// the next token it scores, and the one-token step.  The lane's dims are
-// [8r, 8r + 8) of the row; the lane r ^ (R/2) holds the partner dims
-// (i <-> i + D/2 of the rotate-half pairing).
+// Rotary state of a lane: cos and signed sin of its 8 frequencies at the
+// position of the next token it scores, and the one-token step, as pairs
+// (frequencies 2j, 2j + 1 in element j).  The lane's dims are [8r, 8r + 8) of
+// the row; the lane r ^ (R/2) holds the partner dims (i <-> i + D/2 of the
+// rotate-half pairing).  With sigma = -1 on the first half of the row and +1
+// on the second, a rotated value is x cos + partner sigma sin, so every sine
+// here carries sigma: the recurrence keeps its form because sigma^2 = 1.
 struct RopeLane {
-    float c[8], s[8], c1[8], s1[8];
-    float cp[8], sp[8];  // step from past this lane's tokens of one page to its next page
+    float2 c[4], s[4];             // cos, sigma sin at the next position
+    float2 c1[4], s1[4], ns1[4];   // one-token step: cos, sigma sin, -sigma sin
 };
+
+// (c, s) <- (c, s) turned by the angle whose (cos, sigma sin, -sigma sin) are
+// (cr, sr, nsr): c' = c cr - s sr, s' = s cr + c sr.
+__device__ __forceinline__ void rope_turn(float2& c, float2& s, float2 cr, float2 sr, float2 nsr) {
+    const float2 cn = fma2(c, cr, mul2(s, nsr));
+    const float2 sn = fma2(s, cr, mul2(c, sr));
+    c = cn;
+    s = sn;
+}
 
 // Rotate this lane's 8 K values (kf) with its partner's (pf) and advance the
 // rotary state by one position.
-__device__ __forceinline__ void rope_apply_and_step(float (&kf)[8], const float (&pf)[8],
-                                                    bool low, RopeLane& rl) {
+__device__ __forceinline__ void rope_apply_and_step(float2 (&kf)[4], const float2 (&pf)[4],
+                                                    RopeLane& rl) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float c = rl.c[j], s = rl.s[j];
-        kf[j] = low ? fmaf(kf[j], c, -pf[j] * s) : fmaf(kf[j], c, pf[j] * s);
-        const float cn = fmaf(c, rl.c1[j], -s * rl.s1[j]);
-        const float sn = fmaf(s, rl.c1[j], c * rl.s1[j]);
-        rl.c[j] = cn;
-        rl.s[j] = sn;
+    for (int j = 0; j < 4; ++j) {
+        kf[j] = fma2(kf[j], rl.c[j], mul2(pf[j], rl.s[j]));
+        rope_turn(rl.c[j], rl.s[j], rl.c1[j], rl.s1[j], rl.ns1[j]);
     }
 }
 
@@ -130,14 +143,14 @@ __device__ __forceinline__ void rope_apply_and_step(float (&kf)[8], const float 
 // Tokens are visited in increasing order, which the rotary recurrence relies on.
 template <int D, int G, int LEVEL, typename E>
 __device__ __forceinline__ void qk_tree(float (&res)[G], const unsigned char* kpage, int tok,
-                                        int r, int lane, const float (&qf)[G][8], bool rope,
+                                        int r, int lane, const float2 (&qf)[G][4], bool rope,
                                         RopeLane& rl) {
     if constexpr (LEVEL == 0) {
         const unsigned char* src = kpage + tok * (D * (int)sizeof(E)) + r * (8 * (int)sizeof(E));
-        float kf[8];
+        float2 kf[4];
         if (rope) {  // warp-uniform
             constexpr int kHalf = D / 16;  // lanes per half row
-            float pf[8];
+            float2 pf[4];
             if constexpr (sizeof(E) == 2) {
                 // exchange the packed fp16 words (4 shuffles), then widen
                 const uint4 raw = *reinterpret_cast<const uint4*>(src);
@@ -151,18 +164,22 @@ __device__ __forceinline__ void qk_tree(float (&res)[G], const unsigned char* kp
             } else {
                 load8<E>(src, kf);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) pf[j] = __shfl_xor_sync(0xffffffffu, kf[j], kHalf);
+                for (int j = 0; j < 4; ++j) {
+                    pf[j].x = __shfl_xor_sync(0xffffffffu, kf[j].x, kHalf);
+                    pf[j].y = __shfl_xor_sync(0xffffffffu, kf[j].y, kHalf);
+                }
             }
-            rope_apply_and_step(kf, pf, (r & kHalf) == 0, rl);
+            rope_apply_and_step(kf, pf, rl);
         } else {
             load8<E>(src, kf);
         }
+        // even and odd dims accumulate in the two halves of a pair
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float a = qf[h][0] * kf[0];
+            float2 a = mul2(qf[h][0], kf[0]);
 #pragma unroll
-            for (int j = 1; j < 8; ++j) a = fmaf(qf[h][j], kf[j], a);
-            res[h] = a;
+            for (int j = 1; j < 4; ++j) a = fma2(qf[h][j], kf[j], a);
+            res[h] = a.x + a.y;
         }
     } else {
         float lo[G], hi[G];
@@ -214,13 +231,20 @@ __global__ void __launch_bounds__(kThreads, AttendCfg<D, sizeof(E)>::blocks_for(
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;                                         // [warps][NS][PB]
-    float* pbuf = reinterpret_cast<float*>(smem + Cfg::kRingBytes);     // [warps][16][8]
+    float* pbuf = reinterpret_cast<float*>(smem + Cfg::kRingBytes);     // [warps][16][2 GP]
     int* s_pid = reinterpret_cast<int*>(pbuf + kWarps * Cfg::kPBufFloats);  // [kMaxPagesPerPart]
     float* s_ml = reinterpret_cast<float*>(s_pid + kMaxPagesPerPart);   // [warps][2][8]
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 2);
     __shared__ int s_flag;
+    // rotary page turn per frequency: cos, sin, -sin
+    __shared__ __align__(16) float s_rstep[ROPE ? 3 * (D / 2) : 4];
+    static_assert(Cfg::blocks_for(G) * (Cfg::kSmemBytes + sizeof(s_rstep) + 16 + 1024) <=
+                      228 * 1024,
+                  "CTAs per SM by shared memory, static part included");
 
+    // Programmatic dependent launch (see the tensor-core kernel).
     allow_dependent_launch();
+    wait_for_prerequisite_grid();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int part = blockIdx.x;
@@ -259,6 +283,15 @@ __global__ void __launch_bounds__(kThreads, AttendCfg<D, sizeof(E)>::blocks_for(
         }
         s_pid[j] = id;
     }
+    if constexpr (ROPE) {
+        for (int i = threadIdx.x; i < D / 2; i += kThreads) {
+            float c, sn;
+            rope_twiddle(kWarps * kPageSize - TL, p.rope_phi[0][i], p.rope_phi[1][i], c, sn);
+            s_rstep[i] = c;
+            s_rstep[D / 2 + i] = sn;
+            s_rstep[D + i] = -sn;
+        }
+    }
     __syncthreads();
     if (s_flag) {
         if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
@@ -292,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, AttendCfg<D, sizeof(E)>::blocks_for(
     // ---- q for this lane's 8 dims, all G heads (fp32)
     const int r = lane % R;
     const int rg = lane / R;
-    float qf[G][8];
+    float2 qf[G][4];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         load8<E>(reinterpret_cast<const unsigned char*>(p.q) +
@@ -301,39 +334,50 @@ __global__ void __launch_bounds__(kThreads, AttendCfg<D, sizeof(E)>::blocks_for(
     }
     // Rotary embedding: q to position L - 1; the K rows follow per token.
     constexpr bool rope = ROPE;  // rotary instances are separate, so the plain ones pay nothing
-    const bool rope_low = (r & (D / 16)) == 0;
-    const int rope_f0 = (r & (D / 16 - 1)) * 8;  // this lane's first frequency
+    const float sigma = (r & (D / 16)) == 0 ? -1.f : 1.f;  // first / second half of the row
+    const int rope_f0 = (r & (D / 16 - 1)) * 8;            // this lane's first frequency
     RopeLane rl;
     if (rope) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            rope_twiddle(1, p.rope_phi[0][rope_f0 + j], p.rope_phi[1][rope_f0 + j], rl.c1[j],
-                         rl.s1[j]);
-            rope_twiddle(kWarps * kPageSize - TL, p.rope_phi[0][rope_f0 + j],
-                         p.rope_phi[1][rope_f0 + j], rl.cp[j], rl.sp[j]);
-            rope_twiddle(sp.L - 1, p.rope_phi[0][rope_f0 + j], p.rope_phi[1][rope_f0 + j],
-                         rl.c[j], rl.s[j]);
+        for (int j = 0; j < 4; ++j) {
+            float c[2], sn[2], c1[2], s1[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int f = rope_f0 + 2 * j + e;
+                rope_twiddle(1, p.rope_phi[0][f], p.rope_phi[1][f], c1[e], s1[e]);
+                rope_twiddle(sp.L - 1, p.rope_phi[0][f], p.rope_phi[1][f], c[e], sn[e]);
+            }
+            rl.c1[j] = make_float2(c1[0], c1[1]);
+            rl.s1[j] = make_float2(sigma * s1[0], sigma * s1[1]);
+            rl.ns1[j] = make_float2(-sigma * s1[0], -sigma * s1[1]);
+            rl.c[j] = make_float2(c[0], c[1]);
+            rl.s[j] = make_float2(sigma * sn[0], sigma * sn[1]);
         }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float pq[8];
+            float2 pq[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) pq[j] = __shfl_xor_sync(0xffffffffu, qf[h][j], D / 16);
+            for (int j = 0; j < 4; ++j) {
+                pq[j].x = __shfl_xor_sync(0xffffffffu, qf[h][j].x, D / 16);
+                pq[j].y = __shfl_xor_sync(0xffffffffu, qf[h][j].y, D / 16);
+            }
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                qf[h][j] = rope_low ? fmaf(qf[h][j], rl.c[j], -pq[j] * rl.s[j])
-                                    : fmaf(qf[h][j], rl.c[j], pq[j] * rl.s[j]);
+            for (int j = 0; j < 4; ++j) qf[h][j] = fma2(qf[h][j], rl.c[j], mul2(pq[j], rl.s[j]));
         }
     }
+    // (cos, sigma sin, -sigma sin) of the turn from past this lane's tokens of
+    // one page to its next page, from the shared table
+    const float* rstep_s = s_rstep + (sigma < 0.f ? D : D / 2);
+    const float* rstep_ns = s_rstep + (sigma < 0.f ? D / 2 : D);
 
-    float o[G][8];
+    float2 o[G][4];
     float m[G], lsum[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         m[h] = -INFINITY;
         lsum[h] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) o[h][j] = 0.f;
+        for (int j = 0; j < 4; ++j) o[h][j] = make_float2(0.f, 0.f);
     }
     float* pw = pbuf + warp * Cfg::kPBufFloats;
     const int t_own = lane >> 1;  // token of the page whose scores this lane ends up with
@@ -361,16 +405,23 @@ __global__ void __launch_bounds__(kThreads, AttendCfg<D, sizeof(E)>::blocks_for(
             if (k % kRopeResync == 0) {
                 const int pos0 = (pg0 + warp + k * kWarps) * kPageSize + rg * TL;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    rope_twiddle(pos0, p.rope_phi[0][rope_f0 + j], p.rope_phi[1][rope_f0 + j],
-                                 rl.c[j], rl.s[j]);
+                for (int j = 0; j < 4; ++j) {
+                    float c[2], sn[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int f = rope_f0 + 2 * j + e;
+                        rope_twiddle(pos0, p.rope_phi[0][f], p.rope_phi[1][f], c[e], sn[e]);
+                    }
+                    rl.c[j] = make_float2(c[0], c[1]);
+                    rl.s[j] = make_float2(sigma * sn[0], sigma * sn[1]);
+                }
             } else {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float cn = fmaf(rl.c[j], rl.cp[j], -rl.s[j] * rl.sp[j]);
-                    const float sn = fmaf(rl.s[j], rl.cp[j], rl.c[j] * rl.sp[j]);
-                    rl.c[j] = cn;
-                    rl.s[j] = sn;
+                for (int j = 0; j < 4; ++j) {
+                    const int f = rope_f0 + 2 * j;
+                    rope_turn(rl.c[j], rl.s[j], *reinterpret_cast<const float2*>(s_rstep + f),
+                              *reinterpret_cast<const float2*>(rstep_s + f),
+                              *reinterpret_cast<const float2*>(rstep_ns + f));
                 }
             }
         }
@@ -411,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, AttendCfg<D, sizeof(E)>::blocks_for(
                 m[h] = mn;
                 lsum[h] *= a;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) o[h][j] *= a;
+                for (int j = 0; j < 4; ++j) o[h][j] = mul2(o[h][j], make_float2(a, a));
             }
         }
 #pragma unroll
@@ -420,10 +471,10 @@ __global__ void __launch_bounds__(kThreads, AttendCfg<D, sizeof(E)>::blocks_for(
             lsum[h] += e;
             s[h] = e;
         }
-        if ((lane & 1) == 0) {
+        // lanes 2t and 2t + 1 hold the same scores: each writes one half of
+        // the (p, p) pairs the P.V step multiplies with
 #pragma unroll
-            for (int h = 0; h < G; ++h) pw[t_own * GP + h] = s[h];
-        }
+        for (int h = 0; h < G; ++h) pw[t_own * 2 * GP + 2 * h + (lane & 1)] = s[h];
         __syncwarp();
 
         // ---------------- V page: o += p * V
@@ -439,32 +490,39 @@ __global__ void __launch_bounds__(kThreads, AttendCfg<D, sizeof(E)>::blocks_for(
         }
         const unsigned char* vpage = ring_wp + ((2 * k + 1) % NS) * PB;
         const int vpos0 = (pg0 + warp + k * kWarps) * kPageSize;
+        auto pv_page = [&](auto edge) {
 #pragma unroll
-        for (int i = 0; i < TL; ++i) {
-            const int t = rg * TL + i;
-            float vf[8];
-            load8<E>(vpage + t * (D * ES) + r * (8 * ES), vf);
-            // Slots outside [start, L) carry weight 0; zero their V too so that
-            // whatever an unwritten slot holds (NaN included) cannot leak in.
-            if (vpos0 + t < sp.start || vpos0 + t >= sp.L) {
+            for (int i = 0; i < TL; ++i) {
+                const int t = rg * TL + i;
+                float2 vf[4];
+                load8<E>(vpage + t * (D * ES) + r * (8 * ES), vf);
+                // Slots outside [start, L) carry weight 0; zero their V too so
+                // that whatever an unwritten slot holds (NaN included) cannot
+                // leak in.  Only a page at an edge of the span has such slots.
+                if constexpr (decltype(edge)::value) {
+                    if (vpos0 + t < sp.start || vpos0 + t >= sp.L) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) vf[j] = 0.f;
+                        for (int j = 0; j < 4; ++j) vf[j] = make_float2(0.f, 0.f);
+                    }
+                }
+                float2 pr[GP];
+#pragma unroll
+                for (int h2 = 0; h2 < GP; h2 += 2) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(pw + t * 2 * GP + 2 * h2);
+                    pr[h2] = make_float2(t4.x, t4.y);
+                    pr[h2 + 1] = make_float2(t4.z, t4.w);
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) o[h][j] = fma2(pr[h], vf[j], o[h][j]);
+                }
             }
-            float pr[GP];
-#pragma unroll
-            for (int h4 = 0; h4 < GP; h4 += 4) {
-                const float4 t4 = *reinterpret_cast<const float4*>(pw + t * GP + h4);
-                pr[h4] = t4.x;
-                pr[h4 + 1] = t4.y;
-                pr[h4 + 2] = t4.z;
-                pr[h4 + 3] = t4.w;
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) o[h][j] = fmaf(pr[h], vf[j], o[h][j]);
-            }
-        }
+        };
+        if (vpos0 < sp.start || vpos0 + kPageSize > sp.L)  // warp-uniform
+            pv_page(std::true_type{});
+        else
+            pv_page(std::false_type{});
         __syncwarp();
         if (lane == 0 && 2 * k + 1 + NS < n_items) {
             fence_proxy_async_smem();
@@ -495,7 +553,10 @@ __global__ void __launch_bounds__(kThreads, AttendCfg<D, sizeof(E)>::blocks_for(
 #pragma unroll
         for (int h = 0; h < G; ++h) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) o[h][j] += __shfl_xor_sync(0xffffffffu, o[h][j], mask);
+            for (int j = 0; j < 4; ++j) {
+                o[h][j].x += __shfl_xor_sync(0xffffffffu, o[h][j].x, mask);
+                o[h][j].y += __shfl_xor_sync(0xffffffffu, o[h][j].y, mask);
+            }
         }
     }
     __syncthreads();  // every warp is done with its ring: reuse it for the warp states
@@ -504,8 +565,8 @@ __global__ void __launch_bounds__(kThreads, AttendCfg<D, sizeof(E)>::blocks_for(
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             float4* dst = reinterpret_cast<float4*>(s_o + (warp * G + h) * D + r * 8);
-            dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-            dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+            dst[0] = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+            dst[1] = make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
         }
     }
     if (lane == 0) {
@@ -601,7 +662,17 @@ cudaError_t launch_attend_d(int G, bool split, const AttendParams& p, dim3 grid,
         if (dev >= 0 && dev < kMaxDevices) configured[dev].fetch_or(bit);
     }
     void* args[] = {const_cast<AttendParams*>(&p)};
-    return cudaLaunchKernel(fn, grid, dim3(kThreads), args, Cfg::kSmemBytes, stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace pa

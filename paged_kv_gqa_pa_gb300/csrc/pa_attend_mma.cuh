@@ -276,6 +276,110 @@ __device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, co
     }
 }
 
+// ---- Merge inside a thread-block cluster.  With plan.cluster = C the C
+// partitions of a (sequence, KV head, head chunk) run as one cluster (grid.x =
+// C, cluster C x 1 x 1).  Each CTA leaves its partial -- the normalised o of
+// its G heads and their (m, l) -- in its own shared memory, the cluster
+// synchronises, and every CTA then merges a 1/C share of the (head, 4-dim
+// column) items by reading all C partials through distributed shared memory
+// (the log-sum-exp algebra of Phase 2 in the commit note).  No partial goes
+// through global memory, no counter is needed, and there is no second launch.
+// A second cluster barrier keeps every CTA's shared memory alive until all
+// peers have read it.  Every CTA of the cluster reaches both barriers (no
+// path returns between them), and every wait before them is bounded.
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Shared-memory address `addr` of this CTA mapped to the same offset in CTA
+// `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// Layout of a CTA's partial in its shared memory (the idle page ring):
+// o [G][D] (normalised), then m [G] (log2 domain) and l [G].
+template <int D>
+struct ClusterPartial {
+    __host__ __device__ static constexpr int o_off(int h, int d) { return (h * D + d) * 4; }
+    __host__ __device__ static constexpr int m_off(int G, int h) { return (G * D + h) * 4; }
+    __host__ __device__ static constexpr int l_off(int G, int h) { return (G * D + G + h) * 4; }
+};
+
+// A CTA with nothing to contribute (no page of its partition is attended,
+// or a bad page id: then l = NaN, which the merge carries to the output).
+template <int D>
+__device__ __forceinline__ void cluster_partial_fill(float* part, int G, float m, float l) {
+    for (int h = threadIdx.x; h < G; h += kThreads) {
+        part[ClusterPartial<D>::m_off(G, h) / 4] = m;
+        part[ClusterPartial<D>::l_off(G, h) / 4] = l;
+    }
+}
+
+template <int D, typename T>
+__device__ __forceinline__ void cluster_merge(const AttendParams& p, int b, int h0, int G,
+                                              const float* part) {
+    __syncthreads();    // this CTA's partial is complete
+    cluster_barrier();  // ... and so is every peer's
+    const int C = p.cluster;
+    const int rank = (int)cluster_rank();
+    const uint32_t base = smem_u32(part);
+    constexpr int D4 = D / 4;
+    const int items = G * D4;
+    for (int it = rank + C * (int)threadIdx.x; it < items; it += C * kThreads) {
+        const int h = it / D4;
+        const int d = (it % D4) * 4;
+        float M = -INFINITY;
+        for (int c = 0; c < C; ++c)
+            M = fmaxf(M, ld_cluster_f32(map_to_rank(base + ClusterPartial<D>::m_off(G, h), c)));
+        float lam = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < C; ++c) {
+            const float l = ld_cluster_f32(map_to_rank(base + ClusterPartial<D>::l_off(G, h), c));
+            if (l == 0.f) continue;  // nothing attended there; a NaN is kept
+            const float w =
+                ex2(ld_cluster_f32(map_to_rank(base + ClusterPartial<D>::m_off(G, h), c)) - M) * l;
+            const float4 o = ld_cluster_v4(map_to_rank(base + ClusterPartial<D>::o_off(h, d), c));
+            lam += w;
+            acc.x += w * o.x;
+            acc.y += w * o.y;
+            acc.z += w * o.z;
+            acc.w += w * o.w;
+        }
+        const float inv = lam == 0.f ? 0.f : 1.f / lam;  // empty context: out 0, lse -inf
+        const size_t bh = (size_t)b * p.Hq + h0 + h;
+        store4<T>(reinterpret_cast<T*>(p.out) + bh * D + d, acc.x * inv, acc.y * inv,
+                  acc.z * inv, acc.w * inv);
+        if (d == 0)
+            p.lse[bh] = lam == 0.f ? -INFINITY : (M + log2f(lam)) * 0.69314718055994531f;
+    }
+    cluster_barrier();  // every peer is done reading this CTA's shared memory
+}
+
 template <int D, typename T, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     attend_mma_kernel(const AttendParams p, const __grid_constant__ CUtensorMap tmK,
@@ -298,7 +402,11 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 3);
     __shared__ int s_flag;
 
+    // Programmatic dependent launch: let the merge grid (or the next call's
+    // grid) be scheduled now, and read nothing before the grid this one
+    // depends on has completed.
     allow_dependent_launch();
+    wait_for_prerequisite_grid();
     const int G = p.heads_per_cta;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -338,14 +446,22 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
             if (d == 0) p.lse[bh] = lse_val;
         }
     };
+    const bool clustered = SPLIT && p.cluster > 1;
+    float* const cpart = reinterpret_cast<float*>(ring);  // this CTA's partial (cluster merge)
     if (!sp.valid) {
+        // (the same for every CTA of a cluster: they all leave here)
         if (threadIdx.x == 0 && part0 == 0 && blockIdx.y == 0) atomicOr(p.err, PA_DEVERR_BAD_LENGTH);
-        if (!SPLIT || (fused && blockIdx.x == 0)) final_rows(NAN, NAN);
+        if (!SPLIT || ((fused || clustered) && blockIdx.x == 0)) final_rows(NAN, NAN);
         return;  // with a separate merge, the merge writes the NaN rows
     }
     if (part0 >= sp.num_parts) {
         // Nothing attended here.  The group's rows are written here only for
         // an empty context (out = 0, lse = -inf) when no merge kernel runs.
+        if (clustered) {
+            cluster_partial_fill<D>(cpart, G, -INFINITY, 0.f);
+            cluster_merge<D, T>(p, b, h0, G, cpart);
+            return;
+        }
         if (!SPLIT || (fused && sp.num_parts == 0 && blockIdx.x == 0)) final_rows(0.f, -INFINITY);
         return;
     }
@@ -376,6 +492,11 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     __syncthreads();
     if (s_flag) {
         if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+        if (clustered) {  // no copy has been issued: the ring is free
+            cluster_partial_fill<D>(cpart, G, NAN, NAN);
+            cluster_merge<D, T>(p, b, h0, G, cpart);
+            return;
+        }
         for (int q = 0; q < nparts; ++q) fill_rows(part0 + q, NAN, NAN, NAN, NAN);
         if (fused) group_arrive_and_merge<D, T>(p, sp, b, h0, G, xbuf, s_ml,
                                                 reinterpret_cast<float*>(ring));
@@ -571,9 +692,17 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
             }
             if (2 * k + 1 + NS < n_items) issued = 2 * k + 1 + NS + 1;
         }
-        if (!ok && lane == 0) {
-            atomicOr(p.err, PA_DEVERR_TIMEOUT);
-            s_flag = 1;
+        if (!ok) {
+            if (lane == 0) {
+                atomicOr(p.err, PA_DEVERR_TIMEOUT);
+                s_flag = 1;
+            }
+            // Give every copy this warp issued a bounded chance to land, so
+            // that none writes into shared memory after the CTA exits or
+            // while the ring holds the cluster partial.
+            for (int item = consumed; item < issued; ++item)
+                (void)mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
+            consumed = issued;
         }
 
         // ---- partition qp: combine the four warp states.  Exp-sums: lanes
@@ -646,12 +775,20 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
                 }
                 const size_t bh = (size_t)b * p.Hq + h0 + h;
                 if constexpr (SPLIT) {
-                    const size_t row = bh * p.P + part;
-                    *reinterpret_cast<float4*>(p.ws_o + row * D + d) =
-                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-                    if (d == 0) {
-                        p.ws_m[row] = M;
-                        p.ws_l[row] = Ls;
+                    const float4 ov = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                    if (clustered) {
+                        *reinterpret_cast<float4*>(cpart + ClusterPartial<D>::o_off(h, d) / 4) = ov;
+                        if (d == 0) {
+                            cpart[ClusterPartial<D>::m_off(G, h) / 4] = M;
+                            cpart[ClusterPartial<D>::l_off(G, h) / 4] = Ls;
+                        }
+                    } else {
+                        const size_t row = bh * p.P + part;
+                        *reinterpret_cast<float4*>(p.ws_o + row * D + d) = ov;
+                        if (d == 0) {
+                            p.ws_m[row] = M;
+                            p.ws_l[row] = Ls;
+                        }
                     }
                 } else {
                     store4<T>(out + bh * D + d, acc.x * inv, acc.y * inv, acc.z * inv,
@@ -666,11 +803,9 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         }
     }
 
-    if (!ok) {
-        // Give every copy this warp issued a bounded chance to land, so that
-        // none writes into shared memory after the CTA exits.
-        for (int item = consumed; item < issued; ++item)
-            (void)mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
+    if (clustered) {
+        cluster_merge<D, T>(p, b, h0, G, cpart);
+        return;
     }
     if (fused) group_arrive_and_merge<D, T>(p, sp, b, h0, G, xbuf, s_ml,
                                             reinterpret_cast<float*>(ring));
@@ -695,7 +830,29 @@ cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtenso
     }
     void* args[] = {const_cast<AttendParams*>(&p), const_cast<CUtensorMap*>(&maps[0]),
                     const_cast<CUtensorMap*>(&maps[1])};
-    return cudaLaunchKernel(fn, grid, dim3(kThreads), args, MmaCfg<D>::kSmemBytes, stream);
+    const bool clustered = split && p.cluster > 1;
+    if (clustered && p.cluster > 8 &&
+        (dev < 0 || dev >= kMaxDevices || !(configured[dev].load() & 4u))) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) configured[dev].fetch_or(4u);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = MmaCfg<D>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // Cluster merge: the grid.x = cluster partitions of a group form one cluster.
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = clustered ? (unsigned)p.cluster : 1u;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = clustered ? 2 : 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace pa

@@ -15,6 +15,7 @@ constexpr int kPageSize = 16;     // tokens per page
 constexpr int kWarps = 4;         // consumer warps per CTA of the attention kernel
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxPagesPerPart = 256;  // page ids a CTA stages in shared memory
+constexpr int kMaxClusterParts = 16;   // largest cluster (the non-portable limit)
 constexpr int kMaxPartitions = 4096;   // partitions the merge kernel reduces
 constexpr int kMaxHeadsPerCta = 8;
 constexpr int kCtrlBytes = 256;        // workspace control block (device error word)
@@ -38,6 +39,7 @@ struct AttendParams {
     unsigned* err; // device error word
     unsigned* counters;  // per-(sequence, KV head, head chunk) arrival counters (fused merge)
     int merge_in_kernel; // 1: the last CTA of each group merges its partials
+    int cluster;         // > 1: the group's partitions form one cluster and merge in it
     int B, Hq, Hkv, g, num_pages, maxp, max_ctx, window;
     int P;                  // partitions (grid.x)
     int pages_per_part;     // partition size in pages
@@ -74,7 +76,7 @@ struct AttendCfg {
     static constexpr int kStages =
         ES == 2 ? (D == 256 ? 3 : (D == 128 ? 4 : 6)) : (D == 64 ? 4 : 2);
     static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
-    static constexpr int kPBufFloats = kPageSize * kMaxHeadsPerCta;  // per warp
+    static constexpr int kPBufFloats = kPageSize * kMaxHeadsPerCta * 2;  // per warp: (p, p) pairs
     static constexpr int kSmemBytes = kRingBytes + kWarps * kPBufFloats * 4 +
                                       kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 2 * 4 +
                                       kWarps * kStages * 8 + 16;

@@ -51,11 +51,13 @@ def to_device(case, device="cuda"):
 
 
 def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=None,
-            guard=0, parts_per_cta=None, merge_in_kernel=None, ws=None):
+            guard=0, parts_per_cta=None, merge_in_kernel=None, ws=None, cluster=None):
     """Plan + pa_decode through the C ABI.  Returns (out fp64 numpy, lse fp64
     numpy, device error word, plan).  With guard > 0 the outputs and the
     workspace sit inside larger NaN/0xA5-filled buffers whose guard regions are
-    checked afterwards."""
+    checked afterwards.  cluster: True forces the cluster merge (the plan's
+    partition count must be 2..16), False forbids it, None keeps the planner's
+    choice; forcing several partitions per CTA or the last-CTA merge drops it."""
     ensure_built()
     dev = dev or to_device(case)
     B, Hq, D = case.q.shape
@@ -72,8 +74,19 @@ def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=N
                          rope_theta=case.rope_theta)
     if parts_per_cta is not None:
         plan.parts_per_cta = parts_per_cta
+        if parts_per_cta > 1:
+            plan.cluster = 0
     if merge_in_kernel is not None:
         plan.merge_in_kernel = merge_in_kernel
+        if merge_in_kernel:
+            plan.cluster = 0
+    if cluster is True:
+        assert 2 <= plan.num_partitions <= 16, plan.num_partitions
+        plan.cluster = plan.num_partitions
+        plan.parts_per_cta = 1
+        plan.merge_in_kernel = 0
+    elif cluster is False:
+        plan.cluster = 0
     n_out = B * Hq * D
     et = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[case.dtype]
     out_buf = torch.full((n_out + 2 * guard,), float("nan"), dtype=et, device="cuda")

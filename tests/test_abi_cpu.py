@@ -234,3 +234,39 @@ def test_plan_ex_picks_the_kernel_and_sizes_for_its_residency():
     with pytest.raises(pa.PAError):
         pa.pa_plan_ex(4, 32, 8, 96, 16, 10000, 2048, 32768, 0, 0, 152,
                       kernel=binding.PA_KERNEL_SIMT)
+
+
+def test_plan_picks_the_cluster_merge_for_one_wave_splits():
+    # Gemma-2-2b shape: 16 groups, 257 window pages; one wave of 2-per-SM
+    # tensor-core CTAs holds a 12-CTA cluster per group (not a 13..16 one).
+    gemma = pa.pa_plan_ex(4, 8, 4, 256, 16, 3000, 512, 8192, 4096, 0, 152)
+    assert gemma.cluster == gemma.num_partitions == 12
+    assert gemma.parts_per_cta == 1 and gemma.merge_in_kernel == 0
+    assert gemma.partition_size == 22 * 16 and gemma.ctas == 16 * 12
+    # Llama-3.2-1B shape: 8 groups, 192 pages, 16 partitions of 12 pages.
+    llama = pa.pa_plan_ex(1, 32, 8, 64, 16, 300, 192, 3060, 0, 0, 152)
+    assert llama.cluster == 16 and llama.partition_size == 12 * 16
+    # 100 000 tokens do not fit 16 partitions: many partitions and the merge kernel.
+    long = pa.pa_plan_ex(4, 24, 4, 256, 16, 30000, 6250, 100000, 0, 0, 152)
+    assert long.cluster == 0 and long.num_partitions > 16
+    # The CUDA-core kernel never clusters; an explicit partition size never does.
+    assert pa.pa_plan_ex(4, 8, 4, 256, 16, 3000, 512, 8192, 4096, 0, 152,
+                         kernel=binding.PA_KERNEL_SIMT).cluster == 0
+    assert pa.pa_plan_ex(4, 8, 4, 256, 16, 3000, 512, 8192, 4096, 512, 152).cluster == 0
+    # A short context stays unsplit.
+    assert pa.pa_plan_ex(1, 4, 1, 64, 16, 64, 16, 256, 0, 0, 152).cluster == 0
+
+
+def test_cluster_plan_checks_return_before_launch():
+    plan = pa.pa_plan_ex(4, 8, 4, 256, 16, 3000, 512, 8192, 4096, 0, 152)
+    assert plan.cluster == 12
+    for field, value in (("cluster", 17), ("cluster", 8), ("cluster", -1),
+                         ("parts_per_cta", 2), ("merge_in_kernel", 1),
+                         ("kernel", binding.PA_KERNEL_SIMT)):
+        bad = binding.pa_plan_t.from_buffer_copy(plan)
+        setattr(bad, field, value)
+        assert _call_decode(bad) == binding.PA_ERR_INVALID_ARG, (field, value)
+    # pa_merge has nothing to do after a clustered partition kernel.
+    lib = pa.load()
+    assert lib.pa_merge(ctypes.byref(plan), 0x10000, 0x10000, 0x10000, 0x10000, None) == \
+        binding.PA_OK
