@@ -46,9 +46,9 @@ FALLBACK_HBM_GBS = 6800.0
 # `src_sha` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     # profiles/attend_mma_gqa6_ctx100k_b1.md: one capture of the B = 1 case,
-    # (409.76 + 6.25) MB read + written, scaled by tokens to the B = 4 launch.
-    ("gqa6_ctx100k", "mma"): {"src_sha": "61be43378f5b6cf0", "partition_size": 512,
-                              "bytes_per_launch": 4 * (409.764096e6 + 6.251008e6)},
+    # (409.78 + 6.23) MB read + written, scaled by tokens to the B = 4 launch.
+    ("gqa6_ctx100k", "mma"): {"src_sha": "60aa37d10fd06564", "partition_size": 512,
+                              "bytes_per_launch": 4 * (409.783040e6 + 6.225920e6)},
 }
 
 
@@ -279,21 +279,53 @@ def time_steps(arm, steps, warmup, graph_steps=50):
     return start.elapsed_time(end) / (n * reps), n * reps
 
 
-def time_partition_kernel(arm, steps, flush=None):
-    """Mean duration of the partition kernel alone: events on its stream around
-    each launch (the merge runs between, outside the events)."""
+def time_partition_kernel(arm, steps, flush=None, graph_launches=50):
+    """Average duration of one partition-kernel launch, from CUDA events on the
+    stream it runs on.
+
+    Inputs larger than L2 (flush is None): `steps` launches of the partition
+    kernel alone, captured back to back in a CUDA graph and replayed; the
+    events bracket the replays, so the average is the kernel's own time per
+    launch with no host launch gap and no merge in between.  Small inputs:
+    each launch is bracketed by its own events after an L2 flush (outside the
+    events), and the merge runs between launches outside the events."""
     torch = arm.torch
+    if flush is None:
+        n = max(d for d in range(1, min(graph_launches, steps) + 1) if steps % d == 0)
+        reps = steps // n
+        stream = torch.cuda.Stream(arm.device)
+        saved = arm.stream
+        arm.stream = stream
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(n):
+                    arm.partitions()
+            g.replay()
+            torch.cuda.synchronize()
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            for _ in range(reps):
+                g.replay()
+            end.record(stream)
+            torch.cuda.synchronize()
+        arm.stream = saved
+        del g
+        # the graph's last launch leaves partials unmerged: finish that step
+        arm.merge()
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / (n * reps), "CUDA graph of back-to-back launches"
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     for i in range(steps):
-        if flush is not None:
-            flush.fill_(i & 0xFF)
+        flush.fill_(i & 0xFF)
         ev[i][0].record(arm.stream)
         arm.partitions()
         ev[i][1].record(arm.stream)
         arm.merge()
     torch.cuda.synchronize()
-    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return statistics.mean(a.elapsed_time(b) for a, b in ev), "per-launch events, L2 flushed"
 
 
 def time_flushed(arm, iters, flush):
@@ -419,9 +451,13 @@ def e2e_steps(arm, steps, warmup, upload_kv=False):
 
 
 class OracleSampler:
-    """Times the oracle, as it stands, on a bounded sample of the workload:
-    sequence 0, all its query heads, the last L of its attended tokens, with L
-    sized to a time budget from a one-thread calibration run."""
+    """Times the oracle, as it stands, on a bounded sample of the workload.
+
+    The sample is the whole decode step (every sequence and head), repeated
+    as often as the time budget allows, when one step fits the budget;
+    otherwise sequence 0 with all its query heads over the last L of its
+    attended tokens, L sized to the budget.  The per-token cost comes from a
+    one-thread calibration run."""
 
     def __init__(self, case, threads=0):
         import oracle
@@ -430,10 +466,12 @@ class OracleSampler:
         self.threads = threads or os.cpu_count() or 1
         L0 = int(case.context_lens[0])
         self.att = min(L0, case.window) if case.window > 0 else L0
+        self.total = attended_tokens(case)
         probe = max(1, min(self.att, 512))
         t0 = time.perf_counter()
-        self._run(probe, 1)
-        self.sec_per_token_1thread = max((time.perf_counter() - t0) / probe, 1e-9)
+        self._run(self._sub(probe), 1)
+        # seconds per (attended token, query head) on one thread
+        self.sec_per_unit_1thread = max((time.perf_counter() - t0) / (probe * case.Hq), 1e-12)
 
     def _sub(self, L):
         c = self.case
@@ -444,26 +482,41 @@ class OracleSampler:
                               partition_size=0, seed=c.seed, dtype=c.dtype,
                               rope_theta=c.rope_theta)
 
-    def _run(self, L, threads):
-        s = self._sub(L)
+    def _run(self, s, threads):
         self.oracle.decode(s.q, s.k_cache, s.v_cache, s.block_tables, s.context_lens, s.scale,
                            s.window, num_threads=threads, dtype=s.dtype,
                            rope_theta=s.rope_theta)
 
-    def tokens_for(self, budget_s):
-        par = min(self.threads, self.case.Hq)
-        L = int(budget_s * par / self.sec_per_token_1thread)
-        return max(16, min(self.att, L))
-
-    def run(self, L):
-        t0 = time.perf_counter()
-        self._run(L, self.threads)
-        dt = time.perf_counter() - t0
+    def plan(self, budget_s):
+        """(repeats of the whole step, or 0) and L for a sample of about budget_s."""
         c = self.case
-        byts = 2 * ELEM_BYTES[c.dtype] * c.Hkv * c.D * L
-        used = min(self.threads, c.Hq)
-        desc = (f"sequence 0 of {c.B}, all {c.Hq} query heads, last {L} of {self.att} attended "
-                f"tokens; fp64 C oracle, OpenMP over heads")
+        full_s = self.sec_per_unit_1thread * self.total * c.Hq / min(self.threads, c.B * c.Hq)
+        if full_s <= budget_s:
+            return max(1, int(budget_s / max(full_s, 1e-9))), self.total
+        L = int(budget_s * min(self.threads, c.Hq) / (self.sec_per_unit_1thread * c.Hq))
+        return 0, max(16, min(self.att, L))
+
+    def run(self, sample):
+        """Time one sample from plan(); returns (GB/s, seconds, description, threads)."""
+        reps, L = sample
+        c = self.case
+        t0 = time.perf_counter()
+        if reps:
+            for _ in range(reps):
+                self._run(c, self.threads)
+            tokens = reps * self.total
+            used = min(self.threads, c.B * c.Hq)
+            desc = (f"the whole step ({c.B} sequences x {c.Hq} query heads, {self.total} "
+                    f"attended tokens) run {reps} times; fp64 C oracle, OpenMP over "
+                    f"(sequence, head)")
+        else:
+            self._run(self._sub(L), self.threads)
+            tokens = L
+            used = min(self.threads, c.Hq)
+            desc = (f"sequence 0 of {c.B}, all {c.Hq} query heads, last {L} of {self.att} "
+                    f"attended tokens; fp64 C oracle, OpenMP over heads")
+        dt = time.perf_counter() - t0
+        byts = 2 * ELEM_BYTES[c.dtype] * c.Hkv * c.D * tokens
         return byts / dt / 1e9, dt, desc, used
 
 
@@ -474,13 +527,13 @@ def run_reference(args):
     case = workloads.workload(args.workload)
     sampler = OracleSampler(case)
     per_step_budget = args.reference_budget_s / max(1, args.steps + args.warmup)
-    L = sampler.tokens_for(per_step_budget)
+    sample = sampler.plan(per_step_budget)
     for _ in range(args.warmup):
-        sampler.run(L)
+        sampler.run(sample)
     vals, secs = [], []
     desc, used = "", 1
     for _ in range(args.steps):
-        v, dt, desc, used = sampler.run(L)
+        v, dt, desc, used = sampler.run(sample)
         vals.append(v)
         secs.append(dt)
     value = statistics.median(vals)
@@ -542,7 +595,7 @@ def run_gpu(args):
         else:
             ms, _ = time_flushed(arm, args.steps, flush)
             timed_steps = args.steps
-        kern_ms = time_partition_kernel(arm, min(args.steps, 500), flush)
+        kern_ms, kern_timing = time_partition_kernel(arm, min(args.steps, 500), flush)
     if world > 1:
         torch.distributed.barrier()
     arm.check_error()
@@ -588,10 +641,13 @@ def run_gpu(args):
                 entry[kname] = {"us_per_step": us, "partition_kernel_us": kus,
                                 "kv_gbs": b / (us * 1e-6) / 1e9,
                                 "frac_of_measured_hbm": b / (us * 1e-6) / 1e9 / peak,
-                                "frac_of_nominal_8tbs": b / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS}
-                entry.update({"partitions": plan.num_partitions,
-                              "partition_size": plan.partition_size, "ctas": plan.ctas,
-                              "copies": copies, "l2": l2state})
+                                "frac_of_nominal_8tbs": b / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS,
+                                "plan": {"partitions": plan.num_partitions,
+                                         "partition_size": plan.partition_size,
+                                         "ctas": plan.ctas, "cluster": plan.cluster,
+                                         "merge_in_kernel": plan.merge_in_kernel,
+                                         "parts_per_cta": plan.parts_per_cta}}
+                entry.update({"copies": copies, "l2": l2state})
             entry.update({"kv_bytes": b, "timing": "CUDA graph of back-to-back steps over "
                                                   "rotating K/V copies"})
             per[name] = entry
@@ -599,7 +655,7 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         sampler = OracleSampler(case)
-        v, dt, desc, used = sampler.run(sampler.tokens_for(args.cpu_budget_s))
+        v, dt, desc, used = sampler.run(sampler.plan(args.cpu_budget_s))
         cpu = {"value": v, "unit": UNIT, "cores": used, "kind": "oracle", "sample": desc,
                "seconds": dt}
 
@@ -621,7 +677,8 @@ def run_gpu(args):
                          "frac": kern_gbs / peak, "traffic": traffic,
                          "peak_kind": peak_kind,
                          "kernel": f"partition kernel ({KERNEL_NAMES[arm.plan.kernel]})",
-                         "kernel_us": kern_ms * 1e3, "frac_of_nominal_8tbs":
+                         "kernel_us": kern_ms * 1e3, "kernel_timing": kern_timing,
+                         "frac_of_nominal_8tbs":
                              kern_gbs / NOMINAL_HBM_GBS, "src_sha": sha},
             "cpu_baseline": cpu,
             "e2e": e2e,
