@@ -111,7 +111,13 @@ typedef struct pa_plan {
                                pa_decode_partitions writes out and lse itself and
                                pa_merge has nothing to do (parts_per_cta must be 1 and
                                merge_in_kernel 0); 0 or 1: no cluster */
-    int reserved;
+    int prewait_prefetch;   /* tensor-core kernel: pages per warp (0 = off, at most 8)
+                               requested into L2 before the wait for the grid this call
+                               depends on (programmatic dependent launch).  Each CTA reads
+                               its sequence length and first page ids as hints for them;
+                               everything is read again after the wait, so a stale hint
+                               only prefetches a page that is not used */
+    int reserved[2];
 } pa_plan_t;
 
 /* Element types (pa_plan_t.dtype).  bf16 needs the tensor-core kernel, fp32
@@ -185,11 +191,12 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
              void* workspace, void* stream);
 
 /*
- * pa_decode for callers that cannot allocate device memory when they decode
- * (inside a CUDA graph capture, inside an engine or plugin that only hands
- * over its input and output buffers, or in a loop that must never enter the
- * allocator).  The pages have no counterpart: this is a convenience of the
- * library, not a step of the method.
+ * pa_decode for callers that cannot allocate device memory when they decode:
+ * an engine or plugin that is handed only its own input and output buffers and
+ * has no allocator to draw on, or a latency-critical loop that must never enter
+ * the allocator (cudaMalloc can synchronise the whole device).  The pages have
+ * no counterpart: this is a convenience of the library, not a step of the
+ * method.
  *
  * Same arguments, layouts and result as pa_decode, minus the workspace: the
  * partition partials go to a scratch array of PA_STATIC_WORKSPACE_BYTES
@@ -201,6 +208,8 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture on that device.
+ *   - Every call first clears the array's control bytes (plan.ctrl_bytes) on
+ *     `stream` with cudaMemsetAsync, then runs pa_decode on it.
  *   - All calls on a device share the one array, which keeps the previous
  *     call's contents: calls whose kernels overlap on the GPU (different
  *     streams, no ordering between them) race on it and must not be issued.

@@ -59,7 +59,8 @@ class pa_plan_t(ctypes.Structure):
         ("dtype", ctypes.c_int),
         ("rope_theta", ctypes.c_float),
         ("cluster", ctypes.c_int),
-        ("reserved", ctypes.c_int),
+        ("prewait_prefetch", ctypes.c_int),
+        ("reserved", ctypes.c_int * 2),
     ]
 
     def as_dict(self):

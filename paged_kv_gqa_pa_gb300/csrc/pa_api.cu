@@ -89,13 +89,22 @@ static bool make_page_map(CUtensorMap* map, const void* base, long long rows, in
            CUDA_SUCCESS;
 }
 
-// Clusters of c CTAs that one wave of `slots` resident CTAs holds.  A cluster
-// must fit inside one GPC, so part of the slots stay unused; the fractions
-// are lower bounds of cudaOccupancyMaxActiveClusters measured on GB300 (152
-// SMs, 2 and 3 CTAs per SM) for clusters of up to 8, 9..12 and 13..16 CTAs.
-static long long clusters_per_wave(long long slots, int c) {
-    const long long pct = c <= 8 ? 85 : (c <= 12 ? 80 : 60);
-    return slots * pct / 100 / c;
+// Clusters of c CTAs that one wave holds, with per_sm resident CTAs on each
+// of num_sms SMs.  A cluster must fit inside one GPC, so part of the slots
+// stay unused.  The tables are cudaOccupancyMaxActiveClusters of the
+// tensor-core kernel measured on GB300 (152 SMs) at 2 and 3 CTAs per SM, for
+// c = 1..16; other SM counts use the smaller of the two tables' fill
+// fractions.
+static long long clusters_per_wave(int num_sms, int per_sm, int c) {
+    static const short k2[kMaxClusterParts] = {304, 152, 97, 74, 58, 46, 38, 36,
+                                               30,  28,  23, 23, 19, 14, 14, 14};
+    static const short k3[kMaxClusterParts] = {456, 228, 148, 110, 87, 74, 59, 51,
+                                               46,  43,  36,  36,  28, 26, 26, 21};
+    if (c < 1 || c > kMaxClusterParts) return 0;
+    if (num_sms == 152 && per_sm == 2) return k2[c - 1];
+    if (num_sms == 152 && per_sm == 3) return k3[c - 1];
+    const double f = std::min(k2[c - 1] * (double)c / 304.0, k3[c - 1] * (double)c / 456.0);
+    return (long long)((double)num_sms * per_sm * f / c);
 }
 
 // CTAs of the partition kernel resident per SM (the launch bound, which the
@@ -436,8 +445,9 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         // merge launch saves (measured on GB300).
         constexpr int kClusterMaxPagesPerPart = 64;
         long long cpar = 0;
+        const int per_sm = attend_ctas_per_sm(kernel, dtype, head_dim, G);
         for (int c = kMaxClusterParts; c >= 2 && groups > 0; --c) {
-            if (clusters_per_wave(slots, c) >= groups) {
+            if (clusters_per_wave(num_sms, per_sm, c) >= groups) {
                 cpar = c;
                 break;
             }
@@ -490,6 +500,11 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     // (its last CTA merges them, no second launch); the merge kernel when they
     // are many (the one-CTA merge would then trail the grid).
     plan->cluster = (use_cluster && P >= 2 && P <= kMaxClusterParts) ? P : 0;
+    // Tensor-core kernel: each warp's first two pages are requested into L2
+    // before the dependency wait (measured on GB300: 0.2-1 us less per step
+    // when decode steps follow each other with programmatic dependent launch,
+    // no cost when they do not).
+    plan->prewait_prefetch = kernel == PA_KERNEL_MMA ? 2 : 0;
     plan->merge_in_kernel =
         (kernel == PA_KERNEL_MMA && P > 1 && plan->cluster == 0 && kFusedMergeFits(G, head_dim, P))
             ? 1
@@ -547,6 +562,8 @@ static int check_plan(const pa_plan_t* plan) {
         return PA_ERR_INVALID_ARG;
     if (plan->kernel != PA_KERNEL_SIMT && plan->kernel != PA_KERNEL_MMA) return PA_ERR_INVALID_ARG;
     if (plan->cluster < 0) return PA_ERR_INVALID_ARG;
+    if (plan->prewait_prefetch < 0 || plan->prewait_prefetch > kMaxPrewaitPrefetch)
+        return PA_ERR_INVALID_ARG;
     if (plan->cluster > 1 &&
         (plan->kernel != PA_KERNEL_MMA || plan->cluster > kMaxClusterParts ||
          plan->num_partitions != plan->cluster || plan->parts_per_cta != 1 ||
@@ -632,11 +649,13 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
             !make_page_map(&maps[1], v_cache, rows, D, plan->dtype))
             return PA_ERR_CUDA;
         p.parts_per_cta = plan->parts_per_cta;
+        p.prewait_prefetch = plan->prewait_prefetch;
         const dim3 grid((P + p.parts_per_cta - 1) / p.parts_per_cta, p.Hkv * p.nchunk, p.B);
         e = launch_attend_mma(D, plan->dtype, P > 1, p, maps, grid,
                               static_cast<cudaStream_t>(stream));
     } else {
         p.parts_per_cta = 1;
+        p.prewait_prefetch = 0;
         const dim3 grid(P, p.Hkv * p.nchunk, p.B);
         e = launch_attend(D, plan->heads_per_cta, P > 1, p, grid,
                           static_cast<cudaStream_t>(stream));

@@ -279,14 +279,15 @@ __device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, co
 // ---- Merge inside a thread-block cluster.  With plan.cluster = C the C
 // partitions of a (sequence, KV head, head chunk) run as one cluster (grid.x =
 // C, cluster C x 1 x 1).  Each CTA leaves its partial -- the normalised o of
-// its G heads and their (m, l) -- in its own shared memory, the cluster
-// synchronises, and every CTA then merges a 1/C share of the (head, 4-dim
-// column) items by reading all C partials through distributed shared memory
-// (the log-sum-exp algebra of Phase 2 in the commit note).  No partial goes
-// through global memory, no counter is needed, and there is no second launch.
-// A second cluster barrier keeps every CTA's shared memory alive until all
-// peers have read it.  Every CTA of the cluster reaches both barriers (no
-// path returns between them), and every wait before them is bounded.
+// its G heads and their (m, l) -- in its own shared memory (the idle page
+// ring), the cluster synchronises, and every CTA then merges a 1/C share of
+// the (head, 4-dim column) items by reading all C partials through
+// distributed shared memory (the log-sum-exp algebra of Phase 2 in the commit
+// note).  No partial goes through global memory, no counter is needed, and
+// there is no second launch.  A second cluster barrier keeps every CTA's
+// shared memory alive until all peers have read it.  Every CTA of the cluster
+// reaches both barriers (no path returns between them), and every wait before
+// them is bounded.
 __device__ __forceinline__ void cluster_barrier() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -296,6 +297,12 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
+}
+
+__device__ __forceinline__ int cluster_size() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return (int)n;
 }
 
 // Shared-memory address `addr` of this CTA mapped to the same offset in CTA
@@ -328,10 +335,12 @@ struct ClusterPartial {
     __host__ __device__ static constexpr int o_off(int h, int d) { return (h * D + d) * 4; }
     __host__ __device__ static constexpr int m_off(int G, int h) { return (G * D + h) * 4; }
     __host__ __device__ static constexpr int l_off(int G, int h) { return (G * D + G + h) * 4; }
+    static constexpr int kMaxBytes = (kMaxHeadsPerCta * D + 2 * kMaxHeadsPerCta) * 4;
 };
 
 // A CTA with nothing to contribute (no page of its partition is attended,
 // or a bad page id: then l = NaN, which the merge carries to the output).
+// Its o stays unwritten and is never used: a zero weight selects 0.
 template <int D>
 __device__ __forceinline__ void cluster_partial_fill(float* part, int G, float m, float l) {
     for (int h = threadIdx.x; h < G; h += kThreads) {
@@ -345,30 +354,45 @@ __device__ __forceinline__ void cluster_merge(const AttendParams& p, int b, int 
                                               const float* part) {
     __syncthreads();    // this CTA's partial is complete
     cluster_barrier();  // ... and so is every peer's
-    const int C = p.cluster;
+    const int C = cluster_size();
     const int rank = (int)cluster_rank();
     const uint32_t base = smem_u32(part);
     constexpr int D4 = D / 4;
     const int items = G * D4;
+    // One thread per (head, 4-dim column) item this CTA merges (item it =
+    // rank + C * k).  All C partials' (m, l, o) loads of an item are issued
+    // before any is used, so the merge costs one distributed-shared-memory
+    // round trip.
     for (int it = rank + C * (int)threadIdx.x; it < items; it += C * kThreads) {
         const int h = it / D4;
         const int d = (it % D4) * 4;
+        float mv[kMaxClusterParts], lv[kMaxClusterParts];
+        float4 ov[kMaxClusterParts];
+#pragma unroll
+        for (int c = 0; c < kMaxClusterParts; ++c) {
+            if (c < C) {
+                mv[c] = ld_cluster_f32(map_to_rank(base + ClusterPartial<D>::m_off(G, h), c));
+                lv[c] = ld_cluster_f32(map_to_rank(base + ClusterPartial<D>::l_off(G, h), c));
+                ov[c] = ld_cluster_v4(map_to_rank(base + ClusterPartial<D>::o_off(h, d), c));
+            }
+        }
         float M = -INFINITY;
-        for (int c = 0; c < C; ++c)
-            M = fmaxf(M, ld_cluster_f32(map_to_rank(base + ClusterPartial<D>::m_off(G, h), c)));
+#pragma unroll
+        for (int c = 0; c < kMaxClusterParts; ++c)
+            if (c < C) M = fmaxf(M, mv[c]);
         float lam = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < C; ++c) {
-            const float l = ld_cluster_f32(map_to_rank(base + ClusterPartial<D>::l_off(G, h), c));
-            if (l == 0.f) continue;  // nothing attended there; a NaN is kept
-            const float w =
-                ex2(ld_cluster_f32(map_to_rank(base + ClusterPartial<D>::m_off(G, h), c)) - M) * l;
-            const float4 o = ld_cluster_v4(map_to_rank(base + ClusterPartial<D>::o_off(h, d), c));
-            lam += w;
-            acc.x += w * o.x;
-            acc.y += w * o.y;
-            acc.z += w * o.z;
-            acc.w += w * o.w;
+#pragma unroll
+        for (int c = 0; c < kMaxClusterParts; ++c) {
+            // l == 0: nothing attended there (its o is never written); a NaN is kept
+            if (c < C && lv[c] != 0.f) {
+                const float w = ex2(mv[c] - M) * lv[c];
+                lam += w;
+                acc.x += w * ov[c].x;
+                acc.y += w * ov[c].y;
+                acc.z += w * ov[c].z;
+                acc.w += w * ov[c].w;
+            }
         }
         const float inv = lam == 0.f ? 0.f : 1.f / lam;  // empty context: out 0, lse -inf
         const size_t bh = (size_t)b * p.Hq + h0 + h;
@@ -380,7 +404,44 @@ __device__ __forceinline__ void cluster_merge(const AttendParams& p, int b, int 
     cluster_barrier();  // every peer is done reading this CTA's shared memory
 }
 
-template <int D, typename T, bool SPLIT>
+// Before the dependency wait of a programmatic dependent launch: read this
+// CTA's sequence length and first page ids as hints and request the first
+// prewait_prefetch pages of each warp into L2, so that they stream in while
+// the previous grid drains.  The values read here may be stale (the previous grid
+// may still be writing them); they are only bounds-checked prefetch addresses
+// and everything is read again after the wait.  A stale hint costs one
+// useless prefetch.
+template <int D>
+__device__ __forceinline__ void prefetch_first_pages(const AttendParams& p) {
+    const int pp = p.pages_per_part;
+    const int part0 = blockIdx.x * p.parts_per_cta;
+    const int kvh = blockIdx.y / p.nchunk;
+    const int b = blockIdx.z;
+    const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, pp);
+    if (!sp.valid || part0 >= sp.num_parts) return;
+    const int pgA = sp.first_page + part0 * pp;
+    const int n_range = min(p.parts_per_cta * pp, sp.end_page - pgA);
+    const int n = min(n_range, kWarps * p.prewait_prefetch);  // each warp's first pages
+    for (int j = threadIdx.x; j < n; j += kThreads) {
+        const int id = p.block_tables[(size_t)b * p.maxp + pgA + j];
+        if (id >= 0 && id < p.num_pages) {
+            const size_t off = ((size_t)id * p.Hkv + kvh) * (size_t)(kPageSize * D);
+            prefetch_l2(p.k + off, kPageSize * D * 2);
+            prefetch_l2(p.v + off, kPageSize * D * 2);
+        }
+    }
+}
+
+static_assert(ClusterPartial<64>::kMaxBytes <= MmaCfg<64>::kWideXOff &&
+                  ClusterPartial<96>::kMaxBytes <= MmaCfg<96>::kWideXOff &&
+                  ClusterPartial<128>::kMaxBytes <= MmaCfg<128>::kWideXOff &&
+                  ClusterPartial<256>::kMaxBytes <= MmaCfg<256>::kWideXOff,
+              "the cluster partial sits in the ring in front of the one-round combine");
+
+// SPLIT: partials for a merge (else the final rows).  CLUSTER (with SPLIT):
+// the partitions of a group form one cluster and merge in it; a separate
+// instance, so that the other instances carry none of its code.
+template <int D, typename T, bool SPLIT, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     attend_mma_kernel(const AttendParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
@@ -406,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     // grid) be scheduled now, and read nothing before the grid this one
     // depends on has completed.
     allow_dependent_launch();
+    if (p.prewait_prefetch) prefetch_first_pages<D>(p);
     wait_for_prerequisite_grid();
     const int G = p.heads_per_cta;
     const int warp = threadIdx.x >> 5;
@@ -446,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
             if (d == 0) p.lse[bh] = lse_val;
         }
     };
-    const bool clustered = SPLIT && p.cluster > 1;
+    constexpr bool clustered = SPLIT && CLUSTER;
     float* const cpart = reinterpret_cast<float*>(ring);  // this CTA's partial (cluster merge)
     if (!sp.valid) {
         // (the same for every CTA of a cluster: they all leave here)
@@ -728,27 +790,14 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
             }
         }
         const int part = part0 + qp;
-#pragma unroll
-        for (int r = 0; r < ROUNDS; ++r) {
-#pragma unroll
-            for (int mi = 0; mi < XD / 16; ++mi) {
-                const int mt = r * (XD / 16) + mi;
-                const int d = mi * 16 + (lane >> 2);
-                if (hA < G) {
-                    xbuf[(warp * G + hA) * XD + d] = o[mt][0];
-                    xbuf[(warp * G + hA) * XD + d + 8] = o[mt][2];
-                }
-                if (hA + 1 < G) {
-                    xbuf[(warp * G + hA + 1) * XD + d] = o[mt][1];
-                    xbuf[(warp * G + hA + 1) * XD + d + 8] = o[mt][3];
-                }
-            }
-            __syncthreads();
+        // Combine nd output dims starting at d0 from the four warps' states in
+        // buf ([warp][head][stride] floats) and write them out.
+        auto combine = [&](const float* buf, int stride, int d0, int nd) {
             const bool failed = s_flag != 0;
-            for (int idx = threadIdx.x; idx < G * (XD / 4); idx += kThreads) {
-                const int h = idx / (XD / 4);
-                const int dl = (idx % (XD / 4)) * 4;
-                const int d = r * XD + dl;
+            for (int idx = threadIdx.x; idx < G * (nd / 4); idx += kThreads) {
+                const int h = idx / (nd / 4);
+                const int dl = (idx % (nd / 4)) * 4;
+                const int d = d0 + dl;
                 float M = -INFINITY;
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w * 3 * kMaxHeadsPerCta + h]);
@@ -761,7 +810,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
                     const float c = (mw == -INFINITY) ? 0.f : ex2(mw - M);
                     Ls += c * ml[kMaxHeadsPerCta + h];
                     Ns += c * ml[2 * kMaxHeadsPerCta + h];
-                    const float4 ow = *reinterpret_cast<const float4*>(xbuf + (w * G + h) * XD + dl);
+                    const float4 ow =
+                        *reinterpret_cast<const float4*>(buf + (w * G + h) * stride + dl);
                     acc.x += c * ow.x;
                     acc.y += c * ow.y;
                     acc.z += c * ow.z;
@@ -799,7 +849,49 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
                                                        : -INFINITY);
                 }
             }
-            __syncthreads();  // xbuf and s_ml are rewritten next
+        };
+        if (qp == nparts - 1) {
+            // The CTA's last partition: once every warp is past its last page the
+            // page ring is idle, and all D dims of the four warp states fit in it
+            // at once (behind the cluster partial), so one round combines them.
+            __syncthreads();
+            float* xw = reinterpret_cast<float*>(ring + Cfg::kWideXOff);
+            constexpr int XS = Cfg::kWideXStride;
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+                const int d = mt * 16 + (lane >> 2);
+                if (hA < G) {
+                    xw[(warp * G + hA) * XS + d] = o[mt][0];
+                    xw[(warp * G + hA) * XS + d + 8] = o[mt][2];
+                }
+                if (hA + 1 < G) {
+                    xw[(warp * G + hA + 1) * XS + d] = o[mt][1];
+                    xw[(warp * G + hA + 1) * XS + d + 8] = o[mt][3];
+                }
+            }
+            __syncthreads();
+            combine(xw, XS, 0, D);
+            __syncthreads();  // the ring and s_ml are reused by the merges below
+        } else {
+#pragma unroll
+            for (int r = 0; r < ROUNDS; ++r) {
+#pragma unroll
+                for (int mi = 0; mi < XD / 16; ++mi) {
+                    const int mt = r * (XD / 16) + mi;
+                    const int d = mi * 16 + (lane >> 2);
+                    if (hA < G) {
+                        xbuf[(warp * G + hA) * XD + d] = o[mt][0];
+                        xbuf[(warp * G + hA) * XD + d + 8] = o[mt][2];
+                    }
+                    if (hA + 1 < G) {
+                        xbuf[(warp * G + hA + 1) * XD + d] = o[mt][1];
+                        xbuf[(warp * G + hA + 1) * XD + d + 8] = o[mt][3];
+                    }
+                }
+                __syncthreads();
+                combine(xbuf, XD, r * XD, XD);
+                __syncthreads();  // xbuf and s_ml are rewritten next
+            }
         }
     }
 
@@ -814,14 +906,17 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
 template <int D, typename T>
 cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtensorMap* maps,
                                 dim3 grid, cudaStream_t stream) {
-    const void* fn = split ? reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true>)
-                           : reinterpret_cast<const void*>(&attend_mma_kernel<D, T, false>);
+    const bool clustered = split && p.cluster > 1;
+    const void* fn =
+        !split ? reinterpret_cast<const void*>(&attend_mma_kernel<D, T, false, false>)
+               : clustered ? reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true, true>)
+                           : reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true, false>);
     constexpr int kMaxDevices = 64;
     static std::atomic<uint32_t> configured[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const uint32_t bit = split ? 2u : 1u;
+    const uint32_t bit = !split ? 1u : (clustered ? 8u : 2u);
     if (dev < 0 || dev >= kMaxDevices || !(configured[dev].load() & bit)) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  MmaCfg<D>::kSmemBytes);
@@ -830,7 +925,6 @@ cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtenso
     }
     void* args[] = {const_cast<AttendParams*>(&p), const_cast<CUtensorMap*>(&maps[0]),
                     const_cast<CUtensorMap*>(&maps[1])};
-    const bool clustered = split && p.cluster > 1;
     if (clustered && p.cluster > 8 &&
         (dev < 0 || dev >= kMaxDevices || !(configured[dev].load() & 4u))) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);

@@ -20,6 +20,7 @@ constexpr int kMaxPartitions = 4096;   // partitions the merge kernel reduces
 constexpr int kMaxHeadsPerCta = 8;
 constexpr int kCtrlBytes = 256;        // workspace control block (device error word)
 constexpr int kMaxRopePairs = 128;     // head_dim / 2 of the widest rotary head
+constexpr int kMaxPrewaitPrefetch = 8; // largest prewait_prefetch (pages per warp)
 
 // Bounded waits: a bulk copy that has not landed after this long is reported
 // as PA_DEVERR_TIMEOUT instead of hanging the GPU.
@@ -46,6 +47,7 @@ struct AttendParams {
     int nchunk;             // head chunks per KV head (grid.y = Hkv * nchunk)
     int heads_per_cta;      // G: query heads one CTA serves
     int parts_per_cta;      // consecutive partitions one CTA streams (tensor-core kernel)
+    int prewait_prefetch;   // pages per warp prefetched into L2 before the PDL wait (tensor-core)
     float scale_log2;       // scale * log2(e)
     int rope;               // 1: rotary embedding of q and K (CUDA-core kernel)
     int elem_fp32;          // 1: q, K, V and out are fp32 (CUDA-core kernel)
@@ -103,6 +105,15 @@ struct MmaCfg {
     // output dims combined per round at a partition edge
     static constexpr int kXDims = (D % 64 == 0) ? 64 : 32;
     static constexpr int kXBytes = kWarps * kMaxHeadsPerCta * 64 * 4;
+    // The last partition of a CTA combines all D dims at once in the idle page
+    // ring, behind the cluster partial ([G][D] o, then m and l): rows of
+    // D + 4 floats (the pad spreads the four head rows a store writes over
+    // distinct banks).
+    static constexpr int kWideXOff = ((kMaxHeadsPerCta * D + 2 * kMaxHeadsPerCta) * 4 + 1023) /
+                                     1024 * 1024;
+    static constexpr int kWideXStride = D + 4;
+    static_assert(kWideXOff + kWarps * kMaxHeadsPerCta * kWideXStride * 4 <= kRingBytes,
+                  "one-round combine fits in the page ring");
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes + kXBytes +
                                       kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 3 * 4 +
                                       kWarps * kStages * 8 + 16;
@@ -230,6 +241,11 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Request `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Let a dependent grid launched with programmatic stream serialization (the

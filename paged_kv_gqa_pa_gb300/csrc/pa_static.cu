@@ -1,12 +1,12 @@
 // pa_static.cu -- pa_decode_static: pa_decode without a caller workspace.
 //
-// Some callers cannot allocate device memory at the moment they decode: code
-// that runs while a CUDA graph is being captured (where cudaMalloc is not
-// allowed), engines and plugins that hand out only the input and output
-// buffers they own, and latency-critical loops that must never enter the
-// allocator (cudaMalloc can synchronise the device).  For them the partition
-// partials live in a fixed scratch array compiled into the library instead of
-// a workspace the caller provides.
+// Some callers cannot allocate device memory at the moment they decode:
+// engines and plugins that are handed only the input and output buffers they
+// own and have no allocator of their own to draw on, and latency-critical
+// loops that must never enter the allocator (cudaMalloc can synchronise the
+// device and stall every stream).  For them the partition partials live in a
+// fixed scratch array compiled into the library instead of a workspace the
+// caller provides.
 //
 // The array is a file-scope __device__ variable, so every GPU that loads the
 // library holds PA_STATIC_WORKSPACE_BYTES of it until the process exits.  Its
@@ -57,11 +57,18 @@ extern "C" int pa_decode_static(const pa_plan_t* plan, const void* q, const void
     if (plan->workspace_bytes > (size_t)PA_STATIC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE;
     void* ws = static_workspace_ptr();
     if (!ws) return PA_ERR_CUDA;
-    // The scratch's control bytes (error word, per-group arrival counters)
-    // start at zero because a __device__ array is zero-initialised when the
-    // library loads, and every call leaves them at zero.  The partials need
-    // no clearing: each is written before it is read.  The error word is only
-    // ever OR-ed into; no caller reads it through this entry point.
+    // The scratch keeps whatever the previous call left in it.  Its control
+    // bytes (error word, per-group arrival counters) must start at zero, so
+    // they are cleared on the stream before every call: a call that gave up
+    // on a bounded wait may have left a counter behind.  The partials need no
+    // clearing: each is written before it is read.  cudaMemsetAsync allocates
+    // nothing.
+    if (plan->batch > 0 && plan->ctrl_bytes > 0 &&
+        cudaMemsetAsync(ws, 0, (size_t)plan->ctrl_bytes, static_cast<cudaStream_t>(stream)) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
     return pa_decode(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window, out,
                      lse, ws, stream);
 }

@@ -51,13 +51,15 @@ def to_device(case, device="cuda"):
 
 
 def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=None,
-            guard=0, parts_per_cta=None, merge_in_kernel=None, ws=None, cluster=None):
+            guard=0, parts_per_cta=None, merge_in_kernel=None, ws=None, cluster=None,
+            prewait_prefetch=None):
     """Plan + pa_decode through the C ABI.  Returns (out fp64 numpy, lse fp64
     numpy, device error word, plan).  With guard > 0 the outputs and the
     workspace sit inside larger NaN/0xA5-filled buffers whose guard regions are
     checked afterwards.  cluster: True forces the cluster merge (the plan's
     partition count must be 2..16), False forbids it, None keeps the planner's
-    choice; forcing several partitions per CTA or the last-CTA merge drops it."""
+    choice; forcing several partitions per CTA or the last-CTA merge drops it.
+    prewait_prefetch overrides the plan's pre-wait L2 prefetch (pages per warp)."""
     ensure_built()
     dev = dev or to_device(case)
     B, Hq, D = case.q.shape
@@ -87,6 +89,8 @@ def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=N
         plan.merge_in_kernel = 0
     elif cluster is False:
         plan.cluster = 0
+    if prewait_prefetch is not None:
+        plan.prewait_prefetch = prewait_prefetch
     n_out = B * Hq * D
     et = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[case.dtype]
     out_buf = torch.full((n_out + 2 * guard,), float("nan"), dtype=et, device="cuda")

@@ -51,13 +51,14 @@ def test_plan_struct_layout_matches_header():
     text = open(os.path.join(ROOT, "include", "pa.h")).read()
     body = re.search(r"typedef struct pa_plan \{(.*?)\} pa_plan_t;", text, flags=re.S).group(1)
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
-    fields = re.findall(r"\b(?:int|size_t|float)\s+([a-z_]+)(?:\[\d+\])?\s*;", body)
+    fields = re.findall(r"\b(?:int|size_t|float)\s+([a-z_0-9]+)(?:\[\d+\])?\s*;", body)
     assert fields == [f for f, _ in binding.pa_plan_t._fields_]
-    # 14 ints, a size_t, the kernel id, partitions per CTA, 6 reserved ints.
+    # 14 ints, a size_t, then 10 four-byte fields (kernel ... reserved).
     assert binding.pa_plan_t.workspace_bytes.offset == 56
     assert binding.pa_plan_t.kernel.offset == 64
     assert binding.pa_plan_t.parts_per_cta.offset == 68
-    assert ctypes.sizeof(binding.pa_plan_t) == 96
+    assert binding.pa_plan_t.prewait_prefetch.offset == 92
+    assert ctypes.sizeof(binding.pa_plan_t) == 104
 
 
 def test_status_strings_and_version():
@@ -238,11 +239,13 @@ def test_plan_ex_picks_the_kernel_and_sizes_for_its_residency():
 
 def test_plan_picks_the_cluster_merge_for_one_wave_splits():
     # Gemma-2-2b shape: 16 groups, 257 window pages; one wave of 2-per-SM
-    # tensor-core CTAs holds a 12-CTA cluster per group (not a 13..16 one).
+    # tensor-core CTAs holds 19 clusters of 13 CTAs but only 14 of 14..16, so
+    # each group is a 13-CTA cluster of 20-page partitions.
     gemma = pa.pa_plan_ex(4, 8, 4, 256, 16, 3000, 512, 8192, 4096, 0, 152)
-    assert gemma.cluster == gemma.num_partitions == 12
+    assert gemma.cluster == gemma.num_partitions == 13
     assert gemma.parts_per_cta == 1 and gemma.merge_in_kernel == 0
-    assert gemma.partition_size == 22 * 16 and gemma.ctas == 16 * 12
+    assert gemma.partition_size == 20 * 16 and gemma.ctas == 16 * 13
+    assert gemma.prewait_prefetch == 2
     # Llama-3.2-1B shape: 8 groups, 192 pages, 16 partitions of 12 pages.
     llama = pa.pa_plan_ex(1, 32, 8, 64, 16, 300, 192, 3060, 0, 0, 152)
     assert llama.cluster == 16 and llama.partition_size == 12 * 16
@@ -259,7 +262,7 @@ def test_plan_picks_the_cluster_merge_for_one_wave_splits():
 
 def test_cluster_plan_checks_return_before_launch():
     plan = pa.pa_plan_ex(4, 8, 4, 256, 16, 3000, 512, 8192, 4096, 0, 152)
-    assert plan.cluster == 12
+    assert plan.cluster == 13
     for field, value in (("cluster", 17), ("cluster", 8), ("cluster", -1),
                          ("parts_per_cta", 2), ("merge_in_kernel", 1),
                          ("kernel", binding.PA_KERNEL_SIMT)):

@@ -1,8 +1,8 @@
 """pa_decode_static: the decode entry point that allocates nothing.
 
-It exists for callers that cannot hand the library a workspace -- code that
-runs while a CUDA graph is captured, engines that only pass their own input and
-output buffers, loops that must never enter the allocator.  The partition
+It exists for callers that cannot hand the library a workspace: engines and
+plugins that are given only their own input and output buffers, and loops that
+must never enter the allocator (cudaMalloc can synchronise the device).  The partition
 partials then go to a scratch array built into the library.  These tests call
 it through the C ABI (ctypes on libpa_gb300.so) and check it against pa_decode
 with a caller workspace, on two calls in a row with different problems (the
