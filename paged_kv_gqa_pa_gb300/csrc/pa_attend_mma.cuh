@@ -359,11 +359,14 @@ __device__ __forceinline__ void cluster_merge(const AttendParams& p, int b, int 
     const uint32_t base = smem_u32(part);
     constexpr int D4 = D / 4;
     const int items = G * D4;
-    // One thread per (head, 4-dim column) item this CTA merges (item it =
-    // rank + C * k).  All C partials' (m, l, o) loads of an item are issued
-    // before any is used, so the merge costs one distributed-shared-memory
-    // round trip.
-    for (int it = rank + C * (int)threadIdx.x; it < items; it += C * kThreads) {
+    // This CTA merges a contiguous block of the (head, 4-dim column) items,
+    // one thread per item, so that a warp's loads from one peer (and its
+    // output stores) cover consecutive addresses.  All C partials' (m, l, o)
+    // loads of an item are issued before any is used, so the merge costs one
+    // distributed-shared-memory round trip.
+    const int per = (items + C - 1) / C;
+    const int it_end = min(items, (rank + 1) * per);
+    for (int it = rank * per + (int)threadIdx.x; it < it_end; it += kThreads) {
         const int h = it / D4;
         const int d = (it % D4) * 4;
         float mv[kMaxClusterParts], lv[kMaxClusterParts];
@@ -404,26 +407,27 @@ __device__ __forceinline__ void cluster_merge(const AttendParams& p, int b, int 
     cluster_barrier();  // every peer is done reading this CTA's shared memory
 }
 
-// Before the dependency wait of a programmatic dependent launch: read this
-// CTA's sequence length and first page ids as hints and request the first
-// prewait_prefetch pages of each warp into L2, so that they stream in while
-// the previous grid drains.  The values read here may be stale (the previous grid
-// may still be writing them); they are only bounds-checked prefetch addresses
-// and everything is read again after the wait.  A stale hint costs one
-// useless prefetch.
-template <int D>
-__device__ __forceinline__ void prefetch_first_pages(const AttendParams& p) {
+// Before the dependency wait of a programmatic dependent launch, per warp:
+// read the sequence length and this warp's first page ids as hints and
+// request its first prewait_prefetch pages (K and V) into L2, so that they
+// stream in while the previous grid drains.  The values read here may be
+// stale (the previous grid may still be writing them): they are only
+// bounds-checked prefetch addresses, and everything is read again after the
+// wait, so a stale hint costs one useless prefetch.  L2-only loads, so that
+// nothing read here sits in L1 afterwards.
+__device__ __forceinline__ void prefetch_first_pages(const AttendParams& p, int part0, int kvh,
+                                                     int b, int warp, int lane, int D) {
     const int pp = p.pages_per_part;
-    const int part0 = blockIdx.x * p.parts_per_cta;
-    const int kvh = blockIdx.y / p.nchunk;
-    const int b = blockIdx.z;
-    const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, pp);
+    int Lh = 0;
+    if (lane == 0) Lh = __ldcg(p.context_lens + b);
+    Lh = __shfl_sync(0xffffffffu, Lh, 0);
+    const SeqSpan sp = seq_span(Lh, p.window, p.max_ctx, p.maxp, pp);
     if (!sp.valid || part0 >= sp.num_parts) return;
     const int pgA = sp.first_page + part0 * pp;
     const int n_range = min(p.parts_per_cta * pp, sp.end_page - pgA);
-    const int n = min(n_range, kWarps * p.prewait_prefetch);  // each warp's first pages
-    for (int j = threadIdx.x; j < n; j += kThreads) {
-        const int id = p.block_tables[(size_t)b * p.maxp + pgA + j];
+    const int j = warp + kWarps * lane;  // this lane: page `lane` of the warp
+    if (lane < p.prewait_prefetch && j < n_range) {
+        const int id = __ldcg(p.block_tables + (size_t)b * p.maxp + pgA + j);
         if (id >= 0 && id < p.num_pages) {
             const size_t off = ((size_t)id * p.Hkv + kvh) * (size_t)(kPageSize * D);
             prefetch_l2(p.k + off, kPageSize * D * 2);
@@ -463,12 +467,6 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 3);
     __shared__ int s_flag;
 
-    // Programmatic dependent launch: let the merge grid (or the next call's
-    // grid) be scheduled now, and read nothing before the grid this one
-    // depends on has completed.
-    allow_dependent_launch();
-    if (p.prewait_prefetch) prefetch_first_pages<D>(p);
-    wait_for_prerequisite_grid();
     const int G = p.heads_per_cta;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -478,6 +476,43 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     const int h0 = kvh * p.g + (blockIdx.y % p.nchunk) * G;
     const int b = blockIdx.z;
     const int pp = p.pages_per_part;
+    const uint32_t bar_w = smem_u32(bars) + warp * NS * 8;
+    const uint32_t ring_w = smem_u32(ring) + warp * NS * PB;
+
+    // Ring copy of item `item` (K0, V0, K1, V1, ... of this warp's pages) from
+    // page `id` of the pool.
+    auto issue_page = [&](int item, int id) {
+        const int slot = item % NS;
+        const CUtensorMap* map = (item & 1) ? &tmV : &tmK;
+        const int y = (id * p.Hkv + kvh) * kPageSize;
+        const uint32_t bar = bar_w + slot * 8;
+        mbar_arrive_expect_tx(bar, PB);
+        if constexpr (Cfg::kRows64) {
+            tma_load_3d(ring_w + slot * PB, map, 0, 0, y, bar);
+        } else {
+#pragma unroll
+            for (int s = 0; s < Cfg::kFullSlabs; ++s)
+                tma_load_2d(ring_w + slot * PB + s * Cfg::kSlabBytes, map, s * 64, y, bar);
+        }
+    };
+
+    // Programmatic dependent launch: let the merge grid (or the next call's
+    // grid) be scheduled now, and read nothing before the grid this one
+    // depends on has completed -- except the prefetch hints.
+    allow_dependent_launch();
+    if (threadIdx.x == 0) {
+        s_flag = 0;
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < NS; ++s) mbar_init(bar_w + s * 8, 1);
+        fence_mbar_init();
+    }
+    if (p.prewait_prefetch) prefetch_first_pages(p, part0, kvh, b, warp, lane, D);
+    __syncthreads();  // barriers initialised
+    wait_for_prerequisite_grid();
 
     const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, pp);
     T* const out = reinterpret_cast<T*>(p.out);
@@ -531,18 +566,6 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     const int pgA = sp.first_page + part0 * pp;           // first page of this CTA
     const int n_range = min(nparts * pp, sp.end_page - pgA);  // pages of this CTA
 
-    if (threadIdx.x == 0) {
-        s_flag = 0;
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
-    }
-    const uint32_t bar_w = smem_u32(bars) + warp * NS * 8;
-    if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < NS; ++s) mbar_init(bar_w + s * 8, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
     for (int j = threadIdx.x; j < n_range; j += kThreads) {
         int id = p.block_tables[(size_t)b * p.maxp + pgA + j];
         if (id < 0 || id >= p.num_pages) {
@@ -569,27 +592,12 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     // items K0, V0, K1, V1, ...
     const int nk = n_range > warp ? (n_range - warp + kWarps - 1) / kWarps : 0;
     const int n_items = 2 * nk;
-    const uint32_t ring_w = smem_u32(ring) + warp * NS * PB;
-
-    auto issue = [&](int item) {
-        const int slot = item % NS;
-        const int jj = warp + (item >> 1) * kWarps;
-        const CUtensorMap* map = (item & 1) ? &tmV : &tmK;
-        const int y = (s_pid[jj] * p.Hkv + kvh) * kPageSize;
-        const uint32_t bar = bar_w + slot * 8;
-        mbar_arrive_expect_tx(bar, PB);
-        if constexpr (Cfg::kRows64) {
-            tma_load_3d(ring_w + slot * PB, map, 0, 0, y, bar);
-        } else {
-#pragma unroll
-            for (int s = 0; s < Cfg::kFullSlabs; ++s)
-                tma_load_2d(ring_w + slot * PB + s * Cfg::kSlabBytes, map, s * 64, y, bar);
-        }
-    };
+    auto issue = [&](int item) { issue_page(item, s_pid[warp + (item >> 1) * kWarps]); };
     if (lane == 0) {
         for (int i = 0; i < NS && i < n_items; ++i) issue(i);
     }
     int issued = min(NS, n_items);
+    bool ok = true;
 
     // q as the B operand of q.K: lane holds q[head = lane/4][dims kk*16 + (lane%4)*2 + {0,1}, +8]
     const int qh = lane >> 2;
@@ -613,7 +621,6 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     const int k_chk = ld_j >> 1;
     const int v_row = ld_i + (ld_j >> 1) * 8; // P.V (trans): (chunk +0|+1) x (tokens 0-7|8-15)
     const int v_chk = ld_j & 1;
-    bool ok = true;
     int consumed = 0;
     int k = 0;  // this warp's next page (index into its stream)
 
