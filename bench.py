@@ -53,7 +53,8 @@ NCU_TRAFFIC = {
 
 
 KERNEL_SOURCES = {
-    "mma": ("pa_attend_mma.cuh", "pa_attend_mma_f16.cu", "pa_attend_mma_bf16.cu", "pa_common.cuh"),
+    "mma": ("pa_attend_mma.cuh", "pa_attend_mma_f16.cu", "pa_attend_mma_bf16.cu",
+            "pa_attend_mma_rope.cu", "pa_common.cuh"),
     "simt": ("pa_attend.cuh", "pa_attend_d64.cu", "pa_attend_d128.cu", "pa_attend_d256.cu",
              "pa_attend_f32_d64.cu", "pa_attend_f32_d128.cu", "pa_attend_f32_d256.cu",
              "pa_common.cuh"),
@@ -634,8 +635,8 @@ def run_gpu(args):
             entry = {"dtype": c.dtype, "head_dim": c.D, "rope_theta": c.rope_theta}
             simt_ok = c.dtype in ("f16", "f32") and c.D in (64, 128, 256)
             kernels = ("mma", "simt") if simt_ok else ("mma",)
-            if c.rope_theta > 0 or c.dtype == "f32":
-                kernels = ("simt",)
+            if c.dtype == "f32" or (c.rope_theta > 0 and c.D > 128):
+                kernels = ("simt",)  # no tensor-core build for these
             for kname in kernels:
                 us, kus, copies, l2state, plan = time_graph_rotating(c, device, kname)
                 entry[kname] = {"us_per_step": us, "partition_kernel_us": kus,

@@ -20,6 +20,9 @@ cudaError_t launch_attend_d(int G, bool split, const AttendParams& p, dim3 grid,
 template <int D, typename T>
 cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtensorMap* maps,
                                 dim3 grid, cudaStream_t stream);
+template <int D>
+cudaError_t launch_attend_mma_rope_d(bool split, const AttendParams& p, const CUtensorMap* maps,
+                                     dim3 grid, cudaStream_t stream);
 
 template <typename T>
 static cudaError_t launch_attend_mma_t(int D, bool split, const AttendParams& p,
@@ -35,6 +38,14 @@ static cudaError_t launch_attend_mma_t(int D, bool split, const AttendParams& p,
 
 static cudaError_t launch_attend_mma(int D, int dtype, bool split, const AttendParams& p,
                                      const CUtensorMap* maps, dim3 grid, cudaStream_t stream) {
+    if (p.rope) {  // fp16, head dims up to 128 (checked with the plan)
+        switch (D) {
+            case 64: return launch_attend_mma_rope_d<64>(split, p, maps, grid, stream);
+            case 96: return launch_attend_mma_rope_d<96>(split, p, maps, grid, stream);
+            case 128: return launch_attend_mma_rope_d<128>(split, p, maps, grid, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     return dtype == PA_DTYPE_BF16
                ? launch_attend_mma_t<__nv_bfloat16>(D, split, p, maps, grid, stream)
                : launch_attend_mma_t<__half>(D, split, p, maps, grid, stream);
@@ -110,7 +121,14 @@ static long long clusters_per_wave(int num_sms, int per_sm, int c) {
 // CTAs of the partition kernel resident per SM (the launch bound, which the
 // configurations' static checks also guarantee in shared memory), for G query
 // heads per CTA.
-int attend_ctas_per_sm(int kernel, int dtype, int D, int G) {
+int attend_ctas_per_sm(int kernel, int dtype, int D, int G, bool rope) {
+    if (kernel == PA_KERNEL_MMA && rope) {
+        switch (D) {
+            case 64: return MmaCfg<64, true>::kMinBlocks;
+            case 96: return MmaCfg<96, true>::kMinBlocks;
+            default: return MmaCfg<128, true>::kMinBlocks;
+        }
+    }
     if (kernel == PA_KERNEL_MMA) {
         switch (D) {
             case 64: return MmaCfg<64>::kMinBlocks;
@@ -374,10 +392,13 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     if (dtype != PA_DTYPE_F16 && dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F32)
         return PA_ERR_INVALID_ARG;
     if (!(rope_theta >= 0.f) || rope_theta == INFINITY) return PA_ERR_INVALID_ARG;
-    if (kernel == 0)  // automatic: rotary embedding and fp32 need the CUDA-core kernel
-        kernel = (rope_theta > 0.f || dtype == PA_DTYPE_F32) ? PA_KERNEL_SIMT : PA_KERNEL_MMA;
+    // The tensor-core kernel's rotary instances: fp16, head dims up to 128.
+    const bool mma_rope_ok = dtype == PA_DTYPE_F16 && head_dim <= 128;
+    if (kernel == 0)  // automatic: fp32, and rotary embeddings the tensor-core kernel lacks, need the CUDA-core kernel
+        kernel = (dtype == PA_DTYPE_F32 || (rope_theta > 0.f && !mma_rope_ok)) ? PA_KERNEL_SIMT
+                                                                               : PA_KERNEL_MMA;
     if (kernel != PA_KERNEL_SIMT && kernel != PA_KERNEL_MMA) return PA_ERR_INVALID_ARG;
-    if (kernel == PA_KERNEL_MMA && (dtype == PA_DTYPE_F32 || rope_theta > 0.f))
+    if (kernel == PA_KERNEL_MMA && (dtype == PA_DTYPE_F32 || (rope_theta > 0.f && !mma_rope_ok)))
         return PA_ERR_UNSUPPORTED;
     if (kernel == PA_KERNEL_SIMT && (dtype == PA_DTYPE_BF16 || head_dim == 96))
         return PA_ERR_UNSUPPORTED;
@@ -432,7 +453,7 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         constexpr long long kNoSplitBytes = 128 << 10;
         constexpr int kMinPagesPerPart = 2 * kWarps;
         const long long groups = (long long)batch * num_kv_heads * nchunk;
-        const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim, G);
+        const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim, G, rope_theta > 0.f);
         const long long span_bytes =
             (long long)span * 2 * page_size * head_dim * (dtype == PA_DTYPE_F32 ? 4 : 2);
         // Cluster merge (tensor-core kernel): the largest cluster C (2 ..
@@ -445,7 +466,7 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         // merge launch saves (measured on GB300).
         constexpr int kClusterMaxPagesPerPart = 64;
         long long cpar = 0;
-        const int per_sm = attend_ctas_per_sm(kernel, dtype, head_dim, G);
+        const int per_sm = attend_ctas_per_sm(kernel, dtype, head_dim, G, rope_theta > 0.f);
         for (int c = kMaxClusterParts; c >= 2 && groups > 0; --c) {
             if (clusters_per_wave(num_sms, per_sm, c) >= groups) {
                 cpar = c;
@@ -516,7 +537,7 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     // stays short; longer CTAs (more partitions each) measured slower.
     {
         const long long groups = (long long)batch * num_kv_heads * nchunk;
-        const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim, G);
+        const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim, G, rope_theta > 0.f);
         const bool many_waves = slots > 0 && groups * P > 4 * slots;
         plan->parts_per_cta =
             (plan->cluster == 0 && many_waves && P >= 2 && 2 * pp <= kMaxPagesPerPart) ? 2 : 1;
@@ -542,10 +563,12 @@ static int check_plan(const pa_plan_t* plan) {
         plan->dtype != PA_DTYPE_F32)
         return PA_ERR_INVALID_ARG;
     if (!(plan->rope_theta >= 0.f) || plan->rope_theta == INFINITY) return PA_ERR_INVALID_ARG;
-    // Rotary embedding runs on the CUDA-core kernel, which keeps the rotated
-    // q and K in fp32 (rounding them to fp16/bf16 for the tensor cores would
-    // cost more than the LSE tolerance allows).
-    if (plan->rope_theta > 0.f && plan->kernel != PA_KERNEL_SIMT) return PA_ERR_UNSUPPORTED;
+    // Rotary embedding: the CUDA-core kernel (fp16, fp32), or the tensor-core
+    // kernel's rotary instances (fp16, head dims up to 128), which keep the
+    // rotated q and K as fp16 head + remainder pairs.
+    if (plan->rope_theta > 0.f && plan->kernel == PA_KERNEL_MMA &&
+        (plan->dtype != PA_DTYPE_F16 || plan->head_dim > 128))
+        return PA_ERR_UNSUPPORTED;
     // The CUDA-core kernel is built for fp16/fp32 and head dims 64/128/256;
     // the tensor-core kernel for fp16/bf16.
     if (plan->kernel == PA_KERNEL_SIMT && (plan->dtype == PA_DTYPE_BF16 || plan->head_dim == 96))

@@ -407,6 +407,51 @@ __device__ __forceinline__ void cluster_merge(const AttendParams& p, int b, int 
     cluster_barrier();  // every peer is done reading this CTA's shared memory
 }
 
+// ---- Rotary embedding on the tensor-core path (fp16, head dims up to 128).
+// The rotate-half partner of dim i (i < D/2) is dim i + D/2, which lies in
+// k-step kk + KT/2 of the same mma fragment slot as dim i in k-step kk: a lane
+// rotates its K fragments in registers, pairing fragment kk with kk + KT/2,
+// and never writes a rotated page back.  Rotated values are fp32 split into
+// an fp16 head and an fp16 remainder (about 22 significant bits), and q.K
+// takes K_hi q_hi + K_hi q_lo + K_lo q_hi, so the scores keep fp32-level
+// accuracy (a single fp16 rounding of the rotated q or K would cost ~3e-4 on
+// the LSE).
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// v = hi + lo with hi = fp16(v) and lo = fp16(v - hi), elementwise.
+__device__ __forceinline__ void split_f16x2(float2 v, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __float22half2_rn(v);
+    const float2 hb = __half22float2(h);
+    hi = h2_bits(h);
+    lo = h2_bits(__float22half2_rn(make_float2(v.x - hb.x, v.y - hb.y)));
+}
+
+// x = dims (i, i + 1) of the first half, y = their partners (i + D/2,
+// i + D/2 + 1), as packed fp16; (c, s) = cos, sin of their angles.  The
+// rotated pair x' = x c - y s, y' = y c + x s, split into fp16 head + rest.
+__device__ __forceinline__ void rope_rot_split(uint32_t x16, uint32_t y16, float2 c, float2 s,
+                                               uint32_t& xh, uint32_t& xl, uint32_t& yh,
+                                               uint32_t& yl) {
+    const float2 x = __half22float2(bits_h2(x16));
+    const float2 y = __half22float2(bits_h2(y16));
+    const float2 xr = __ffma2_rn(x, c, __fmul2_rn(y, make_float2(-s.x, -s.y)));
+    const float2 yr = __ffma2_rn(y, c, __fmul2_rn(x, s));
+    split_f16x2(xr, xh, xl);
+    split_f16x2(yr, yh, yl);
+}
+
+// (c, s) <- (c, s) turned by the angles whose cos/sin are t = (cos f, sin f,
+// cos f+1, sin f+1): c' = c cr - s sr, s' = s cr + c sr, per element.
+__device__ __forceinline__ void rope_turn_pair(float2& c, float2& s, float4 t) {
+    const float2 cr = make_float2(t.x, t.z), sr = make_float2(t.y, t.w);
+    const float2 cn = __ffma2_rn(c, cr, __fmul2_rn(s, make_float2(-sr.x, -sr.y)));
+    const float2 sn = __ffma2_rn(s, cr, __fmul2_rn(c, sr));
+    c = cn;
+    s = sn;
+}
+
 // Before the dependency wait of a programmatic dependent launch, per warp:
 // read the sequence length and this warp's first page ids as hints and
 // request its first prewait_prefetch pages (K and V) into L2, so that they
@@ -444,12 +489,14 @@ static_assert(ClusterPartial<64>::kMaxBytes <= MmaCfg<64>::kWideXOff &&
 
 // SPLIT: partials for a merge (else the final rows).  CLUSTER (with SPLIT):
 // the partitions of a group form one cluster and merge in it; a separate
-// instance, so that the other instances carry none of its code.
-template <int D, typename T, bool SPLIT, bool CLUSTER>
-__global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
+// instance, so that the other instances carry none of its code.  ROPE: q and
+// each K row are rotated to their positions before q.K (fp16 only).
+template <int D, typename T, bool SPLIT, bool CLUSTER, bool ROPE>
+__global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     attend_mma_kernel(const AttendParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
-    using Cfg = MmaCfg<D>;
+    using Cfg = MmaCfg<D, ROPE>;
+    static_assert(!ROPE || std::is_same<T, __half>::value, "rotary instances are fp16");
     constexpr int NS = Cfg::kStages;
     constexpr int PB = Cfg::kPageBytes;
     constexpr int KT = D / 16;  // k-steps of q.K, m-tiles of P.V
@@ -465,6 +512,9 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
     int* s_pid = reinterpret_cast<int*>(base + Cfg::kRingBytes + Cfg::kXBytes);
     float* s_ml = reinterpret_cast<float*>(s_pid + kMaxPagesPerPart);  // [warps][m|l|n][8]
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 3);
+    // rotary tables (ROPE): (cos, sin) of the 8-token and the 64-token turn per frequency
+    float2* s_r8 = reinterpret_cast<float2*>(bars + kWarps * NS);
+    float2* s_r64 = s_r8 + D / 2;
     __shared__ int s_flag;
 
     const int G = p.heads_per_cta;
@@ -511,7 +561,17 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
         fence_mbar_init();
     }
     if (p.prewait_prefetch) prefetch_first_pages(p, part0, kvh, b, warp, lane, D);
-    __syncthreads();  // barriers initialised
+    if constexpr (ROPE) {
+        // (kernel parameters only: no input is read)
+        for (int f = threadIdx.x; f < D / 2; f += kThreads) {
+            float c, sn;
+            rope_twiddle(8, p.rope_phi[0][f], p.rope_phi[1][f], c, sn);
+            s_r8[f] = make_float2(c, sn);
+            rope_twiddle(kWarps * kPageSize, p.rope_phi[0][f], p.rope_phi[1][f], c, sn);
+            s_r64[f] = make_float2(c, sn);
+        }
+    }
+    __syncthreads();  // barriers and rotary tables initialised
     wait_for_prerequisite_grid();
 
     const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, pp);
@@ -611,6 +671,34 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
             qb[kk][1] = q_ok ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8) : 0u;
         }
     }
+    // Rotary instances: q rotated to position L - 1, as fp16 head (qb) + rest
+    // (ql).  Slot r of k-step kk holds dims kk*16 + (lane%4)*2 + r*8 + {0, 1};
+    // their partners sit in the same slot of k-step kk + KT/2.
+    uint32_t ql[ROPE ? KT : 1][2];
+    if constexpr (ROPE) {
+        const int qpos = sp.L - 1;
+#pragma unroll
+        for (int kk = 0; kk < KT / 2; ++kk) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int f = kk * 16 + (lane & 3) * 2 + r * 8;
+                float c0, s0, c1, s1;
+                rope_twiddle(qpos, p.rope_phi[0][f], p.rope_phi[1][f], c0, s0);
+                rope_twiddle(qpos, p.rope_phi[0][f + 1], p.rope_phi[1][f + 1], c1, s1);
+                rope_rot_split(qb[kk][r], qb[kk + KT / 2][r], make_float2(c0, c1),
+                               make_float2(s0, s1), qb[kk][r], ql[kk][r], qb[kk + KT / 2][r],
+                               ql[kk + KT / 2][r]);
+            }
+        }
+    }
+    // Rotary state (ROPE): cos/sin of this lane's frequencies at its first
+    // token row of the current page, slot i = kk*2 + r <-> frequencies
+    // kk*16 + (lane%4)*2 + r*8 + {0, 1}.  Evaluated exactly on every 32nd
+    // page of the warp and turned by 64 tokens (one step of the warp's pages)
+    // in between: 31 turns add a few 1e-6 of relative error to the angles'
+    // cos/sin, far below what the scores can show, and the exact evaluations
+    // (32 per lane) are the costliest part of a page.
+    float2 rc[ROPE ? KT : 1], rs[ROPE ? KT : 1];
 
     const int tok0 = lane >> 2;  // this lane's tokens of a page: tok0 and tok0 + 8
     const int hA = (lane & 3) * 2;  // and its heads hA, hA + 1
@@ -647,14 +735,57 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
             }
             const uint32_t kaddr = ring_w + ((2 * k) % NS) * PB;
             float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (ROPE) {
+                // the rotary state at this page's row tok0, and at row tok0 + 8
+                float2 c8[KT], s8[KT];
 #pragma unroll
-            for (int kk = 0; kk < KT; ++kk) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(kaddr + swz<D>(k_row, kk * 2 + k_chk), a0, a1, a2, a3);
-                if (kk & 1)
-                    Elem<T>::mma(cb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
-                else
-                    Elem<T>::mma(ca, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+                for (int i = 0; i < KT; ++i) {
+                    const int f = (i >> 1) * 16 + (lane & 3) * 2 + (i & 1) * 8;
+                    if ((k & 31) == 0) {
+                        float c0, s0, c1, s1;
+                        rope_twiddle(page_pos + tok0, p.rope_phi[0][f], p.rope_phi[1][f], c0, s0);
+                        rope_twiddle(page_pos + tok0, p.rope_phi[0][f + 1], p.rope_phi[1][f + 1],
+                                     c1, s1);
+                        rc[i] = make_float2(c0, c1);
+                        rs[i] = make_float2(s0, s1);
+                    } else {
+                        rope_turn_pair(rc[i], rs[i], *reinterpret_cast<const float4*>(s_r64 + f));
+                    }
+                    c8[i] = rc[i];
+                    s8[i] = rs[i];
+                    rope_turn_pair(c8[i], s8[i], *reinterpret_cast<const float4*>(s_r8 + f));
+                }
+#pragma unroll
+                for (int kk = 0; kk < KT / 2; ++kk) {
+                    // fragments: a0/a2 row tok0, a1/a3 row tok0 + 8; a0/a1 slot r = 0, a2/a3 r = 1
+                    uint32_t x[4], y[4], xh[4], xl[4], yh[4], yl[4];
+                    ldsm_x4(kaddr + swz<D>(k_row, kk * 2 + k_chk), x[0], x[1], x[2], x[3]);
+                    ldsm_x4(kaddr + swz<D>(k_row, (kk + KT / 2) * 2 + k_chk), y[0], y[1], y[2],
+                            y[3]);
+                    rope_rot_split(x[0], y[0], rc[2 * kk], rs[2 * kk], xh[0], xl[0], yh[0], yl[0]);
+                    rope_rot_split(x[1], y[1], c8[2 * kk], s8[2 * kk], xh[1], xl[1], yh[1], yl[1]);
+                    rope_rot_split(x[2], y[2], rc[2 * kk + 1], rs[2 * kk + 1], xh[2], xl[2], yh[2],
+                                   yl[2]);
+                    rope_rot_split(x[3], y[3], c8[2 * kk + 1], s8[2 * kk + 1], xh[3], xl[3], yh[3],
+                                   yl[3]);
+                    const int k2 = kk + KT / 2;
+                    Elem<T>::mma(ca, xh[0], xh[1], xh[2], xh[3], qb[kk][0], qb[kk][1]);
+                    Elem<T>::mma(ca, xh[0], xh[1], xh[2], xh[3], ql[kk][0], ql[kk][1]);
+                    Elem<T>::mma(ca, xl[0], xl[1], xl[2], xl[3], qb[kk][0], qb[kk][1]);
+                    Elem<T>::mma(cb, yh[0], yh[1], yh[2], yh[3], qb[k2][0], qb[k2][1]);
+                    Elem<T>::mma(cb, yh[0], yh[1], yh[2], yh[3], ql[k2][0], ql[k2][1]);
+                    Elem<T>::mma(cb, yl[0], yl[1], yl[2], yl[3], qb[k2][0], qb[k2][1]);
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < KT; ++kk) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(kaddr + swz<D>(k_row, kk * 2 + k_chk), a0, a1, a2, a3);
+                    if (kk & 1)
+                        Elem<T>::mma(cb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+                    else
+                        Elem<T>::mma(ca, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+                }
             }
             __syncwarp();
             if (lane == 0 && 2 * k + NS < n_items) {
@@ -910,14 +1041,14 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D>::kMinBlocks)
                                             reinterpret_cast<float*>(ring));
 }
 
-template <int D, typename T>
-cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtensorMap* maps,
-                                dim3 grid, cudaStream_t stream) {
+template <int D, typename T, bool ROPE>
+cudaError_t launch_attend_mma_dr(bool split, const AttendParams& p, const CUtensorMap* maps,
+                                 dim3 grid, cudaStream_t stream) {
     const bool clustered = split && p.cluster > 1;
     const void* fn =
-        !split ? reinterpret_cast<const void*>(&attend_mma_kernel<D, T, false, false>)
-               : clustered ? reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true, true>)
-                           : reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true, false>);
+        !split ? reinterpret_cast<const void*>(&attend_mma_kernel<D, T, false, false, ROPE>)
+        : clustered ? reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true, true, ROPE>)
+                    : reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true, false, ROPE>);
     constexpr int kMaxDevices = 64;
     static std::atomic<uint32_t> configured[kMaxDevices];
     int dev = 0;
@@ -926,7 +1057,7 @@ cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtenso
     const uint32_t bit = !split ? 1u : (clustered ? 8u : 2u);
     if (dev < 0 || dev >= kMaxDevices || !(configured[dev].load() & bit)) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 MmaCfg<D>::kSmemBytes);
+                                 MmaCfg<D, ROPE>::kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDevices) configured[dev].fetch_or(bit);
     }
@@ -941,7 +1072,7 @@ cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtenso
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = MmaCfg<D>::kSmemBytes;
+    cfg.dynamicSmemBytes = MmaCfg<D, ROPE>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -954,6 +1085,19 @@ cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtenso
     cfg.attrs = attr;
     cfg.numAttrs = clustered ? 2 : 1;
     return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// Launchers of the plain instances (fp16 / bf16) and of the rotary ones (fp16).
+template <int D, typename T>
+cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtensorMap* maps,
+                                dim3 grid, cudaStream_t stream) {
+    return launch_attend_mma_dr<D, T, false>(split, p, maps, grid, stream);
+}
+
+template <int D>
+cudaError_t launch_attend_mma_rope_d(bool split, const AttendParams& p, const CUtensorMap* maps,
+                                     dim3 grid, cudaStream_t stream) {
+    return launch_attend_mma_dr<D, __half, true>(split, p, maps, grid, stream);
 }
 
 }  // namespace pa

@@ -90,17 +90,22 @@ struct AttendCfg {
 };
 
 // Tensor-core kernel configuration per head dim (see pa_attend_mma.cuh).
-template <int D>
+// ROPE: the rotary instances, which keep the rotated q (hi + lo) and the
+// lane's rotary state in registers; they run 2 CTAs per SM (3 at D = 64) with
+// deeper rings, plus the per-CTA tables of the 8- and 64-token rotations.
+template <int D, bool ROPE = false>
 struct MmaCfg {
     static_assert(D % 64 == 0 || (D % 64 == 32 && (D / 32) % 2 == 1),
                   "head dim: 64-column slabs, or an odd number of 32-column units");
+    static_assert(!ROPE || D <= 128, "rotary instances: head dims up to 128");
     static constexpr bool kRows64 = (D % 64) != 0;  // one 3-D box, 64-byte units, 64-byte swizzle
     static constexpr int kFullSlabs = D / 64;       // else: 128-byte slabs (128-byte swizzle)
     static constexpr int kSlabBytes = kPageSize * 128;
     static constexpr int kPageBytes = kPageSize * D * 2;
     // pages in flight per warp; with the fixed buffers below this keeps
     // kMinBlocks CTAs per SM within 228 KiB of shared memory
-    static constexpr int kStages = D == 256 ? 3 : (D == 128 ? 4 : (D == 96 ? 5 : 6));
+    static constexpr int kStages = ROPE ? (D == 128 ? 6 : (D == 96 ? 8 : 6))
+                                        : (D == 256 ? 3 : (D == 128 ? 4 : (D == 96 ? 5 : 6)));
     static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
     // output dims combined per round at a partition edge
     static constexpr int kXDims = (D % 64 == 0) ? 64 : 32;
@@ -114,10 +119,12 @@ struct MmaCfg {
     static constexpr int kWideXStride = D + 4;
     static_assert(kWideXOff + kWarps * kMaxHeadsPerCta * kWideXStride * 4 <= kRingBytes,
                   "one-round combine fits in the page ring");
+    // rotary tables: (cos, sin) of the 8- and 64-token turns, D/2 frequencies each
+    static constexpr int kRopeBytes = ROPE ? 2 * (D / 2) * 8 : 0;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes + kXBytes +
                                       kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 3 * 4 +
-                                      kWarps * kStages * 8 + 16;
-    static constexpr int kMinBlocks = D == 256 ? 2 : 3;
+                                      kWarps * kStages * 8 + kRopeBytes + 16;
+    static constexpr int kMinBlocks = ROPE ? (D == 64 ? 3 : 2) : (D == 256 ? 2 : 3);
     static_assert(kMinBlocks * (kSmemBytes + 1024) <= 228 * 1024, "CTAs per SM by shared memory");
     static_assert(kRows64 || kPageBytes == kFullSlabs * kSlabBytes, "slab layout");
     static_assert(kPageBytes % 1024 == 0, "page slots keep the 1 KiB swizzle alignment");
@@ -267,5 +274,5 @@ __device__ __forceinline__ void wait_for_prerequisite_grid() {
 namespace pa {
 cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 grid,
                           cudaStream_t stream);
-int attend_ctas_per_sm(int kernel, int dtype, int D, int G);
+int attend_ctas_per_sm(int kernel, int dtype, int D, int G, bool rope);
 }  // namespace pa

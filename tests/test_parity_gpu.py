@@ -32,8 +32,10 @@ def test_workload_full_size(name):
     case = workloads.workload(name)
     if gpu_helpers.KERNEL == "simt" and (case.dtype == "bf16" or case.D == 96):
         pytest.skip("the CUDA-core kernel is built for fp16/fp32 and head dims 64/128/256")
-    if gpu_helpers.KERNEL == "mma" and (case.rope_theta > 0 or case.dtype == "f32"):
-        pytest.skip("rotary embedding and fp32 caches run on the CUDA-core kernel")
+    if gpu_helpers.KERNEL == "mma" and ((case.rope_theta > 0 and case.D > 128) or
+                                        case.dtype == "f32"):
+        pytest.skip("fp32 caches, and rotary embeddings at head dims above 128, run on the "
+                    "CUDA-core kernel")
     out, lse, err, plan = run_gpu(case)
     assert err == 0
     rel = assert_matches_oracle(case, out, lse, what=name)
@@ -325,11 +327,13 @@ def test_wider_paths_window_ragged_and_invariants(dtype, D):
             assert np.array_equal(out[b, h], vals.astype(np.float64))
 
 
-@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("D", [64, 96, 128, 256])
 @pytest.mark.parametrize("theta", [10000.0, 500000.0])
 def test_rotary_embedding_in_kernel(D, theta):
-    if gpu_helpers.KERNEL == "mma":
-        pytest.skip("rotary embedding runs on the CUDA-core kernel")
+    if gpu_helpers.KERNEL == "mma" and D > 128:
+        pytest.skip("rotary embeddings at head dims above 128 run on the CUDA-core kernel")
+    if gpu_helpers.KERNEL == "simt" and D == 96:
+        pytest.skip("the CUDA-core kernel is built for head dims 64/128/256")
     case = workloads.make_case("rope", len(LENS), 8, 2, D, LENS, seed=800 + D, q_std=2.0,
                                rope_theta=theta)
     for S in (0, 64, 4096):
@@ -364,3 +368,29 @@ def test_fp32_cache(D):
         out, lse, err, _ = run_gpu(wcase, guard=64)
         assert err == 0
         assert_matches_oracle(wcase, out, lse, what=f"f32 rope window D{D} S{S}")
+
+
+# ---- rotary embedding on the tensor-core kernel, over its plan shapes
+ROPE_PLANS = {
+    "one_partition": dict(partition_size=4096),
+    "merge_kernel": dict(partition_size=96, cluster=False, merge_in_kernel=0),
+    "two_per_cta": dict(partition_size=64, parts_per_cta=2, merge_in_kernel=0),
+    "last_cta_merge": dict(partition_size=1024, merge_in_kernel=1),
+    "cluster": dict(partition_size=256, cluster=True),
+}
+
+
+@pytest.mark.parametrize("plan_kind", sorted(ROPE_PLANS))
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 8, 2), (96, 12, 4), (128, 32, 8)])
+def test_rotary_tensor_core_plan_shapes(plan_kind, D, Hq, Hkv):
+    if gpu_helpers.KERNEL != "mma":
+        pytest.skip("tensor-core plan shapes")
+    kw = dict(ROPE_PLANS[plan_kind])
+    if kw.get("merge_in_kernel") == 1 and (Hq // Hkv) * (D // 4) > 128:
+        pytest.skip("the last-CTA merge serves at most 128 (head, 4-dim column) items")
+    lens = [1, 17, 700, 2049, 3333]
+    case = workloads.make_case("ropep", len(lens), Hq, Hkv, D, lens, seed=1600 + D, q_std=2.0,
+                               rope_theta=500000.0, window=3000 if plan_kind == "cluster" else 0)
+    out, lse, err, plan = run_gpu(case, guard=16, **kw)
+    assert err == 0 and plan.kernel == 2 and plan.rope_theta > 0
+    assert_matches_oracle(case, out, lse, what=f"rope mma {plan_kind} D{D}")
