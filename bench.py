@@ -403,50 +403,91 @@ def time_graph_rotating(case, device, kernel, min_steps=40, max_copies=64,
     return out
 
 
-def e2e_steps(arm, steps, warmup, upload_kv=False):
+def e2e_steps(arm, steps, warmup, upload_kv=False, pipelined=True):
     """Through the public API with host buffers: per step, copy the step's inputs
-    from pinned host memory, decode, read out + LSE back to pinned host."""
+    (q, block table, context lengths; with upload_kv also the K/V pools) from
+    pinned host memory, decode, and read out + LSE back to pinned host memory.
+
+    pipelined: the way a serving loop runs it -- two sets of per-step device
+    and host buffers, the input copies on one stream, the decode on the
+    compute stream, the result copies on a third, ordered by events, so that
+    step i+1's inputs and step i-1's results move while step i computes.
+    Otherwise every copy and the decode run in order on one stream.
+    Returns (ms per step, H2D bytes per step, D2H bytes per step)."""
     torch = arm.torch
     c = arm.case
+    dev = arm.device
+
     def host(a):
         t = torch.from_numpy(a)
         return (t.view(torch.bfloat16) if c.dtype == "bf16" else t).pin_memory()
 
-    hq = host(c.q)
-    hbt = torch.from_numpy(c.block_tables).pin_memory()
-    hcl = torch.from_numpy(c.context_lens).pin_memory()
-    hout = torch.empty(arm.out.shape, dtype=arm.out.dtype).pin_memory()
-    hlse = torch.empty(arm.lse.shape, dtype=arm.lse.dtype).pin_memory()
+    nbuf = 2 if pipelined else 1
+    hq = [host(c.q) for _ in range(nbuf)]
+    hbt = [torch.from_numpy(c.block_tables).pin_memory() for _ in range(nbuf)]
+    hcl = [torch.from_numpy(c.context_lens).pin_memory() for _ in range(nbuf)]
+    hout = [torch.empty(arm.out.shape, dtype=arm.out.dtype).pin_memory() for _ in range(nbuf)]
+    hlse = [torch.empty(arm.lse.shape, dtype=arm.lse.dtype).pin_memory() for _ in range(nbuf)]
+    dq = [arm.q] + [torch.empty_like(arm.q) for _ in range(nbuf - 1)]
+    dbt = [arm.bt] + [torch.empty_like(arm.bt) for _ in range(nbuf - 1)]
+    dcl = [arm.cl] + [torch.empty_like(arm.cl) for _ in range(nbuf - 1)]
+    dout = [arm.out] + [torch.empty_like(arm.out) for _ in range(nbuf - 1)]
+    dlse = [arm.lse] + [torch.empty_like(arm.lse) for _ in range(nbuf - 1)]
     hk = hv = None
     if upload_kv:
         hk = host(c.k_cache)
         hv = host(c.v_cache)
-    h2d = hq.numel() * 2 + hbt.numel() * 4 + hcl.numel() * 4
+    h2d = hq[0].numel() * hq[0].element_size() + hbt[0].numel() * 4 + hcl[0].numel() * 4
     if upload_kv:
-        h2d += hk.numel() * 2 + hv.numel() * 2
-    d2h = hout.numel() * 2 + hlse.numel() * 4
+        h2d += hk.numel() * hk.element_size() + hv.numel() * hv.element_size()
+    d2h = hout[0].numel() * hout[0].element_size() + hlse[0].numel() * 4
 
-    def one():
-        arm.q.copy_(hq, non_blocking=True)
-        arm.bt.copy_(hbt, non_blocking=True)
-        arm.cl.copy_(hcl, non_blocking=True)
-        if upload_kv:
-            arm.k.copy_(hk, non_blocking=True)
-            arm.v.copy_(hv, non_blocking=True)
+    comp = arm.stream
+    s_in = torch.cuda.Stream(dev) if pipelined else comp
+    s_out = torch.cuda.Stream(dev) if pipelined else comp
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_done = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_read = [torch.cuda.Event() for _ in range(nbuf)]
+    saved = (arm.q, arm.bt, arm.cl, arm.out, arm.lse)
+
+    def one(i):
+        j = i % nbuf
+        with torch.cuda.stream(s_in):
+            if i >= nbuf:
+                s_in.wait_event(ev_done[j])   # buffer set j's previous decode is done
+            dq[j].copy_(hq[j], non_blocking=True)
+            dbt[j].copy_(hbt[j], non_blocking=True)
+            dcl[j].copy_(hcl[j], non_blocking=True)
+            if upload_kv:
+                arm.k.copy_(hk, non_blocking=True)
+                arm.v.copy_(hv, non_blocking=True)
+            ev_in[j].record(s_in)
+        comp.wait_event(ev_in[j])
+        if i >= nbuf:
+            comp.wait_event(ev_read[j])       # its previous results have been read
+        arm.q, arm.bt, arm.cl, arm.out, arm.lse = dq[j], dbt[j], dcl[j], dout[j], dlse[j]
         arm.step()
-        hout.copy_(arm.out, non_blocking=True)
-        hlse.copy_(arm.lse, non_blocking=True)
+        ev_done[j].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[j])
+            hout[j].copy_(dout[j], non_blocking=True)
+            hlse[j].copy_(dlse[j], non_blocking=True)
+            ev_read[j].record(s_out)
 
-    for _ in range(warmup):
-        one()
+    for i in range(warmup):
+        one(i)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(arm.stream)
-    for _ in range(steps):
-        one()
-    b.record(arm.stream)
+    a.record(s_in)
+    for i in range(steps):
+        one(warmup + i)
+    # the end: every stream's work of the timed steps
+    comp.wait_stream(s_in)
+    comp.wait_stream(s_out)
+    b.record(comp)
     torch.cuda.synchronize()
+    arm.q, arm.bt, arm.cl, arm.out, arm.lse = saved
     ms = a.elapsed_time(b) / steps
     return ms, h2d, d2h
 
@@ -614,13 +655,17 @@ def run_gpu(args):
         traffic = tr["bytes_per_launch"]
 
     e2e_ms, h2d, d2h = e2e_steps(arm, max(10, min(args.steps, 200)), 3)
+    ser_ms, _, _ = e2e_steps(arm, max(10, min(args.steps, 200)), 3, pipelined=False)
     e2e = {"value": byts / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
            "note": "per step: H2D of q, block table, context lengths (KV cache resident); "
-                   "D2H of out and LSE"}
+                   "pa_decode; D2H of out and LSE -- pipelined over two buffer sets and three "
+                   "streams as a serving loop runs it",
+           "serial": {"value": byts / (ser_ms * 1e-3) / 1e9, "ms_per_step": ser_ms,
+                      "note": "the same with every copy and the decode in order on one stream"}}
     e2e_kv = None
     if not args.no_kv_upload:
-        kv_ms, kv_h2d, kv_d2h = e2e_steps(arm, 5, 1, upload_kv=True)
+        kv_ms, kv_h2d, kv_d2h = e2e_steps(arm, 5, 1, upload_kv=True, pipelined=False)
         e2e_kv = {"value": byts / (kv_ms * 1e-3) / 1e9, "unit": UNIT,
                   "h2d_bytes_per_step": kv_h2d, "d2h_bytes_per_step": kv_d2h,
                   "ms_per_step": kv_ms}
