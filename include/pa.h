@@ -89,8 +89,9 @@ typedef struct pa_plan {
     int kernel;             /* PA_KERNEL_* used for the partition kernel; pa_plan picks
                                one, a caller may overwrite it before pa_decode */
     int parts_per_cta;      /* consecutive partitions one CTA of the tensor-core kernel
-                               streams (one partial per partition all the same); the
-                               CUDA-core kernel always serves one */
+                               serves, 1, 2 or 4 (each gets 4 / parts_per_cta warps;
+                               one partial per partition all the same); the CUDA-core
+                               kernel always serves one */
     int merge_in_kernel;    /* 1: with the tensor-core kernel, the last CTA of each
                                (sequence, KV head) merges that group's partials and
                                pa_merge has nothing to do; 0: pa_merge launches the

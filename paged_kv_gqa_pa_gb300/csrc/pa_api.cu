@@ -70,10 +70,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // The K (or V) cache as a tensor of 16-bit elements for the tensor-core
-// kernel's page copies.  D a multiple of 64: 2-D [rows = num_pages*Hkv*16, D],
-// box 16 rows x 64 columns (one 128-byte slab of a page), 128-byte swizzle.
-// D = 96: 3-D [rows][D/32][32], box 16 x D/32 x 32 (a whole page), 64-byte
-// swizzle.
+// kernel's page copies, one copy per page.  D a multiple of 64: 3-D
+// [D/64 slabs][rows = num_pages*Hkv*16][64 columns] -- the slab dimension
+// outermost (stride 128 bytes) so that the box, 64 x 16 x D/64, lands as the
+// page's slabs back to back (16 rows x 128 bytes each) -- with the 128-byte
+// swizzle.  D = 96: 3-D [rows][D/32][32], box 32 x D/32 x 16 (a whole page),
+// 64-byte swizzle.
 static bool make_page_map(CUtensorMap* map, const void* base, long long rows, int D,
                           int dtype) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -81,11 +83,11 @@ static bool make_page_map(CUtensorMap* map, const void* base, long long rows, in
     const CUtensorMapDataType et =
         dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (D % 64 == 0) {
-        const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-        const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-        const cuuint32_t box[2] = {64u, (cuuint32_t)kPageSize};
-        const cuuint32_t estr[2] = {1, 1};
-        return enc(map, et, 2, const_cast<void*>(base), dims, strides, box, estr,
+        const cuuint64_t dims[3] = {64u, (cuuint64_t)rows, (cuuint64_t)(D / 64)};
+        const cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128u};
+        const cuuint32_t box[3] = {64u, (cuuint32_t)kPageSize, (cuuint32_t)(D / 64)};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        return enc(map, et, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
                CUDA_SUCCESS;
@@ -595,6 +597,10 @@ static int check_plan(const pa_plan_t* plan) {
     if (plan->parts_per_cta < 1 ||
         (long long)plan->parts_per_cta * (plan->partition_size / kPageSize) > kMaxPagesPerPart)
         return PA_ERR_INVALID_ARG;
+    // The tensor-core kernel gives each of a CTA's partitions 4 / parts_per_cta warps.
+    if (plan->kernel == PA_KERNEL_MMA && plan->parts_per_cta != 1 && plan->parts_per_cta != 2 &&
+        plan->parts_per_cta != 4)
+        return PA_ERR_INVALID_ARG;
     // TMA row coordinates are signed 32-bit.
     if (plan->kernel == PA_KERNEL_MMA &&
         (long long)plan->num_pages * Hkv * kPageSize > 0x7fffffffLL)
@@ -671,7 +677,7 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
         if (!make_page_map(&maps[0], k_cache, rows, D, plan->dtype) ||
             !make_page_map(&maps[1], v_cache, rows, D, plan->dtype))
             return PA_ERR_CUDA;
-        p.parts_per_cta = plan->parts_per_cta;
+        p.parts_per_cta = P > 1 ? plan->parts_per_cta : 1;  // one partition: all warps on it
         p.prewait_prefetch = plan->prewait_prefetch;
         const dim3 grid((P + p.parts_per_cta - 1) / p.parts_per_cta, p.Hkv * p.nchunk, p.B);
         e = launch_attend_mma(D, plan->dtype, P > 1, p, maps, grid,

@@ -5,11 +5,13 @@
 // page pipelines, online softmax per page, warp states merged at the end.
 // What differs is how a page is staged and contracted:
 //
-//  * Staging.  K and V pages arrive through 2-D TMA tensor copies
-//    (cp.async.bulk.tensor) of the cache viewed as a [num_pages*Hkv*16, D]
-//    matrix, one 16-row x 64-column box per 128-byte slab of the row, with the
-//    128-byte swizzle: the 16-byte chunk c of row r lands at chunk c ^ (r & 7)
-//    of that row, so the ldmatrix reads below are free of bank conflicts.
+//  * Staging.  A K or V page arrives through one TMA tensor copy
+//    (cp.async.bulk.tensor.3d) of the cache viewed as [D/64 slabs][rows =
+//    num_pages*Hkv*16][64 columns] (slab stride 128 bytes, row stride 2D
+//    bytes), a box of 64 columns x 16 rows x D/64 slabs, with the 128-byte
+//    swizzle: in shared memory the page is its slabs back to back, and the
+//    16-byte chunk c of row r of a slab lands at chunk c ^ (r & 7), so the
+//    ldmatrix reads below are free of bank conflicts.
 //    A head dim that is not a multiple of 64 (96) is copied instead as one
 //    3-D box per page, [16 rows][D/32 units of 64 bytes], with the 64-byte
 //    swizzle: chunk c of 64-byte unit u (u = row * D/32 + slab) lands at
@@ -33,12 +35,13 @@
 //    ldmatrix.trans of the same swizzled page, P^T from S^T by movmatrix.trans.
 //    The accumulator of a lane holds two heads, so the online rescale needs
 //    no data exchange.
-//  * Several partitions per CTA.  A CTA may stream parts_per_cta consecutive
-//    partitions of its (sequence, KV head); the warps' page pipelines run on
-//    across partition edges, and at each edge the four warp states are
-//    combined through a small shared buffer (64 output dims per round) into
-//    that partition's partial.  Fewer, longer CTAs spend less time in
-//    prologues and epilogues; the partials stay one per partition.
+//  * Several partitions per CTA.  A CTA may serve parts_per_cta (1, 2 or 4)
+//    consecutive partitions of its (sequence, KV head): each partition gets
+//    4 / parts_per_cta of the warps, so no warp crosses a partition edge,
+//    and at the end, with the page ring idle, one round combines each
+//    partition's warp states into that partition's partial.  Fewer, longer
+//    CTAs spend less time in prologues and epilogues; the partials stay one
+//    per partition.
 #pragma once
 
 #include <cuda.h>
@@ -108,15 +111,6 @@ __device__ __forceinline__ void store4(T* dst, float a, float b, float c, float 
     packed.x = Elem<T>::pack2(a, b, ra, rb);
     packed.y = Elem<T>::pack2(c, d, rc, rd);
     *reinterpret_cast<uint2*>(dst) = packed;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2,
@@ -453,15 +447,17 @@ __device__ __forceinline__ void rope_turn_pair(float2& c, float2& s, float4 t) {
 }
 
 // Before the dependency wait of a programmatic dependent launch, per warp:
-// read the sequence length and this warp's first page ids as hints and
-// request its first prewait_prefetch pages (K and V) into L2, so that they
+// read the sequence length and this warp's first page ids (relative pages
+// first, first + step, ... below limit) as hints and request its first
+// prewait_prefetch pages (K and V) into L2, so that they
 // stream in while the previous grid drains.  The values read here may be
 // stale (the previous grid may still be writing them): they are only
 // bounds-checked prefetch addresses, and everything is read again after the
 // wait, so a stale hint costs one useless prefetch.  L2-only loads, so that
 // nothing read here sits in L1 afterwards.
 __device__ __forceinline__ void prefetch_first_pages(const AttendParams& p, int part0, int kvh,
-                                                     int b, int warp, int lane, int D) {
+                                                     int b, int first, int step, int limit,
+                                                     int lane, int D) {
     const int pp = p.pages_per_part;
     int Lh = 0;
     if (lane == 0) Lh = __ldcg(p.context_lens + b);
@@ -470,8 +466,8 @@ __device__ __forceinline__ void prefetch_first_pages(const AttendParams& p, int 
     if (!sp.valid || part0 >= sp.num_parts) return;
     const int pgA = sp.first_page + part0 * pp;
     const int n_range = min(p.parts_per_cta * pp, sp.end_page - pgA);
-    const int j = warp + kWarps * lane;  // this lane: page `lane` of the warp
-    if (lane < p.prewait_prefetch && j < n_range) {
+    const int j = first + step * lane;  // this lane: page `lane` of the warp
+    if (lane < p.prewait_prefetch && j < min(n_range, limit)) {
         const int id = __ldcg(p.block_tables + (size_t)b * p.maxp + pgA + j);
         if (id >= 0 && id < p.num_pages) {
             const size_t off = ((size_t)id * p.Hkv + kvh) * (size_t)(kPageSize * D);
@@ -500,15 +496,13 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     constexpr int NS = Cfg::kStages;
     constexpr int PB = Cfg::kPageBytes;
     constexpr int KT = D / 16;  // k-steps of q.K, m-tiles of P.V
-    constexpr int XD = Cfg::kXDims;
-    constexpr int ROUNDS = D / XD;
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;  // 128-byte swizzle needs 1 KiB alignment
     unsigned char* base = smem_raw + (base_u32 - raw_u32);
     unsigned char* ring = base;
-    float* xbuf = reinterpret_cast<float*>(base + Cfg::kRingBytes);  // [warps][G][XD]
+    float* xbuf = reinterpret_cast<float*>(base + Cfg::kRingBytes);  // last-CTA merge scratch
     int* s_pid = reinterpret_cast<int*>(base + Cfg::kRingBytes + Cfg::kXBytes);
     float* s_ml = reinterpret_cast<float*>(s_pid + kMaxPagesPerPart);  // [warps][m|l|n][8]
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 3);
@@ -526,6 +520,17 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     const int h0 = kvh * p.g + (blockIdx.y % p.nchunk) * G;
     const int b = blockIdx.z;
     const int pp = p.pages_per_part;
+    const int wpp = kWarps / ppc;  // warps per partition (ppc is 1, 2 or 4)
+    const int wq = warp / wpp;     // this warp's partition slot within the CTA
+    const int wl = warp % wpp;     // and its place among that partition's warps
+    // relative page of this warp's i-th page, and its page count in a range
+    // of n_range pages
+    auto wpage = [&](int i) { return wq * pp + wl + i * wpp; };
+    auto warp_pages = [&](int n_range) {
+        const int q_end = min((wq + 1) * pp, n_range);
+        const int first = wq * pp + wl;
+        return q_end > first ? (q_end - first + wpp - 1) / wpp : 0;
+    };
     const uint32_t bar_w = smem_u32(bars) + warp * NS * 8;
     const uint32_t ring_w = smem_u32(ring) + warp * NS * PB;
 
@@ -540,9 +545,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
         if constexpr (Cfg::kRows64) {
             tma_load_3d(ring_w + slot * PB, map, 0, 0, y, bar);
         } else {
-#pragma unroll
-            for (int s = 0; s < Cfg::kFullSlabs; ++s)
-                tma_load_2d(ring_w + slot * PB + s * Cfg::kSlabBytes, map, s * 64, y, bar);
+            tma_load_3d(ring_w + slot * PB, map, 0, y, 0, bar);  // the whole page, all slabs
         }
     };
 
@@ -560,14 +563,15 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
         for (int s = 0; s < NS; ++s) mbar_init(bar_w + s * 8, 1);
         fence_mbar_init();
     }
-    if (p.prewait_prefetch) prefetch_first_pages(p, part0, kvh, b, warp, lane, D);
+    if (p.prewait_prefetch)
+        prefetch_first_pages(p, part0, kvh, b, wq * pp + wl, wpp, (wq + 1) * pp, lane, D);
     if constexpr (ROPE) {
         // (kernel parameters only: no input is read)
         for (int f = threadIdx.x; f < D / 2; f += kThreads) {
             float c, sn;
             rope_twiddle(8, p.rope_phi[0][f], p.rope_phi[1][f], c, sn);
             s_r8[f] = make_float2(c, sn);
-            rope_twiddle(kWarps * kPageSize, p.rope_phi[0][f], p.rope_phi[1][f], c, sn);
+            rope_twiddle(wpp * kPageSize, p.rope_phi[0][f], p.rope_phi[1][f], c, sn);
             s_r64[f] = make_float2(c, sn);
         }
     }
@@ -648,11 +652,13 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
         return;
     }
 
-    // ---- this warp's pages over the whole range: j = warp, warp + 4, ...;
+    // ---- this warp's pages: the CTA's ppc partitions each get kWarps / ppc
+    // warps (wpp), and warp wl of partition slot wq streams the partition's
+    // pages wl, wl + wpp, ... (relative page j = wq * pp + wl + i * wpp);
     // items K0, V0, K1, V1, ...
-    const int nk = n_range > warp ? (n_range - warp + kWarps - 1) / kWarps : 0;
+    const int nk = warp_pages(n_range);
     const int n_items = 2 * nk;
-    auto issue = [&](int item) { issue_page(item, s_pid[warp + (item >> 1) * kWarps]); };
+    auto issue = [&](int item) { issue_page(item, s_pid[wpage(item >> 1)]); };
     if (lane == 0) {
         for (int i = 0; i < NS && i < n_items; ++i) issue(i);
     }
@@ -712,8 +718,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     int consumed = 0;
     int k = 0;  // this warp's next page (index into its stream)
 
-    for (int qp = 0; qp < nparts; ++qp) {
-        const int qend = min((qp + 1) * pp, n_range);  // end of partition qp, relative page
+    {
         float o[KT][4];
 #pragma unroll
         for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -721,8 +726,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
         float l_run[2] = {0.f, 0.f};   // exp-sum of the fp32 weights
         float n_run[2] = {0.f, 0.f};   // exp-sum of the fp16-rounded weights
 
-        for (; ok && k < nk && warp + k * kWarps < qend; ++k) {
-            const int page_pos = (pgA + warp + k * kWarps) * kPageSize;
+        for (; ok && k < nk; ++k) {
+            const int page_pos = (pgA + wpage(k)) * kPageSize;
             // ---------------- K page: S^T = K . Q^T
             {
                 const int item = 2 * k;
@@ -905,8 +910,9 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
             consumed = issued;
         }
 
-        // ---- partition qp: combine the four warp states.  Exp-sums: lanes
-        // with equal lane%4 hold the same heads over different tokens.
+        // ---- combine the warp states of each of the CTA's partitions (wpp
+        // warps each).  Exp-sums: lanes with equal lane%4 hold the same heads
+        // over different tokens.
 #pragma unroll
         for (int mask = 4; mask < 32; mask <<= 1) {
             l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], mask);
@@ -927,110 +933,80 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
                 ml[2 * kMaxHeadsPerCta + hA + 1] = n_run[1];
             }
         }
-        const int part = part0 + qp;
-        // Combine nd output dims starting at d0 from the four warps' states in
-        // buf ([warp][head][stride] floats) and write them out.
-        auto combine = [&](const float* buf, int stride, int d0, int nd) {
-            const bool failed = s_flag != 0;
-            for (int idx = threadIdx.x; idx < G * (nd / 4); idx += kThreads) {
-                const int h = idx / (nd / 4);
-                const int dl = (idx % (nd / 4)) * 4;
-                const int d = d0 + dl;
-                float M = -INFINITY;
+        // Every warp is past its last page, so the page ring is idle: all D
+        // dims of every warp state go there at once (behind the cluster
+        // partial) and one round combines them.
+        __syncthreads();
+        float* xw = reinterpret_cast<float*>(ring + Cfg::kWideXOff);
+        constexpr int XS = Cfg::kWideXStride;
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w * 3 * kMaxHeadsPerCta + h]);
-                float Ls = 0.f, Ns = 0.f;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const float* ml = s_ml + w * 3 * kMaxHeadsPerCta;
-                    const float mw = ml[h];
-                    const float c = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-                    Ls += c * ml[kMaxHeadsPerCta + h];
-                    Ns += c * ml[2 * kMaxHeadsPerCta + h];
-                    const float4 ow =
-                        *reinterpret_cast<const float4*>(buf + (w * G + h) * stride + dl);
-                    acc.x += c * ow.x;
-                    acc.y += c * ow.y;
-                    acc.z += c * ow.z;
-                    acc.w += c * ow.w;
-                }
-                float inv = Ns > 0.f ? 1.f / Ns : 0.f;
-                if (failed) {
-                    inv = NAN;
-                    M = NAN;
-                    Ls = NAN;
-                }
-                const size_t bh = (size_t)b * p.Hq + h0 + h;
-                if constexpr (SPLIT) {
-                    const float4 ov = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-                    if (clustered) {
-                        *reinterpret_cast<float4*>(cpart + ClusterPartial<D>::o_off(h, d) / 4) = ov;
-                        if (d == 0) {
-                            cpart[ClusterPartial<D>::m_off(G, h) / 4] = M;
-                            cpart[ClusterPartial<D>::l_off(G, h) / 4] = Ls;
-                        }
-                    } else {
-                        const size_t row = bh * p.P + part;
-                        *reinterpret_cast<float4*>(p.ws_o + row * D + d) = ov;
-                        if (d == 0) {
-                            p.ws_m[row] = M;
-                            p.ws_l[row] = Ls;
-                        }
-                    }
-                } else {
-                    store4<T>(out + bh * D + d, acc.x * inv, acc.y * inv, acc.z * inv,
-                              acc.w * inv);
-                    if (d == 0)
-                        p.lse[bh] = failed ? NAN
-                                           : (Ls > 0.f ? M * 0.69314718055994531f + logf(Ls)
-                                                       : -INFINITY);
-                }
+        for (int mt = 0; mt < KT; ++mt) {
+            const int d = mt * 16 + (lane >> 2);
+            if (hA < G) {
+                xw[(warp * G + hA) * XS + d] = o[mt][0];
+                xw[(warp * G + hA) * XS + d + 8] = o[mt][2];
             }
-        };
-        if (qp == nparts - 1) {
-            // The CTA's last partition: once every warp is past its last page the
-            // page ring is idle, and all D dims of the four warp states fit in it
-            // at once (behind the cluster partial), so one round combines them.
-            __syncthreads();
-            float* xw = reinterpret_cast<float*>(ring + Cfg::kWideXOff);
-            constexpr int XS = Cfg::kWideXStride;
-#pragma unroll
-            for (int mt = 0; mt < KT; ++mt) {
-                const int d = mt * 16 + (lane >> 2);
-                if (hA < G) {
-                    xw[(warp * G + hA) * XS + d] = o[mt][0];
-                    xw[(warp * G + hA) * XS + d + 8] = o[mt][2];
-                }
-                if (hA + 1 < G) {
-                    xw[(warp * G + hA + 1) * XS + d] = o[mt][1];
-                    xw[(warp * G + hA + 1) * XS + d + 8] = o[mt][3];
-                }
-            }
-            __syncthreads();
-            combine(xw, XS, 0, D);
-            __syncthreads();  // the ring and s_ml are reused by the merges below
-        } else {
-#pragma unroll
-            for (int r = 0; r < ROUNDS; ++r) {
-#pragma unroll
-                for (int mi = 0; mi < XD / 16; ++mi) {
-                    const int mt = r * (XD / 16) + mi;
-                    const int d = mi * 16 + (lane >> 2);
-                    if (hA < G) {
-                        xbuf[(warp * G + hA) * XD + d] = o[mt][0];
-                        xbuf[(warp * G + hA) * XD + d + 8] = o[mt][2];
-                    }
-                    if (hA + 1 < G) {
-                        xbuf[(warp * G + hA + 1) * XD + d] = o[mt][1];
-                        xbuf[(warp * G + hA + 1) * XD + d + 8] = o[mt][3];
-                    }
-                }
-                __syncthreads();
-                combine(xbuf, XD, r * XD, XD);
-                __syncthreads();  // xbuf and s_ml are rewritten next
+            if (hA + 1 < G) {
+                xw[(warp * G + hA + 1) * XS + d] = o[mt][1];
+                xw[(warp * G + hA + 1) * XS + d + 8] = o[mt][3];
             }
         }
+        __syncthreads();
+        const bool failed = s_flag != 0;
+        constexpr int D4 = D / 4;
+        for (int idx = threadIdx.x; idx < nparts * G * D4; idx += kThreads) {
+            const int qp = idx / (G * D4);  // partition slot: warps qp * wpp ..
+            const int h = (idx / D4) % G;
+            const int d = (idx % D4) * 4;
+            const int w0 = qp * wpp;
+            float M = -INFINITY;
+            for (int w = w0; w < w0 + wpp; ++w) M = fmaxf(M, s_ml[w * 3 * kMaxHeadsPerCta + h]);
+            float Ls = 0.f, Ns = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int w = w0; w < w0 + wpp; ++w) {
+                const float* ml = s_ml + w * 3 * kMaxHeadsPerCta;
+                const float mw = ml[h];
+                const float c = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+                Ls += c * ml[kMaxHeadsPerCta + h];
+                Ns += c * ml[2 * kMaxHeadsPerCta + h];
+                const float4 ow = *reinterpret_cast<const float4*>(xw + (w * G + h) * XS + d);
+                acc.x += c * ow.x;
+                acc.y += c * ow.y;
+                acc.z += c * ow.z;
+                acc.w += c * ow.w;
+            }
+            float inv = Ns > 0.f ? 1.f / Ns : 0.f;
+            if (failed) {
+                inv = NAN;
+                M = NAN;
+                Ls = NAN;
+            }
+            const size_t bh = (size_t)b * p.Hq + h0 + h;
+            if constexpr (SPLIT) {
+                const float4 ov = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                if (clustered) {
+                    *reinterpret_cast<float4*>(cpart + ClusterPartial<D>::o_off(h, d) / 4) = ov;
+                    if (d == 0) {
+                        cpart[ClusterPartial<D>::m_off(G, h) / 4] = M;
+                        cpart[ClusterPartial<D>::l_off(G, h) / 4] = Ls;
+                    }
+                } else {
+                    const size_t row = bh * p.P + part0 + qp;
+                    *reinterpret_cast<float4*>(p.ws_o + row * D + d) = ov;
+                    if (d == 0) {
+                        p.ws_m[row] = M;
+                        p.ws_l[row] = Ls;
+                    }
+                }
+            } else {
+                store4<T>(out + bh * D + d, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                if (d == 0)
+                    p.lse[bh] = failed ? NAN
+                                       : (Ls > 0.f ? M * 0.69314718055994531f + logf(Ls)
+                                                   : -INFINITY);
+            }
+        }
+        __syncthreads();  // the ring and s_ml are reused by the merges below
     }
 
     if (clustered) {

@@ -107,13 +107,12 @@ struct MmaCfg {
     static constexpr int kStages = ROPE ? (D == 128 ? 6 : (D == 96 ? 8 : 6))
                                         : (D == 256 ? 3 : (D == 128 ? 4 : (D == 96 ? 5 : 6)));
     static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
-    // output dims combined per round at a partition edge
-    static constexpr int kXDims = (D % 64 == 0) ? 64 : 32;
+    // scratch of the last-CTA merge ((m, weight) pairs of a group's partials)
     static constexpr int kXBytes = kWarps * kMaxHeadsPerCta * 64 * 4;
-    // The last partition of a CTA combines all D dims at once in the idle page
-    // ring, behind the cluster partial ([G][D] o, then m and l): rows of
-    // D + 4 floats (the pad spreads the four head rows a store writes over
-    // distinct banks).
+    // A CTA combines its warp states at the end, all D dims at once, in the
+    // idle page ring behind the cluster partial ([G][D] o, then m and l):
+    // rows of D + 4 floats (the pad spreads the four head rows a store writes
+    // over distinct banks).
     static constexpr int kWideXOff = ((kMaxHeadsPerCta * D + 2 * kMaxHeadsPerCta) * 4 + 1023) /
                                      1024 * 1024;
     static constexpr int kWideXStride = D + 4;

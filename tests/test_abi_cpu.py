@@ -146,6 +146,11 @@ def test_decode_argument_checks_return_before_launch():
     small = binding.pa_plan_t.from_buffer_copy(plan)
     small.workspace_bytes = 256
     assert _call_decode(small) == binding.PA_ERR_INVALID_ARG
+    # the tensor-core kernel gives each of a CTA's partitions 4 / parts_per_cta warps
+    for ppc in (3, 5, 8):
+        odd = binding.pa_plan_t.from_buffer_copy(plan)
+        odd.parts_per_cta = ppc
+        assert _call_decode(odd) == binding.PA_ERR_INVALID_ARG, ppc
     bad = binding.pa_plan_t.from_buffer_copy(plan)
     bad.heads_per_cta = 3
     assert _call_decode(bad) == binding.PA_ERR_INVALID_ARG

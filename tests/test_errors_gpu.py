@@ -38,7 +38,7 @@ def test_bad_page_id_sets_error_and_nan_rows(S, bad, fused):
     case = workloads.make_case("bad", 3, 8, 2, 128, [700, 1200, 90], seed=600, partition_size=S)
     good_ref = _ref_rows(case, [0, 2])
     case.block_tables[1, 5] = case.num_pages if bad == "past_pool" else -1
-    out, lse, err, _ = run_gpu(case, guard=64, parts_per_cta=3 if S == 64 else None,
+    out, lse, err, _ = run_gpu(case, guard=64, parts_per_cta=4 if S == 64 else None,
                                merge_in_kernel=fused)
     assert err & pa.binding.PA_DEVERR_BAD_PAGE
     assert np.isnan(out[1]).all() and np.isnan(lse[1]).all()

@@ -225,7 +225,7 @@ def test_unwritten_slots_never_leak():
         assert_matches_oracle(case, out, lse, what=f"tail S{S}")
 
 
-@pytest.mark.parametrize("ppc", [1, 2, 3, 8])
+@pytest.mark.parametrize("ppc", [1, 2, 4])
 def test_several_partitions_per_cta(ppc):
     """A CTA streaming several consecutive partitions writes the same partials
     as one CTA per partition (the CUDA-core kernel ignores the setting)."""
@@ -311,7 +311,7 @@ def test_wider_paths_window_ragged_and_invariants(dtype, D):
     case = workloads.make_case("wide", len(lens), 8, 2, D, lens, seed=720 + D, window=1000,
                                q_std=3.0, dtype=dtype)
     # The in-kernel merge covers G x D/4 <= 128 items: not D = 256 with G = 4.
-    for S, fused, ppc in ((0, None, None), (256, 1 if D < 256 else 0, None), (64, 0, 3)):
+    for S, fused, ppc in ((0, None, None), (256, 1 if D < 256 else 0, None), (64, 0, 4)):
         case.partition_size = S
         out, lse, err, _ = run_gpu(case, guard=64, merge_in_kernel=fused, parts_per_cta=ppc)
         assert err == 0
