@@ -933,6 +933,60 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
                 ml[2 * kMaxHeadsPerCta + hA + 1] = n_run[1];
             }
         }
+        constexpr int D4 = D / 4;
+        if (SPLIT && !clustered && wpp == 1) {
+            // One warp per partition: the warp's state is its partition's
+            // partial.  It stages the state in its own ring slots (idle: it
+            // has consumed every page it issued) and stores it coalesced, with
+            // no barrier shared with the other warps.
+            float* xs = reinterpret_cast<float*>(ring + warp * NS * PB);
+            constexpr int XS = Cfg::kWideXStride;
+            float* xml = xs + kMaxHeadsPerCta * XS;  // [m | l | n][8]
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+                const int d = mt * 16 + (lane >> 2);
+                if (hA < G) {
+                    xs[hA * XS + d] = o[mt][0];
+                    xs[hA * XS + d + 8] = o[mt][2];
+                }
+                if (hA + 1 < G) {
+                    xs[(hA + 1) * XS + d] = o[mt][1];
+                    xs[(hA + 1) * XS + d + 8] = o[mt][3];
+                }
+            }
+            if (lane < 4) {
+                xml[hA] = m_run[0];
+                xml[hA + 1] = m_run[1];
+                xml[kMaxHeadsPerCta + hA] = l_run[0];
+                xml[kMaxHeadsPerCta + hA + 1] = l_run[1];
+                xml[2 * kMaxHeadsPerCta + hA] = n_run[0];
+                xml[2 * kMaxHeadsPerCta + hA + 1] = n_run[1];
+            }
+            __syncwarp();
+            if (wq < nparts) {
+                const bool failed = !ok;
+                for (int idx = lane; idx < G * D4; idx += 32) {
+                    const int h = idx / D4;
+                    const int d = (idx % D4) * 4;
+                    float M = xml[h], Ls = xml[kMaxHeadsPerCta + h];
+                    const float Ns = xml[2 * kMaxHeadsPerCta + h];
+                    float inv = Ns > 0.f ? 1.f / Ns : 0.f;
+                    if (failed) {
+                        inv = NAN;
+                        M = NAN;
+                        Ls = NAN;
+                    }
+                    const float4 ow = *reinterpret_cast<const float4*>(xs + h * XS + d);
+                    const size_t row = ((size_t)b * p.Hq + h0 + h) * p.P + part0 + wq;
+                    *reinterpret_cast<float4*>(p.ws_o + row * D + d) =
+                        make_float4(ow.x * inv, ow.y * inv, ow.z * inv, ow.w * inv);
+                    if (d == 0) {
+                        p.ws_m[row] = M;
+                        p.ws_l[row] = Ls;
+                    }
+                }
+            }
+        } else {
         // Every warp is past its last page, so the page ring is idle: all D
         // dims of every warp state go there at once (behind the cluster
         // partial) and one round combines them.
@@ -953,7 +1007,6 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
         }
         __syncthreads();
         const bool failed = s_flag != 0;
-        constexpr int D4 = D / 4;
         for (int idx = threadIdx.x; idx < nparts * G * D4; idx += kThreads) {
             const int qp = idx / (G * D4);  // partition slot: warps qp * wpp ..
             const int h = (idx / D4) % G;
@@ -1007,6 +1060,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
             }
         }
         __syncthreads();  // the ring and s_ml are reused by the merges below
+        }
     }
 
     if (clustered) {

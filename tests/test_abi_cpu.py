@@ -83,8 +83,11 @@ def test_plan_long_context_workload():
     plan = pa.pa_plan(4, 24, 4, 256, 16, 31250, 6250, 100000, 0, 512, 152)
     assert plan.num_partitions == 196 and plan.heads_per_cta == 6
     # 3136 one-partition CTAs would be ~10 waves of 304 resident CTAs; each
-    # CTA streams 2 consecutive partitions instead (98 per group, 1568 CTAs).
-    assert plan.parts_per_cta == 2 and plan.ctas == 98 * 4 * 4
+    # CTA serves 4 consecutive partitions instead (49 per group, 784 CTAs).
+    assert plan.parts_per_cta == 4 and plan.ctas == 49 * 4 * 4
+    # between 4 and 8 waves: 2 per CTA (B = 2: 1568 one-partition CTAs)
+    half = pa.pa_plan(2, 24, 4, 256, 16, 31250, 6250, 100000, 0, 512, 152)
+    assert half.parts_per_cta == 2 and half.ctas == 98 * 4 * 2
     rows = 4 * 24 * 196
     assert plan.workspace_bytes >= 256 + rows * 4 * 2 + rows * 256 * 4
 

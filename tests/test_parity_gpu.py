@@ -242,6 +242,13 @@ def test_several_partitions_per_cta(ppc):
     out, lse, err, _ = run_gpu(wcase, parts_per_cta=ppc)
     assert err == 0
     assert_matches_oracle(wcase, out, lse, what=f"ppc{ppc} window")
+    if gpu_helpers.KERNEL == "mma":
+        # with the last-CTA merge: 8 partitions of 512 tokens, G x D/4 = 128 items
+        fcase = workloads.make_case("ppcf", 3, 16, 4, 128, [4096, 1000, 2], seed=511)
+        fcase.partition_size = 512
+        out, lse, err, plan = run_gpu(fcase, guard=16, parts_per_cta=ppc, merge_in_kernel=1)
+        assert err == 0 and plan.merge_in_kernel == 1 and plan.num_partitions == 8
+        assert_matches_oracle(fcase, out, lse, what=f"ppc{ppc} last-CTA merge")
 
 
 @pytest.mark.parametrize("fused", [0, 1])
