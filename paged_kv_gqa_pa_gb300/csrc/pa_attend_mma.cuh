@@ -401,39 +401,65 @@ __device__ __forceinline__ void cluster_merge(const AttendParams& p, int b, int 
     cluster_barrier();  // every peer is done reading this CTA's shared memory
 }
 
-// ---- Rotary embedding on the tensor-core path (fp16, head dims up to 128).
+// ---- Rotary embedding on the tensor-core path (fp16 and bf16, head dims up
+// to 128).
 // The rotate-half partner of dim i (i < D/2) is dim i + D/2, which lies in
 // k-step kk + KT/2 of the same mma fragment slot as dim i in k-step kk: a lane
 // rotates its K fragments in registers, pairing fragment kk with kk + KT/2,
 // and never writes a rotated page back.  Rotated values are fp32 split into
-// an fp16 head and an fp16 remainder (about 22 significant bits), and q.K
-// takes K_hi q_hi + K_hi q_lo + K_lo q_hi, so the scores keep fp32-level
-// accuracy (a single fp16 rounding of the rotated q or K would cost ~3e-4 on
-// the LSE).
+// a head and a remainder of the cache's type (about 22 significant bits for
+// fp16, 16 for bf16), and q.K takes K_hi q_hi + K_hi q_lo + K_lo q_hi, so the
+// scores keep nearly fp32 accuracy (a single fp16 rounding of the rotated q
+// or K would cost ~3e-4 on the LSE).
 
-__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+// Packed 16-bit pairs <-> fp32 pairs, and the head + remainder split, per
+// element type.
+template <typename T>
+struct RopeIO;
 
-// v = hi + lo with hi = fp16(v) and lo = fp16(v - hi), elementwise.
-__device__ __forceinline__ void split_f16x2(float2 v, uint32_t& hi, uint32_t& lo) {
-    const __half2 h = __float22half2_rn(v);
-    const float2 hb = __half22float2(h);
-    hi = h2_bits(h);
-    lo = h2_bits(__float22half2_rn(make_float2(v.x - hb.x, v.y - hb.y)));
-}
+template <>
+struct RopeIO<__half> {
+    __device__ static __forceinline__ float2 unpack(uint32_t u) {
+        return __half22float2(*reinterpret_cast<__half2*>(&u));
+    }
+    // v = hi + lo with hi = fp16(v) and lo = fp16(v - hi), elementwise.
+    __device__ static __forceinline__ void split(float2 v, uint32_t& hi, uint32_t& lo) {
+        __half2 h = __float22half2_rn(v);
+        const float2 hb = __half22float2(h);
+        __half2 l = __float22half2_rn(make_float2(v.x - hb.x, v.y - hb.y));
+        hi = *reinterpret_cast<uint32_t*>(&h);
+        lo = *reinterpret_cast<uint32_t*>(&l);
+    }
+};
+
+template <>
+struct RopeIO<__nv_bfloat16> {
+    __device__ static __forceinline__ float2 unpack(uint32_t u) {
+        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
+    }
+    // v = hi + lo with hi = bf16(v) and lo = bf16(v - hi): about 16 significant bits.
+    __device__ static __forceinline__ void split(float2 v, uint32_t& hi, uint32_t& lo) {
+        __nv_bfloat162 h = __float22bfloat162_rn(v);
+        const float2 hb = __bfloat1622float2(h);
+        __nv_bfloat162 l = __float22bfloat162_rn(make_float2(v.x - hb.x, v.y - hb.y));
+        hi = *reinterpret_cast<uint32_t*>(&h);
+        lo = *reinterpret_cast<uint32_t*>(&l);
+    }
+};
 
 // x = dims (i, i + 1) of the first half, y = their partners (i + D/2,
-// i + D/2 + 1), as packed fp16; (c, s) = cos, sin of their angles.  The
-// rotated pair x' = x c - y s, y' = y c + x s, split into fp16 head + rest.
+// i + D/2 + 1), as packed 16-bit pairs; (c, s) = cos, sin of their angles.
+// The rotated pair x' = x c - y s, y' = y c + x s, split into head + rest.
+template <typename T>
 __device__ __forceinline__ void rope_rot_split(uint32_t x16, uint32_t y16, float2 c, float2 s,
                                                uint32_t& xh, uint32_t& xl, uint32_t& yh,
                                                uint32_t& yl) {
-    const float2 x = __half22float2(bits_h2(x16));
-    const float2 y = __half22float2(bits_h2(y16));
+    const float2 x = RopeIO<T>::unpack(x16);
+    const float2 y = RopeIO<T>::unpack(y16);
     const float2 xr = __ffma2_rn(x, c, __fmul2_rn(y, make_float2(-s.x, -s.y)));
     const float2 yr = __ffma2_rn(y, c, __fmul2_rn(x, s));
-    split_f16x2(xr, xh, xl);
-    split_f16x2(yr, yh, yl);
+    RopeIO<T>::split(xr, xh, xl);
+    RopeIO<T>::split(yr, yh, yl);
 }
 
 // (c, s) <- (c, s) turned by the angles whose cos/sin are t = (cos f, sin f,
@@ -486,13 +512,12 @@ static_assert(ClusterPartial<64>::kMaxBytes <= MmaCfg<64>::kWideXOff &&
 // SPLIT: partials for a merge (else the final rows).  CLUSTER (with SPLIT):
 // the partitions of a group form one cluster and merge in it; a separate
 // instance, so that the other instances carry none of its code.  ROPE: q and
-// each K row are rotated to their positions before q.K (fp16 only).
+// each K row are rotated to their positions before q.K (head dims up to 128).
 template <int D, typename T, bool SPLIT, bool CLUSTER, bool ROPE>
 __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     attend_mma_kernel(const AttendParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
     using Cfg = MmaCfg<D, ROPE>;
-    static_assert(!ROPE || std::is_same<T, __half>::value, "rotary instances are fp16");
     constexpr int NS = Cfg::kStages;
     constexpr int PB = Cfg::kPageBytes;
     constexpr int KT = D / 16;  // k-steps of q.K, m-tiles of P.V
@@ -691,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
                 float c0, s0, c1, s1;
                 rope_twiddle(qpos, p.rope_phi[0][f], p.rope_phi[1][f], c0, s0);
                 rope_twiddle(qpos, p.rope_phi[0][f + 1], p.rope_phi[1][f + 1], c1, s1);
-                rope_rot_split(qb[kk][r], qb[kk + KT / 2][r], make_float2(c0, c1),
+                rope_rot_split<T>(qb[kk][r], qb[kk + KT / 2][r], make_float2(c0, c1),
                                make_float2(s0, s1), qb[kk][r], ql[kk][r], qb[kk + KT / 2][r],
                                ql[kk + KT / 2][r]);
             }
@@ -767,11 +792,11 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
                     ldsm_x4(kaddr + swz<D>(k_row, kk * 2 + k_chk), x[0], x[1], x[2], x[3]);
                     ldsm_x4(kaddr + swz<D>(k_row, (kk + KT / 2) * 2 + k_chk), y[0], y[1], y[2],
                             y[3]);
-                    rope_rot_split(x[0], y[0], rc[2 * kk], rs[2 * kk], xh[0], xl[0], yh[0], yl[0]);
-                    rope_rot_split(x[1], y[1], c8[2 * kk], s8[2 * kk], xh[1], xl[1], yh[1], yl[1]);
-                    rope_rot_split(x[2], y[2], rc[2 * kk + 1], rs[2 * kk + 1], xh[2], xl[2], yh[2],
+                    rope_rot_split<T>(x[0], y[0], rc[2 * kk], rs[2 * kk], xh[0], xl[0], yh[0], yl[0]);
+                    rope_rot_split<T>(x[1], y[1], c8[2 * kk], s8[2 * kk], xh[1], xl[1], yh[1], yl[1]);
+                    rope_rot_split<T>(x[2], y[2], rc[2 * kk + 1], rs[2 * kk + 1], xh[2], xl[2], yh[2],
                                    yl[2]);
-                    rope_rot_split(x[3], y[3], c8[2 * kk + 1], s8[2 * kk + 1], xh[3], xl[3], yh[3],
+                    rope_rot_split<T>(x[3], y[3], c8[2 * kk + 1], s8[2 * kk + 1], xh[3], xl[3], yh[3],
                                    yl[3]);
                     const int k2 = kk + KT / 2;
                     Elem<T>::mma(ca, xh[0], xh[1], xh[2], xh[3], qb[kk][0], qb[kk][1]);
@@ -1117,17 +1142,17 @@ cudaError_t launch_attend_mma_dr(bool split, const AttendParams& p, const CUtens
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-// Launchers of the plain instances (fp16 / bf16) and of the rotary ones (fp16).
+// Launchers of the plain instances and of the rotary ones (fp16 / bf16 each).
 template <int D, typename T>
 cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtensorMap* maps,
                                 dim3 grid, cudaStream_t stream) {
     return launch_attend_mma_dr<D, T, false>(split, p, maps, grid, stream);
 }
 
-template <int D>
+template <int D, typename T>
 cudaError_t launch_attend_mma_rope_d(bool split, const AttendParams& p, const CUtensorMap* maps,
                                      dim3 grid, cudaStream_t stream) {
-    return launch_attend_mma_dr<D, __half, true>(split, p, maps, grid, stream);
+    return launch_attend_mma_dr<D, T, true>(split, p, maps, grid, stream);
 }
 
 }  // namespace pa

@@ -166,11 +166,12 @@ def test_decode_argument_checks_return_before_launch():
     assert p96.kernel == binding.PA_KERNEL_MMA
     p96.kernel = binding.PA_KERNEL_SIMT
     assert _call_decode(p96) == binding.PA_ERR_UNSUPPORTED
-    # Rotary embedding on the tensor-core kernel needs fp16 and a head dim up
-    # to 128; a negative base is invalid.
+    # Rotary embedding: the tensor-core kernel up to head dim 128, the
+    # CUDA-core kernel without bf16; a negative base is invalid.
     rope_bf16 = binding.pa_plan_t.from_buffer_copy(plan)
     rope_bf16.rope_theta = 10000.0
     rope_bf16.dtype = binding.PA_DTYPE_BF16
+    rope_bf16.kernel = binding.PA_KERNEL_SIMT
     assert _call_decode(rope_bf16) == binding.PA_ERR_UNSUPPORTED
     p256 = pa.pa_plan(2, 8, 2, 256, 16, 100, 50, 800, 0, 64, 152)
     p256.rope_theta = 10000.0
@@ -233,7 +234,10 @@ def test_plan_ex_picks_the_kernel_and_sizes_for_its_residency():
     assert rope.kernel == binding.PA_KERNEL_MMA and rope.rope_theta == 10000.0
     # the rotary tensor-core instances run 2 CTAs per SM at D = 128 (the plain ones 3)
     assert rope.ctas < f16.ctas
-    # fp32, bf16 or D = 256 with a rotary embedding: the CUDA-core kernel, or nothing
+    # bf16 with a rotary embedding: the tensor-core kernel; fp32 or D = 256:
+    # the CUDA-core kernel, or nothing (bf16 at D = 256)
+    assert pa.pa_plan_ex(*args, rope_theta=1e4, dtype=binding.PA_DTYPE_BF16).kernel == \
+        binding.PA_KERNEL_MMA
     assert pa.pa_plan_ex(*args, rope_theta=1e4, dtype=binding.PA_DTYPE_F32).kernel == \
         binding.PA_KERNEL_SIMT
     wide_args = (4, 24, 4, 256, 16, 10000, 2048, 32768, 0, 0, 152)
@@ -245,8 +249,9 @@ def test_plan_ex_picks_the_kernel_and_sizes_for_its_residency():
     for kw, st in ((dict(dtype=binding.PA_DTYPE_F32, kernel=binding.PA_KERNEL_MMA),
                     binding.PA_ERR_UNSUPPORTED),
                    (dict(rope_theta=1e4, kernel=binding.PA_KERNEL_MMA,
+                         dtype=binding.PA_DTYPE_F32), binding.PA_ERR_UNSUPPORTED),
+                   (dict(rope_theta=1e4, kernel=binding.PA_KERNEL_SIMT,
                          dtype=binding.PA_DTYPE_BF16), binding.PA_ERR_UNSUPPORTED),
-                   (dict(rope_theta=1e4, dtype=binding.PA_DTYPE_BF16), binding.PA_ERR_UNSUPPORTED),
                    (dict(dtype=binding.PA_DTYPE_BF16, kernel=binding.PA_KERNEL_SIMT),
                     binding.PA_ERR_UNSUPPORTED),
                    (dict(dtype=9), binding.PA_ERR_INVALID_ARG),

@@ -387,9 +387,10 @@ ROPE_PLANS = {
 }
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("plan_kind", sorted(ROPE_PLANS))
 @pytest.mark.parametrize("D,Hq,Hkv", [(64, 8, 2), (96, 12, 4), (128, 32, 8)])
-def test_rotary_tensor_core_plan_shapes(plan_kind, D, Hq, Hkv):
+def test_rotary_tensor_core_plan_shapes(plan_kind, D, Hq, Hkv, dtype):
     if gpu_helpers.KERNEL != "mma":
         pytest.skip("tensor-core plan shapes")
     kw = dict(ROPE_PLANS[plan_kind])
@@ -397,7 +398,8 @@ def test_rotary_tensor_core_plan_shapes(plan_kind, D, Hq, Hkv):
         pytest.skip("the last-CTA merge serves at most 128 (head, 4-dim column) items")
     lens = [1, 17, 700, 2049, 3333]
     case = workloads.make_case("ropep", len(lens), Hq, Hkv, D, lens, seed=1600 + D, q_std=2.0,
-                               rope_theta=500000.0, window=3000 if plan_kind == "cluster" else 0)
+                               rope_theta=500000.0, window=3000 if plan_kind == "cluster" else 0,
+                               dtype=dtype)
     out, lse, err, plan = run_gpu(case, guard=16, **kw)
     assert err == 0 and plan.kernel == 2 and plan.rope_theta > 0
-    assert_matches_oracle(case, out, lse, what=f"rope mma {plan_kind} D{D}")
+    assert_matches_oracle(case, out, lse, what=f"rope mma {plan_kind} D{D} {dtype}")
