@@ -120,7 +120,13 @@ typedef struct pa_plan {
                                its sequence length and first page ids as hints for them;
                                everything is read again after the wait, so a stale hint
                                only prefetches a page that is not used */
-    int reserved[2];
+    int test_stall_bytes;   /* test hook, 0 in normal use.  > 0 (at most 4096): in the
+                               tensor-core kernel each warp's first page copy expects
+                               this many bytes more than it carries, so the bounded
+                               wait on it runs out (after 1 s): the call then takes its
+                               copy-timeout path (PA_DEVERR_TIMEOUT, NaN rows) without
+                               any fault.  Lets a test exercise that path */
+    int reserved;
 } pa_plan_t;
 
 /* Element types (pa_plan_t.dtype).  bf16 needs the tensor-core kernel, fp32

@@ -60,7 +60,8 @@ class pa_plan_t(ctypes.Structure):
         ("rope_theta", ctypes.c_float),
         ("cluster", ctypes.c_int),
         ("prewait_prefetch", ctypes.c_int),
-        ("reserved", ctypes.c_int * 2),
+        ("test_stall_bytes", ctypes.c_int),
+        ("reserved", ctypes.c_int),
     ]
 
     def as_dict(self):

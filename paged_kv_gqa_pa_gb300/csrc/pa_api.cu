@@ -602,6 +602,7 @@ static int check_plan(const pa_plan_t* plan) {
     if (plan->cluster < 0) return PA_ERR_INVALID_ARG;
     if (plan->prewait_prefetch < 0 || plan->prewait_prefetch > kMaxPrewaitPrefetch)
         return PA_ERR_INVALID_ARG;
+    if (plan->test_stall_bytes < 0 || plan->test_stall_bytes > 4096) return PA_ERR_INVALID_ARG;
     if (plan->cluster > 1 &&
         (plan->kernel != PA_KERNEL_MMA || plan->cluster > kMaxClusterParts ||
          plan->num_partitions != plan->cluster || plan->parts_per_cta != 1 ||
@@ -692,12 +693,14 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
             return PA_ERR_CUDA;
         p.parts_per_cta = P > 1 ? plan->parts_per_cta : 1;  // one partition: all warps on it
         p.prewait_prefetch = plan->prewait_prefetch;
+        p.stall_tx = plan->test_stall_bytes;
         const dim3 grid((P + p.parts_per_cta - 1) / p.parts_per_cta, p.Hkv * p.nchunk, p.B);
         e = launch_attend_mma(D, plan->dtype, P > 1, p, maps, grid,
                               static_cast<cudaStream_t>(stream));
     } else {
         p.parts_per_cta = 1;
         p.prewait_prefetch = 0;
+        p.stall_tx = 0;
         const dim3 grid(P, p.Hkv * p.nchunk, p.B);
         e = launch_attend(D, plan->heads_per_cta, P > 1, p, grid,
                           static_cast<cudaStream_t>(stream));

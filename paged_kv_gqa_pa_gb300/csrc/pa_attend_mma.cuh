@@ -566,7 +566,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
         const CUtensorMap* map = (item & 1) ? &tmV : &tmK;
         const int y = (id * p.Hkv + kvh) * kPageSize;
         const uint32_t bar = bar_w + slot * 8;
-        mbar_arrive_expect_tx(bar, PB);
+        // (stall_tx, a test hook, is 0 outside tests)
+        mbar_arrive_expect_tx(bar, PB + (item == 0 ? p.stall_tx : 0));
         if constexpr (Cfg::kRows64) {
             tma_load_3d(ring_w + slot * PB, map, 0, 0, y, bar);
         } else {

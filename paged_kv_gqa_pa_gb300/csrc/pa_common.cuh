@@ -48,6 +48,7 @@ struct AttendParams {
     int heads_per_cta;      // G: query heads one CTA serves
     int parts_per_cta;      // consecutive partitions one CTA streams (tensor-core kernel)
     int prewait_prefetch;   // pages per warp prefetched into L2 before the PDL wait (tensor-core)
+    int stall_tx;           // test hook: extra bytes each warp's first copy expects (0 normally)
     float scale_log2;       // scale * log2(e)
     int rope;               // 1: rotary embedding of q and K (CUDA-core kernel)
     int elem_fp32;          // 1: q, K, V and out are fp32 (CUDA-core kernel)

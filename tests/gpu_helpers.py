@@ -52,14 +52,15 @@ def to_device(case, device="cuda"):
 
 def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=None,
             guard=0, parts_per_cta=None, merge_in_kernel=None, ws=None, cluster=None,
-            prewait_prefetch=None):
+            prewait_prefetch=None, test_stall_bytes=None):
     """Plan + pa_decode through the C ABI.  Returns (out fp64 numpy, lse fp64
     numpy, device error word, plan).  With guard > 0 the outputs and the
     workspace sit inside larger NaN/0xA5-filled buffers whose guard regions are
     checked afterwards.  cluster: True forces the cluster merge (the plan's
     partition count must be 2..16), False forbids it, None keeps the planner's
     choice; forcing several partitions per CTA or the last-CTA merge drops it.
-    prewait_prefetch overrides the plan's pre-wait L2 prefetch (pages per warp)."""
+    prewait_prefetch overrides the plan's pre-wait L2 prefetch (pages per warp);
+    test_stall_bytes sets the plan's copy-timeout test hook."""
     ensure_built()
     dev = dev or to_device(case)
     B, Hq, D = case.q.shape
@@ -91,6 +92,8 @@ def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=N
         plan.cluster = 0
     if prewait_prefetch is not None:
         plan.prewait_prefetch = prewait_prefetch
+    if test_stall_bytes is not None:
+        plan.test_stall_bytes = test_stall_bytes
     n_out = B * Hq * D
     et = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[case.dtype]
     out_buf = torch.full((n_out + 2 * guard,), float("nan"), dtype=et, device="cuda")
