@@ -531,7 +531,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     int* s_pid = reinterpret_cast<int*>(base + Cfg::kRingBytes + Cfg::kXBytes);
     float* s_ml = reinterpret_cast<float*>(s_pid + kMaxPagesPerPart);  // [warps][m|l|n][8]
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 3);
-    // rotary tables (ROPE): (cos, sin) of the 8-token and the 64-token turn per frequency
+    // rotary tables (ROPE): (cos, sin) per frequency of the 8-token turn and of
+    // the turn by one step of a warp's pages (16 * wpp tokens; "r64")
     float2* s_r8 = reinterpret_cast<float2*>(bars + kWarps * NS);
     float2* s_r64 = s_r8 + D / 2;
     __shared__ int s_flag;
@@ -726,8 +727,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     // Rotary state (ROPE): cos/sin of this lane's frequencies at its first
     // token row of the current page, slot i = kk*2 + r <-> frequencies
     // kk*16 + (lane%4)*2 + r*8 + {0, 1}.  Evaluated exactly on every 32nd
-    // page of the warp and turned by 64 tokens (one step of the warp's pages)
-    // in between: 31 turns add a few 1e-6 of relative error to the angles'
+    // page of the warp and turned by one step of the warp's pages (wpp pages,
+    // the s_r64 table) in between: 31 turns add a few 1e-6 of relative error to the angles'
     // cos/sin, far below what the scores can show, and the exact evaluations
     // (32 per lane) are the costliest part of a page.
     float2 rc[ROPE ? KT : 1], rs[ROPE ? KT : 1];
