@@ -56,6 +56,7 @@ KERNEL_SOURCES = {
     "mma": ("pa_attend_mma.cuh", "pa_attend_mma_f16.cu", "pa_attend_mma_bf16.cu",
             "pa_attend_mma_rope.cu", "pa_common.cuh"),
     "simt": ("pa_attend.cuh", "pa_attend_d64.cu", "pa_attend_d128.cu", "pa_attend_d256.cu",
+             "pa_attend_bf16_d64.cu", "pa_attend_bf16_d128.cu", "pa_attend_bf16_d256.cu",
              "pa_attend_f32_d64.cu", "pa_attend_f32_d128.cu", "pa_attend_f32_d256.cu",
              "pa_common.cuh"),
 }
@@ -678,7 +679,7 @@ def run_gpu(args):
             c = case if name == args.workload else workloads.workload(name)
             b = kv_bytes(c)
             entry = {"dtype": c.dtype, "head_dim": c.D, "rope_theta": c.rope_theta}
-            simt_ok = c.dtype in ("f16", "f32") and c.D in (64, 128, 256)
+            simt_ok = c.D in (64, 128, 256)
             kernels = ("mma", "simt") if simt_ok else ("mma",)
             if c.dtype == "f32" or (c.rope_theta > 0 and c.D > 128):
                 kernels = ("simt",)  # no tensor-core build for these

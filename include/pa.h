@@ -28,8 +28,8 @@
  *   context_lens int32 [B]
  *   out          T     [B, Hq, D]   (round to nearest even)
  *   lse          fp32  [B, Hq]
- * Supported: head_dim in {64, 96, 128, 256} (96 and bf16 with the tensor-core
- * kernel only, fp32 with the CUDA-core kernel only); page_size 16;
+ * Supported: head_dim in {64, 96, 128, 256} (96 with the tensor-core kernel
+ * only, fp32 with the CUDA-core kernel only); page_size 16;
  * Hq % Hkv == 0 with g = Hq / Hkv split into at most ceil(g / 8) equal head
  * chunks per CTA.
  * q, k_cache, v_cache, out and workspace must be 16-byte aligned.
@@ -105,8 +105,8 @@ typedef struct pa_plan {
                                pairing of dim i and i + D/2, frequency
                                rope_theta^(-2i/D); q at position L - 1, K_t at t, V
                                untouched): the tensor-core kernel (fp16, bf16, head
-                               dims up to 128) or the CUDA-core kernel (fp16, fp32);
-                               0 = none */
+                               dims up to 128) or the CUDA-core kernel (fp16, bf16,
+                               fp32); 0 = none */
     int cluster;            /* > 1: with the tensor-core kernel, the num_partitions
                                (== cluster, at most 16) CTAs of each (sequence, KV head,
                                head chunk) run as one thread-block cluster and merge the
@@ -129,16 +129,16 @@ typedef struct pa_plan {
     int reserved;
 } pa_plan_t;
 
-/* Element types (pa_plan_t.dtype).  bf16 needs the tensor-core kernel, fp32
- * the CUDA-core kernel (fp32 FMA throughout; head_dim 64/128/256). */
+/* Element types (pa_plan_t.dtype).  fp16 and bf16 run on either kernel, fp32
+ * on the CUDA-core kernel only (fp32 FMA throughout; head_dim 64/128/256). */
 #define PA_DTYPE_F16 0
 #define PA_DTYPE_BF16 1
 #define PA_DTYPE_F32 2
 
 /* Partition-kernel variants (pa_plan_t.kernel). */
 #define PA_KERNEL_SIMT 1   /* fp32 FMA on CUDA cores; pages by 1-D bulk copies */
-#define PA_KERNEL_MMA 2    /* mma.sync tensor cores (fp16 in, fp32 accumulate); pages by
-                              2-D TMA tensor copies with the 128-byte swizzle */
+#define PA_KERNEL_MMA 2    /* mma.sync tensor cores (fp16/bf16 in, fp32 accumulate);
+                              pages by TMA tensor copies with the 128-byte swizzle */
 
 /*
  * Choose the partitioning for a decode call (host only, no device access

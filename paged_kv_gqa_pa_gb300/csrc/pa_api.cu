@@ -167,8 +167,11 @@ static cudaError_t launch_attend_e(int D, int G, bool split, const AttendParams&
 
 cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 grid,
                           cudaStream_t stream) {
-    return p.elem_fp32 ? launch_attend_e<float>(D, G, split, p, grid, stream)
-                       : launch_attend_e<__half>(D, G, split, p, grid, stream);
+    switch (p.dtype) {
+        case PA_DTYPE_F32: return launch_attend_e<float>(D, G, split, p, grid, stream);
+        case PA_DTYPE_BF16: return launch_attend_e<__nv_bfloat16>(D, G, split, p, grid, stream);
+        default: return launch_attend_e<__half>(D, G, split, p, grid, stream);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -409,7 +412,7 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     if (kernel != PA_KERNEL_SIMT && kernel != PA_KERNEL_MMA) return PA_ERR_INVALID_ARG;
     if (kernel == PA_KERNEL_MMA && (dtype == PA_DTYPE_F32 || (rope_theta > 0.f && !mma_rope_ok)))
         return PA_ERR_UNSUPPORTED;
-    if (kernel == PA_KERNEL_SIMT && (dtype == PA_DTYPE_BF16 || head_dim == 96))
+    if (kernel == PA_KERNEL_SIMT && head_dim == 96)
         return PA_ERR_UNSUPPORTED;
     if (batch < 0 || batch > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         num_q_heads % num_kv_heads != 0 || head_dim <= 0 || page_size <= 0 || num_pages <= 0 ||
@@ -584,9 +587,9 @@ static int check_plan(const pa_plan_t* plan) {
     // the rotated q and K as head + remainder pairs.
     if (plan->rope_theta > 0.f && plan->kernel == PA_KERNEL_MMA && plan->head_dim > 128)
         return PA_ERR_UNSUPPORTED;
-    // The CUDA-core kernel is built for fp16/fp32 and head dims 64/128/256;
-    // the tensor-core kernel for fp16/bf16.
-    if (plan->kernel == PA_KERNEL_SIMT && (plan->dtype == PA_DTYPE_BF16 || plan->head_dim == 96))
+    // The CUDA-core kernel is built for fp16/bf16/fp32 and head dims
+    // 64/128/256; the tensor-core kernel for fp16/bf16 and head dims 64/96/128/256.
+    if (plan->kernel == PA_KERNEL_SIMT && plan->head_dim == 96)
         return PA_ERR_UNSUPPORTED;
     if (plan->kernel == PA_KERNEL_MMA && plan->dtype == PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
     const int g = Hq / Hkv;
@@ -674,7 +677,7 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     p.heads_per_cta = plan->heads_per_cta;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.rope = plan->rope_theta > 0.f ? 1 : 0;
-    p.elem_fp32 = plan->dtype == PA_DTYPE_F32 ? 1 : 0;
+    p.dtype = plan->dtype;
     if (p.rope) {
         // theta_i / (2 pi) in double, split into two floats.
         for (int i = 0; i < D / 2; ++i) {

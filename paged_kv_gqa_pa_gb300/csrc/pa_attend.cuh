@@ -29,6 +29,7 @@
 // the end, the same log-sum-exp algebra as the cross-partition merge.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <math.h>
 
 #include <atomic>
@@ -54,16 +55,29 @@ struct Lanes {
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
-// This lane's 8 consecutive elements starting at `src` (16 bytes of fp16 or
-// 32 bytes of fp32), as 4 float pairs (dims 2j, 2j + 1 in f[j]).
+// 8 packed 16-bit elements (fp16 or bf16) widened to 4 float pairs.
 template <typename E>
-__device__ __forceinline__ void load8(const unsigned char* src, float2 (&f)[4]);
-
-__device__ __forceinline__ void half8_to_float(const uint4 raw, float2 (&f)[4]);
+__device__ __forceinline__ void wide8(const uint4 raw, float2 (&f)[4]);
 
 template <>
-__device__ __forceinline__ void load8<__half>(const unsigned char* src, float2 (&f)[4]) {
-    half8_to_float(*reinterpret_cast<const uint4*>(src), f);
+__device__ __forceinline__ void wide8<__half>(const uint4 raw, float2 (&f)[4]) {
+    const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) f[j] = __half22float2(h[j]);
+}
+
+template <>
+__device__ __forceinline__ void wide8<__nv_bfloat16>(const uint4 raw, float2 (&f)[4]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) f[j] = __bfloat1622float2(h[j]);
+}
+
+// This lane's 8 consecutive elements starting at `src` (16 bytes of fp16 or
+// bf16, 32 bytes of fp32), as 4 float pairs (dims 2j, 2j + 1 in f[j]).
+template <typename E>
+__device__ __forceinline__ void load8(const unsigned char* src, float2 (&f)[4]) {
+    wide8<E>(*reinterpret_cast<const uint4*>(src), f);
 }
 
 template <>
@@ -81,28 +95,39 @@ __device__ __forceinline__ E from_float_e(float v);
 template <>
 __device__ __forceinline__ __half from_float_e<__half>(float v) { return __float2half_rn(v); }
 template <>
+__device__ __forceinline__ __nv_bfloat16 from_float_e<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Two floats packed into one 32-bit word of E (round to nearest even).
+template <typename E>
+__device__ __forceinline__ uint32_t pack2e(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2e<__half>(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2e<__nv_bfloat16>(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
 __device__ __forceinline__ float from_float_e<float>(float v) { return v; }
 
-// Four consecutive outputs of type E (8-byte aligned fp16, 16-byte fp32).
+// Four consecutive outputs of type E (8-byte aligned fp16/bf16, 16-byte fp32).
 template <typename E>
 __device__ __forceinline__ void store4e(E* dst, float a, float b, float c, float d) {
     if constexpr (sizeof(E) == 2) {
-        __half2 lo = __floats2half2_rn(a, b);
-        __half2 hi = __floats2half2_rn(c, d);
         uint2 packed;
-        packed.x = *reinterpret_cast<uint32_t*>(&lo);
-        packed.y = *reinterpret_cast<uint32_t*>(&hi);
+        packed.x = pack2e<E>(a, b);
+        packed.y = pack2e<E>(c, d);
         *reinterpret_cast<uint2*>(dst) = packed;
     } else {
         *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
     }
 }
 
-__device__ __forceinline__ void half8_to_float(const uint4 raw, float2 (&f)[4]) {
-    const __half2* h = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) f[j] = __half22float2(h[j]);
-}
 
 // Rotary state of a lane: cos and signed sin of its 8 frequencies at the
 // position of the next token it scores, and the one-token step, as pairs
@@ -152,15 +177,15 @@ __device__ __forceinline__ void qk_tree(float (&res)[G], const unsigned char* kp
             constexpr int kHalf = D / 16;  // lanes per half row
             float2 pf[4];
             if constexpr (sizeof(E) == 2) {
-                // exchange the packed fp16 words (4 shuffles), then widen
+                // exchange the packed 16-bit words (4 shuffles), then widen
                 const uint4 raw = *reinterpret_cast<const uint4*>(src);
                 uint4 praw;
                 praw.x = __shfl_xor_sync(0xffffffffu, raw.x, kHalf);
                 praw.y = __shfl_xor_sync(0xffffffffu, raw.y, kHalf);
                 praw.z = __shfl_xor_sync(0xffffffffu, raw.z, kHalf);
                 praw.w = __shfl_xor_sync(0xffffffffu, raw.w, kHalf);
-                half8_to_float(raw, kf);
-                half8_to_float(praw, pf);
+                wide8<E>(raw, kf);
+                wide8<E>(praw, pf);
             } else {
                 load8<E>(src, kf);
 #pragma unroll

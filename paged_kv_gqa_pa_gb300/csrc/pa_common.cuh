@@ -51,7 +51,7 @@ struct AttendParams {
     int stall_tx;           // test hook: extra bytes each warp's first copy expects (0 normally)
     float scale_log2;       // scale * log2(e)
     int rope;               // 1: rotary embedding of q and K (CUDA-core kernel)
-    int elem_fp32;          // 1: q, K, V and out are fp32 (CUDA-core kernel)
+    int dtype;              // PA_DTYPE_*: q, K, V and out (the CUDA-core kernel's instance)
     // Rotary frequency i as a fraction of a turn, theta_i / (2 pi), split into
     // two floats (rope_phi[0][i] + rope_phi[1][i]) so that pos * theta_i
     // reduces modulo one turn with fp32 accuracy for any position below 2^24.

@@ -157,22 +157,15 @@ def test_decode_argument_checks_return_before_launch():
     bad = binding.pa_plan_t.from_buffer_copy(plan)
     bad.heads_per_cta = 3
     assert _call_decode(bad) == binding.PA_ERR_INVALID_ARG
-    # The CUDA-core kernel has no bf16 or head_dim-96 build.
-    simt_bf16 = binding.pa_plan_t.from_buffer_copy(plan)
-    simt_bf16.kernel = binding.PA_KERNEL_SIMT
-    simt_bf16.dtype = binding.PA_DTYPE_BF16
-    assert _call_decode(simt_bf16) == binding.PA_ERR_UNSUPPORTED
+    # The CUDA-core kernel has no head_dim-96 build, in any element type.
     p96 = pa.pa_plan(2, 8, 2, 96, 16, 100, 50, 800, 0, 64, 152)
     assert p96.kernel == binding.PA_KERNEL_MMA
     p96.kernel = binding.PA_KERNEL_SIMT
     assert _call_decode(p96) == binding.PA_ERR_UNSUPPORTED
-    # Rotary embedding: the tensor-core kernel up to head dim 128, the
-    # CUDA-core kernel without bf16; a negative base is invalid.
-    rope_bf16 = binding.pa_plan_t.from_buffer_copy(plan)
-    rope_bf16.rope_theta = 10000.0
-    rope_bf16.dtype = binding.PA_DTYPE_BF16
-    rope_bf16.kernel = binding.PA_KERNEL_SIMT
-    assert _call_decode(rope_bf16) == binding.PA_ERR_UNSUPPORTED
+    p96.dtype = binding.PA_DTYPE_BF16
+    assert _call_decode(p96) == binding.PA_ERR_UNSUPPORTED
+    # Rotary embedding: the tensor-core kernel up to head dim 128 (the
+    # CUDA-core kernel takes the rest); a negative base is invalid.
     p256 = pa.pa_plan(2, 8, 2, 256, 16, 100, 50, 800, 0, 64, 152)
     p256.rope_theta = 10000.0
     assert p256.kernel == binding.PA_KERNEL_MMA
@@ -235,13 +228,15 @@ def test_plan_ex_picks_the_kernel_and_sizes_for_its_residency():
     # the rotary tensor-core instances run 2 CTAs per SM at D = 128 (the plain ones 3)
     assert rope.ctas < f16.ctas
     # bf16 with a rotary embedding: the tensor-core kernel; fp32 or D = 256:
-    # the CUDA-core kernel, or nothing (bf16 at D = 256)
+    # the CUDA-core kernel (bf16 included)
     assert pa.pa_plan_ex(*args, rope_theta=1e4, dtype=binding.PA_DTYPE_BF16).kernel == \
         binding.PA_KERNEL_MMA
     assert pa.pa_plan_ex(*args, rope_theta=1e4, dtype=binding.PA_DTYPE_F32).kernel == \
         binding.PA_KERNEL_SIMT
     wide_args = (4, 24, 4, 256, 16, 10000, 2048, 32768, 0, 0, 152)
     assert pa.pa_plan_ex(*wide_args, rope_theta=1e4).kernel == binding.PA_KERNEL_SIMT
+    assert pa.pa_plan_ex(*wide_args, rope_theta=1e4, dtype=binding.PA_DTYPE_BF16).kernel == \
+        binding.PA_KERNEL_SIMT
     # fp32 at D = 256 keeps one CTA per SM, so its automatic grid is smaller
     wide = (4, 24, 4, 256, 16, 10000, 2048, 32768, 0, 0, 152)
     assert (pa.pa_plan_ex(*wide, dtype=binding.PA_DTYPE_F32).ctas <
@@ -250,16 +245,20 @@ def test_plan_ex_picks_the_kernel_and_sizes_for_its_residency():
                     binding.PA_ERR_UNSUPPORTED),
                    (dict(rope_theta=1e4, kernel=binding.PA_KERNEL_MMA,
                          dtype=binding.PA_DTYPE_F32), binding.PA_ERR_UNSUPPORTED),
-                   (dict(rope_theta=1e4, kernel=binding.PA_KERNEL_SIMT,
-                         dtype=binding.PA_DTYPE_BF16), binding.PA_ERR_UNSUPPORTED),
-                   (dict(dtype=binding.PA_DTYPE_BF16, kernel=binding.PA_KERNEL_SIMT),
-                    binding.PA_ERR_UNSUPPORTED),
                    (dict(dtype=9), binding.PA_ERR_INVALID_ARG),
                    (dict(kernel=7), binding.PA_ERR_INVALID_ARG),
                    (dict(rope_theta=-2.0), binding.PA_ERR_INVALID_ARG)):
         with pytest.raises(pa.PAError) as e:
             pa.pa_plan_ex(*args, **kw)
         assert e.value.status == st
+    # bf16 on the CUDA-core kernel, with or without a rotary embedding
+    for kw in (dict(dtype=binding.PA_DTYPE_BF16, kernel=binding.PA_KERNEL_SIMT),
+               dict(dtype=binding.PA_DTYPE_BF16, kernel=binding.PA_KERNEL_SIMT, rope_theta=1e4)):
+        assert pa.pa_plan_ex(*args, **kw).kernel == binding.PA_KERNEL_SIMT
+    d96 = (4, 32, 8, 96, 16, 10000, 2048, 32768, 0, 0, 152)
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_plan_ex(*d96, dtype=binding.PA_DTYPE_BF16, kernel=binding.PA_KERNEL_SIMT)
+    assert e.value.status == binding.PA_ERR_UNSUPPORTED
     with pytest.raises(pa.PAError):
         pa.pa_plan_ex(4, 32, 8, 96, 16, 10000, 2048, 32768, 0, 0, 152,
                       kernel=binding.PA_KERNEL_SIMT)

@@ -74,8 +74,8 @@ def test_negative_context_length():
 
 @pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f16", 96)])
 def test_bad_page_on_wider_paths(dtype, D):
-    if gpu_helpers.KERNEL == "simt":
-        pytest.skip("the CUDA-core kernel is built for fp16 and head dims 64/128/256")
+    if gpu_helpers.KERNEL == "simt" and D == 96:
+        pytest.skip("the CUDA-core kernel is built for head dims 64/128/256")
     case = workloads.make_case("badw", 3, 8, 2, D, [700, 1200, 90], seed=610, partition_size=256,
                                dtype=dtype)
     good_ref = _ref_rows(case, [0, 2])

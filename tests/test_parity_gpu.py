@@ -30,8 +30,8 @@ def kernel_variant(request):
 @pytest.mark.parametrize("name", workloads.WORKLOAD_ORDER + workloads.EXTRA_ORDER)
 def test_workload_full_size(name):
     case = workloads.workload(name)
-    if gpu_helpers.KERNEL == "simt" and (case.dtype == "bf16" or case.D == 96):
-        pytest.skip("the CUDA-core kernel is built for fp16/fp32 and head dims 64/128/256")
+    if gpu_helpers.KERNEL == "simt" and case.D == 96:
+        pytest.skip("the CUDA-core kernel is built for head dims 64/128/256")
     if gpu_helpers.KERNEL == "mma" and ((case.rope_theta > 0 and case.D > 128) or
                                         case.dtype == "f32"):
         pytest.skip("fp32 caches, and rotary embeddings at head dims above 128, run on the "
@@ -284,14 +284,14 @@ def test_workspace_reused_across_calls_and_shapes():
         assert_matches_oracle(c, out, lse, what=c.name)
 
 
-def _mma_only():
-    if gpu_helpers.KERNEL == "simt":
-        pytest.skip("the CUDA-core kernel is built for fp16 and head dims 64/128/256")
+def _skip_d96_on_cuda_cores(D):
+    if gpu_helpers.KERNEL == "simt" and D == 96:
+        pytest.skip("the CUDA-core kernel is built for head dims 64/128/256")
 
 
 @pytest.mark.parametrize("partition_size", [0, 16, 64, 512, 4096])
 def test_head_dim_96(partition_size):
-    _mma_only()
+    _skip_d96_on_cuda_cores(96)
     case = workloads.make_case("d96", len(LENS), 12, 2, 96, LENS, seed=700,
                                partition_size=partition_size, q_std=2.0)
     out, lse, err, plan = run_gpu(case, guard=64)
@@ -302,7 +302,7 @@ def test_head_dim_96(partition_size):
 @pytest.mark.parametrize("D", [64, 96, 128, 256])
 @pytest.mark.parametrize("partition_size", [0, 64, 4096])
 def test_bf16_cache(D, partition_size):
-    _mma_only()
+    _skip_d96_on_cuda_cores(D)
     case = workloads.make_case("bf16", len(LENS), 16, 4, D, LENS, seed=710 + D,
                                partition_size=partition_size, q_std=2.0, dtype="bf16")
     out, lse, err, plan = run_gpu(case, guard=64)
@@ -313,7 +313,7 @@ def test_bf16_cache(D, partition_size):
 
 @pytest.mark.parametrize("dtype,D", [("bf16", 256), ("bf16", 96), ("f16", 96)])
 def test_wider_paths_window_ragged_and_invariants(dtype, D):
-    _mma_only()
+    _skip_d96_on_cuda_cores(D)
     lens = [0, 1, 3001, 17, 5000]
     case = workloads.make_case("wide", len(lens), 8, 2, D, lens, seed=720 + D, window=1000,
                                q_std=3.0, dtype=dtype)
@@ -334,26 +334,27 @@ def test_wider_paths_window_ragged_and_invariants(dtype, D):
             assert np.array_equal(out[b, h], vals.astype(np.float64))
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("D", [64, 96, 128, 256])
 @pytest.mark.parametrize("theta", [10000.0, 500000.0])
-def test_rotary_embedding_in_kernel(D, theta):
+def test_rotary_embedding_in_kernel(D, theta, dtype):
     if gpu_helpers.KERNEL == "mma" and D > 128:
         pytest.skip("rotary embeddings at head dims above 128 run on the CUDA-core kernel")
     if gpu_helpers.KERNEL == "simt" and D == 96:
         pytest.skip("the CUDA-core kernel is built for head dims 64/128/256")
     case = workloads.make_case("rope", len(LENS), 8, 2, D, LENS, seed=800 + D, q_std=2.0,
-                               rope_theta=theta)
+                               rope_theta=theta, dtype=dtype)
     for S in (0, 64, 4096):
         case.partition_size = S
         out, lse, err, _ = run_gpu(case, guard=64)
         assert err == 0
-        assert_matches_oracle(case, out, lse, what=f"rope D{D} S{S}")
+        assert_matches_oracle(case, out, lse, what=f"rope D{D} S{S} {dtype}")
     # with a window, and positions past 2^16
     wcase = workloads.make_case("ropew", 2, 6, 2, D, [70000, 999], seed=801 + D, window=3000,
-                                rope_theta=theta)
+                                rope_theta=theta, dtype=dtype)
     out, lse, err, _ = run_gpu(wcase)
     assert err == 0
-    assert_matches_oracle(wcase, out, lse, what=f"rope window D{D}")
+    assert_matches_oracle(wcase, out, lse, what=f"rope window D{D} {dtype}")
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
