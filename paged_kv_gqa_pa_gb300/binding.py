@@ -241,21 +241,28 @@ def new_workspace(plan, device=None) -> torch.Tensor:
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, window=0,
-           partition_size=0, max_context_len=None, stream=None):
+           partition_size=0, max_context_len=None, rope_theta=0.0, stream=None):
     """Convenience call: plan, allocate out/lse/workspace with torch, decode.
 
-    max_context_len defaults to the table's capacity (block_tables.shape[1] *
-    page_size), which needs no device read.  Returns (out, lse, plan,
-    device_error) -- device_error is read back, so this call synchronises.
+    The element type (fp16, bf16 or fp32) follows q; k_cache and v_cache must
+    match it.  max_context_len defaults to the table's capacity
+    (block_tables.shape[1] * page_size), which needs no device read.
+    rope_theta > 0 applies the in-kernel rotary embedding with that base.
+    Returns (out, lse, plan, device_error) -- device_error is read back, so
+    this call synchronises.
     """
+    dtypes = {v: k for k, v in _TORCH_DTYPE.items()}
+    if q.dtype not in dtypes:
+        raise TypeError(f"q must be fp16, bf16 or fp32, got {q.dtype}")
     B, Hq, D = q.shape
     num_pages, Hkv, ps, _ = k_cache.shape
     maxp = block_tables.shape[1]
     if max_context_len is None:
         max_context_len = maxp * ps
-    plan = pa_plan(B, Hq, Hkv, D, ps, num_pages, maxp, max_context_len, window, partition_size,
-                   torch.cuda.get_device_properties(q.device).multi_processor_count)
-    out = torch.empty((B, Hq, D), dtype=torch.float16, device=q.device)
+    plan = pa_plan_ex(B, Hq, Hkv, D, ps, num_pages, maxp, max_context_len, window, partition_size,
+                      torch.cuda.get_device_properties(q.device).multi_processor_count,
+                      dtype=dtypes[q.dtype], kernel=0, rope_theta=rope_theta)
+    out = torch.empty((B, Hq, D), dtype=q.dtype, device=q.device)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     ws = new_workspace(plan, q.device)
     pa_decode(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window, out, lse, ws,

@@ -59,3 +59,20 @@ def test_tensor_core_and_cuda_core_kernels_agree(D, Hq, Hkv, dtype, window, thet
         assert np.array_equal(np.isfinite(lm), np.isfinite(ls))
         fin = np.isfinite(lm)
         assert np.abs(lm[fin] - ls[fin]).max() <= gpu_helpers.LSE_TOL
+
+
+@pytest.mark.parametrize("dtype,theta", [("f16", 0.0), ("bf16", 0.0), ("f32", 0.0),
+                                         ("f16", 10000.0), ("bf16", 10000.0)])
+def test_convenience_decode_follows_q_dtype(dtype, theta):
+    # binding.decode plans, allocates and decodes in one call; the element
+    # type comes from q.
+    import torch
+    import paged_kv_gqa_pa_gb300 as pa
+    case = workloads.make_case("conv", 3, 8, 2, 128, [1, 700, 3060], seed=1900, window=1500,
+                               dtype=dtype, rope_theta=theta)
+    dev = gpu_helpers.to_device(case)
+    out, lse, plan, err = pa.decode(dev["q"], dev["k"], dev["v"], dev["bt"], dev["cl"],
+                                    case.scale, window=case.window, rope_theta=theta)
+    assert err == 0 and out.dtype == dev["q"].dtype and plan.rope_theta == theta
+    assert_matches_oracle(case, out.double().cpu().numpy(), lse.double().cpu().numpy(),
+                          what=f"decode() {dtype} theta {theta}")
