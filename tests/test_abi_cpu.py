@@ -117,6 +117,7 @@ def test_auto_plan_is_consistent(num_sms, B, Hkv, L, W):
     ((1, 8, 8, 128, 16, 10, 10, 161, 0, 0, 152), binding.PA_ERR_INVALID_ARG),   # Lmax > table
     ((1, 18, 2, 128, 16, 10, 10, 100, 0, 0, 152), binding.PA_ERR_UNSUPPORTED),  # g = 9
     ((1, 8, 8, 128, 16, 10, 10, 100, 0, 8192, 152), binding.PA_ERR_UNSUPPORTED),  # S > 256 pages
+    ((1, 4, 1, 64, 16, 4200, 4200, 65552, 0, 16, 152), binding.PA_ERR_UNSUPPORTED),  # 4097 partitions
     ((-1, 8, 8, 128, 16, 10, 10, 100, 0, 0, 152), binding.PA_ERR_INVALID_ARG),
     ((1, 8, 8, 128, 16, 10, 10, 100, -1, 0, 152), binding.PA_ERR_INVALID_ARG),
 ])
@@ -300,3 +301,9 @@ def test_cluster_plan_checks_return_before_launch():
     lib = pa.load()
     assert lib.pa_merge(ctypes.byref(plan), 0x10000, 0x10000, 0x10000, 0x10000, None) == \
         binding.PA_OK
+
+
+def test_partition_count_limit():
+    # the merge kernel reduces at most 4096 partitions per head
+    ok = pa.pa_plan(1, 4, 1, 64, 16, 4200, 4096, 65536, 0, 16, 152)
+    assert ok.num_partitions == 4096

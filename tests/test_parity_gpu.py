@@ -163,6 +163,15 @@ def test_partition_count_invariance():
         assert np.abs(o - outs[0]).max() < 1e-2
 
 
+def test_largest_partition_count():
+    # 65 536 tokens in 16-token partitions: 4096 partitions per head, the most
+    # the merge kernel reduces (16 chunks of 256).
+    case = workloads.make_case("p4096", 1, 4, 1, 64, [65536], seed=504, partition_size=16)
+    out, lse, err, plan = run_gpu(case)
+    assert err == 0 and plan.num_partitions == 4096
+    assert_matches_oracle(case, out, lse, what="4096 partitions")
+
+
 def test_window_at_least_context_is_no_window():
     case = workloads.make_case("wl", 2, 8, 2, 64, [500, 64], seed=504)
     case.partition_size = 128
