@@ -104,9 +104,8 @@ typedef struct pa_plan {
     float rope_theta;       /* > 0: rotary embedding inside the kernel (rotate-half
                                pairing of dim i and i + D/2, frequency
                                rope_theta^(-2i/D); q at position L - 1, K_t at t, V
-                               untouched): the tensor-core kernel (fp16, bf16, head
-                               dims up to 128) or the CUDA-core kernel (fp16, bf16,
-                               fp32); 0 = none */
+                               untouched): the tensor-core kernel (fp16, bf16) or the
+                               CUDA-core kernel (fp16, bf16, fp32); 0 = none */
     int cluster;            /* > 1: with the tensor-core kernel, the num_partitions
                                (== cluster, at most 16) CTAs of each (sequence, KV head,
                                head chunk) run as one thread-block cluster and merge the

@@ -38,7 +38,7 @@ static cudaError_t launch_attend_mma_t(int D, bool split, const AttendParams& p,
 
 static cudaError_t launch_attend_mma(int D, int dtype, bool split, const AttendParams& p,
                                      const CUtensorMap* maps, dim3 grid, cudaStream_t stream) {
-    if (p.rope) {  // head dims up to 128 (checked with the plan)
+    if (p.rope) {
         const bool bf = dtype == PA_DTYPE_BF16;
         switch (D) {
             case 64:
@@ -50,6 +50,9 @@ static cudaError_t launch_attend_mma(int D, int dtype, bool split, const AttendP
             case 128:
                 return bf ? launch_attend_mma_rope_d<128, __nv_bfloat16>(split, p, maps, grid, stream)
                           : launch_attend_mma_rope_d<128, __half>(split, p, maps, grid, stream);
+            case 256:
+                return bf ? launch_attend_mma_rope_d<256, __nv_bfloat16>(split, p, maps, grid, stream)
+                          : launch_attend_mma_rope_d<256, __half>(split, p, maps, grid, stream);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -135,7 +138,8 @@ int attend_ctas_per_sm(int kernel, int dtype, int D, int G, bool rope) {
         switch (D) {
             case 64: return MmaCfg<64, true>::kMinBlocks;
             case 96: return MmaCfg<96, true>::kMinBlocks;
-            default: return MmaCfg<128, true>::kMinBlocks;
+            case 128: return MmaCfg<128, true>::kMinBlocks;
+            default: return MmaCfg<256, true>::kMinBlocks;
         }
     }
     if (kernel == PA_KERNEL_MMA) {
@@ -404,8 +408,8 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     if (dtype != PA_DTYPE_F16 && dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F32)
         return PA_ERR_INVALID_ARG;
     if (!(rope_theta >= 0.f) || rope_theta == INFINITY) return PA_ERR_INVALID_ARG;
-    // The tensor-core kernel's rotary instances: fp16 and bf16, head dims up to 128.
-    const bool mma_rope_ok = dtype != PA_DTYPE_F32 && head_dim <= 128;
+    // The tensor-core kernel's rotary instances: fp16 and bf16, every head dim.
+    const bool mma_rope_ok = dtype != PA_DTYPE_F32;
     if (kernel == 0)  // automatic: fp32, and rotary embeddings the tensor-core kernel lacks, need the CUDA-core kernel
         kernel = (dtype == PA_DTYPE_F32 || (rope_theta > 0.f && !mma_rope_ok)) ? PA_KERNEL_SIMT
                                                                                : PA_KERNEL_MMA;
@@ -583,10 +587,8 @@ static int check_plan(const pa_plan_t* plan) {
         return PA_ERR_INVALID_ARG;
     if (!(plan->rope_theta >= 0.f) || plan->rope_theta == INFINITY) return PA_ERR_INVALID_ARG;
     // Rotary embedding: the CUDA-core kernel (fp16, fp32), or the tensor-core
-    // kernel's rotary instances (fp16, bf16, head dims up to 128), which keep
+    // kernel's rotary instances (fp16, bf16), which keep
     // the rotated q and K as head + remainder pairs.
-    if (plan->rope_theta > 0.f && plan->kernel == PA_KERNEL_MMA && plan->head_dim > 128)
-        return PA_ERR_UNSUPPORTED;
     // The CUDA-core kernel is built for fp16/bf16/fp32 and head dims
     // 64/128/256; the tensor-core kernel for fp16/bf16 and head dims 64/96/128/256.
     if (plan->kernel == PA_KERNEL_SIMT && plan->head_dim == 96)

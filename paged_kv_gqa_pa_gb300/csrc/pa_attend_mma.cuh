@@ -512,7 +512,7 @@ static_assert(ClusterPartial<64>::kMaxBytes <= MmaCfg<64>::kWideXOff &&
 // SPLIT: partials for a merge (else the final rows).  CLUSTER (with SPLIT):
 // the partitions of a group form one cluster and merge in it; a separate
 // instance, so that the other instances carry none of its code.  ROPE: q and
-// each K row are rotated to their positions before q.K (head dims up to 128).
+// each K row are rotated to their positions before q.K.
 template <int D, typename T, bool SPLIT, bool CLUSTER, bool ROPE>
 __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     attend_mma_kernel(const AttendParams p, const __grid_constant__ CUtensorMap tmK,
@@ -768,8 +768,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
             const uint32_t kaddr = ring_w + ((2 * k) % NS) * PB;
             float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
             if constexpr (ROPE) {
-                // the rotary state at this page's row tok0, and at row tok0 + 8
-                float2 c8[KT], s8[KT];
+                // the rotary state at this page's row tok0 (rc, rs); row tok0 + 8
+                // is derived per k-step below, for the two slots it uses
 #pragma unroll
                 for (int i = 0; i < KT; ++i) {
                     const int f = (i >> 1) * 16 + (lane & 3) * 2 + (i & 1) * 8;
@@ -783,23 +783,24 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
                     } else {
                         rope_turn_pair(rc[i], rs[i], *reinterpret_cast<const float4*>(s_r64 + f));
                     }
-                    c8[i] = rc[i];
-                    s8[i] = rs[i];
-                    rope_turn_pair(c8[i], s8[i], *reinterpret_cast<const float4*>(s_r8 + f));
                 }
 #pragma unroll
                 for (int kk = 0; kk < KT / 2; ++kk) {
                     // fragments: a0/a2 row tok0, a1/a3 row tok0 + 8; a0/a1 slot r = 0, a2/a3 r = 1
+                    const int f0 = kk * 16 + (lane & 3) * 2;
+                    float2 c8a = rc[2 * kk], s8a = rs[2 * kk];
+                    float2 c8b = rc[2 * kk + 1], s8b = rs[2 * kk + 1];
+                    rope_turn_pair(c8a, s8a, *reinterpret_cast<const float4*>(s_r8 + f0));
+                    rope_turn_pair(c8b, s8b, *reinterpret_cast<const float4*>(s_r8 + f0 + 8));
                     uint32_t x[4], y[4], xh[4], xl[4], yh[4], yl[4];
                     ldsm_x4(kaddr + swz<D>(k_row, kk * 2 + k_chk), x[0], x[1], x[2], x[3]);
                     ldsm_x4(kaddr + swz<D>(k_row, (kk + KT / 2) * 2 + k_chk), y[0], y[1], y[2],
                             y[3]);
                     rope_rot_split<T>(x[0], y[0], rc[2 * kk], rs[2 * kk], xh[0], xl[0], yh[0], yl[0]);
-                    rope_rot_split<T>(x[1], y[1], c8[2 * kk], s8[2 * kk], xh[1], xl[1], yh[1], yl[1]);
+                    rope_rot_split<T>(x[1], y[1], c8a, s8a, xh[1], xl[1], yh[1], yl[1]);
                     rope_rot_split<T>(x[2], y[2], rc[2 * kk + 1], rs[2 * kk + 1], xh[2], xl[2], yh[2],
-                                   yl[2]);
-                    rope_rot_split<T>(x[3], y[3], c8[2 * kk + 1], s8[2 * kk + 1], xh[3], xl[3], yh[3],
-                                   yl[3]);
+                                      yl[2]);
+                    rope_rot_split<T>(x[3], y[3], c8b, s8b, xh[3], xl[3], yh[3], yl[3]);
                     const int k2 = kk + KT / 2;
                     Elem<T>::mma(ca, xh[0], xh[1], xh[2], xh[3], qb[kk][0], qb[kk][1]);
                     Elem<T>::mma(ca, xh[0], xh[1], xh[2], xh[3], ql[kk][0], ql[kk][1]);

@@ -1,5 +1,5 @@
 // Tensor-core partition-kernel instances with the rotary embedding (fp16 and
-// bf16 caches, head dims 64, 96 and 128), in a translation unit of their own
+// bf16 caches, head dims 64, 96, 128 and 256), in a translation unit of their own
 // so the build compiles them in parallel with the plain instances.
 #include "pa_attend_mma.cuh"
 
@@ -10,8 +10,10 @@ namespace pa {
 PA_ROPE_INSTANCE(64, __half)
 PA_ROPE_INSTANCE(96, __half)
 PA_ROPE_INSTANCE(128, __half)
+PA_ROPE_INSTANCE(256, __half)
 PA_ROPE_INSTANCE(64, __nv_bfloat16)
 PA_ROPE_INSTANCE(96, __nv_bfloat16)
 PA_ROPE_INSTANCE(128, __nv_bfloat16)
+PA_ROPE_INSTANCE(256, __nv_bfloat16)
 #undef PA_ROPE_INSTANCE
 }  // namespace pa

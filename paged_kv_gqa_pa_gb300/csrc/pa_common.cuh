@@ -98,14 +98,13 @@ template <int D, bool ROPE = false>
 struct MmaCfg {
     static_assert(D % 64 == 0 || (D % 64 == 32 && (D / 32) % 2 == 1),
                   "head dim: 64-column slabs, or an odd number of 32-column units");
-    static_assert(!ROPE || D <= 128, "rotary instances: head dims up to 128");
     static constexpr bool kRows64 = (D % 64) != 0;  // one 3-D box, 64-byte units, 64-byte swizzle
     static constexpr int kFullSlabs = D / 64;       // else: 128-byte slabs (128-byte swizzle)
     static constexpr int kSlabBytes = kPageSize * 128;
     static constexpr int kPageBytes = kPageSize * D * 2;
     // pages in flight per warp; with the fixed buffers below this keeps
     // kMinBlocks CTAs per SM within 228 KiB of shared memory
-    static constexpr int kStages = ROPE ? (D == 128 ? 6 : (D == 96 ? 8 : 6))
+    static constexpr int kStages = ROPE ? (D == 256 ? 3 : (D == 128 ? 6 : (D == 96 ? 8 : 6)))
                                         : (D == 256 ? 3 : (D == 128 ? 4 : (D == 96 ? 5 : 6)));
     static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
     // scratch of the last-CTA merge ((m, weight) pairs of a group's partials)

@@ -165,12 +165,7 @@ def test_decode_argument_checks_return_before_launch():
     assert _call_decode(p96) == binding.PA_ERR_UNSUPPORTED
     p96.dtype = binding.PA_DTYPE_BF16
     assert _call_decode(p96) == binding.PA_ERR_UNSUPPORTED
-    # Rotary embedding: the tensor-core kernel up to head dim 128 (the
-    # CUDA-core kernel takes the rest); a negative base is invalid.
-    p256 = pa.pa_plan(2, 8, 2, 256, 16, 100, 50, 800, 0, 64, 152)
-    p256.rope_theta = 10000.0
-    assert p256.kernel == binding.PA_KERNEL_MMA
-    assert _call_decode(p256) == binding.PA_ERR_UNSUPPORTED
+    # Rotary embedding: a negative base is invalid.
     rope_neg = binding.pa_plan_t.from_buffer_copy(plan)
     rope_neg.rope_theta = -1.0
     assert _call_decode(rope_neg) == binding.PA_ERR_INVALID_ARG
@@ -228,15 +223,18 @@ def test_plan_ex_picks_the_kernel_and_sizes_for_its_residency():
     assert rope.kernel == binding.PA_KERNEL_MMA and rope.rope_theta == 10000.0
     # the rotary tensor-core instances run 2 CTAs per SM at D = 128 (the plain ones 3)
     assert rope.ctas < f16.ctas
-    # bf16 with a rotary embedding: the tensor-core kernel; fp32 or D = 256:
-    # the CUDA-core kernel (bf16 included)
+    # bf16 with a rotary embedding: the tensor-core kernel; fp32: the
+    # CUDA-core kernel
     assert pa.pa_plan_ex(*args, rope_theta=1e4, dtype=binding.PA_DTYPE_BF16).kernel == \
         binding.PA_KERNEL_MMA
     assert pa.pa_plan_ex(*args, rope_theta=1e4, dtype=binding.PA_DTYPE_F32).kernel == \
         binding.PA_KERNEL_SIMT
     wide_args = (4, 24, 4, 256, 16, 10000, 2048, 32768, 0, 0, 152)
-    assert pa.pa_plan_ex(*wide_args, rope_theta=1e4).kernel == binding.PA_KERNEL_SIMT
+    # head dim 256: the tensor-core rotary instances too (3 ring stages, 2 CTAs per SM)
+    assert pa.pa_plan_ex(*wide_args, rope_theta=1e4).kernel == binding.PA_KERNEL_MMA
     assert pa.pa_plan_ex(*wide_args, rope_theta=1e4, dtype=binding.PA_DTYPE_BF16).kernel == \
+        binding.PA_KERNEL_MMA
+    assert pa.pa_plan_ex(*wide_args, rope_theta=1e4, dtype=binding.PA_DTYPE_F32).kernel == \
         binding.PA_KERNEL_SIMT
     # fp32 at D = 256 keeps one CTA per SM, so its automatic grid is smaller
     wide = (4, 24, 4, 256, 16, 10000, 2048, 32768, 0, 0, 152)

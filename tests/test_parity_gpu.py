@@ -32,10 +32,8 @@ def test_workload_full_size(name):
     case = workloads.workload(name)
     if gpu_helpers.KERNEL == "simt" and case.D == 96:
         pytest.skip("the CUDA-core kernel is built for head dims 64/128/256")
-    if gpu_helpers.KERNEL == "mma" and ((case.rope_theta > 0 and case.D > 128) or
-                                        case.dtype == "f32"):
-        pytest.skip("fp32 caches, and rotary embeddings at head dims above 128, run on the "
-                    "CUDA-core kernel")
+    if gpu_helpers.KERNEL == "mma" and case.dtype == "f32":
+        pytest.skip("fp32 caches run on the CUDA-core kernel")
     out, lse, err, plan = run_gpu(case)
     assert err == 0
     rel = assert_matches_oracle(case, out, lse, what=name)
@@ -347,8 +345,6 @@ def test_wider_paths_window_ragged_and_invariants(dtype, D):
 @pytest.mark.parametrize("D", [64, 96, 128, 256])
 @pytest.mark.parametrize("theta", [10000.0, 500000.0])
 def test_rotary_embedding_in_kernel(D, theta, dtype):
-    if gpu_helpers.KERNEL == "mma" and D > 128:
-        pytest.skip("rotary embeddings at head dims above 128 run on the CUDA-core kernel")
     if gpu_helpers.KERNEL == "simt" and D == 96:
         pytest.skip("the CUDA-core kernel is built for head dims 64/128/256")
     case = workloads.make_case("rope", len(LENS), 8, 2, D, LENS, seed=800 + D, q_std=2.0,
@@ -399,7 +395,7 @@ ROPE_PLANS = {
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("plan_kind", sorted(ROPE_PLANS))
-@pytest.mark.parametrize("D,Hq,Hkv", [(64, 8, 2), (96, 12, 4), (128, 32, 8)])
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 8, 2), (96, 12, 4), (128, 32, 8), (256, 8, 4)])
 def test_rotary_tensor_core_plan_shapes(plan_kind, D, Hq, Hkv, dtype):
     if gpu_helpers.KERNEL != "mma":
         pytest.skip("tensor-core plan shapes")
