@@ -85,13 +85,15 @@ typedef struct pa_plan {
     int heads_per_cta;      /* query heads one CTA serves (g or a divisor of it) */
     int num_sms;            /* SM count the plan was made for */
     int ctas;               /* CTAs of the attention kernel */
-    size_t workspace_bytes; /* bytes of device workspace pa_decode needs */
+    size_t workspace_bytes; /* bytes of device workspace pa_decode needs (enough for
+                               one partial per partition, whatever parts_per_cta) */
     int kernel;             /* PA_KERNEL_* used for the partition kernel; pa_plan picks
                                one, a caller may overwrite it before pa_decode */
     int parts_per_cta;      /* consecutive partitions one CTA of the tensor-core kernel
-                               serves, 1, 2 or 4 (each gets 4 / parts_per_cta warps;
-                               one partial per partition all the same); the CUDA-core
-                               kernel always serves one */
+                               serves, 1, 2 or 4 (each gets 4 / parts_per_cta warps);
+                               the CTA merges them (log-sum-exp) into one partial, so
+                               each head has ceil(num_partitions / parts_per_cta)
+                               partials.  The CUDA-core kernel always serves one */
     int merge_in_kernel;    /* 1: with the tensor-core kernel, the last CTA of each
                                (sequence, KV head) merges that group's partials and
                                pa_merge has nothing to do; 0: pa_merge launches the

@@ -345,8 +345,9 @@ cudaError_t launch_merge(int D, const MergeParams& p, cudaStream_t stream) {
 }
 
 // Workspace layout: [control block | arrival counters (one per group) |
-// m (B*Hq*P) | l (B*Hq*P) | o (B*Hq*P*D)], each region 256-byte aligned.  The
-// control block's first word is the device error word; it and the counters
+// m (B*Hq*R) | l (B*Hq*R) | o (B*Hq*R*D)], each region 256-byte aligned, for
+// R partials per head (partials_per_head; none when P = 1).  The control
+// block's first word is the device error word; it and the counters
 // (ctrl_bytes in all) must start at zero and are left at zero by every call.
 struct WsLayout {
     size_t ctr_off, ctrl_bytes, m_off, l_off, o_off, total;
@@ -355,7 +356,7 @@ struct WsLayout {
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // groups = B * Hkv * head chunks (one arrival counter each).
-static WsLayout ws_layout(int B, int Hq, int D, int P, long long groups) {
+static WsLayout ws_layout(int B, int Hq, int D, int P, int R, long long groups) {
     WsLayout w;
     w.ctr_off = kCtrlBytes;
     if (P <= 1) {
@@ -363,7 +364,7 @@ static WsLayout ws_layout(int B, int Hq, int D, int P, long long groups) {
         w.total = kCtrlBytes;
         return w;
     }
-    const size_t rows = (size_t)B * Hq * P;
+    const size_t rows = (size_t)B * Hq * R;
     w.ctrl_bytes = kCtrlBytes + align256((size_t)groups * 4);
     w.m_off = w.ctrl_bytes;
     w.l_off = w.m_off + align256(rows * 4);
@@ -527,7 +528,9 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     plan->num_sms = num_sms;
     plan->ctas = P * num_kv_heads * nchunk * batch;
     const long long groups_all = (long long)batch * num_kv_heads * nchunk;
-    const WsLayout wl = ws_layout(batch, num_q_heads, head_dim, P, groups_all);
+    // Sized for one partial per partition, the most any parts_per_cta needs,
+    // so that a caller may lower parts_per_cta in this plan.
+    const WsLayout wl = ws_layout(batch, num_q_heads, head_dim, P, P, groups_all);
     plan->workspace_bytes = wl.total;
     plan->ctrl_bytes = (int)wl.ctrl_bytes;
     plan->kernel = kernel;
@@ -548,10 +551,10 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
             : 0;
     // Partitions per CTA (tensor-core kernel): when the one-partition grid
     // runs many waves of resident CTAs, let each CTA serve 4 consecutive
-    // partitions (one warp each, whose epilogue needs no CTA barrier) if at
-    // least two waves remain, else 2.  That cuts the CTA prologues and
-    // epilogues; measured on GB300 at the 100K workload (196 partitions of
-    // 512 tokens): 4 per CTA 236 us, 2 per CTA 242 us, 1 per CTA 240 us.
+    // partitions (one warp each) if at least two waves remain, else 2, and
+    // merge them into one partial.  That cuts the CTA prologues and
+    // epilogues, the partials written and the merge's reads; measured on
+    // GB300 at the 100K workload (196 partitions of 512 tokens).
     {
         const long long groups = (long long)batch * num_kv_heads * nchunk;
         const long long slots = (long long)num_sms *
@@ -568,6 +571,19 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     plan->ctas = (int)(((P + plan->parts_per_cta - 1) / plan->parts_per_cta) * num_kv_heads *
                        nchunk * (long long)batch);
     return PA_OK;
+}
+
+// Partitions per partial row: the tensor-core kernel merges the
+// parts_per_cta partitions of a CTA into one partial; the CUDA-core kernel
+// writes one per partition.
+static int parts_per_partial(const pa_plan_t* plan) {
+    return (plan->kernel == PA_KERNEL_MMA && plan->num_partitions > 1) ? plan->parts_per_cta : 1;
+}
+
+// Partial rows per (sequence, query head): one per CTA along the partitions.
+static int partials_per_head(const pa_plan_t* plan) {
+    const int c = parts_per_partial(plan);
+    return (plan->num_partitions + c - 1) / c;
 }
 
 static int check_plan(const pa_plan_t* plan) {
@@ -597,13 +613,14 @@ static int check_plan(const pa_plan_t* plan) {
     const int g = Hq / Hkv;
     const int G = plan->heads_per_cta;
     if (G < 1 || G > kMaxHeadsPerCta || g % G != 0) return PA_ERR_INVALID_ARG;
-    const WsLayout wl = ws_layout(B, Hq, plan->head_dim, plan->num_partitions,
+    if (plan->kernel != PA_KERNEL_SIMT && plan->kernel != PA_KERNEL_MMA) return PA_ERR_INVALID_ARG;
+    if (plan->parts_per_cta < 1) return PA_ERR_INVALID_ARG;
+    const int R = partials_per_head(plan);
+    const WsLayout wl = ws_layout(B, Hq, plan->head_dim, plan->num_partitions, R,
                                   (long long)B * Hkv * (Hq / Hkv / plan->heads_per_cta));
     if (plan->workspace_bytes < wl.total) return PA_ERR_INVALID_ARG;
-    if (plan->merge_in_kernel &&
-        !kFusedMergeFits(plan->heads_per_cta, plan->head_dim, plan->num_partitions))
+    if (plan->merge_in_kernel && !kFusedMergeFits(plan->heads_per_cta, plan->head_dim, R))
         return PA_ERR_INVALID_ARG;
-    if (plan->kernel != PA_KERNEL_SIMT && plan->kernel != PA_KERNEL_MMA) return PA_ERR_INVALID_ARG;
     if (plan->cluster < 0) return PA_ERR_INVALID_ARG;
     if (plan->prewait_prefetch < 0 || plan->prewait_prefetch > kMaxPrewaitPrefetch)
         return PA_ERR_INVALID_ARG;
@@ -646,8 +663,9 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
 
     const int D = plan->head_dim;
     const int P = plan->num_partitions;
+    const int R = partials_per_head(plan);
     const int nchunk = plan->num_q_heads / plan->num_kv_heads / plan->heads_per_cta;
-    const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, D, P,
+    const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, D, P, R,
                                   (long long)plan->batch * plan->num_kv_heads * nchunk);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     AttendParams p;
@@ -673,7 +691,7 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     p.maxp = plan->max_pages_per_seq;
     p.max_ctx = plan->max_context_len;
     p.window = plan->window;
-    p.P = P;
+    p.P = R;  // partial rows per head: one per CTA along x
     p.pages_per_part = plan->partition_size / kPageSize;
     p.nchunk = p.g / plan->heads_per_cta;
     p.heads_per_cta = plan->heads_per_cta;
@@ -729,7 +747,8 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
     if (!context_lens || !out || !lse || !aligned16(out)) return PA_ERR_INVALID_ARG;
     const int D = plan->head_dim;
     const int nchunk = plan->num_q_heads / plan->num_kv_heads / plan->heads_per_cta;
-    const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, D, plan->num_partitions,
+    const int R = partials_per_head(plan);
+    const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, D, plan->num_partitions, R,
                                   (long long)plan->batch * plan->num_kv_heads * nchunk);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     MergeParams p;
@@ -743,8 +762,10 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
     p.B = plan->batch;
     p.Hq = plan->num_q_heads;
     p.D = D;
-    p.P = plan->num_partitions;
-    p.pages_per_part = plan->partition_size / kPageSize;
+    // Partial i covers parts_per_cta consecutive partitions from partition
+    // i * parts_per_cta on.
+    p.P = R;
+    p.pages_per_part = (plan->partition_size / kPageSize) * parts_per_partial(plan);
     p.maxp = plan->max_pages_per_seq;
     p.max_ctx = plan->max_context_len;
     p.window = plan->window;

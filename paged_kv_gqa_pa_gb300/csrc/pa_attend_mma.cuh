@@ -165,10 +165,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 // Nobody waits: a CTA that is not last simply exits.
 //
 // The merge issues all of its loads at once, so it costs one memory round
-// trip: the (m, l) pairs of the G x P partials, and for each (head, 4-dim
+// trip: the (m, l) pairs of the G x R partials (R = the group's CTAs that
+// attend anything, one partial each), and for each (head, 4-dim
 // column) item the partials' o values, spread over kThreads / items threads
 // of kFusedLoads loads each.  The planner enables it only where that covers
-// the group (kFusedMergeFits).  xbuf holds the G x P (m, weight) pairs, the
+// the group (kFusedMergeFits).  xbuf holds the G x R (m, weight) pairs, the
 // idle page ring the per-thread partial sums.
 template <int D, typename T>
 __device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, const SeqSpan& sp,
@@ -190,7 +191,7 @@ __device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, co
     if (!s_last) return;
 
     constexpr int D4 = D / 4;
-    const int np = sp.num_parts;
+    const int np = (sp.num_parts + p.parts_per_cta - 1) / p.parts_per_cta;  // partials
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int items = G * D4;               // (head, float4 column) pairs, <= kThreads
     const int tpi = kThreads / items;        // threads per item, each a stride-tpi slice of partitions
@@ -607,12 +608,12 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
 
     const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, pp);
     T* const out = reinterpret_cast<T*>(p.out);
-    auto fill_rows = [&](int part, float o_val, float m_val, float l_val, float lse_val) {
+    auto fill_rows = [&](int slot, float o_val, float m_val, float l_val, float lse_val) {
         for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
             const int h = idx / D, d = idx % D;
             const size_t bh = (size_t)b * p.Hq + h0 + h;
             if constexpr (SPLIT) {
-                const size_t row = bh * p.P + part;
+                const size_t row = bh * p.P + slot;  // (the CTA's partial row)
                 p.ws_o[row * D + d] = o_val;
                 if (d == 0) {
                     p.ws_m[row] = m_val;
@@ -673,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
             cluster_merge<D, T>(p, b, h0, G, cpart);
             return;
         }
-        for (int q = 0; q < nparts; ++q) fill_rows(part0 + q, NAN, NAN, NAN, NAN);
+        fill_rows(blockIdx.x, NAN, NAN, NAN, NAN);
         if (fused) group_arrive_and_merge<D, T>(p, sp, b, h0, G, xbuf, s_ml,
                                                 reinterpret_cast<float*>(ring));
         return;
@@ -962,62 +963,11 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
             }
         }
         constexpr int D4 = D / 4;
-        if (SPLIT && !clustered && wpp == 1) {
-            // One warp per partition: the warp's state is its partition's
-            // partial.  It stages the state in its own ring slots (idle: it
-            // has consumed every page it issued) and stores it coalesced, with
-            // no barrier shared with the other warps.
-            float* xs = reinterpret_cast<float*>(ring + warp * NS * PB);
-            constexpr int XS = Cfg::kWideXStride;
-            float* xml = xs + kMaxHeadsPerCta * XS;  // [m | l | n][8]
-#pragma unroll
-            for (int mt = 0; mt < KT; ++mt) {
-                const int d = mt * 16 + (lane >> 2);
-                if (hA < G) {
-                    xs[hA * XS + d] = o[mt][0];
-                    xs[hA * XS + d + 8] = o[mt][2];
-                }
-                if (hA + 1 < G) {
-                    xs[(hA + 1) * XS + d] = o[mt][1];
-                    xs[(hA + 1) * XS + d + 8] = o[mt][3];
-                }
-            }
-            if (lane < 4) {
-                xml[hA] = m_run[0];
-                xml[hA + 1] = m_run[1];
-                xml[kMaxHeadsPerCta + hA] = l_run[0];
-                xml[kMaxHeadsPerCta + hA + 1] = l_run[1];
-                xml[2 * kMaxHeadsPerCta + hA] = n_run[0];
-                xml[2 * kMaxHeadsPerCta + hA + 1] = n_run[1];
-            }
-            __syncwarp();
-            if (wq < nparts) {
-                const bool failed = !ok;
-                for (int idx = lane; idx < G * D4; idx += 32) {
-                    const int h = idx / D4;
-                    const int d = (idx % D4) * 4;
-                    float M = xml[h], Ls = xml[kMaxHeadsPerCta + h];
-                    const float Ns = xml[2 * kMaxHeadsPerCta + h];
-                    float inv = Ns > 0.f ? 1.f / Ns : 0.f;
-                    if (failed) {
-                        inv = NAN;
-                        M = NAN;
-                        Ls = NAN;
-                    }
-                    const float4 ow = *reinterpret_cast<const float4*>(xs + h * XS + d);
-                    const size_t row = ((size_t)b * p.Hq + h0 + h) * p.P + part0 + wq;
-                    *reinterpret_cast<float4*>(p.ws_o + row * D + d) =
-                        make_float4(ow.x * inv, ow.y * inv, ow.z * inv, ow.w * inv);
-                    if (d == 0) {
-                        p.ws_m[row] = M;
-                        p.ws_l[row] = Ls;
-                    }
-                }
-            }
-        } else {
         // Every warp is past its last page, so the page ring is idle: all D
         // dims of every warp state go there at once (behind the cluster
-        // partial) and one round combines them.
+        // partial) and one round combines them, with the merge's log-sum-exp
+        // algebra, into the CTA's one partial (its ppc partitions together)
+        // or into the final rows.
         __syncthreads();
         float* xw = reinterpret_cast<float*>(ring + Cfg::kWideXOff);
         constexpr int XS = Cfg::kWideXStride;
@@ -1035,16 +985,16 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
         }
         __syncthreads();
         const bool failed = s_flag != 0;
-        for (int idx = threadIdx.x; idx < nparts * G * D4; idx += kThreads) {
-            const int qp = idx / (G * D4);  // partition slot: warps qp * wpp ..
-            const int h = (idx / D4) % G;
+        for (int idx = threadIdx.x; idx < G * D4; idx += kThreads) {
+            const int h = idx / D4;
             const int d = (idx % D4) * 4;
-            const int w0 = qp * wpp;
             float M = -INFINITY;
-            for (int w = w0; w < w0 + wpp; ++w) M = fmaxf(M, s_ml[w * 3 * kMaxHeadsPerCta + h]);
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w * 3 * kMaxHeadsPerCta + h]);
             float Ls = 0.f, Ns = 0.f;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int w = w0; w < w0 + wpp; ++w) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
                 const float* ml = s_ml + w * 3 * kMaxHeadsPerCta;
                 const float mw = ml[h];
                 const float c = (mw == -INFINITY) ? 0.f : ex2(mw - M);
@@ -1072,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
                         cpart[ClusterPartial<D>::l_off(G, h) / 4] = Ls;
                     }
                 } else {
-                    const size_t row = bh * p.P + part0 + qp;
+                    const size_t row = bh * p.P + blockIdx.x;
                     *reinterpret_cast<float4*>(p.ws_o + row * D + d) = ov;
                     if (d == 0) {
                         p.ws_m[row] = M;
@@ -1088,7 +1038,6 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
             }
         }
         __syncthreads();  // the ring and s_ml are reused by the merges below
-        }
     }
 
     if (clustered) {

@@ -234,8 +234,9 @@ def test_unwritten_slots_never_leak():
 
 @pytest.mark.parametrize("ppc", [1, 2, 4])
 def test_several_partitions_per_cta(ppc):
-    """A CTA streaming several consecutive partitions writes the same partials
-    as one CTA per partition (the CUDA-core kernel ignores the setting)."""
+    """A CTA streaming several consecutive partitions (and merging them into
+    one partial) gives the oracle's result, as one CTA per partition does;
+    the CUDA-core kernel ignores the setting."""
     case = workloads.make_case("ppc", 3, 12, 2, 256, [20000, 7777, 1], seed=509, window=0)
     ref = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
                         case.context_lens, case.scale)
@@ -244,6 +245,13 @@ def test_several_partitions_per_cta(ppc):
         out, lse, err, plan = run_gpu(case, guard=64, parts_per_cta=ppc)
         assert err == 0
         assert_matches_oracle(case, out, lse, ref=ref, what=f"ppc{ppc} S{S}")
+    # one CTA (one partial) for all of a head's partitions: 2, 3 or 4
+    # partitions of 32 tokens, and a sequence with a single partition
+    scase = workloads.make_case("ppcs", 4, 8, 2, 128, [100, 70, 33, 20], seed=512, q_std=2.0)
+    scase.partition_size = 32
+    out, lse, err, plan = run_gpu(scase, guard=64, parts_per_cta=ppc)
+    assert err == 0 and plan.num_partitions == 4
+    assert_matches_oracle(scase, out, lse, what=f"ppc{ppc} one partial")
     wcase = workloads.make_case("ppcw", 2, 8, 4, 128, [9000, 3001], seed=510, window=2500)
     wcase.partition_size = 128
     out, lse, err, _ = run_gpu(wcase, parts_per_cta=ppc)
