@@ -549,22 +549,31 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         (kernel == PA_KERNEL_MMA && P > 1 && plan->cluster == 0 && kFusedMergeFits(G, head_dim, P))
             ? 1
             : 0;
-    // Partitions per CTA (tensor-core kernel): when the one-partition grid
-    // runs many waves of resident CTAs, let each CTA serve 4 consecutive
-    // partitions (one warp each) if at least two waves remain, else 2, and
-    // merge them into one partial.  That cuts the CTA prologues and
-    // epilogues, the partials written and the merge's reads; measured on
-    // GB300 at the 100K workload (196 partitions of 512 tokens).
+    // Partitions per CTA (tensor-core kernel, split plans without a
+    // cluster): a CTA may serve 2 or 4 consecutive partitions and merge them
+    // into one partial, which cuts CTA prologues and epilogues, the partials
+    // written and the merge's reads.  Measured on GB300 (1, 2 and 4 per CTA
+    // over batches 1-16, head dims 64-256, 32K-128K tokens): a grid of just
+    // over one wave of resident CTAs is the slow case (its last wave runs a
+    // few CTAs alone, 1.1-1.3 waves measured 3-12 % slower), while one wave
+    // that still covers every SM, or 1.5 waves and more, run fast.  So keep
+    // one partition per CTA when that grid already fits in one wave, and
+    // otherwise take the largest of 4 and 2 whose grid is either.
     {
         const long long groups = (long long)batch * num_kv_heads * nchunk;
         const long long slots = (long long)num_sms *
                                 attend_ctas_per_sm(kernel, dtype, head_dim, G, rope_theta > 0.f);
         int ppc = 1;  // (the CUDA-core kernel always serves one)
-        if (kernel == PA_KERNEL_MMA && plan->cluster == 0 && slots > 0 && P >= 2) {
-            if (groups * P > 8 * slots && 4 * pp <= kMaxPagesPerPart)
-                ppc = 4;
-            else if (groups * P > 4 * slots && 2 * pp <= kMaxPagesPerPart)
-                ppc = 2;
+        if (kernel == PA_KERNEL_MMA && plan->cluster == 0 && slots > 0 && P >= 2 &&
+            groups * P > slots) {
+            for (int c = 4; c >= 2; c /= 2) {
+                if (c > P || (long long)c * pp > kMaxPagesPerPart) continue;
+                const long long n = groups * ((P + c - 1) / c);
+                if ((n >= num_sms && n <= slots) || 2 * n >= 3 * slots) {
+                    ppc = c;
+                    break;
+                }
+            }
         }
         plan->parts_per_cta = ppc;
     }

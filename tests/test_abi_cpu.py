@@ -88,6 +88,18 @@ def test_plan_long_context_workload():
     # between 4 and 8 waves: 2 per CTA (B = 2: 1568 one-partition CTAs)
     half = pa.pa_plan(2, 24, 4, 256, 16, 31250, 6250, 100000, 0, 512, 152)
     assert half.parts_per_cta == 2 and half.ctas == 98 * 4 * 2
+    # 4 per CTA would be 392 CTAs, 1.3 waves of 304: the slow case.
+    # B = 1: 784 one-partition CTAs (2.6 waves); 4 per CTA makes one wave of
+    # 196 CTAs that still covers all 152 SMs.
+    one = pa.pa_plan(1, 24, 4, 256, 16, 6250, 6250, 100000, 0, 512, 152)
+    assert one.parts_per_cta == 4 and one.ctas == 49 * 4
+    # 50K tokens: 392 CTAs; 4 per CTA would leave SMs idle (100 CTAs), 2 per
+    # CTA gives one wave of 196.
+    mid = pa.pa_plan(1, 24, 4, 256, 16, 3125, 3125, 50000, 0, 512, 152)
+    assert mid.parts_per_cta == 2 and mid.ctas == 49 * 4
+    # 32K tokens: 256 one-partition CTAs already fit in one wave.
+    short = pa.pa_plan(1, 24, 4, 256, 16, 2048, 2048, 32768, 0, 512, 152)
+    assert short.parts_per_cta == 1 and short.ctas == 64 * 4
     rows = 4 * 24 * 196
     assert plan.workspace_bytes >= 256 + rows * 4 * 2 + rows * 256 * 4
 
