@@ -46,9 +46,9 @@ FALLBACK_HBM_GBS = 6800.0
 # `src_sha` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     # profiles/attend_mma_gqa6_ctx100k_b1.md: one capture of the B = 1 case,
-    # (409.95 + 6.18) MB read + written, scaled by tokens to the B = 4 launch.
-    ("gqa6_ctx100k", "mma"): {"src_sha": "9812327eb9a89a55", "partition_size": 512,
-                              "bytes_per_launch": 4 * (409.947392e6 + 6.184960e6)},
+    # (409.72 + 3.65) MB read + written, scaled by tokens to the B = 4 launch.
+    ("gqa6_ctx100k", "mma"): {"src_sha": "6d4bdb940867319f", "partition_size": 512,
+                              "bytes_per_launch": 4 * (409.717504e6 + 3.650048e6)},
 }
 
 
