@@ -38,6 +38,7 @@ from paged_kv_gqa_pa_gb300 import workloads  # noqa: E402
 METRIC = "decode-attn KV-read GB/s (fraction of GB300 HBM peak); µs per decode step"
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "gqa6_ctx100k"
+PER_WORKLOAD_EAGER_ITERS = 50
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -675,18 +676,26 @@ def run_gpu(args):
     per = None
     if not args.no_per_workload and rank == 0:
         per = {}
+        wl_flush = flush if flush is not None else l2_flush_buffer(torch, device)
         for name in workloads.WORKLOAD_ORDER + workloads.EXTRA_ORDER:
             c = case if name == args.workload else workloads.workload(name)
             b = kv_bytes(c)
             entry = {"dtype": c.dtype, "head_dim": c.D, "rope_theta": c.rope_theta}
             simt_ok = c.D in (64, 128, 256)
             kernels = ("mma", "simt") if simt_ok else ("mma",)
-            if c.dtype == "f32" or (c.rope_theta > 0 and c.D > 128):
-                kernels = ("simt",)  # no tensor-core build for these
+            if c.dtype == "f32":
+                kernels = ("simt",)  # no tensor-core build for fp32 caches
             for kname in kernels:
                 us, kus, copies, l2state, plan = time_graph_rotating(c, device, kname)
+                # single calls: CUDA events around one pa_decode, L2 flushed before each
+                earm = GpuArm(c, device, kernel=kname)
+                eager_ms, _ = time_flushed(earm, PER_WORKLOAD_EAGER_ITERS, wl_flush)
+                earm.check_error()
+                del earm
                 entry[kname] = {"us_per_step": us, "partition_kernel_us": kus,
                                 "kv_gbs": b / (us * 1e-6) / 1e9,
+                                "eager_flushed_us": eager_ms * 1e3,
+                                "eager_flushed_kv_gbs": b / (eager_ms * 1e-3) / 1e9,
                                 "frac_of_measured_hbm": b / (us * 1e-6) / 1e9 / peak,
                                 "frac_of_nominal_8tbs": b / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS,
                                 "plan": {"partitions": plan.num_partitions,
@@ -695,8 +704,11 @@ def run_gpu(args):
                                          "merge_in_kernel": plan.merge_in_kernel,
                                          "parts_per_cta": plan.parts_per_cta}}
                 entry.update({"copies": copies, "l2": l2state})
-            entry.update({"kv_bytes": b, "timing": "CUDA graph of back-to-back steps over "
-                                                  "rotating K/V copies"})
+            entry.update({"kv_bytes": b,
+                          "timing": "us_per_step: CUDA graph of back-to-back steps over "
+                                    "rotating K/V copies; eager_flushed_us: median of "
+                                    f"{PER_WORKLOAD_EAGER_ITERS} single steps, CUDA events "
+                                    "on the stream, L2 flushed before each"})
             per[name] = entry
 
     cpu = None

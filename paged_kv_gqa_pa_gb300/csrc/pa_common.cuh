@@ -118,9 +118,6 @@ struct MmaCfg {
     static constexpr int kWideXStride = D + 4;
     static_assert(kWideXOff + kWarps * kMaxHeadsPerCta * kWideXStride * 4 <= kRingBytes,
                   "one-round combine fits in the page ring");
-    static_assert(kMaxHeadsPerCta * kWideXStride * 4 + 3 * kMaxHeadsPerCta * 4 <=
-                      kStages * kPageBytes,
-                  "a warp's state fits in its own ring slots");
     // rotary tables: (cos, sin) of the 8- and 64-token turns, D/2 frequencies each
     static constexpr int kRopeBytes = ROPE ? 2 * (D / 2) * 8 : 0;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes + kXBytes +
