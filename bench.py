@@ -47,9 +47,9 @@ FALLBACK_HBM_GBS = 6800.0
 # `src_sha` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     # profiles/attend_mma_gqa6_ctx100k_b1.md: one capture of the B = 1 case,
-    # (409.72 + 3.65) MB read + written, scaled by tokens to the B = 4 launch.
-    ("gqa6_ctx100k", "mma"): {"src_sha": "6d4bdb940867319f", "partition_size": 512,
-                              "bytes_per_launch": 4 * (409.717504e6 + 3.650048e6)},
+    # (409.72 + 3.24) MB read + written, scaled by tokens to the B = 4 launch.
+    ("gqa6_ctx100k", "mma"): {"src_sha": "e41c7bd071232665", "partition_size": 512,
+                              "bytes_per_launch": 4 * (409.722880e6 + 3.242496e6)},
 }
 
 
