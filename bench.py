@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import glob
 import json
 import math
@@ -48,7 +49,7 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # profiles/attend_mma_gqa6_ctx100k_b1.md: one capture of the B = 1 case,
     # (409.72 + 3.24) MB read + written, scaled by tokens to the B = 4 launch.
-    ("gqa6_ctx100k", "mma"): {"src_sha": "e41c7bd071232665", "partition_size": 512,
+    ("gqa6_ctx100k", "mma"): {"src_sha": "48df20b5eca0e158", "partition_size": 512,
                               "bytes_per_launch": 4 * (409.722880e6 + 3.242496e6)},
 }
 
@@ -63,13 +64,26 @@ KERNEL_SOURCES = {
 }
 
 
+_BLOCK_COMMENT = re.compile(r"/\*.*?\*/", re.S)
+_LINE_COMMENT = re.compile(r"//[^\n]*")
+
+
+def code_only(text: str) -> str:
+    """C++/CUDA source without comments, trailing blanks and empty lines, so
+    that editing a comment leaves the hash of the code unchanged.  (The
+    kernel sources hold no string literal with a comment marker.)"""
+    text = _LINE_COMMENT.sub("", _BLOCK_COMMENT.sub("", text))
+    return "\n".join(l.rstrip() for l in text.splitlines() if l.strip())
+
+
 def kernel_src_sha(kernel: str) -> str:
-    """Hash of the sources that define one partition-kernel variant."""
+    """Hash of the code (comments stripped) of the sources that define one
+    partition-kernel variant."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "paged_kv_gqa_pa_gb300", "csrc", name), "rb") as f:
+        with open(os.path.join(ROOT, "paged_kv_gqa_pa_gb300", "csrc", name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,9 +1,10 @@
 // pa_attend_mma.cuh -- tensor-core variant of the partition kernel.
 //
-// Same work split, result and epilogue as attend_kernel (pa_attend.cuh): one
-// CTA per (partition, KV head, head chunk, sequence), four warps with their own
-// page pipelines, online softmax per page, warp states merged at the end.
-// What differs is how a page is staged and contracted:
+// Same result as attend_kernel (pa_attend.cuh), and the same shape of work: a
+// CTA per (partitions, KV head, head chunk, sequence), four warps with their
+// own page pipelines, online softmax per page, warp states merged at the end.
+// What differs is how a page is staged and contracted, and that a CTA may
+// serve several partitions:
 //
 //  * Staging.  A K or V page arrives through one TMA tensor copy
 //    (cp.async.bulk.tensor.3d) of the cache viewed as [D/64 slabs][rows =
@@ -38,10 +39,10 @@
 //  * Several partitions per CTA.  A CTA may serve parts_per_cta (1, 2 or 4)
 //    consecutive partitions of its (sequence, KV head): each partition gets
 //    4 / parts_per_cta of the warps, so no warp crosses a partition edge,
-//    and at the end, with the page ring idle, one round combines each
-//    partition's warp states into that partition's partial.  Fewer, longer
-//    CTAs spend less time in prologues and epilogues; the partials stay one
-//    per partition.
+//    and at the end, with the page ring idle, one round combines all the
+//    CTA's warp states (the merge's log-sum-exp algebra) into one partial
+//    row for its partitions together.  Fewer, longer CTAs spend less time in
+//    prologues and epilogues, and write and merge fewer partials.
 #pragma once
 
 #include <cuda.h>

@@ -205,6 +205,14 @@ def test_binding_rejects_host_tensors():
         pa.pa_decode(plan, t, t, t, t, t, 0.1, 0, t, t, t)
 
 
+def test_kernel_hash_ignores_comments_only():
+    import bench
+    code = "int f(int a) {\n  return a + 1;  // one\n}\n"
+    assert bench.code_only(code) == bench.code_only(
+        "/* header\n   lines */\nint f(int a) {\n\n  return a + 1;  // another note\n}\n")
+    assert bench.code_only(code) != bench.code_only(code.replace("a + 1", "a + 2"))
+
+
 def test_bench_kernel_source_lists_exist():
     import bench
     for kernel in bench.KERNEL_SOURCES:
