@@ -112,6 +112,44 @@ static bool make_page_map(CUtensorMap* map, const void* base, long long rows, in
            CUDA_SUCCESS;
 }
 
+// make_page_map through a small per-thread cache keyed by every input of the
+// encoding (base address, rows, head dim, element type): a map is a pure
+// function of them, so a hit is the map the encoder would return.  Decode
+// steps reuse the same K/V pools.  Measured on GB300 (Grace host, bursts of
+// calls from an idle stream): 1.94 -> 1.75 us of host time per pa_decode, and
+// 2.24 -> 1.74 us for a rotary plan together with the cached frequency table
+// below.
+static bool cached_page_map(CUtensorMap* map, const void* base, long long rows, int D,
+                            int dtype) {
+    struct Entry {
+        alignas(64) CUtensorMap map;
+        const void* base;
+        long long rows;
+        int D, dtype;
+        bool valid;
+    };
+    constexpr int kEntries = 8;
+    thread_local Entry cache[kEntries] = {};
+    thread_local int next = 0;
+    for (int i = 0; i < kEntries; ++i) {
+        const Entry& e = cache[i];
+        if (e.valid && e.base == base && e.rows == rows && e.D == D && e.dtype == dtype) {
+            *map = e.map;
+            return true;
+        }
+    }
+    if (!make_page_map(map, base, rows, D, dtype)) return false;
+    Entry& e = cache[next];
+    next = (next + 1) % kEntries;
+    e.map = *map;
+    e.base = base;
+    e.rows = rows;
+    e.D = D;
+    e.dtype = dtype;
+    e.valid = true;
+    return true;
+}
+
 // Clusters of c CTAs that one wave holds, with per_sm resident CTAs on each
 // of num_sms SMs.  A cluster must fit inside one GPC, so part of the slots
 // stay unused.  The tables are cudaOccupancyMaxActiveClusters of the
@@ -708,20 +746,30 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     p.rope = plan->rope_theta > 0.f ? 1 : 0;
     p.dtype = plan->dtype;
     if (p.rope) {
-        // theta_i / (2 pi) in double, split into two floats.
-        for (int i = 0; i < D / 2; ++i) {
-            const double turn = pow((double)plan->rope_theta, -2.0 * i / D) / (2.0 * M_PI);
-            const float hi = (float)turn;
-            p.rope_phi[0][i] = hi;
-            p.rope_phi[1][i] = (float)(turn - (double)hi);
+        // theta_i / (2 pi) in double, split into two floats; the table of the
+        // last (base, head dim) this thread used is kept.
+        thread_local float t_base = 0.f;
+        thread_local int t_D = 0;
+        thread_local float t_phi[2][kMaxRopePairs];
+        if (t_base != plan->rope_theta || t_D != D) {
+            for (int i = 0; i < D / 2; ++i) {
+                const double turn = pow((double)plan->rope_theta, -2.0 * i / D) / (2.0 * M_PI);
+                const float hi = (float)turn;
+                t_phi[0][i] = hi;
+                t_phi[1][i] = (float)(turn - (double)hi);
+            }
+            t_base = plan->rope_theta;
+            t_D = D;
         }
+        memcpy(p.rope_phi[0], t_phi[0], sizeof(float) * (D / 2));
+        memcpy(p.rope_phi[1], t_phi[1], sizeof(float) * (D / 2));
     }
     cudaError_t e;
     if (plan->kernel == PA_KERNEL_MMA) {
         alignas(64) CUtensorMap maps[2];  // K, V
         const long long rows = (long long)plan->num_pages * p.Hkv * kPageSize;
-        if (!make_page_map(&maps[0], k_cache, rows, D, plan->dtype) ||
-            !make_page_map(&maps[1], v_cache, rows, D, plan->dtype))
+        if (!cached_page_map(&maps[0], k_cache, rows, D, plan->dtype) ||
+            !cached_page_map(&maps[1], v_cache, rows, D, plan->dtype))
             return PA_ERR_CUDA;
         p.parts_per_cta = P > 1 ? plan->parts_per_cta : 1;  // one partition: all warps on it
         p.prewait_prefetch = plan->prewait_prefetch;
