@@ -509,6 +509,11 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         constexpr int kMinPagesPerPart = 2 * kWarps;
         const long long groups = (long long)batch * num_kv_heads * nchunk;
         const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim, G, rope_theta > 0.f);
+        // A wave is filled to a little under its slots: a grid that needs
+        // every slot measured slow at 3 CTAs per SM (head dims 64 and 128,
+        // B = 1: 456 CTAs 92.5 us, 448 CTAs 81.6 us on GB300) and no faster
+        // at 2 per SM.
+        const long long fill = slots - slots / 64;
         const long long span_bytes =
             (long long)span * 2 * page_size * head_dim * (dtype == PA_DTYPE_F32 ? 4 : 2);
         // Cluster merge (tensor-core kernel): the largest cluster C (2 ..
@@ -538,7 +543,7 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         } else {
             pp = span;
             for (long long waves = 1; waves <= 64; ++waves) {
-                long long parts = waves * slots / groups;
+                long long parts = waves * fill / groups;
                 if (parts < 1) parts = 1;
                 pp = (int)((span + parts - 1) / parts);
                 if (pp <= kMaxPagesPerPart) break;
@@ -595,19 +600,21 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     // over one wave of resident CTAs is the slow case (its last wave runs a
     // few CTAs alone, 1.1-1.3 waves measured 3-12 % slower), while one wave
     // that still covers every SM, or 1.5 waves and more, run fast.  So keep
-    // one partition per CTA when that grid already fits in one wave, and
-    // otherwise take the largest of 4 and 2 whose grid is either.
+    // one partition per CTA when that grid already fits in one wave (filled
+    // to a little under its slots, as above), and otherwise take the largest
+    // of 4 and 2 whose grid is either.
     {
         const long long groups = (long long)batch * num_kv_heads * nchunk;
         const long long slots = (long long)num_sms *
                                 attend_ctas_per_sm(kernel, dtype, head_dim, G, rope_theta > 0.f);
+        const long long fill = slots - slots / 64;
         int ppc = 1;  // (the CUDA-core kernel always serves one)
         if (kernel == PA_KERNEL_MMA && plan->cluster == 0 && slots > 0 && P >= 2 &&
-            groups * P > slots) {
+            groups * P > fill) {
             for (int c = 4; c >= 2; c /= 2) {
                 if (c > P || (long long)c * pp > kMaxPagesPerPart) continue;
                 const long long n = groups * ((P + c - 1) / c);
-                if ((n >= num_sms && n <= slots) || 2 * n >= 3 * slots) {
+                if ((n >= num_sms && n <= fill) || 2 * n >= 3 * slots) {
                     ppc = c;
                     break;
                 }

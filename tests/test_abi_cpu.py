@@ -97,6 +97,11 @@ def test_plan_long_context_workload():
     # CTA gives one wave of 196.
     mid = pa.pa_plan(1, 24, 4, 256, 16, 3125, 3125, 50000, 0, 512, 152)
     assert mid.parts_per_cta == 2 and mid.ctas == 49 * 4
+    # The whole-wave split fills a wave to a little under its slots: 8 KV
+    # heads at head_dim 128 (3 CTAs per SM, 456 slots) take 56 partitions,
+    # not the 57 that would need every slot.
+    l8 = pa.pa_plan(1, 32, 8, 128, 16, 8192, 8192, 131072, 0, 0, 152)
+    assert l8.num_partitions == 56 and l8.ctas == 448
     # 32K tokens: 256 one-partition CTAs already fit in one wave.
     short = pa.pa_plan(1, 24, 4, 256, 16, 2048, 2048, 32768, 0, 512, 152)
     assert short.parts_per_cta == 1 and short.ctas == 64 * 4
