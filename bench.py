@@ -596,11 +596,13 @@ def run_reference(args):
         secs.append(dt)
     value = statistics.median(vals)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        # n_gpus: the launch's N, as on the other arm's line; this arm runs on
+        # rank 0's host cores only (config.device, cpu_baseline.cores)
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": statistics.median(secs) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "l2": "host CPU"},
+        "config": {"workload": args.workload, "device": "host CPU (oracle)", "l2": "host CPU"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
