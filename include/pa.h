@@ -84,7 +84,8 @@ typedef struct pa_plan {
     int num_partitions;     /* partitions per (sequence, KV head); 1 = no split, no merge */
     int heads_per_cta;      /* query heads one CTA serves (g or a divisor of it) */
     int num_sms;            /* SM count the plan was made for */
-    int ctas;               /* CTAs of the attention kernel */
+    int ctas;               /* CTAs of the attention kernel (INT_MAX if more);
+                               informational */
     size_t workspace_bytes; /* bytes of device workspace pa_decode needs (enough for
                                one partial per partition, whatever parts_per_cta) */
     int kernel;             /* PA_KERNEL_* used for the partition kernel; pa_plan picks

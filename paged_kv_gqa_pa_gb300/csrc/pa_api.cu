@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <climits>
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -569,7 +570,6 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     plan->num_partitions = P;
     plan->heads_per_cta = G;
     plan->num_sms = num_sms;
-    plan->ctas = P * num_kv_heads * nchunk * batch;
     const long long groups_all = (long long)batch * num_kv_heads * nchunk;
     // Sized for one partial per partition, the most any parts_per_cta needs,
     // so that a caller may lower parts_per_cta in this plan.
@@ -622,8 +622,9 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         }
         plan->parts_per_cta = ppc;
     }
-    plan->ctas = (int)(((P + plan->parts_per_cta - 1) / plan->parts_per_cta) * num_kv_heads *
-                       nchunk * (long long)batch);
+    const long long ctas = (long long)((P + plan->parts_per_cta - 1) / plan->parts_per_cta) *
+                           num_kv_heads * nchunk * batch;
+    plan->ctas = (int)std::min<long long>(ctas, INT_MAX);
     return PA_OK;
 }
 

@@ -210,6 +210,16 @@ def test_binding_rejects_host_tensors():
         pa.pa_decode(plan, t, t, t, t, t, 0.1, 0, t, t, t)
 
 
+def test_plan_cta_count_saturates_instead_of_wrapping():
+    # 65535 sequences x 64 KV heads x 1024 CTAs along the partitions is more
+    # than an int holds; the informational count saturates
+    p = pa.pa_plan(65535, 64, 64, 128, 16, 10**6, 4096, 65536, 0, 16, 152)
+    assert p.ctas == 2**31 - 1 and p.num_partitions == 4096
+    small = pa.pa_plan(2, 8, 2, 128, 16, 100, 50, 800, 0, 64, 152)
+    assert small.ctas == small.batch * small.num_kv_heads * (
+        -(-small.num_partitions // small.parts_per_cta))
+
+
 def test_kernel_hash_ignores_comments_only():
     import bench
     code = "int f(int a) {\n  return a + 1;  // one\n}\n"
