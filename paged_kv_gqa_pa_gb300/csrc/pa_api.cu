@@ -512,8 +512,10 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, head_dim, G, rope_theta > 0.f);
         // A wave is filled to a little under its slots: a grid that needs
         // every slot measured slow at 3 CTAs per SM (head dims 64 and 128,
-        // B = 1: 456 CTAs 92.5 us, 448 CTAs 81.6 us on GB300) and no faster
-        // at 2 per SM.
+        // B = 1: 456 CTAs 92.5 us, 448 CTAs 81.6 us per step on GB300) and
+        // no faster at 2 per SM.  The partition kernel alone runs the same
+        // either way; the merge kernel's CTAs, resident early under
+        // programmatic dependent launch, leave a full grid short of slots.
         const long long fill = slots - slots / 64;
         const long long span_bytes =
             (long long)span * 2 * page_size * head_dim * (dtype == PA_DTYPE_F32 ? 4 : 2);
