@@ -200,6 +200,10 @@ EXTRA_WORKLOADS = {
     # Rotary embedding inside the kernel (Llama-3 frequency base), fp16, D 128.
     "gqa4_rope_ctx32k": dict(B=4, Hq=32, Hkv=8, D=128, lens=[32768] * 4, seed=1008,
                              rope_theta=500000.0),
+    # Rotary embedding at head_dim 256 (the long-context GQA-6 shapes, Gemma
+    # frequency base 10 000), fp16.
+    "gqa6_rope_ctx32k": dict(B=4, Hq=24, Hkv=4, D=256, lens=[32768] * 4, seed=1010,
+                             rope_theta=10000.0),
     # An fp32 cache (the dtype the PagedAttention-V2 commit note sizes), D 128.
     "gqa4_f32_ctx32k": dict(B=4, Hq=32, Hkv=8, D=128, lens=[32768] * 4, seed=1009,
                             dtype="f32"),
