@@ -189,9 +189,11 @@ int pa_decode(const pa_plan_t* plan, const void* q, const void* k_cache, const v
 
 /*
  * The two halves of pa_decode, for callers (and the benchmark) that time or
- * schedule them separately.  pa_decode_partitions writes the partition
- * partials to the workspace (or, with one partition, out and lse directly);
- * pa_merge reads them and writes out and lse (a no-op with one partition).
+ * schedule them separately.  pa_decode_partitions writes the partials to the
+ * workspace, one per CTA along the partitions (its parts_per_cta partitions
+ * already merged), or, with one partition, out and lse directly; pa_merge
+ * reads them and writes out and lse (a no-op with one partition, or when the
+ * partition kernel merged them itself: merge_in_kernel or a cluster).
  * Same arguments and rules as pa_decode.
  */
 int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cache,
