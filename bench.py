@@ -9,6 +9,12 @@ line.  The metric is KV-read bandwidth: algorithmic bytes = 2 * Hkv * D *
 element bytes (one K and one V row) per attended token, divided by the time
 per step.
 
+Besides the headline workload, every measured workload gets an entry in
+`per_workload` (graph-timed step, single-call time, plan, and the oracle timed
+on a bounded sample on the host cores), and the line ends with a compact
+`configs` table of the same figures and the pages' own numbers (`context`,
+another GPU under WebGPU: context only).
+
 --impl reference times the fp64 CPU oracle on the host cores instead (the only
 other path that runs the oracle), on bounded samples of the same workload.
 Under torchrun every rank runs its own replica of the workload (weak scaling,
@@ -47,8 +53,9 @@ FALLBACK_HBM_GBS = 6800.0
 # capture, keyed by workload; valid only while the kernel sources hash to
 # `src_sha` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
-    # profiles/attend_mma_gqa6_ctx100k_b1.md: one capture of the B = 1 case,
-    # (409.72 + 3.24) MB read + written, scaled by tokens to the B = 4 launch.
+    # One ncu capture of this kernel on the same workload cut to its first
+    # sequence (B = 1): (409.72 + 3.24) MB read + written per launch, scaled by
+    # tokens to the B = 4 launch.
     ("gqa6_ctx100k", "mma"): {"src_sha": "48df20b5eca0e158", "partition_size": 512,
                               "bytes_per_launch": 4 * (409.722880e6 + 3.242496e6)},
 }
@@ -198,6 +205,33 @@ def dist_setup():
     return world, rank, local
 
 
+# The pages' own measurements of this path, quoted as context only: another
+# GPU under another API, so nothing here is comparable with the numbers of
+# this bench (apache/tvm PR #20426, opening paragraph and section
+# Measurements).
+PAGES_CONTEXT = {
+    "note": "context only; WebGPU, Apple M4 Max; unavailable on this box",
+    "sharded_vs_tiled_speedup_3060_tokens": {"D64": 2.95, "D128": 3.89, "D256": 3.49},
+    "tiled_kv_read_gbs": 13,
+}
+
+
+def plan_summary(plan):
+    """The plan fields that shape a launch, plus a short label."""
+    # P<n>: no split; S<tokens> P<partitions> then cl<C> (cluster merge of C
+    # CTAs), or x<partitions per CTA> with lc (last-CTA merge) or mk (merge kernel)
+    if plan.num_partitions == 1:
+        short = "P1"
+    elif plan.cluster > 1:
+        short = f"S{plan.partition_size} P{plan.num_partitions} cl{plan.cluster}"
+    else:
+        short = (f"S{plan.partition_size} P{plan.num_partitions} x{plan.parts_per_cta} "
+                 + ("lc" if plan.merge_in_kernel else "mk"))
+    return {"partitions": plan.num_partitions, "partition_size": plan.partition_size,
+            "ctas": plan.ctas, "cluster": plan.cluster, "merge_in_kernel": plan.merge_in_kernel,
+            "parts_per_cta": plan.parts_per_cta, "short": short}
+
+
 KERNEL_IDS = {"simt": 1, "mma": 2}
 KERNEL_NAMES = {v: k for k, v in KERNEL_IDS.items()}
 
@@ -247,8 +281,10 @@ class GpuArm:
         self.pa.pa_merge(self.plan, self.cl, self.out, self.lse, self.ws, self.stream)
 
     def step(self):
-        self.partitions()
-        self.merge()
+        """One decode step through the public call, pa_decode (the partition
+        kernel and, where the plan needs it, the merge)."""
+        self.pa.pa_decode(self.plan, self.q, self.k, self.v, self.bt, self.cl, self.case.scale,
+                          self.case.window, self.out, self.lse, self.ws, self.stream)
 
     def check_error(self):
         err = self.pa.pa_get_error(self.ws, self.stream)
@@ -258,7 +294,8 @@ class GpuArm:
 
 def l2_flush_buffer(torch, device):
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    return torch.empty(max(4 * l2, 1 << 20), dtype=torch.uint8, device=device)
+    n = max(4 * l2, 1 << 20)
+    return torch.ones(n + (-n) % 8, dtype=torch.uint8, device=device)
 
 
 def time_steps(arm, steps, warmup, graph_steps=50):
@@ -336,7 +373,7 @@ def time_partition_kernel(arm, steps, flush=None, graph_launches=50):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     for i in range(steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush)
         ev[i][0].record(arm.stream)
         arm.partitions()
         ev[i][1].record(arm.stream)
@@ -345,24 +382,38 @@ def time_partition_kernel(arm, steps, flush=None, graph_launches=50):
     return statistics.mean(a.elapsed_time(b) for a, b in ev), "per-launch events, L2 flushed"
 
 
-def time_flushed(arm, iters, flush):
-    """Per-iteration step time with an L2 flush (outside the events) before each."""
+def flush_l2(flush):
+    """Evict L2 by READING a buffer larger than it (a sum on the device): the
+    lines it leaves are clean, so the next kernel's reads do not pay for
+    writing the flush back."""
+    import torch
+    return flush.view(torch.int64).sum()
+
+
+def time_flushed(arm, iters, flush, idle_s=0.002):
+    """Single-call time: per iteration, evict L2 (by reading), wait until the
+    GPU is idle plus a short host gap, then bracket ONE pa_decode call with
+    CUDA events on its stream.  Returns (median ms per call, median host
+    microseconds spent inside the pa_decode call itself)."""
     torch = arm.torch
     for _ in range(3):
         arm.step()
-    res, kres = [], []
-    for i in range(iters):
-        flush.fill_(i & 0xFF)
-        a, m, b = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    torch.cuda.synchronize()
+    res, host = [], []
+    for _ in range(iters):
+        flush_l2(flush)
+        torch.cuda.synchronize()
+        time.sleep(idle_s)
+        a, b = (torch.cuda.Event(enable_timing=True) for _ in range(2))
         a.record(arm.stream)
-        arm.partitions()
-        m.record(arm.stream)
-        arm.merge()
+        t0 = time.perf_counter()
+        arm.step()
+        t1 = time.perf_counter()
         b.record(arm.stream)
         torch.cuda.synchronize()
         res.append(a.elapsed_time(b))
-        kres.append(a.elapsed_time(m))
-    return statistics.median(res), statistics.median(kres)
+        host.append((t1 - t0) * 1e6)
+    return statistics.median(res), statistics.median(host)
 
 
 def time_graph_rotating(case, device, kernel, min_steps=40, max_copies=64,
@@ -374,7 +425,7 @@ def time_graph_rotating(case, device, kernel, min_steps=40, max_copies=64,
     import torch
     arm = GpuArm(case, device, kernel=kernel, partition_size=partition_size)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    pool = arm.k.numel() * 2 * 2
+    pool = arm.k.numel() * arm.k.element_size() * 2  # K and V
     C = max(1, min(max_copies, math.ceil(3 * l2 / max(pool, 1)), max(1, max_bytes // pool)))
     ks = [arm.k] + [arm.k.clone() for _ in range(C - 1)]
     vs = [arm.v] + [arm.v.clone() for _ in range(C - 1)]
@@ -690,8 +741,11 @@ def run_gpu(args):
     arm.check_error()
 
     per = None
+    summary = None
     if not args.no_per_workload and rank == 0:
         per = {}
+        summary = {"fields": ["kernel", "us/step (graph)", "KV GB/s", "frac of measured HBM",
+                              "single-call us", "oracle GB/s (host cores)", "plan"]}
         wl_flush = flush if flush is not None else l2_flush_buffer(torch, device)
         for name in workloads.WORKLOAD_ORDER + workloads.EXTRA_ORDER:
             c = case if name == args.workload else workloads.workload(name)
@@ -703,29 +757,41 @@ def run_gpu(args):
                 kernels = ("simt",)  # no tensor-core build for fp32 caches
             for kname in kernels:
                 us, kus, copies, l2state, plan = time_graph_rotating(c, device, kname)
-                # single calls: CUDA events around one pa_decode, L2 flushed before each
+                # single calls: CUDA events around one pa_decode on an idle GPU,
+                # L2 evicted (by reading) before each
                 earm = GpuArm(c, device, kernel=kname)
-                eager_ms, _ = time_flushed(earm, PER_WORKLOAD_EAGER_ITERS, wl_flush)
+                eager_ms, host_us = time_flushed(earm, args.per_workload_iters, wl_flush)
                 earm.check_error()
                 del earm
                 entry[kname] = {"us_per_step": us, "partition_kernel_us": kus,
                                 "kv_gbs": b / (us * 1e-6) / 1e9,
-                                "eager_flushed_us": eager_ms * 1e3,
-                                "eager_flushed_kv_gbs": b / (eager_ms * 1e-3) / 1e9,
+                                "single_call_us": eager_ms * 1e3,
+                                "single_call_kv_gbs": b / (eager_ms * 1e-3) / 1e9,
+                                "host_us_in_pa_decode": host_us,
                                 "frac_of_measured_hbm": b / (us * 1e-6) / 1e9 / peak,
                                 "frac_of_nominal_8tbs": b / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS,
-                                "plan": {"partitions": plan.num_partitions,
-                                         "partition_size": plan.partition_size,
-                                         "ctas": plan.ctas, "cluster": plan.cluster,
-                                         "merge_in_kernel": plan.merge_in_kernel,
-                                         "parts_per_cta": plan.parts_per_cta}}
+                                "plan": plan_summary(plan)}
                 entry.update({"copies": copies, "l2": l2state})
-            entry.update({"kv_bytes": b,
+            oracle_cpu = None
+            if not args.no_cpu_baseline:
+                # the oracle beside each workload: a bounded sample on the host cores
+                sampler = OracleSampler(c)
+                v, dt, desc, used = sampler.run(sampler.plan(args.per_workload_cpu_budget_s))
+                oracle_cpu = {"value": v, "unit": UNIT, "cores": used, "kind": "oracle",
+                              "sample": desc, "seconds": dt}
+            entry.update({"kv_bytes": b, "cpu_baseline": oracle_cpu,
                           "timing": "us_per_step: CUDA graph of back-to-back steps over "
-                                    "rotating K/V copies; eager_flushed_us: median of "
-                                    f"{PER_WORKLOAD_EAGER_ITERS} single steps, CUDA events "
-                                    "on the stream, L2 flushed before each"})
+                                    "rotating K/V copies; single_call_us: median of "
+                                    f"{args.per_workload_iters} single pa_decode calls, CUDA "
+                                    "events on the stream, GPU idle and L2 evicted before each"})
             per[name] = entry
+            k0 = kernels[0]
+            e0 = entry[k0]
+            summary[name] = [k0, round(e0["us_per_step"], 2), round(e0["kv_gbs"]),
+                             round(e0["frac_of_measured_hbm"], 3),
+                             round(e0["single_call_us"], 1),
+                             round(oracle_cpu["value"], 3) if oracle_cpu else None,
+                             e0["plan"]["short"]]
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -738,7 +804,7 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "us_per_step": ms_max * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
             "data": "synthetic",
             "config": {"workload": args.workload, "batch": case.B, "num_q_heads": case.Hq,
                        "num_kv_heads": case.Hkv, "head_dim": case.D, "page_size": case.page_size,
@@ -763,6 +829,10 @@ def run_gpu(args):
                           "per-step launches, L2 flushed between steps",
             "clocks": clk.summary(),
             "per_workload": per,
+            # Last, so that a tail of the output keeps them: the pages' own
+            # figures (context only) and one compact line per workload.
+            "context": PAGES_CONTEXT,
+            "configs": summary,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -786,7 +856,8 @@ def main():
                     help="keep only the workload's first sequences (profiler captures)")
     ap.add_argument("--profile-only", action="store_true",
                     help="run warm-up + steps untimed (for ncu captures) and exit")
-    ap.add_argument("--per-workload-iters", type=int, default=50)
+    ap.add_argument("--per-workload-iters", type=int, default=PER_WORKLOAD_EAGER_ITERS)
+    ap.add_argument("--per-workload-cpu-budget-s", type=float, default=2.0)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
     args = ap.parse_args()

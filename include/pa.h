@@ -34,11 +34,14 @@
  * chunks per CTA.
  * q, k_cache, v_cache, out and workspace must be 16-byte aligned.
  *
- * Ownership: every pointer is caller-owned device memory (the library
- * allocates nothing, holds no device memory and keeps no per-call state).
- * Calls are asynchronous on the given stream (a cudaStream_t passed as void*;
- * NULL = the legacy default stream) and never synchronise the host, except
- * pa_get_error.
+ * Ownership: every pointer is caller-owned device memory.  No call allocates
+ * or frees device memory.  Two things are held by the library itself: the
+ * fixed scratch array behind pa_decode_static (a __device__ array of
+ * PA_STATIC_WORKSPACE_BYTES on every GPU that loads the library), and small
+ * per-thread host caches (tensor-map encodings of the last K/V pools, the
+ * last rotary frequency table).  Calls are asynchronous on the given stream
+ * (a cudaStream_t passed as void*; NULL = the legacy default stream) and
+ * never synchronise the host, except pa_get_error and pa_get_error_ex.
  *
  * Errors: every call returns a pa_status.  Argument checks happen on the host
  * before anything is launched.  Data-dependent faults found on the device (a
@@ -100,8 +103,11 @@ typedef struct pa_plan {
                                pa_merge has nothing to do; 0: pa_merge launches the
                                merge kernel */
     int ctrl_bytes;         /* leading workspace bytes that must be zero before the
-                               first call (error word, per-group arrival counters); the
-                               library leaves them zero after every call */
+                               first call (error word, per-group arrival counters).
+                               Every call leaves the counters zero; the error word
+                               keeps its bits until pa_get_error_ex clears them.  A
+                               plan edited after pa_plan is rejected when this no
+                               longer covers its counters */
     int dtype;              /* PA_DTYPE_*: element type of q, k_cache, v_cache and out
                                (pa_plan sets fp16; a caller may set bf16 or fp32) */
     float rope_theta;       /* > 0: rotary embedding inside the kernel (rotate-half
@@ -179,9 +185,13 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
  * log-sum-exp merge.  `window` must equal plan->window.
  * workspace: >= plan->workspace_bytes of device memory whose first
  * plan->ctrl_bytes are zero before the first call (zero-fill it once when
- * allocated; every call leaves those bytes zero again).  They hold the device
- * error word and per-group arrival counters; the rest holds the partition
- * partials between the kernels.  Concurrent calls must not share a workspace.
+ * allocated).  They hold the device error word and per-group arrival
+ * counters; every call leaves the counters zero again, and the error word
+ * keeps its bits until read with pa_get_error_ex(clear = 1).  The rest holds
+ * the partition partials between the kernels.  A workspace reused with a
+ * different plan must have the new plan's ctrl_bytes zeroed first (the
+ * counters may then lie where the old plan kept partials).  Concurrent calls
+ * must not share a workspace.
  */
 int pa_decode(const pa_plan_t* plan, const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, const int32_t* context_lens, float scale, int window,
@@ -216,13 +226,17 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
  * compiled into the library (a __device__ array, so every GPU that loads the
  * library keeps that much memory until the process exits).  Nothing is
  * allocated or freed by this call.
- *   - A plan with workspace_bytes > PA_STATIC_WORKSPACE_BYTES is rejected with
- *     PA_ERR_WORKSPACE before anything is launched.
+ *   - The plan is checked on the host first, by pa_decode's rules.  Then the
+ *     workspace extent its launches use is worked out from its shapes (not
+ *     read from its ctrl_bytes field); a plan whose workspace_bytes, extent
+ *     or ctrl_bytes exceeds PA_STATIC_WORKSPACE_BYTES is rejected with
+ *     PA_ERR_WORKSPACE.  A rejected call touches no device memory.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture on that device.
- *   - Every call first clears the array's control bytes (plan.ctrl_bytes) on
- *     `stream` with cudaMemsetAsync, then runs pa_decode on it.
+ *   - Every call first clears the control bytes this plan uses (error word
+ *     and arrival counters) on `stream` with cudaMemsetAsync, since the
+ *     previous call may have used another plan, then runs pa_decode on it.
  *   - All calls on a device share the one array, which keeps the previous
  *     call's contents: calls whose kernels overlap on the GPU (different
  *     streams, no ordering between them) race on it and must not be issued.
@@ -236,11 +250,20 @@ int pa_decode_static(const pa_plan_t* plan, const void* q, const void* k_cache,
                      float* lse, void* stream);
 
 /*
- * Synchronise `stream`, read the device error word kept in `workspace`
- * (PA_DEVERR_* bits, 0 = none) into *device_error, and reset it to 0 when
- * `clear` is non-zero.
+ * Synchronise `stream` and read the device error word kept in `workspace`
+ * (PA_DEVERR_* bits, 0 = none) into *device_error.  The word is left as it
+ * is: its bits accumulate over calls until pa_get_error_ex clears them.
+ * Returns PA_ERR_INVALID_ARG for a null pointer, PA_ERR_CUDA if the copy or
+ * the synchronisation fails.
  */
-int pa_get_error(void* workspace, void* stream, int clear, unsigned* device_error);
+int pa_get_error(void* workspace, void* stream, int* device_error);
+
+/*
+ * pa_get_error with a choice to clear: the word is read into *device_error
+ * and, when `clear` is non-zero, reset to 0 on `stream` (then synchronised),
+ * so that the next read reports only faults of later calls.
+ */
+int pa_get_error_ex(void* workspace, void* stream, int clear, unsigned* device_error);
 
 /* Static text for a pa_status value. */
 const char* pa_status_string(int status);

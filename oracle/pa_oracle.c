@@ -102,8 +102,6 @@ static double bf16_bits_to_double(uint16_t h) {
 
 double pa_oracle_bf16_to_double(uint16_t h) { return bf16_bits_to_double(h); }
 
-typedef double (*to_double_fn)(uint16_t);
-
 /* Element e of an array of the given type, exactly as a double. */
 static double elem(const void* base, size_t e, int dtype) {
     if (dtype == 2) return (double)((const float*)base)[e];

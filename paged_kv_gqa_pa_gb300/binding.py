@@ -32,7 +32,8 @@ _TORCH_DTYPE = {PA_DTYPE_F16: torch.float16, PA_DTYPE_BF16: torch.bfloat16,
                 PA_DTYPE_F32: torch.float32}
 
 EXPORTED = ("pa_plan", "pa_plan_ex", "pa_decode", "pa_decode_partitions", "pa_merge",
-            "pa_get_error", "pa_status_string", "pa_version", "pa_decode_static")
+            "pa_get_error", "pa_get_error_ex", "pa_status_string", "pa_version",
+            "pa_decode_static")
 
 
 class pa_plan_t(ctypes.Structure):
@@ -108,8 +109,10 @@ def load():
         lib.pa_decode_partitions.restype = i
         lib.pa_merge.argtypes = [pp, P, P, P, P, P]
         lib.pa_merge.restype = i
-        lib.pa_get_error.argtypes = [P, P, i, ctypes.POINTER(ctypes.c_uint)]
+        lib.pa_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
         lib.pa_get_error.restype = i
+        lib.pa_get_error_ex.argtypes = [P, P, i, ctypes.POINTER(ctypes.c_uint)]
+        lib.pa_get_error_ex.restype = i
         lib.pa_status_string.argtypes = [i]
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_version.argtypes = []
@@ -226,12 +229,23 @@ def pa_decode_static(plan, q, k_cache, v_cache, block_tables, context_lens, scal
         raise PAError("pa_decode_static", st)
 
 
-def pa_get_error(workspace, stream=None, clear=True) -> int:
-    v = ctypes.c_uint(0)
+def pa_get_error(workspace, stream=None) -> int:
+    """Synchronise and read the device error word (PA_DEVERR_* bits), leaving it set."""
+    v = ctypes.c_int(0)
     st = load().pa_get_error(_dev_ptr(workspace, "workspace"), _stream_ptr(stream),
-                             1 if clear else 0, ctypes.byref(v))
+                             ctypes.byref(v))
     if st != PA_OK:
         raise PAError("pa_get_error", st)
+    return int(v.value) & 0xFFFFFFFF
+
+
+def pa_get_error_ex(workspace, stream=None, clear=True) -> int:
+    """Synchronise, read the device error word and (clear=True) reset it to 0."""
+    v = ctypes.c_uint(0)
+    st = load().pa_get_error_ex(_dev_ptr(workspace, "workspace"), _stream_ptr(stream),
+                                1 if clear else 0, ctypes.byref(v))
+    if st != PA_OK:
+        raise PAError("pa_get_error_ex", st)
     return int(v.value)
 
 

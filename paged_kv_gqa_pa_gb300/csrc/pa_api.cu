@@ -676,6 +676,12 @@ static int check_plan(const pa_plan_t* plan) {
     const WsLayout wl = ws_layout(B, Hq, plan->head_dim, plan->num_partitions, R,
                                   (long long)B * Hkv * (Hq / Hkv / plan->heads_per_cta));
     if (plan->workspace_bytes < wl.total) return PA_ERR_INVALID_ARG;
+    // The control bytes a caller keeps zero must cover the error word and
+    // every arrival counter this plan's launch uses (a plan edited after
+    // pa_plan, e.g. a different heads_per_cta, may need more of them).
+    if (plan->ctrl_bytes < 0 || (size_t)plan->ctrl_bytes < wl.ctrl_bytes ||
+        (size_t)plan->ctrl_bytes > plan->workspace_bytes)
+        return PA_ERR_INVALID_ARG;
     if (plan->merge_in_kernel && !kFusedMergeFits(plan->heads_per_cta, plan->head_dim, R))
         return PA_ERR_INVALID_ARG;
     if (plan->cluster < 0) return PA_ERR_INVALID_ARG;
@@ -853,7 +859,15 @@ int pa_decode(const pa_plan_t* plan, const void* q, const void* k_cache, const v
     return pa_merge(plan, context_lens, out, lse, workspace, stream);
 }
 
-int pa_get_error(void* workspace, void* stream, int clear, unsigned* device_error) {
+int pa_get_error(void* workspace, void* stream, int* device_error) {
+    if (!workspace || !device_error) return PA_ERR_INVALID_ARG;
+    unsigned v = 0;
+    const int st = pa_get_error_ex(workspace, stream, 0, &v);
+    if (st == PA_OK) *device_error = (int)v;
+    return st;
+}
+
+int pa_get_error_ex(void* workspace, void* stream, int clear, unsigned* device_error) {
     if (!workspace || !device_error) return PA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned v = 0;
@@ -874,3 +888,20 @@ int pa_get_error(void* workspace, void* stream, int clear, unsigned* device_erro
 }
 
 }  // extern "C"
+
+namespace pa {
+// check_plan, then the extent of the workspace the plan's launches touch:
+// its control bytes (error word and arrival counters, which must be zero
+// before a call) and its total bytes.  Host only; nothing is launched.
+int plan_workspace_extent(const pa_plan_t* plan, size_t* ctrl_bytes, size_t* total_bytes) {
+    const int st = check_plan(plan);
+    if (st != PA_OK) return st;
+    const int nchunk = plan->num_q_heads / plan->num_kv_heads / plan->heads_per_cta;
+    const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, plan->head_dim,
+                                  plan->num_partitions, partials_per_head(plan),
+                                  (long long)plan->batch * plan->num_kv_heads * nchunk);
+    *ctrl_bytes = wl.ctrl_bytes;
+    *total_bytes = wl.total;
+    return PA_OK;
+}
+}  // namespace pa

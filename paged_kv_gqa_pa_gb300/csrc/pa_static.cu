@@ -20,6 +20,12 @@
 
 #include "../../include/pa.h"
 
+namespace pa {
+// pa_api.cu: the plan checks of pa_decode, then the control and total bytes
+// of the workspace the plan's launches use.
+int plan_workspace_extent(const pa_plan_t* plan, size_t* ctrl_bytes, size_t* total_bytes);
+}  // namespace pa
+
 namespace {
 
 __device__ __align__(256) unsigned char g_static_workspace[PA_STATIC_WORKSPACE_BYTES];
@@ -53,19 +59,27 @@ extern "C" int pa_decode_static(const pa_plan_t* plan, const void* q, const void
                                 const void* v_cache, const int32_t* block_tables,
                                 const int32_t* context_lens, float scale, int window, void* out,
                                 float* lse, void* stream) {
-    if (!plan) return PA_ERR_INVALID_ARG;
-    if (plan->workspace_bytes > (size_t)PA_STATIC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE;
+    // Every check runs on the host before anything touches the GPU: the plan
+    // itself (the same rules as pa_decode), then the workspace extent its
+    // launches use, worked out from the plan's shapes rather than taken from
+    // its ctrl_bytes field, against the size of the built-in array.
+    size_t ctrl = 0, total = 0;
+    const int st = pa::plan_workspace_extent(plan, &ctrl, &total);
+    if (st != PA_OK) return st;
+    const size_t cap = (size_t)PA_STATIC_WORKSPACE_BYTES;
+    if (plan->workspace_bytes > cap || total > cap || ctrl > cap ||
+        (size_t)plan->ctrl_bytes > cap)
+        return PA_ERR_WORKSPACE;
     void* ws = static_workspace_ptr();
     if (!ws) return PA_ERR_CUDA;
-    // The scratch keeps whatever the previous call left in it.  Its control
-    // bytes (error word, per-group arrival counters) must start at zero, so
-    // they are cleared on the stream before every call: a call that gave up
-    // on a bounded wait may have left a counter behind.  The partials need no
-    // clearing: each is written before it is read.  cudaMemsetAsync allocates
-    // nothing.
-    if (plan->batch > 0 && plan->ctrl_bytes > 0 &&
-        cudaMemsetAsync(ws, 0, (size_t)plan->ctrl_bytes, static_cast<cudaStream_t>(stream)) !=
-            cudaSuccess) {
+    // The array keeps whatever the previous call left in it, and that call may
+    // have used another plan: its partials may sit where this plan keeps its
+    // arrival counters, and its device error word stays set until cleared.
+    // So this plan's control bytes are cleared on the stream before every
+    // call (cudaMemsetAsync allocates nothing).  The partials need no
+    // clearing: each is written before it is read.
+    if (plan->batch > 0 &&
+        cudaMemsetAsync(ws, 0, ctrl, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return PA_ERR_CUDA;
     }

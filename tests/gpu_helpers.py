@@ -112,7 +112,7 @@ def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=N
         assert ws.numel() >= ws_bytes
     pa.pa_decode(plan, dev["q"], dev["k"], dev["v"], dev["bt"], dev["cl"], case.scale,
                  case.window, out, lse, ws)
-    err = pa.pa_get_error(ws)
+    err = pa.pa_get_error_ex(ws, clear=True)
     torch.cuda.synchronize()
     # Every call leaves the control bytes (error word, arrival counters) zero.
     assert int(ws[:plan.ctrl_bytes].count_nonzero()) == 0, "control bytes not left zero"

@@ -199,7 +199,8 @@ def test_decode_argument_checks_return_before_launch():
                          0, 0x10000, 0x10000, 0x10000, None) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_merge(ctypes.byref(plan), 0x10000, 0x10000, 0x10000, None, None) == \
         binding.PA_ERR_WORKSPACE
-    assert lib.pa_get_error(None, None, 0, None) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_get_error(None, None, None) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_get_error_ex(None, None, 0, None) == binding.PA_ERR_INVALID_ARG
 
 
 def test_binding_rejects_host_tensors():
@@ -340,3 +341,60 @@ def test_partition_count_limit():
     # the merge kernel reduces at most 4096 partitions per head
     ok = pa.pa_plan(1, 4, 1, 64, 16, 4200, 4096, 65536, 0, 16, 152)
     assert ok.num_partitions == 4096
+
+
+STATIC_BYTES = 32 << 20  # PA_STATIC_WORKSPACE_BYTES in include/pa.h
+
+
+def test_static_entry_point_checks_the_plan_before_touching_the_gpu():
+    """pa_decode_static runs pa_decode's plan checks, then sizes the workspace
+    extent from the plan's shapes, all on the host: these calls are rejected
+    on a machine without a GPU, so none of them reaches a CUDA call."""
+    lib = pa.load()
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced
+
+    def call(plan):
+        return lib.pa_decode_static(ctypes.byref(plan), fake, fake, fake, fake, fake,
+                                    ctypes.c_float(0.1), plan.window, fake, fake, None)
+
+    plan = pa.pa_plan(4, 32, 8, 128, 16, 4000, 256, 4096, 0, 256, 152)
+    assert plan.num_partitions > 1 and plan.workspace_bytes <= STATIC_BYTES
+    # A control region claimed larger than the whole scratch (a stale or
+    # hand-edited plan) never reaches the clearing memset.
+    huge = binding.pa_plan_t.from_buffer_copy(plan)
+    huge.ctrl_bytes = 64 << 20
+    assert call(huge) == binding.PA_ERR_INVALID_ARG
+    huge.workspace_bytes = 80 << 20
+    assert call(huge) == binding.PA_ERR_WORKSPACE
+    # A control region too small for the arrival counters the launch uses
+    # (heads_per_cta edited after pa_plan: 4 head chunks per KV head instead of 1).
+    chunks = binding.pa_plan_t.from_buffer_copy(plan)
+    chunks.heads_per_cta = 1
+    chunks.merge_in_kernel = 0
+    assert call(chunks) == binding.PA_ERR_INVALID_ARG
+    negative = binding.pa_plan_t.from_buffer_copy(plan)
+    negative.ctrl_bytes = -1
+    assert call(negative) == binding.PA_ERR_INVALID_ARG
+    # A plan whose partials need more than the built-in scratch.
+    big = pa.pa_plan(4, 64, 8, 256, 16, 1 << 16, 4096, 65536, 0, 16, 152)
+    assert big.workspace_bytes > STATIC_BYTES
+    assert call(big) == binding.PA_ERR_WORKSPACE
+    # Everything else pa_decode rejects, pa_decode_static rejects the same way.
+    bad = binding.pa_plan_t.from_buffer_copy(plan)
+    bad.parts_per_cta = 3
+    assert call(bad) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_static(None, fake, fake, fake, fake, fake, ctypes.c_float(0.1), 0,
+                                fake, fake, None) == binding.PA_ERR_INVALID_ARG
+
+
+def test_plan_rejects_control_bytes_that_miss_counters():
+    plan = pa.pa_plan(4, 32, 8, 128, 16, 4000, 256, 4096, 0, 256, 152)
+    edited = binding.pa_plan_t.from_buffer_copy(plan)
+    edited.heads_per_cta = 1
+    edited.merge_in_kernel = 0
+    # 4 x 32 groups of counters need more control bytes than the 4 x 8 of the plan
+    assert _call_decode(edited) == binding.PA_ERR_INVALID_ARG
+    # a control region larger than the workspace is inconsistent too
+    over = binding.pa_plan_t.from_buffer_copy(plan)
+    over.ctrl_bytes = int(over.workspace_bytes) + 256
+    assert _call_decode(over) == binding.PA_ERR_INVALID_ARG
