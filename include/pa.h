@@ -134,8 +134,26 @@ typedef struct pa_plan {
                                wait on it runs out (after 1 s): the call then takes its
                                copy-timeout path (PA_DEVERR_TIMEOUT, NaN rows) without
                                any fault.  Lets a test exercise that path */
-    int reserved;
+    int balanced;           /* > 0: work-balanced partitions (tensor-core kernel).  The
+                               grid has `balanced` CTAs (X) per (KV head, head chunk),
+                               shared by the whole batch, and the partition size is
+                               chosen on the device from the actual context lengths:
+                               with T the batch's attended pages, every partition has
+                               pp = clamp(ceil(T / (X - B)), 8, 256) pages and sequence
+                               b gets max(1, ceil(pages_b / pp)) CTAs, so a long
+                               sequence gets more CTAs than a short one.  Its partials
+                               are merged by the last CTA of each group
+                               (merge_in_kernel = 1, cluster 0, parts_per_cta 1).
+                               num_partitions then holds X (the most partials a
+                               sequence can have) and partition_size the largest pp
+                               any lengths within max_context_len can give.  Set by
+                               pa_plan_ex (partition_size PA_PARTITION_BALANCED, or
+                               its automatic choice); 0 = fixed-size partitions */
 } pa_plan_t;
+
+/* pa_plan / pa_plan_ex partition_size: work-balanced partitions sized on the
+ * device (pa_plan_t.balanced); PA_ERR_UNSUPPORTED where none can be made. */
+#define PA_PARTITION_BALANCED (-1)
 
 /* Element types (pa_plan_t.dtype).  fp16 and bf16 run on either kernel, fp32
  * on the CUDA-core kernel only (fp32 FMA throughout; head_dim 64/128/256). */
@@ -152,7 +170,9 @@ typedef struct pa_plan {
  * Choose the partitioning for a decode call (host only, no device access
  * unless num_sms == 0, which queries the current device).
  *   partition_size  0 = automatic (enough partitions to fill num_sms SMs),
- *                   else the tokens per partition (multiple of page_size).
+ *                   PA_PARTITION_BALANCED = work-balanced partitions over the
+ *                   batch (pa_plan_t.balanced), else the tokens per partition
+ *                   (multiple of page_size).
  * The attended span of a sequence is at most ceil(max_context_len / ps) pages,
  * or ceil((window - 1) / ps) + 1 pages with a window; num_partitions =
  * ceil(span / (partition_size / ps)).  The 100000-token, 512-token-partition

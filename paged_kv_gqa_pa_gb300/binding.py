@@ -28,6 +28,7 @@ PA_KERNEL_MMA = 2
 PA_DTYPE_F16 = 0
 PA_DTYPE_BF16 = 1
 PA_DTYPE_F32 = 2
+PA_PARTITION_BALANCED = -1
 _TORCH_DTYPE = {PA_DTYPE_F16: torch.float16, PA_DTYPE_BF16: torch.bfloat16,
                 PA_DTYPE_F32: torch.float32}
 
@@ -62,11 +63,11 @@ class pa_plan_t(ctypes.Structure):
         ("cluster", ctypes.c_int),
         ("prewait_prefetch", ctypes.c_int),
         ("test_stall_bytes", ctypes.c_int),
-        ("reserved", ctypes.c_int),
+        ("balanced", ctypes.c_int),
     ]
 
     def as_dict(self):
-        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class PAError(RuntimeError):
@@ -273,9 +274,10 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, window=0,
     maxp = block_tables.shape[1]
     if max_context_len is None:
         max_context_len = maxp * ps
-    plan = pa_plan_ex(B, Hq, Hkv, D, ps, num_pages, maxp, max_context_len, window, partition_size,
-                      torch.cuda.get_device_properties(q.device).multi_processor_count,
-                      dtype=dtypes[q.dtype], kernel=0, rope_theta=rope_theta)
+    with torch.cuda.device(q.device):  # num_sms 0: plan for q's device, asking it
+        plan = pa_plan_ex(B, Hq, Hkv, D, ps, num_pages, maxp, max_context_len, window,
+                          partition_size, 0, dtype=dtypes[q.dtype], kernel=0,
+                          rope_theta=rope_theta)
     out = torch.empty((B, Hq, D), dtype=q.dtype, device=q.device)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     ws = new_workspace(plan, q.device)

@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <mutex>
 
@@ -24,6 +25,9 @@ cudaError_t launch_attend_mma_d(bool split, const AttendParams& p, const CUtenso
 template <int D, typename T>
 cudaError_t launch_attend_mma_rope_d(bool split, const AttendParams& p, const CUtensorMap* maps,
                                      dim3 grid, cudaStream_t stream);
+
+template <int D, typename T, bool ROPE>
+cudaError_t attend_mma_cluster_occupancy(int c, int* clusters);
 
 template <typename T>
 static cudaError_t launch_attend_mma_t(int D, bool split, const AttendParams& p,
@@ -152,11 +156,13 @@ static bool cached_page_map(CUtensorMap* map, const void* base, long long rows, 
 }
 
 // Clusters of c CTAs that one wave holds, with per_sm resident CTAs on each
-// of num_sms SMs.  A cluster must fit inside one GPC, so part of the slots
-// stay unused.  The tables are cudaOccupancyMaxActiveClusters of the
-// tensor-core kernel measured on GB300 (152 SMs) at 2 and 3 CTAs per SM, for
-// c = 1..16; other SM counts use the smaller of the two tables' fill
-// fractions.
+// of num_sms SMs, for a plan made for an explicit SM count (no device is
+// asked).  A cluster must fit inside one GPC, so part of the slots stay
+// unused.  The tables are cudaOccupancyMaxActiveClusters of the tensor-core
+// kernel measured on GB300 (152 SMs) at 2 and 3 CTAs per SM, for c = 1..16;
+// other SM counts use the smaller of the two tables' fill fractions.  A plan
+// for the current device (num_sms = 0) asks the device instead
+// (device_clusters_per_wave).
 static long long clusters_per_wave(int num_sms, int per_sm, int c) {
     static const short k2[kMaxClusterParts] = {304, 152, 97, 74, 58, 46, 38, 36,
                                                30,  28,  23, 23, 19, 14, 14, 14};
@@ -167,6 +173,48 @@ static long long clusters_per_wave(int num_sms, int per_sm, int c) {
     if (num_sms == 152 && per_sm == 3) return k3[c - 1];
     const double f = std::min(k2[c - 1] * (double)c / 304.0, k3[c - 1] * (double)c / 456.0);
     return (long long)((double)num_sms * per_sm * f / c);
+}
+
+// cudaOccupancyMaxActiveClusters of the cluster-merge instance for (head
+// dim, element type, rotary) and clusters of c CTAs on the current device,
+// queried once per device and cached; -1 if the query fails.
+static long long device_clusters_per_wave(int D, int dtype, bool rope, int c) {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cache[kMaxDevices][4][2][2][kMaxClusterParts];  // value + 1; 0 = unknown
+    int dev = 0;
+    if (c < 2 || c > kMaxClusterParts || cudaGetDevice(&dev) != cudaSuccess || dev < 0 ||
+        dev >= kMaxDevices) {
+        cudaGetLastError();
+        return -1;
+    }
+    const int di = D == 64 ? 0 : D == 96 ? 1 : D == 128 ? 2 : 3;
+    const int ti = dtype == PA_DTYPE_BF16 ? 1 : 0;
+    std::atomic<int>& slot = cache[dev][di][ti][rope ? 1 : 0][c - 1];
+    const int known = slot.load();
+    if (known > 0) return known - 1;
+    int n = 0;
+    cudaError_t e = cudaErrorInvalidValue;
+#define PA_OCC(DD, TT, RR) e = attend_mma_cluster_occupancy<DD, TT, RR>(c, &n)
+#define PA_OCC_D(TT, RR)                                                          \
+    switch (D) {                                                                  \
+        case 64: PA_OCC(64, TT, RR); break;                                       \
+        case 96: PA_OCC(96, TT, RR); break;                                       \
+        case 128: PA_OCC(128, TT, RR); break;                                     \
+        default: PA_OCC(256, TT, RR); break;                                      \
+    }
+    if (ti) {
+        if (rope) { PA_OCC_D(__nv_bfloat16, true) } else { PA_OCC_D(__nv_bfloat16, false) }
+    } else {
+        if (rope) { PA_OCC_D(__half, true) } else { PA_OCC_D(__half, false) }
+    }
+#undef PA_OCC_D
+#undef PA_OCC
+    if (e != cudaSuccess || n < 0) {
+        cudaGetLastError();
+        return -1;
+    }
+    slot.store(n + 1);
+    return n;
 }
 
 // CTAs of the partition kernel resident per SM (the launch bound, which the
@@ -195,6 +243,38 @@ int attend_ctas_per_sm(int kernel, int dtype, int D, int G, bool rope) {
         case 128: return f32 ? AttendCfg<128, 4>::blocks_for(G) : AttendCfg<128>::blocks_for(G);
         default: return f32 ? AttendCfg<256, 4>::blocks_for(G) : AttendCfg<256>::blocks_for(G);
     }
+}
+
+// Pages a sequence can attend: ceil(Lmax / ps), or with a window at most
+// ceil((window - 1) / ps) + 1 (the window need not start on a page edge).
+static int attended_span_pages(int max_context_len, int window) {
+    int span = (max_context_len + kPageSize - 1) / kPageSize;
+    if (window > 0) {
+        const int wspan = (window - 1 + kPageSize - 1) / kPageSize + 1;
+        if (wspan < span) span = wspan;
+    }
+    return span < 1 ? 1 : span;
+}
+
+// CTAs per (KV head, head chunk) of a work-balanced plan, or 0 where none can
+// be made: the tensor-core kernel without rotary embedding (its rotary
+// instances are built without the run-time mapping), B <= kMaxBalancedBatch, one wave of
+// resident CTAs over all groups (filled to a little under its slots), the
+// last-CTA merge able to stage G x X partials, and partitions of at most
+// kMaxStagedPages pages for any lengths within the plan's bound
+// (ceil(B * span / (X - B)) <= kMaxStagedPages).
+static int balanced_ctas(int kernel, int dtype, int D, int G, bool rope, int batch,
+                         int groups_per_seq, int span, int num_sms) {
+    if (kernel != PA_KERNEL_MMA || rope || batch < 1 || batch > kMaxBalancedBatch) return 0;
+    if (G * (D / 4) > kThreads) return 0;  // the last-CTA merge's one item per thread
+    const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, D, G, rope);
+    const long long fill = slots - slots / 64;
+    long long x = fill / groups_per_seq;
+    x = std::min<long long>(x, kFusedMaxStaged / G);
+    x = std::min<long long>(x, kMaxPartitions);
+    if (x <= batch) return 0;
+    if ((long long)batch * span > (long long)kMaxStagedPages * (x - batch)) return 0;
+    return (int)x;
 }
 
 template <typename E>
@@ -460,14 +540,17 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         return PA_ERR_UNSUPPORTED;
     if (batch < 0 || batch > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         num_q_heads % num_kv_heads != 0 || head_dim <= 0 || page_size <= 0 || num_pages <= 0 ||
-        max_pages_per_seq <= 0 || max_context_len < 0 || window < 0 || partition_size < 0 ||
-        num_sms < 0)
+        max_pages_per_seq <= 0 || max_context_len < 0 || window < 0 ||
+        (partition_size < 0 && partition_size != PA_PARTITION_BALANCED) || num_sms < 0)
         return PA_ERR_INVALID_ARG;
     if ((long long)max_context_len > (long long)max_pages_per_seq * page_size)
         return PA_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 96 && head_dim != 128 && head_dim != 256)
         return PA_ERR_UNSUPPORTED;
     if (page_size != kPageSize) return PA_ERR_UNSUPPORTED;
+    bool want_balanced = partition_size == PA_PARTITION_BALANCED;
+    if (want_balanced) partition_size = 0;
+    bool one_wave_split = false;  // the automatic fixed split fits one wave
     if (partition_size % page_size != 0) return PA_ERR_INVALID_ARG;
 
     const int g = num_q_heads / num_kv_heads;
@@ -476,6 +559,7 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     const int G = g / nchunk;
     if ((long long)num_kv_heads * nchunk > 65535) return PA_ERR_UNSUPPORTED;
 
+    const bool this_device = num_sms == 0;  // plan for the current device: ask it
     if (num_sms == 0) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -485,14 +569,12 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         }
     }
 
-    // Pages a sequence can attend: ceil(Lmax / ps), or with a window at most
-    // ceil((window - 1) / ps) + 1 (the window need not start on a page edge).
-    int span = (max_context_len + page_size - 1) / page_size;
-    if (window > 0) {
-        const int wspan = (window - 1 + page_size - 1) / page_size + 1;
-        if (wspan < span) span = wspan;
-    }
-    if (span < 1) span = 1;
+    const int span = attended_span_pages(max_context_len, window);
+    // Work-balanced partitions: X CTAs per (KV head, head chunk), one wave
+    // over all groups, when the batch's pages always fit X partitions.
+    const int bal_x = balanced_ctas(kernel, dtype, head_dim, G, rope_theta > 0.f, batch,
+                                    num_kv_heads * nchunk, span, num_sms);
+    if (want_balanced && bal_x == 0) return PA_ERR_UNSUPPORTED;
 
     int pp;  // pages per partition
     bool use_cluster = false;
@@ -531,7 +613,11 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         long long cpar = 0;
         const int per_sm = attend_ctas_per_sm(kernel, dtype, head_dim, G, rope_theta > 0.f);
         for (int c = kMaxClusterParts; c >= 2 && groups > 0; --c) {
-            if (clusters_per_wave(num_sms, per_sm, c) >= groups) {
+            long long held = -1;
+            if (this_device && kernel == PA_KERNEL_MMA)
+                held = device_clusters_per_wave(head_dim, dtype, rope_theta > 0.f, c);
+            if (held < 0) held = clusters_per_wave(num_sms, per_sm, c);
+            if (held >= groups) {
                 cpar = c;
                 break;
             }
@@ -549,14 +635,34 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
                 long long parts = waves * fill / groups;
                 if (parts < 1) parts = 1;
                 pp = (int)((span + parts - 1) / parts);
-                if (pp <= kMaxPagesPerPart) break;
+                if (pp <= kMaxPagesPerPart) {
+                    one_wave_split = waves == 1;
+                    break;
+                }
             }
             if (pp < kMinPagesPerPart) pp = kMinPagesPerPart;
         }
         if (pp > kMaxPagesPerPart) pp = kMaxPagesPerPart;
     }
-    if (pp > kMaxPagesPerPart) return PA_ERR_UNSUPPORTED;
-    const int P = (span + pp - 1) / pp;
+    // A batch whose automatic split is one wave takes work-balanced
+    // partitions: the host knows only the bound on the lengths, and a fixed
+    // split sized for it leaves the CTAs of short sequences idle while the long
+    // ones stream.  Measured on GB300 (B = 4, 32 query / 8 KV heads, head dim
+    // 128, lengths {100, 200, 300, 50000}): 54.7 us with fixed partitions,
+    // 39.1 us balanced; on uniform lengths the two are within 2 %.  (Short
+    // contexts keep the cluster merge: the last-CTA merge balanced plans use
+    // costs about 2 us more than it.)
+    if (!want_balanced && partition_size == 0 && one_wave_split && batch >= 2 && bal_x > 0)
+        want_balanced = true;
+    if (want_balanced) {
+        // the largest partition any lengths within max_context_len can give
+        pp = (int)(((long long)batch * span + (bal_x - batch) - 1) / (bal_x - batch));
+        pp = std::max(kMinBalancedPages, std::min(pp, kMaxStagedPages));
+        use_cluster = false;
+    }
+    if (pp > (kernel == PA_KERNEL_MMA ? kMaxStagedPages : kMaxPagesPerPart))
+        return PA_ERR_UNSUPPORTED;
+    const int P = want_balanced ? bal_x : (span + pp - 1) / pp;
     if (P > kMaxPartitions) return PA_ERR_UNSUPPORTED;
 
     plan->batch = batch;
@@ -594,6 +700,8 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         (kernel == PA_KERNEL_MMA && P > 1 && plan->cluster == 0 && kFusedMergeFits(G, head_dim, P))
             ? 1
             : 0;
+    plan->balanced = want_balanced ? bal_x : 0;
+    if (want_balanced) plan->merge_in_kernel = 1;
     // Partitions per CTA (tensor-core kernel, split plans without a
     // cluster): a CTA may serve 2 or 4 consecutive partitions and merge them
     // into one partial, which cuts CTA prologues and epilogues, the partials
@@ -611,8 +719,8 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
                                 attend_ctas_per_sm(kernel, dtype, head_dim, G, rope_theta > 0.f);
         const long long fill = slots - slots / 64;
         int ppc = 1;  // (the CUDA-core kernel always serves one)
-        if (kernel == PA_KERNEL_MMA && plan->cluster == 0 && slots > 0 && P >= 2 &&
-            groups * P > fill) {
+        if (kernel == PA_KERNEL_MMA && plan->cluster == 0 && !plan->balanced && slots > 0 &&
+            P >= 2 && groups * P > fill) {
             for (int c = 4; c >= 2; c /= 2) {
                 if (c > P || (long long)c * pp > kMaxPagesPerPart) continue;
                 const long long n = groups * ((P + c - 1) / c);
@@ -624,8 +732,10 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
         }
         plan->parts_per_cta = ppc;
     }
-    const long long ctas = (long long)((P + plan->parts_per_cta - 1) / plan->parts_per_cta) *
-                           num_kv_heads * nchunk * batch;
+    const long long ctas =
+        plan->balanced ? (long long)plan->balanced * num_kv_heads * nchunk
+                       : (long long)((P + plan->parts_per_cta - 1) / plan->parts_per_cta) *
+                             num_kv_heads * nchunk * batch;
     plan->ctas = (int)std::min<long long>(ctas, INT_MAX);
     return PA_OK;
 }
@@ -649,7 +759,7 @@ static int check_plan(const pa_plan_t* plan) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || plan->page_size != kPageSize ||
         plan->num_partitions < 1 || plan->num_partitions > kMaxPartitions ||
         plan->partition_size < kPageSize || plan->partition_size % kPageSize != 0 ||
-        plan->partition_size / kPageSize > kMaxPagesPerPart || plan->num_pages <= 0 ||
+        plan->num_pages <= 0 ||
         plan->max_pages_per_seq <= 0 || plan->max_context_len < 0 || plan->window < 0)
         return PA_ERR_INVALID_ARG;
     if (plan->head_dim != 64 && plan->head_dim != 96 && plan->head_dim != 128 &&
@@ -682,8 +792,21 @@ static int check_plan(const pa_plan_t* plan) {
     if (plan->ctrl_bytes < 0 || (size_t)plan->ctrl_bytes < wl.ctrl_bytes ||
         (size_t)plan->ctrl_bytes > plan->workspace_bytes)
         return PA_ERR_INVALID_ARG;
-    if (plan->merge_in_kernel && !kFusedMergeFits(plan->heads_per_cta, plan->head_dim, R))
+    if (plan->merge_in_kernel && !kFusedMergeLegal(plan->heads_per_cta, plan->head_dim, R))
         return PA_ERR_INVALID_ARG;
+    if (plan->balanced < 0) return PA_ERR_INVALID_ARG;
+    if (plan->balanced > 0) {
+        // Work-balanced partitions: the last-CTA merge, one partition per CTA,
+        // no cluster, one load of all B lengths per CTA, and no partition
+        // longer than kMaxStagedPages for lengths within the plan's bound.
+        const int X = plan->balanced;
+        const int span = attended_span_pages(plan->max_context_len, plan->window);
+        if (plan->kernel != PA_KERNEL_MMA || !plan->merge_in_kernel || plan->cluster > 1 ||
+            plan->parts_per_cta != 1 || B > kMaxBalancedBatch || X <= B ||
+            plan->num_partitions != X || plan->rope_theta > 0.f ||
+            (long long)B * span > (long long)kMaxStagedPages * (X - B))
+            return PA_ERR_INVALID_ARG;
+    }
     if (plan->cluster < 0) return PA_ERR_INVALID_ARG;
     if (plan->prewait_prefetch < 0 || plan->prewait_prefetch > kMaxPrewaitPrefetch)
         return PA_ERR_INVALID_ARG;
@@ -693,8 +816,11 @@ static int check_plan(const pa_plan_t* plan) {
          plan->num_partitions != plan->cluster || plan->parts_per_cta != 1 ||
          plan->merge_in_kernel))
         return PA_ERR_INVALID_ARG;
+    // Page ids a CTA stages: kMaxStagedPages (tensor-core kernel) or
+    // kMaxPagesPerPart (CUDA-core kernel) for its parts_per_cta partitions.
+    const int staged = plan->kernel == PA_KERNEL_MMA ? kMaxStagedPages : kMaxPagesPerPart;
     if (plan->parts_per_cta < 1 ||
-        (long long)plan->parts_per_cta * (plan->partition_size / kPageSize) > kMaxPagesPerPart)
+        (long long)plan->parts_per_cta * (plan->partition_size / kPageSize) > staged)
         return PA_ERR_INVALID_ARG;
     // The tensor-core kernel gives each of a CTA's partitions 4 / parts_per_cta warps.
     if (plan->kernel == PA_KERNEL_MMA && plan->parts_per_cta != 1 && plan->parts_per_cta != 2 &&
@@ -790,13 +916,19 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
         p.parts_per_cta = P > 1 ? plan->parts_per_cta : 1;  // one partition: all warps on it
         p.prewait_prefetch = plan->prewait_prefetch;
         p.stall_tx = plan->test_stall_bytes;
-        const dim3 grid((P + p.parts_per_cta - 1) / p.parts_per_cta, p.Hkv * p.nchunk, p.B);
+        p.balanced = plan->balanced;
+        // A work-balanced plan spreads the batch over grid.x (X CTAs per group).
+        const dim3 grid = plan->balanced
+                              ? dim3(plan->balanced, p.Hkv * p.nchunk, 1)
+                              : dim3((P + p.parts_per_cta - 1) / p.parts_per_cta,
+                                     p.Hkv * p.nchunk, p.B);
         e = launch_attend_mma(D, plan->dtype, P > 1, p, maps, grid,
                               static_cast<cudaStream_t>(stream));
     } else {
         p.parts_per_cta = 1;
         p.prewait_prefetch = 0;
         p.stall_tx = 0;
+        p.balanced = 0;
         const dim3 grid(P, p.Hkv * p.nchunk, p.B);
         e = launch_attend(D, plan->heads_per_cta, P > 1, p, grid,
                           static_cast<cudaStream_t>(stream));

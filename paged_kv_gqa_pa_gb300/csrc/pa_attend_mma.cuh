@@ -177,16 +177,23 @@ __device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, co
                                                        int b, int h0, int G, float* xbuf,
                                                        float* s_small, float* scratch) {
     __shared__ int s_last;
-    __threadfence();  // this CTA's partials, before the arrival below
+    // Arrival: the CTA barrier orders every thread's partial stores before
+    // thread 0's arrival, and the arrival is one acquire-release atomic at GPU
+    // scope (cumulative, so it releases the whole CTA's stores, and for the
+    // last CTA acquires every other CTA's); the closing barrier passes that on
+    // to the threads that read the partials.
     __syncthreads();
     if (threadIdx.x == 0) {
         const int target = (sp.num_parts + p.parts_per_cta - 1) / p.parts_per_cta;
         unsigned* ctr = p.counters + ((size_t)b * gridDim.y + blockIdx.y);
-        const unsigned prev = atomicAdd(ctr, 1u);
+        unsigned prev;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(ctr)
+                     : "memory");
         const int last = (int)(prev + 1u) == target;
-        if (last) atomicExch(ctr, 0u);
+        if (last) atomicExch(ctr, 0u);  // ready for the next call
         s_last = last;
-        __threadfence();
     }
     __syncthreads();
     if (!s_last) return;
@@ -207,51 +214,60 @@ __device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, co
     float* s_M = s_small;        // [G]
     float* s_L = s_small + kMaxHeadsPerCta;
 
-    // One round trip: the (m, l) pairs and this thread's o slices together.
+    // The (m, l) pairs and this thread's first chunk of o slices go out
+    // together, so a group of up to kFusedLoads x tpi partials costs one
+    // round trip; each further chunk of that many costs one more.
     for (int idx = threadIdx.x; idx < G * np; idx += kThreads) {
         const int h = idx / np, i = idx % np;
         s_m[idx] = __ldcg(p.ws_m + row0 + (size_t)h * p.P + i);
         s_w[idx] = __ldcg(p.ws_l + row0 + (size_t)h * p.P + i);
     }
-    float4 ov[kFusedLoads];
     const float* src = p.ws_o + (row0 + (size_t)ih * p.P) * D + id;
-#pragma unroll
-    for (int u = 0; u < kFusedLoads; ++u) {
-        const int i = sub + u * tpi;
-        ov[u] = (active && i < np) ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)i * D))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    __syncthreads();
-    for (int h = warp; h < G; h += kWarps) {
-        float mx = -INFINITY;
-        for (int i = lane; i < np; i += 32) mx = fmaxf(mx, s_m[h * np + i]);
-#pragma unroll
-        for (int mask = 16; mask > 0; mask >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, mask));
-        float sum = 0.f;
-        for (int i = lane; i < np; i += 32) {
-            const float l = s_w[h * np + i];
-            // l == 0: nothing attended; a NaN (bad page) is kept so it reaches the output.
-            const float w = (l == 0.f) ? 0.f : ex2(s_m[h * np + i] - mx) * l;
-            s_w[h * np + i] = w;
-            sum += w;
-        }
-#pragma unroll
-        for (int mask = 16; mask > 0; mask >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, mask);
-        if (lane == 0) {
-            s_M[h] = mx;
-            s_L[h] = sum;
-        }
-    }
-    __syncthreads();
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < np; c0 += kFusedLoads * tpi) {
+        float4 ov[kFusedLoads];
 #pragma unroll
-    for (int u = 0; u < kFusedLoads; ++u) {
-        const int i = sub + u * tpi;
-        const float w = (active && i < np) ? s_w[ih * np + i] : 0.f;
-        acc.x += w * ov[u].x;
-        acc.y += w * ov[u].y;
-        acc.z += w * ov[u].z;
-        acc.w += w * ov[u].w;
+        for (int u = 0; u < kFusedLoads; ++u) {
+            const int i = c0 + sub + u * tpi;
+            ov[u] = (active && i < np)
+                        ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)i * D))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (c0 == 0) {  // (the same branch for every thread)
+            __syncthreads();
+            for (int h = warp; h < G; h += kWarps) {
+                float mx = -INFINITY;
+                for (int i = lane; i < np; i += 32) mx = fmaxf(mx, s_m[h * np + i]);
+#pragma unroll
+                for (int mask = 16; mask > 0; mask >>= 1)
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, mask));
+                float sum = 0.f;
+                for (int i = lane; i < np; i += 32) {
+                    const float l = s_w[h * np + i];
+                    // l == 0: nothing attended; a NaN (bad page) is kept so it reaches the output.
+                    const float w = (l == 0.f) ? 0.f : ex2(s_m[h * np + i] - mx) * l;
+                    s_w[h * np + i] = w;
+                    sum += w;
+                }
+#pragma unroll
+                for (int mask = 16; mask > 0; mask >>= 1)
+                    sum += __shfl_xor_sync(0xffffffffu, sum, mask);
+                if (lane == 0) {
+                    s_M[h] = mx;
+                    s_L[h] = sum;
+                }
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int u = 0; u < kFusedLoads; ++u) {
+            const int i = c0 + sub + u * tpi;
+            const float w = (active && i < np) ? s_w[ih * np + i] : 0.f;
+            acc.x += w * ov[u].x;
+            acc.y += w * ov[u].y;
+            acc.z += w * ov[u].z;
+            acc.w += w * ov[u].w;
+        }
     }
     if (active) reinterpret_cast<float4*>(scratch)[sub * items + item] = acc;
     __syncthreads();
@@ -484,9 +500,8 @@ __device__ __forceinline__ void rope_turn_pair(float2& c, float2& s, float4 t) {
 // wait, so a stale hint costs one useless prefetch.  L2-only loads, so that
 // nothing read here sits in L1 afterwards.
 __device__ __forceinline__ void prefetch_first_pages(const AttendParams& p, int part0, int kvh,
-                                                     int b, int first, int step, int limit,
-                                                     int lane, int D) {
-    const int pp = p.pages_per_part;
+                                                     int b, int pp, int first, int step,
+                                                     int limit, int lane, int D) {
     int Lh = 0;
     if (lane == 0) Lh = __ldcg(p.context_lens + b);
     Lh = __shfl_sync(0xffffffffu, Lh, 0);
@@ -503,6 +518,87 @@ __device__ __forceinline__ void prefetch_first_pages(const AttendParams& p, int 
             prefetch_l2(p.v + off, kPageSize * D * 2);
         }
     }
+}
+
+// Work-balanced partitions (plan.balanced = X > 0): the X CTAs along grid.x
+// of a (KV head, head chunk) share the whole batch, so that a long sequence
+// gets more CTAs than a short one.  With pages_b the attended pages of
+// sequence b (0 for a length out of bounds), every sequence gets
+// n_b(pp) = max(1, ceil(pages_b / pp)) consecutive CTAs, in batch order, and
+// pp is the smallest partition size with sum_b n_b(pp) <= X, found by
+// bisection between ceil(T / X) and ceil(T / (X - B)) (T = sum_b pages_b;
+// the upper end always fits, since sum_b n_b <= T / pp + B), clamped to
+// [kMinBalancedPages, kMaxStagedPages] (the plan guarantees the clamp never
+// binds for lengths within its bound).  Every CTA computes this map from the
+// same B lengths (one load per thread, B <= kThreads) and takes the
+// (sequence, partition) item its x falls in; with x >= sum_b n_b it has none.
+// `hint`: lengths read with L2-only loads, for the prefetch addresses before
+// the dependency wait (they may be stale).
+struct BalancedItem {
+    int b, part, pp;
+};
+
+// Sum over the CTA's threads of v (all threads call it; s_red: kWarps ints).
+__device__ __forceinline__ int cta_sum(int v, int* s_red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    __syncthreads();  // earlier reads of s_red are done
+    if (lane == 0) s_red[warp] = v;
+    __syncthreads();
+    int t = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t += s_red[w];
+    return t;
+}
+
+__device__ __forceinline__ bool balanced_item(const AttendParams& p, int x, bool hint,
+                                              BalancedItem& it) {
+    __shared__ int s_red[kWarps];
+    __shared__ int s_item[2];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int B = p.B, X = p.balanced;
+    int pages = 0;
+    if (t < B) {
+        const int L = hint ? __ldcg(p.context_lens + t) : p.context_lens[t];
+        const SeqSpan sp = seq_span(L, p.window, p.max_ctx, p.maxp, 1);
+        pages = sp.valid ? sp.end_page - sp.first_page : 0;
+    }
+    if (t == 0) s_item[0] = -1;
+    const int T = cta_sum(pages, s_red);
+    int lo = max(kMinBalancedPages, (T + X - 1) / X);
+    int hi = max(lo, min((T + (X - B) - 1) / (X - B), kMaxStagedPages));
+    while (lo < hi) {  // (the same bounds in every thread)
+        const int mid = (lo + hi) >> 1;
+        const int need = cta_sum(t < B ? max(1, (pages + mid - 1) / mid) : 0, s_red);
+        if (need <= X)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    const int pp = lo;
+    const int n = t < B ? max(1, (pages + pp - 1) / pp) : 0;
+    int inc = n;  // inclusive scan of n over the CTA
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, m);
+        if (lane >= m) inc += o;
+    }
+    __syncthreads();  // every read of s_red above is done
+    if (lane == 31) s_red[warp] = inc;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) inc += s_red[w];
+    const int exc = inc - n;
+    if (t < B && x >= exc && x < inc) {
+        s_item[0] = t;
+        s_item[1] = x - exc;
+    }
+    __syncthreads();
+    it.b = s_item[0];
+    it.part = s_item[1];
+    it.pp = pp;
+    __syncthreads();  // s_item and s_red may be reused by a second call
+    return it.b >= 0;
 }
 
 static_assert(ClusterPartial<64>::kMaxBytes <= MmaCfg<64>::kWideXOff &&
@@ -530,8 +626,10 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     unsigned char* base = smem_raw + (base_u32 - raw_u32);
     unsigned char* ring = base;
     float* xbuf = reinterpret_cast<float*>(base + Cfg::kRingBytes);  // last-CTA merge scratch
-    int* s_pid = reinterpret_cast<int*>(base + Cfg::kRingBytes + Cfg::kXBytes);
-    float* s_ml = reinterpret_cast<float*>(s_pid + kMaxPagesPerPart);  // [warps][m|l|n][8]
+    // The CTA's page ids (up to kMaxStagedPages) live in the merge scratch:
+    // they are read only while pages stream, the merge runs after the last page.
+    int* s_pid = reinterpret_cast<int*>(xbuf);
+    float* s_ml = reinterpret_cast<float*>(base + Cfg::kRingBytes + Cfg::kXBytes);  // [warps][m|l|n][8]
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_ml + kWarps * kMaxHeadsPerCta * 3);
     // rotary tables (ROPE): (cos, sin) per frequency of the 8-token turn and of
     // the turn by one step of a warp's pages (16 * wpp tokens; "r64")
@@ -543,11 +641,16 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int ppc = p.parts_per_cta;
-    const int part0 = blockIdx.x * ppc;
     const int kvh = blockIdx.y / p.nchunk;
     const int h0 = kvh * p.g + (blockIdx.y % p.nchunk) * G;
-    const int b = blockIdx.z;
-    const int pp = p.pages_per_part;
+    // This CTA's sequence, first partition, partition size in pages and
+    // partial row.  A work-balanced plan (p.balanced) decides them on the
+    // device from the batch's lengths (balanced_item): first from hints for
+    // the prefetch, then for real after the dependency wait.
+    int b = blockIdx.z;
+    int part0 = blockIdx.x * ppc;
+    int pp = p.pages_per_part;
+    int slot = blockIdx.x;
     const int wpp = kWarps / ppc;  // warps per partition (ppc is 1, 2 or 4)
     const int wq = warp / wpp;     // this warp's partition slot within the CTA
     const int wl = warp % wpp;     // and its place among that partition's warps
@@ -592,8 +695,16 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
         for (int s = 0; s < NS; ++s) mbar_init(bar_w + s * 8, 1);
         fence_mbar_init();
     }
-    if (p.prewait_prefetch)
-        prefetch_first_pages(p, part0, kvh, b, wq * pp + wl, wpp, (wq + 1) * pp, lane, D);
+    // Work-balanced plans: split instances without a cluster or rotary
+    // embedding (the run-time sequence and partition cost the D = 256 rotary
+    // instances, already at 255 registers, a spill).
+    constexpr bool kBalancedInstance = SPLIT && !CLUSTER && !ROPE;
+    if (p.prewait_prefetch) {
+        BalancedItem hi{b, part0, pp};
+        if (!(kBalancedInstance && p.balanced) || balanced_item(p, blockIdx.x, true, hi))
+            prefetch_first_pages(p, hi.part, kvh, hi.b, hi.pp, wq * hi.pp + wl, wpp,
+                                 (wq + 1) * hi.pp, lane, D);
+    }
     if constexpr (ROPE) {
         // (kernel parameters only: no input is read)
         for (int f = threadIdx.x; f < D / 2; f += kThreads) {
@@ -606,6 +717,14 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     }
     __syncthreads();  // barriers and rotary tables initialised
     wait_for_prerequisite_grid();
+    if (kBalancedInstance && p.balanced) {
+        BalancedItem it;
+        if (!balanced_item(p, blockIdx.x, false, it)) return;  // more CTAs than items
+        b = it.b;
+        part0 = it.part;  // (one partition per CTA)
+        pp = it.pp;
+        slot = it.part;
+    }
 
     const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, pp);
     T* const out = reinterpret_cast<T*>(p.out);
@@ -626,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
             }
         }
     };
-    const bool fused = SPLIT && p.merge_in_kernel;
+    const bool fused = SPLIT && !CLUSTER && p.merge_in_kernel;
     // Final rows written without any partial (used when nothing is merged).
     auto final_rows = [&](float o_val, float lse_val) {
         for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
@@ -641,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     if (!sp.valid) {
         // (the same for every CTA of a cluster: they all leave here)
         if (threadIdx.x == 0 && part0 == 0 && blockIdx.y == 0) atomicOr(p.err, PA_DEVERR_BAD_LENGTH);
-        if (!SPLIT || ((fused || clustered) && blockIdx.x == 0)) final_rows(NAN, NAN);
+        if (!SPLIT || ((fused || clustered) && slot == 0)) final_rows(NAN, NAN);
         return;  // with a separate merge, the merge writes the NaN rows
     }
     if (part0 >= sp.num_parts) {
@@ -652,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
             cluster_merge<D, T>(p, b, h0, G, cpart);
             return;
         }
-        if (!SPLIT || (fused && sp.num_parts == 0 && blockIdx.x == 0)) final_rows(0.f, -INFINITY);
+        if (!SPLIT || (fused && sp.num_parts == 0 && slot == 0)) final_rows(0.f, -INFINITY);
         return;
     }
     const int nparts = min(ppc, sp.num_parts - part0);
@@ -675,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
             cluster_merge<D, T>(p, b, h0, G, cpart);
             return;
         }
-        fill_rows(blockIdx.x, NAN, NAN, NAN, NAN);
+        fill_rows(slot, NAN, NAN, NAN, NAN);
         if (fused) group_arrive_and_merge<D, T>(p, sp, b, h0, G, xbuf, s_ml,
                                                 reinterpret_cast<float*>(ring));
         return;
@@ -1023,7 +1142,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
                         cpart[ClusterPartial<D>::l_off(G, h) / 4] = Ls;
                     }
                 } else {
-                    const size_t row = bh * p.P + blockIdx.x;
+                    const size_t row = bh * p.P + slot;
                     *reinterpret_cast<float4*>(p.ws_o + row * D + d) = ov;
                     if (d == 0) {
                         p.ws_m[row] = M;
@@ -1093,6 +1212,34 @@ cudaError_t launch_attend_mma_dr(bool split, const AttendParams& p, const CUtens
     cfg.attrs = attr;
     cfg.numAttrs = clustered ? 2 : 1;
     return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// Clusters of c CTAs (2 .. kMaxClusterParts) of the cluster-merge instance
+// that the current device holds at once, for the planner: the exact figure
+// for this device (its SM count and GPC layout), where a table measured on one
+// part would only be a guess on another.
+template <int D, typename T, bool ROPE>
+cudaError_t attend_mma_cluster_occupancy(int c, int* clusters) {
+    const void* fn = reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true, true, ROPE>);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         MmaCfg<D, ROPE>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (c > 8) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)c, 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = MmaCfg<D, ROPE>::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, fn, &cfg);
 }
 
 // Launchers of the plain instances and of the rotary ones (fp16 / bf16 each).

@@ -14,13 +14,21 @@ namespace pa {
 constexpr int kPageSize = 16;     // tokens per page
 constexpr int kWarps = 4;         // consumer warps per CTA of the attention kernel
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxPagesPerPart = 256;  // page ids a CTA stages in shared memory
+constexpr int kMaxPagesPerPart = 256;  // page ids a CUDA-core CTA stages; the longest
+                                       // partition the planner's fixed split makes
+constexpr int kMaxStagedPages = 2048;  // page ids a tensor-core CTA stages (in the
+                                       // merge scratch, idle while pages stream)
 constexpr int kMaxClusterParts = 16;   // largest cluster (the non-portable limit)
 constexpr int kMaxPartitions = 4096;   // partitions the merge kernel reduces
 constexpr int kMaxHeadsPerCta = 8;
 constexpr int kCtrlBytes = 256;        // workspace control block (device error word)
 constexpr int kMaxRopePairs = 128;     // head_dim / 2 of the widest rotary head
 constexpr int kMaxPrewaitPrefetch = 8; // largest prewait_prefetch (pages per warp)
+constexpr int kMinBalancedPages = 2 * kWarps;  // smallest partition of a work-balanced plan
+constexpr int kMaxBalancedBatch = kThreads;    // sequences a work-balanced plan can spread
+// Partials one (sequence, head chunk) can merge in the last CTA: its G x R
+// (m, weight) pairs are staged in the 8 KiB combine buffer.
+constexpr int kFusedMaxStaged = 1024;
 
 // Bounded waits: a bulk copy that has not landed after this long is reported
 // as PA_DEVERR_TIMEOUT instead of hanging the GPU.
@@ -48,6 +56,8 @@ struct AttendParams {
     int heads_per_cta;      // G: query heads one CTA serves
     int parts_per_cta;      // consecutive partitions one CTA streams (tensor-core kernel)
     int prewait_prefetch;   // pages per warp prefetched into L2 before the PDL wait (tensor-core)
+    int balanced;           // > 0: work-balanced partitions over the batch, this many CTAs
+                            // along grid.x per (KV head, head chunk) (tensor-core kernel)
     int stall_tx;           // test hook: extra bytes each warp's first copy expects (0 normally)
     float scale_log2;       // scale * log2(e)
     int rope;               // 1: rotary embedding of q and K (CUDA-core kernel)
@@ -107,7 +117,8 @@ struct MmaCfg {
     static constexpr int kStages = ROPE ? (D == 256 ? 3 : (D == 128 ? 6 : (D == 96 ? 8 : 6)))
                                         : (D == 256 ? 3 : (D == 128 ? 4 : (D == 96 ? 5 : 6)));
     static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
-    // scratch of the last-CTA merge ((m, weight) pairs of a group's partials)
+    // scratch of the last-CTA merge ((m, weight) pairs of a group's partials);
+    // while pages stream it holds the CTA's page ids
     static constexpr int kXBytes = kWarps * kMaxHeadsPerCta * 64 * 4;
     // A CTA combines its warp states at the end, all D dims at once, in the
     // idle page ring behind the cluster partial ([G][D] o, then m and l):
@@ -120,9 +131,10 @@ struct MmaCfg {
                   "one-round combine fits in the page ring");
     // rotary tables: (cos, sin) of the 8- and 64-token turns, D/2 frequencies each
     static constexpr int kRopeBytes = ROPE ? 2 * (D / 2) * 8 : 0;
+    static_assert(kXBytes >= kMaxStagedPages * 4, "page ids staged in the merge scratch");
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes + kXBytes +
-                                      kMaxPagesPerPart * 4 + kWarps * kMaxHeadsPerCta * 3 * 4 +
-                                      kWarps * kStages * 8 + kRopeBytes + 16;
+                                      kWarps * kMaxHeadsPerCta * 3 * 4 + kWarps * kStages * 8 +
+                                      kRopeBytes + 16;
     static constexpr int kMinBlocks = ROPE ? (D == 64 ? 3 : 2) : (D == 256 ? 2 : 3);
     static_assert(kMinBlocks * (kSmemBytes + 1024) <= 228 * 1024, "CTAs per SM by shared memory");
     static_assert(kRows64 || kPageBytes == kFullSlabs * kSlabBytes, "slab layout");
@@ -144,6 +156,15 @@ __host__ __device__ constexpr bool kFusedMergeFits(int G, int D, int P) {
            (P + (kThreads / (G * (D / 4))) - 1) / (kThreads / (G * (D / 4))) <= kFusedLoads &&
            2 * G * P * 4 <= kWarps * kMaxHeadsPerCta * 64 * 4;
 }
+
+// What the last-CTA merge can take at all: one thread (or more) per (head,
+// 4-dim column) item, and the G x R (m, weight) pairs in the combine buffer.
+// Partials beyond kFusedLoads per thread cost one more round trip per chunk.
+__host__ __device__ constexpr bool kFusedMergeLegal(int G, int D, int R) {
+    return G * (D / 4) <= kThreads && G * R <= kFusedMaxStaged;
+}
+static_assert(2 * kFusedMaxStaged * 4 <= kWarps * kMaxHeadsPerCta * 64 * 4,
+              "the staged (m, weight) pairs fit the combine buffer");
 
 // Span of pages a sequence attends, shared by the partition and merge kernels
 // so both agree on the partition count of every sequence.

@@ -207,6 +207,13 @@ EXTRA_WORKLOADS = {
     # An fp32 cache (the dtype the PagedAttention-V2 commit note sizes), D 128.
     "gqa4_f32_ctx32k": dict(B=4, Hq=32, Hkv=8, D=128, lens=[32768] * 4, seed=1009,
                             dtype="f32"),
+    # Skewed batches (Llama-3-8B-style heads, 32 query / 8 KV, D 128): one long
+    # context among short ones, where a split sized for the longest length
+    # leaves most CTAs idle.
+    "skewed4_d128_ctx50k": dict(B=4, Hq=32, Hkv=8, D=128, lens=[100, 200, 300, 50000],
+                                seed=1011),
+    "skewed16_d128_ctx12k": dict(B=16, Hq=32, Hkv=8, D=128, lens=[12000] + [200] * 15,
+                                 seed=1012),
 }
 EXTRA_ORDER = list(EXTRA_WORKLOADS)
 ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}

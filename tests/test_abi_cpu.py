@@ -53,7 +53,7 @@ def test_plan_struct_layout_matches_header():
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     fields = re.findall(r"\b(?:int|size_t|float)\s+([a-z_0-9]+)(?:\[\d+\])?\s*;", body)
     assert fields == [f for f, _ in binding.pa_plan_t._fields_]
-    # 14 ints, a size_t, then 10 four-byte fields (kernel ... reserved).
+    # 14 ints, a size_t, then 10 four-byte fields (kernel ... balanced).
     assert binding.pa_plan_t.workspace_bytes.offset == 56
     assert binding.pa_plan_t.kernel.offset == 64
     assert binding.pa_plan_t.parts_per_cta.offset == 68
@@ -115,9 +115,17 @@ def test_plan_long_context_workload():
 def test_auto_plan_is_consistent(num_sms, B, Hkv, L, W):
     maxp = -(-L // 16)
     plan = pa.pa_plan(B, Hkv * 4, Hkv, 128, 16, maxp * B, maxp, L, W, 0, num_sms)
-    assert plan.partition_size % 16 == 0 and plan.partition_size // 16 <= 256
     span = maxp if W == 0 else min(maxp, -(-(W - 1) // 16) + 1)
-    assert plan.num_partitions == -(-span // (plan.partition_size // 16))
+    if plan.balanced:
+        # work-balanced: X CTAs per KV head over the batch; any lengths within
+        # the bound fit X partitions of at most 2048 pages
+        X = plan.balanced
+        assert B >= 2 and plan.num_partitions == X and X > B
+        assert B * span <= 2048 * (X - B)
+        assert plan.partition_size // 16 == max(8, -(-(B * span) // (X - B)))
+    else:
+        assert plan.partition_size % 16 == 0 and plan.partition_size // 16 <= 256
+        assert plan.num_partitions == -(-span // (plan.partition_size // 16))
     if plan.num_partitions == 1:
         assert plan.workspace_bytes == 256
     # The window bound covers every placement of the window.
@@ -133,7 +141,7 @@ def test_auto_plan_is_consistent(num_sms, B, Hkv, L, W):
     ((1, 8, 8, 128, 16, 10, 10, 100, 0, 24, 152), binding.PA_ERR_INVALID_ARG),  # S % 16
     ((1, 8, 8, 128, 16, 10, 10, 161, 0, 0, 152), binding.PA_ERR_INVALID_ARG),   # Lmax > table
     ((1, 18, 2, 128, 16, 10, 10, 100, 0, 0, 152), binding.PA_ERR_UNSUPPORTED),  # g = 9
-    ((1, 8, 8, 128, 16, 10, 10, 100, 0, 8192, 152), binding.PA_ERR_UNSUPPORTED),  # S > 256 pages
+    ((1, 8, 8, 128, 16, 10, 10, 100, 0, 32784, 152), binding.PA_ERR_UNSUPPORTED),  # S > 2048 pages
     ((1, 4, 1, 64, 16, 4200, 4200, 65552, 0, 16, 152), binding.PA_ERR_UNSUPPORTED),  # 4097 partitions
     ((-1, 8, 8, 128, 16, 10, 10, 100, 0, 0, 152), binding.PA_ERR_INVALID_ARG),
     ((1, 8, 8, 128, 16, 10, 10, 100, -1, 0, 152), binding.PA_ERR_INVALID_ARG),
@@ -142,6 +150,21 @@ def test_plan_rejects(args, status):
     with pytest.raises(pa.PAError) as e:
         pa.pa_plan(*args)
     assert e.value.status == status
+
+
+def test_partition_size_limits_per_kernel():
+    # A tensor-core CTA stages up to 2048 page ids, a CUDA-core CTA 256.
+    ok = pa.pa_plan_ex(1, 8, 8, 128, 16, 4096, 4096, 65536, 0, 2048 * 16, 152)
+    assert ok.partition_size == 2048 * 16 and ok.num_partitions == 2
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_plan_ex(1, 8, 8, 128, 16, 4096, 4096, 65536, 0, 257 * 16, 152,
+                      kernel=binding.PA_KERNEL_SIMT)
+    assert e.value.status == binding.PA_ERR_UNSUPPORTED
+    simt = pa.pa_plan_ex(1, 8, 8, 128, 16, 4096, 4096, 65536, 0, 256 * 16, 152,
+                         kernel=binding.PA_KERNEL_SIMT)
+    simt.partition_size = 512 * 16
+    simt.num_partitions = 8
+    assert _call_decode(simt) == binding.PA_ERR_INVALID_ARG
 
 
 def _call_decode(plan, **over):
@@ -320,6 +343,11 @@ def test_plan_picks_the_cluster_merge_for_one_wave_splits():
     assert pa.pa_plan_ex(4, 8, 4, 256, 16, 3000, 512, 8192, 4096, 512, 152).cluster == 0
     # A short context stays unsplit.
     assert pa.pa_plan_ex(1, 4, 1, 64, 16, 64, 16, 256, 0, 0, 152).cluster == 0
+    # An explicit SM count other than the measured part's scales the table's
+    # fill fraction: on 76 SMs a wave holds 17 clusters of 8 (>= 16 groups)
+    # but only 15 of 9.
+    half = pa.pa_plan_ex(4, 8, 4, 256, 16, 3000, 512, 8192, 4096, 0, 76)
+    assert half.cluster == half.num_partitions == 8
 
 
 def test_cluster_plan_checks_return_before_launch():
@@ -398,3 +426,36 @@ def test_plan_rejects_control_bytes_that_miss_counters():
     over = binding.pa_plan_t.from_buffer_copy(plan)
     over.ctrl_bytes = int(over.workspace_bytes) + 256
     assert _call_decode(over) == binding.PA_ERR_INVALID_ARG
+
+
+def test_balanced_plans():
+    """partition_size = PA_PARTITION_BALANCED: X CTAs per (KV head, head
+    chunk) over the whole batch, one wave, the last-CTA merge."""
+    BAL = binding.PA_PARTITION_BALANCED
+    # the ragged batch-8 shape: 8 groups, 3 CTAs per SM -> 448 of 456 slots
+    p = pa.pa_plan_ex(8, 32, 8, 128, 16, 1250, 256, 4096, 0, BAL, 152)
+    assert p.balanced == 56 and p.num_partitions == 56 and p.ctas == 56 * 8
+    assert p.merge_in_kernel == 1 and p.cluster == 0 and p.parts_per_cta == 1
+    # the largest partition any lengths within the bound can give: 8 x 256 pages over 48
+    assert p.partition_size == 16 * 43
+    assert p.workspace_bytes >= 8 * 32 * 56 * (128 + 2) * 4
+    # none for the CUDA-core kernel, a rotary embedding, more than 128 sequences,
+    # or a bound whose pages could not fit X partitions of 2048 pages
+    for args, kw in (((8, 32, 8, 128, 16, 1250, 256, 4096, 0, BAL, 152),
+                      dict(kernel=binding.PA_KERNEL_SIMT)),
+                     ((8, 32, 8, 128, 16, 1250, 256, 4096, 0, BAL, 152),
+                      dict(rope_theta=10000.0)),
+                     ((129, 8, 2, 64, 16, 9000, 64, 1024, 0, BAL, 152), {}),
+                     ((8, 32, 8, 128, 16, 200000, 16384, 262144, 0, BAL, 152), {})):
+        with pytest.raises(pa.PAError) as e:
+            pa.pa_plan_ex(*args, **kw)
+        assert e.value.status == binding.PA_ERR_UNSUPPORTED, (args, kw)
+    # edits that break the plan's rules are rejected before any launch
+    for field, value in (("merge_in_kernel", 0), ("cluster", 8), ("parts_per_cta", 2),
+                         ("balanced", 8), ("balanced", -1), ("rope_theta", 10000.0),
+                         ("kernel", binding.PA_KERNEL_SIMT)):
+        bad = binding.pa_plan_t.from_buffer_copy(p)
+        setattr(bad, field, value)
+        assert _call_decode(bad) == binding.PA_ERR_INVALID_ARG, (field, value)
+    # a fixed-size plan never sets it
+    assert pa.pa_plan_ex(8, 32, 8, 128, 16, 1250, 256, 4096, 0, 512, 152).balanced == 0

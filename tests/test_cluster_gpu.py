@@ -147,3 +147,23 @@ def test_cluster_plan_validation():
     with pytest.raises(pa.binding.PAError):
         pa.pa_decode(bad, dev["q"], dev["k"], dev["v"], dev["bt"], dev["cl"], case.scale, 0, out,
                      lse, ws)
+
+
+@pytest.mark.parametrize("D,dtype,rope", [(256, 0, 0.0), (128, 0, 0.0), (64, 1, 0.0),
+                                          (96, 0, 0.0), (128, 0, 10000.0), (256, 1, 10000.0)])
+def test_plan_for_this_device_asks_it_and_agrees_with_the_gb300_table(D, dtype, rope):
+    """A plan for the current device (num_sms = 0) takes the clusters a wave
+    holds from cudaOccupancyMaxActiveClusters; a plan for an explicit SM count
+    takes them from the table measured on a 152-SM GB300.  On that part the
+    two must pick the same cluster for every group count: the sweep crosses
+    every cluster size's threshold."""
+    import torch
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the table was measured on the 152-SM GB300")
+    for B in range(1, 161):
+        args = (B, 4, 1, D, 16, 100000, 128, 2048, 0, 0)
+        asked = pa.pa_plan_ex(*args, 0, dtype=dtype, rope_theta=rope)
+        table = pa.pa_plan_ex(*args, 152, dtype=dtype, rope_theta=rope)
+        assert asked.num_sms == 152
+        assert (asked.cluster, asked.num_partitions, asked.partition_size) == \
+            (table.cluster, table.num_partitions, table.partition_size), (B, D, dtype, rope)
