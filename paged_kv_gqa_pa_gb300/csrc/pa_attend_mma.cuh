@@ -715,6 +715,19 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
             s_r64[f] = make_float2(c, sn);
         }
     }
+    // Page ids read together with the length (instances without rotary
+    // embedding, fixed partitions): the length read before the dependency
+    // wait, as a hint, says which block-table entries this CTA will most
+    // likely stage -- its range plus one page either side.  Those entries
+    // are loaded after the wait, in the same round trip as the length
+    // itself, and used only if the length's real range lies inside them
+    // (otherwise they are loaded again).  A decode step moves the range by at
+    // most a page, so this saves one dependent memory round trip per CTA.
+    constexpr bool kSpecIds = !ROPE;
+    constexpr int kSpecLoads = 3;  // per thread: ranges of up to 3 * kThreads entries
+    const bool spec_ids = kSpecIds && !(kBalancedInstance && p.balanced);
+    int len_hint = 0;
+    if (spec_ids) len_hint = __ldcg(p.context_lens + b);
     __syncthreads();  // barriers and rotary tables initialised
     wait_for_prerequisite_grid();
     if (kBalancedInstance && p.balanced) {
@@ -726,7 +739,25 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
         slot = it.part;
     }
 
-    const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, pp);
+    const int len = p.context_lens[b];
+    int spec_lo = 0, spec_n = 0;  // block-table entries [spec_lo, spec_lo + spec_n) of row b
+    int spec[kSpecIds ? kSpecLoads : 1];
+    if (spec_ids) {
+        const SeqSpan hs = seq_span(len_hint, p.window, p.max_ctx, p.maxp, pp);
+        if (hs.valid && part0 < hs.num_parts) {
+            const int a = hs.first_page + part0 * pp;
+            const int n = min(ppc * pp, hs.end_page - a);
+            spec_lo = max(0, a - 1);
+            spec_n = min(p.maxp, a + n + 1) - spec_lo;
+            if (spec_n > kSpecLoads * kThreads) spec_n = 0;
+        }
+#pragma unroll
+        for (int u = 0; u < (kSpecIds ? kSpecLoads : 1); ++u) {
+            const int j = u * kThreads + (int)threadIdx.x;
+            spec[u] = j < spec_n ? p.block_tables[(size_t)b * p.maxp + spec_lo + j] : 0;
+        }
+    }
+    const SeqSpan sp = seq_span(len, p.window, p.max_ctx, p.maxp, pp);
     T* const out = reinterpret_cast<T*>(p.out);
     auto fill_rows = [&](int slot, float o_val, float m_val, float l_val, float lse_val) {
         for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
@@ -778,13 +809,32 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     const int pgA = sp.first_page + part0 * pp;           // first page of this CTA
     const int n_range = min(nparts * pp, sp.end_page - pgA);  // pages of this CTA
 
-    for (int j = threadIdx.x; j < n_range; j += kThreads) {
-        int id = p.block_tables[(size_t)b * p.maxp + pgA + j];
-        if (id < 0 || id >= p.num_pages) {
-            s_flag = 1;
-            id = 0;
+    // Stage the CTA's page ids, each checked before any copy (a bad id is
+    // never read through): from the entries loaded with the length when
+    // they cover the range, else loaded now.
+    if (spec_ids && spec_n > 0 && pgA >= spec_lo && pgA + n_range <= spec_lo + spec_n) {
+        const int shift = pgA - spec_lo;
+#pragma unroll
+        for (int u = 0; u < (kSpecIds ? kSpecLoads : 1); ++u) {
+            const int j = u * kThreads + (int)threadIdx.x - shift;
+            if (j >= 0 && j < n_range) {
+                int id = spec[u];
+                if (id < 0 || id >= p.num_pages) {
+                    s_flag = 1;
+                    id = 0;
+                }
+                s_pid[j] = id;
+            }
         }
-        s_pid[j] = id;
+    } else {
+        for (int j = threadIdx.x; j < n_range; j += kThreads) {
+            int id = p.block_tables[(size_t)b * p.maxp + pgA + j];
+            if (id < 0 || id >= p.num_pages) {
+                s_flag = 1;
+                id = 0;
+            }
+            s_pid[j] = id;
+        }
     }
     __syncthreads();
     if (s_flag) {

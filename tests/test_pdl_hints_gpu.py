@@ -46,19 +46,26 @@ def _slack_pages(case):
     return np.array(sorted(set(range(case.num_pages)) - used), dtype=np.int32)
 
 
-@pytest.mark.parametrize("lens_change", [False, True])
+# lens_delta: how far the old lengths (the hints) lie from the real ones.  The
+# kernel stages the block-table entries of the hint's range plus a page on
+# either side together with the real length: with a window, 5 tokens keep the
+# real range inside them (the entries are reused, shifted), 37 tokens move it
+# out (they are loaded again).
+@pytest.mark.parametrize("window", [0, 1000])
+@pytest.mark.parametrize("lens_delta", [0, 5, 37])
 @pytest.mark.parametrize("plan_kind", ["cluster", "merge_kernel", "unsplit"])
-def test_stale_hints_are_replaced(writer, lens_change, plan_kind):
+def test_stale_hints_are_replaced(writer, lens_delta, plan_kind, window):
     ensure_built()
     lens = [3000, 1200, 2049, 77]
-    case = workloads.make_case("pdl", len(lens), 16, 4, 128, lens, seed=1500, q_std=2.0)
+    case = workloads.make_case("pdl", len(lens), 16, 4, 128, lens, seed=1500, q_std=2.0,
+                               window=window)
     slack = _slack_pages(case)
     assert len(slack) > 0
     # The old values: every table entry a NaN slack page, lengths near the cap.
     old_bt = slack[np.arange(case.block_tables.size) % len(slack)].reshape(case.block_tables.shape)
     old_cl = case.context_lens.copy()
-    if lens_change:
-        old_cl = np.minimum(old_cl + 37, case.max_context_len).astype(np.int32)
+    if lens_delta:
+        old_cl = np.minimum(old_cl + lens_delta, case.max_context_len).astype(np.int32)
     dev = to_device(case)
     new_bt, new_cl = dev["bt"].clone(), dev["cl"].clone()
     dev["bt"].copy_(torch.from_numpy(old_bt))
@@ -66,7 +73,8 @@ def test_stale_hints_are_replaced(writer, lens_change, plan_kind):
     B, Hq, D = case.q.shape
     S = {"cluster": 256, "merge_kernel": 96, "unsplit": 4096}[plan_kind]
     plan = pa.pa_plan(B, Hq, case.Hkv, D, 16, case.num_pages, case.max_pages_per_seq,
-                      case.max_context_len, 0, S, torch.cuda.get_device_properties(0).multi_processor_count)
+                      case.max_context_len, window, S,
+                      torch.cuda.get_device_properties(0).multi_processor_count)
     if plan_kind == "cluster":
         plan.cluster, plan.parts_per_cta, plan.merge_in_kernel = plan.num_partitions, 1, 0
         assert 2 <= plan.num_partitions <= 16
@@ -80,10 +88,10 @@ def test_stale_hints_are_replaced(writer, lens_change, plan_kind):
     assert writer.launch_delayed_copy(new_bt.data_ptr(), dev["bt"].data_ptr(), new_bt.numel(),
                                       new_cl.data_ptr(), dev["cl"].data_ptr(), new_cl.numel(),
                                       20000, stream.cuda_stream) == 0
-    pa.pa_decode(plan, dev["q"], dev["k"], dev["v"], dev["bt"], dev["cl"], case.scale, 0, out, lse,
-                 ws, stream)
+    pa.pa_decode(plan, dev["q"], dev["k"], dev["v"], dev["bt"], dev["cl"], case.scale, window,
+                 out, lse, ws, stream)
     assert pa.pa_get_error(ws) == 0
     torch.cuda.synchronize()
     assert torch.equal(dev["bt"], new_bt) and torch.equal(dev["cl"], new_cl)
     assert_matches_oracle(case, out.double().cpu().numpy(), lse.double().cpu().numpy(),
-                          what=f"stale hints {plan_kind} lens_change={lens_change}")
+                          what=f"stale hints {plan_kind} lens_delta={lens_delta} window={window}")
