@@ -109,6 +109,21 @@ def kv_bytes(case) -> int:
     return 2 * ELEM_BYTES[case.dtype] * case.Hkv * case.D * attended_tokens(case)
 
 
+GB300_L2_BYTES = 129 * 10**6  # nominal L2 of one GB300 (the GPU arm asks its device)
+
+
+def workload_config(case, world: int, l2_bytes: int) -> dict:
+    """The `config` of the JSON line: the workload's shapes and how the L2 is
+    handled, the same dict for both arms of a run."""
+    big = kv_bytes(case) > 2 * l2_bytes
+    return {"workload": case.name, "batch": case.B, "num_q_heads": case.Hq,
+            "num_kv_heads": case.Hkv, "head_dim": case.D, "page_size": case.page_size,
+            "context_lens": "x".join(str(int(x)) for x in sorted(set(case.context_lens.tolist()))),
+            "window": case.window, "kv_bytes_per_step": kv_bytes(case),
+            "l2": "inputs larger than L2" if big else "L2 flushed between steps",
+            "parallelism": f"replicas x{world}"}
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -654,7 +669,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": statistics.median(secs) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "device": "host CPU (oracle)", "l2": "host CPU"},
+        "config": workload_config(case, world, GB300_L2_BYTES),
+        "device": "host CPU (oracle)",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -808,14 +824,8 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": ms_max, "us_per_step": ms_max * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
             "data": "synthetic",
-            "config": {"workload": args.workload, "batch": case.B, "num_q_heads": case.Hq,
-                       "num_kv_heads": case.Hkv, "head_dim": case.D, "page_size": case.page_size,
-                       "context_lens": "x".join(str(int(x)) for x in
-                                                sorted(set(case.context_lens.tolist()))),
-                       "window": case.window, "partition_size": arm.plan.partition_size,
-                       "partitions": arm.plan.num_partitions, "kv_bytes_per_step": byts,
-                       "l2": "inputs larger than L2" if big else "L2 flushed between steps",
-                       "parallelism": f"replicas x{world}"},
+            "config": workload_config(case, world, l2),
+            "plan": plan_summary(arm.plan),
             "roofline": {"bound": "hbm", "achieved": kern_gbs, "peak": peak, "unit": "GB/s",
                          "frac": kern_gbs / peak, "traffic": traffic,
                          "peak_kind": peak_kind,
