@@ -143,12 +143,16 @@ typedef struct pa_plan {
                                b gets max(1, ceil(pages_b / pp)) CTAs, so a long
                                sequence gets more CTAs than a short one.  Its partials
                                are merged by the last CTA of each group
-                               (merge_in_kernel = 1, cluster 0, parts_per_cta 1).
+                               (merge_in_kernel = 1, the choice pa_plan_ex makes) or
+                               by the merge kernel (0); cluster 0, parts_per_cta 1.
                                num_partitions then holds X (the most partials a
                                sequence can have) and partition_size the largest pp
                                any lengths within max_context_len can give.  Set by
-                               pa_plan_ex (partition_size PA_PARTITION_BALANCED, or
-                               its automatic choice); 0 = fixed-size partitions */
+                               pa_plan_ex: with partition_size PA_PARTITION_BALANCED,
+                               or automatically for a batch of several sequences
+                               whose automatic plan would be a fixed split (not a
+                               cluster merge, not unsplit); 0 = fixed-size
+                               partitions */
 } pa_plan_t;
 
 /* pa_plan / pa_plan_ex partition_size: work-balanced partitions sized on the

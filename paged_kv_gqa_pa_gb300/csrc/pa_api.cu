@@ -311,6 +311,7 @@ cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 
 // griddepcontrol.wait before touching the workspace.
 // ---------------------------------------------------------------------------
 constexpr int kMergeThreads = 128;
+static_assert(kMergeThreads == kThreads, "balanced_pp sums over kWarps warps");
 constexpr int kMergeCols = 16;                          // float4 columns per CTA (64 dims)
 constexpr int kMergeGroups = kMergeThreads / kMergeCols;  // partition groups (8)
 
@@ -361,7 +362,16 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergePara
     const size_t row0 = bh * p.P;
     allow_dependent_launch();  // the next call's partition grid may be scheduled now
     wait_for_prerequisite_grid();
-    const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, p.pages_per_part);
+    int pages_per_part = p.pages_per_part;
+    if (p.balanced) {  // the partition size the partition kernel chose from the lengths
+        __shared__ int s_bal[kWarps];
+        const int t = threadIdx.x;
+        const int pages = t < p.B ? balanced_seq_pages(p.context_lens[t], p.window, p.max_ctx,
+                                                       p.maxp)
+                                  : 0;
+        pages_per_part = balanced_pp(pages, p.B, p.balanced, s_bal);
+    }
+    const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, pages_per_part);
     T* orow = reinterpret_cast<T*>(p.out) + bh * D + d0;
     const int ncols = min(kMergeCols * 4, D - d0);  // a 96-dim head ends in a half chunk
     if (!sp.valid) {
@@ -550,7 +560,7 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     if (page_size != kPageSize) return PA_ERR_UNSUPPORTED;
     bool want_balanced = partition_size == PA_PARTITION_BALANCED;
     if (want_balanced) partition_size = 0;
-    bool one_wave_split = false;  // the automatic fixed split fits one wave
+    bool auto_split = false;  // the automatic plan is a whole-wave fixed split
     if (partition_size % page_size != 0) return PA_ERR_INVALID_ARG;
 
     const int g = num_q_heads / num_kv_heads;
@@ -635,24 +645,23 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
                 long long parts = waves * fill / groups;
                 if (parts < 1) parts = 1;
                 pp = (int)((span + parts - 1) / parts);
-                if (pp <= kMaxPagesPerPart) {
-                    one_wave_split = waves == 1;
-                    break;
-                }
+                if (pp <= kMaxPagesPerPart) break;
             }
             if (pp < kMinPagesPerPart) pp = kMinPagesPerPart;
+            auto_split = true;
         }
         if (pp > kMaxPagesPerPart) pp = kMaxPagesPerPart;
     }
-    // A batch whose automatic split is one wave takes work-balanced
-    // partitions: the host knows only the bound on the lengths, and a fixed
-    // split sized for it leaves the CTAs of short sequences idle while the long
-    // ones stream.  Measured on GB300 (B = 4, 32 query / 8 KV heads, head dim
-    // 128, lengths {100, 200, 300, 50000}): 54.7 us with fixed partitions,
-    // 39.1 us balanced; on uniform lengths the two are within 2 %.  (Short
-    // contexts keep the cluster merge: the last-CTA merge balanced plans use
-    // costs about 2 us more than it.)
-    if (!want_balanced && partition_size == 0 && one_wave_split && batch >= 2 && bal_x > 0)
+    // A batch of several sequences whose automatic plan is a fixed split
+    // takes work-balanced partitions instead: the host knows only the bound
+    // on the lengths, and a split sized for it leaves the CTAs of short
+    // sequences idle while the long ones stream.  Measured on GB300 (32 query
+    // / 8 KV heads, head dim 128): lengths {100, 200, 300, 50000} 54.7 ->
+    // 39.1 us, {100000, 500, 800, 20} 82.1 -> 68.4 us, eight lengths up to
+    // 64K 174.4 -> 170.9 us; uniform lengths lose 1-2 % (4 x 100000: 236.0 ->
+    // 240.5 us).  Short contexts keep the cluster merge: the last-CTA merge
+    // that balanced plans use costs about 2 us more than it.
+    if (!want_balanced && partition_size == 0 && auto_split && batch >= 2 && bal_x > 0)
         want_balanced = true;
     if (want_balanced) {
         // the largest partition any lengths within max_context_len can give
@@ -796,12 +805,14 @@ static int check_plan(const pa_plan_t* plan) {
         return PA_ERR_INVALID_ARG;
     if (plan->balanced < 0) return PA_ERR_INVALID_ARG;
     if (plan->balanced > 0) {
-        // Work-balanced partitions: the last-CTA merge, one partition per CTA,
-        // no cluster, one load of all B lengths per CTA, and no partition
-        // longer than kMaxStagedPages for lengths within the plan's bound.
+        // Work-balanced partitions: one partition per CTA, no cluster, one
+        // load of all B lengths per CTA, and no partition longer than
+        // kMaxStagedPages for lengths within the plan's bound.  Either merge:
+        // the last CTA of each group, or the merge kernel (which works out
+        // the same partition size from the lengths).
         const int X = plan->balanced;
         const int span = attended_span_pages(plan->max_context_len, plan->window);
-        if (plan->kernel != PA_KERNEL_MMA || !plan->merge_in_kernel || plan->cluster > 1 ||
+        if (plan->kernel != PA_KERNEL_MMA || plan->cluster > 1 ||
             plan->parts_per_cta != 1 || B > kMaxBalancedBatch || X <= B ||
             plan->num_partitions != X || plan->rope_theta > 0.f ||
             (long long)B * span > (long long)kMaxStagedPages * (X - B))
@@ -975,6 +986,7 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
     p.max_ctx = plan->max_context_len;
     p.window = plan->window;
     p.dtype = plan->dtype;
+    p.balanced = plan->balanced;
     if (launch_merge(D, p, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return PA_ERR_CUDA;

@@ -522,35 +522,15 @@ __device__ __forceinline__ void prefetch_first_pages(const AttendParams& p, int 
 
 // Work-balanced partitions (plan.balanced = X > 0): the X CTAs along grid.x
 // of a (KV head, head chunk) share the whole batch, so that a long sequence
-// gets more CTAs than a short one.  With pages_b the attended pages of
-// sequence b (0 for a length out of bounds), every sequence gets
-// n_b(pp) = max(1, ceil(pages_b / pp)) consecutive CTAs, in batch order, and
-// pp is the smallest partition size with sum_b n_b(pp) <= X, found by
-// bisection between ceil(T / X) and ceil(T / (X - B)) (T = sum_b pages_b;
-// the upper end always fits, since sum_b n_b <= T / pp + B), clamped to
-// [kMinBalancedPages, kMaxStagedPages] (the plan guarantees the clamp never
-// binds for lengths within its bound).  Every CTA computes this map from the
-// same B lengths (one load per thread, B <= kThreads) and takes the
-// (sequence, partition) item its x falls in; with x >= sum_b n_b it has none.
-// `hint`: lengths read with L2-only loads, for the prefetch addresses before
-// the dependency wait (they may be stale).
+// gets more CTAs than a short one.  With pp from balanced_pp, sequence b gets
+// n_b = max(1, ceil(pages_b / pp)) consecutive CTAs, in batch order.  Every
+// CTA computes this map from the same B lengths (one load per thread, B <=
+// kThreads) and takes the (sequence, partition) item its x falls in; with
+// x >= sum_b n_b it has none.  `hint`: lengths read with L2-only loads, for
+// the prefetch addresses before the dependency wait (they may be stale).
 struct BalancedItem {
     int b, part, pp;
 };
-
-// Sum over the CTA's threads of v (all threads call it; s_red: kWarps ints).
-__device__ __forceinline__ int cta_sum(int v, int* s_red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-    __syncthreads();  // earlier reads of s_red are done
-    if (lane == 0) s_red[warp] = v;
-    __syncthreads();
-    int t = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) t += s_red[w];
-    return t;
-}
 
 __device__ __forceinline__ bool balanced_item(const AttendParams& p, int x, bool hint,
                                               BalancedItem& it) {
@@ -561,22 +541,10 @@ __device__ __forceinline__ bool balanced_item(const AttendParams& p, int x, bool
     int pages = 0;
     if (t < B) {
         const int L = hint ? __ldcg(p.context_lens + t) : p.context_lens[t];
-        const SeqSpan sp = seq_span(L, p.window, p.max_ctx, p.maxp, 1);
-        pages = sp.valid ? sp.end_page - sp.first_page : 0;
+        pages = balanced_seq_pages(L, p.window, p.max_ctx, p.maxp);
     }
     if (t == 0) s_item[0] = -1;
-    const int T = cta_sum(pages, s_red);
-    int lo = max(kMinBalancedPages, (T + X - 1) / X);
-    int hi = max(lo, min((T + (X - B) - 1) / (X - B), kMaxStagedPages));
-    while (lo < hi) {  // (the same bounds in every thread)
-        const int mid = (lo + hi) >> 1;
-        const int need = cta_sum(t < B ? max(1, (pages + mid - 1) / mid) : 0, s_red);
-        if (need <= X)
-            hi = mid;
-        else
-            lo = mid + 1;
-    }
-    const int pp = lo;
+    const int pp = balanced_pp(pages, B, X, s_red);
     const int n = t < B ? max(1, (pages + pp - 1) / pp) : 0;
     int inc = n;  // inclusive scan of n over the CTA
 #pragma unroll

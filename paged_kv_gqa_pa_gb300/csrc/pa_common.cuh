@@ -78,6 +78,7 @@ struct MergeParams {
     unsigned* err;
     int B, Hq, D, P, pages_per_part, maxp, max_ctx, window;
     int dtype;               // PA_DTYPE_*
+    int balanced;            // > 0: work-balanced plan (partition size from the lengths)
 };
 
 // Pipeline depth (pages of K or V in flight per warp) for each head dim; the
@@ -184,6 +185,51 @@ __device__ __forceinline__ SeqSpan seq_span(int L, int window, int max_ctx, int 
     const int np = s.valid ? s.end_page - s.first_page : 0;
     s.num_parts = np > 0 ? (np + pages_per_part - 1) / pages_per_part : 0;
     return s;
+}
+
+// Sum of v over a CTA of kWarps warps (every thread calls it and gets the
+// sum; s_red: kWarps ints of shared memory).
+__device__ __forceinline__ int cta_sum(int v, int* s_red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    __syncthreads();  // earlier reads of s_red are done
+    if (lane == 0) s_red[warp] = v;
+    __syncthreads();
+    int t = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t += s_red[w];
+    return t;
+}
+
+// Work-balanced partitions (plan.balanced = X CTAs per (KV head, head chunk)
+// over the whole batch).  Thread t < B passes the attended pages of sequence
+// t (balanced_seq_pages), every thread gets the partition size pp: the
+// smallest with sum_b max(1, ceil(pages_b / pp)) <= X, by bisection between
+// ceil(T / X) and ceil(T / (X - B)) (T = sum_b pages_b; the upper end always
+// fits since sum_b ceil(pages_b / pp) <= T / pp + B), clamped to
+// [kMinBalancedPages, kMaxStagedPages] (the plan guarantees the clamp never
+// binds for lengths within its bound).  The partition kernel and the merge
+// kernel compute the same pp from the same lengths.
+__device__ __forceinline__ int balanced_seq_pages(int L, int window, int max_ctx, int maxp) {
+    const SeqSpan sp = seq_span(L, window, max_ctx, maxp, 1);
+    return sp.valid ? sp.end_page - sp.first_page : 0;  // (0 for a length out of bounds)
+}
+
+__device__ __forceinline__ int balanced_pp(int pages, int B, int X, int* s_red) {
+    const int t = threadIdx.x;
+    const int T = cta_sum(t < B ? pages : 0, s_red);
+    int lo = max(kMinBalancedPages, (T + X - 1) / X);
+    int hi = max(lo, min((T + (X - B) - 1) / (X - B), kMaxStagedPages));
+    while (lo < hi) {  // (the same bounds in every thread)
+        const int mid = (lo + hi) >> 1;
+        const int need = cta_sum(t < B ? max(1, (pages + mid - 1) / mid) : 0, s_red);
+        if (need <= X)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return lo;
 }
 
 // ---------------------------------------------------------------------------

@@ -451,7 +451,7 @@ def test_balanced_plans():
             pa.pa_plan_ex(*args, **kw)
         assert e.value.status == binding.PA_ERR_UNSUPPORTED, (args, kw)
     # edits that break the plan's rules are rejected before any launch
-    for field, value in (("merge_in_kernel", 0), ("cluster", 8), ("parts_per_cta", 2),
+    for field, value in (("cluster", 8), ("parts_per_cta", 2),
                          ("balanced", 8), ("balanced", -1), ("rope_theta", 10000.0),
                          ("kernel", binding.PA_KERNEL_SIMT)):
         bad = binding.pa_plan_t.from_buffer_copy(p)

@@ -8,7 +8,8 @@ sequence's partials are merged by its last CTA.  These tests force such plans
 corners: ragged lengths with empty and single-token sequences, windows, one
 long sequence among short ones (more partials than one load round of the
 last-CTA merge takes), the largest batch the mapping spreads, bf16, bad page
-ids and lengths, and a copy timeout."""
+ids and lengths, and a copy timeout; with either merge (the last CTA of each
+group, or the merge kernel working out the same partition size)."""
 import numpy as np
 import pytest
 
@@ -30,37 +31,44 @@ def tensor_core_kernel():
     gpu_helpers.KERNEL = None
 
 
-def _check_plan(plan, B):
+def _check_plan(plan, B, fused=None):
     assert plan.balanced > B and plan.num_partitions == plan.balanced
-    assert plan.merge_in_kernel == 1 and plan.cluster == 0 and plan.parts_per_cta == 1
+    assert plan.cluster == 0 and plan.parts_per_cta == 1
+    if fused is not None:
+        assert plan.merge_in_kernel == fused
 
 
-def test_ragged_workload_full_size():
+# Both merges: the last CTA of each group (fused 1), or the merge kernel,
+# which works out the same partition size from the lengths (fused 0).
+@pytest.mark.parametrize("fused", [1, 0])
+def test_ragged_workload_full_size(fused):
     case = workloads.workload("batch8_ragged_d128")
-    out, lse, err, plan = run_gpu(case, partition_size=BAL, guard=64)
+    out, lse, err, plan = run_gpu(case, partition_size=BAL, guard=64, merge_in_kernel=fused)
     assert err == 0
-    _check_plan(plan, case.B)
+    _check_plan(plan, case.B, fused)
     assert_matches_oracle(case, out, lse, what="balanced batch8_ragged_d128")
 
 
+@pytest.mark.parametrize("fused", [1, 0])
 @pytest.mark.parametrize("window", [0, 1000])
-def test_ragged_with_empty_and_unit_sequences(window):
+def test_ragged_with_empty_and_unit_sequences(window, fused):
     lens = [0, 1, 4096, 17, 0, 1000, 2, 3333]
     case = workloads.make_case("r", len(lens), 32, 8, 128, lens, seed=1400, window=window)
-    out, lse, err, plan = run_gpu(case, partition_size=BAL, guard=64)
+    out, lse, err, plan = run_gpu(case, partition_size=BAL, guard=64, merge_in_kernel=fused)
     assert err == 0
-    _check_plan(plan, case.B)
+    _check_plan(plan, case.B, fused)
     assert np.all(out[[0, 4]] == 0) and np.all(np.isneginf(lse[[0, 4]]))
     assert_matches_oracle(case, out, lse, what=f"balanced ragged, window {window}")
 
 
-def test_one_long_sequence_many_partials():
+@pytest.mark.parametrize("fused", [1, 0])
+def test_one_long_sequence_many_partials(fused):
     # Nearly all of the grid goes to the long sequence: its partials exceed
     # one load round of the last-CTA merge (24 per thread at one thread per item).
     case = workloads.make_case("long1", 3, 32, 8, 128, [1, 60000, 5], seed=1401)
-    out, lse, err, plan = run_gpu(case, partition_size=BAL)
+    out, lse, err, plan = run_gpu(case, partition_size=BAL, merge_in_kernel=fused)
     assert err == 0
-    _check_plan(plan, case.B)
+    _check_plan(plan, case.B, fused)
     pages = -(-60000 // 16)
     pp = -(-(pages + 2) // (plan.balanced - 3))
     assert -(-pages // pp) > 24
@@ -77,11 +85,12 @@ def test_head_dims_and_groups(D, Hq, Hkv):
     assert_matches_oracle(case, out, lse, what=f"balanced D{D}")
 
 
-def test_largest_batch():
+@pytest.mark.parametrize("fused", [1, 0])
+def test_largest_batch(fused):
     rng = np.random.default_rng(1403)
     lens = rng.integers(0, 600, size=128).tolist()
     case = workloads.make_case("b128", 128, 8, 2, 64, lens, seed=1404)
-    out, lse, err, plan = run_gpu(case, partition_size=BAL)
+    out, lse, err, plan = run_gpu(case, partition_size=BAL, merge_in_kernel=fused)
     assert err == 0
     _check_plan(plan, case.B)
     assert_matches_oracle(case, out, lse, what="balanced, 128 sequences")
@@ -97,14 +106,16 @@ def test_bf16_window():
     assert_matches_oracle(case, out, lse, what="balanced bf16 window")
 
 
-def test_bad_page_and_bad_length_only_poison_their_sequence():
+@pytest.mark.parametrize("fused", [1, 0])
+def test_bad_page_and_bad_length_only_poison_their_sequence(fused):
     lens = [700, 1200, 90, 2000]
     case = workloads.make_case("badb", 4, 8, 2, 128, lens, seed=1406)
     ref_out, ref_lse = oracle.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
                                      case.context_lens, case.scale, case.window)
     orig = int(case.block_tables[1, 5])
     case.block_tables[1, 5] = case.num_pages
-    out, lse, err, plan = run_gpu(case, partition_size=BAL, max_context_len=2000)
+    out, lse, err, plan = run_gpu(case, partition_size=BAL, max_context_len=2000,
+                                  merge_in_kernel=fused)
     _check_plan(plan, case.B)
     assert err & binding.PA_DEVERR_BAD_PAGE
     assert np.isnan(out[1]).all() and np.isnan(lse[1]).all()
@@ -113,7 +124,8 @@ def test_bad_page_and_bad_length_only_poison_their_sequence():
     assert gpu_helpers.rel_l2(out[good], ref_out[good]) <= gpu_helpers.REL_L2_TOL
     # A length beyond the plan's bound: that sequence is NaN, the rest exact.
     case.block_tables[1, 5] = orig
-    out, lse, err, plan = run_gpu(case, partition_size=BAL, max_context_len=1500)
+    out, lse, err, plan = run_gpu(case, partition_size=BAL, max_context_len=1500,
+                                  merge_in_kernel=fused)
     assert err & binding.PA_DEVERR_BAD_LENGTH
     assert np.isnan(out[3]).all() and np.isnan(lse[3]).all()
     good = [0, 1, 2]
