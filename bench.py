@@ -432,6 +432,23 @@ def time_flushed(arm, iters, flush):
     return statistics.median(res), statistics.median(host)
 
 
+def host_us_prepared(arm, calls=200):
+    """Host microseconds per launch through a prepared pa_decode (arguments
+    checked once; the C call alone per step), averaged over `calls` calls
+    issued back to back."""
+    torch = arm.torch
+    call = arm.pa.prepare_decode(arm.plan, arm.q, arm.k, arm.v, arm.bt, arm.cl, arm.case.scale,
+                                 arm.case.window, arm.out, arm.lse, arm.ws, arm.stream)
+    call()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        call()
+    t1 = time.perf_counter()
+    torch.cuda.synchronize()
+    return (t1 - t0) * 1e6 / calls
+
+
 def time_graph_rotating(case, device, kernel, min_steps=40, max_copies=64,
                         max_bytes=4 << 30, partition_size=None):
     """Steps captured in one CUDA graph, cycling over C copies of the K/V pools so
@@ -778,6 +795,7 @@ def run_gpu(args):
                 # (by reading) before each
                 earm = GpuArm(c, device, kernel=kname)
                 eager_ms, host_us = time_flushed(earm, args.per_workload_iters, wl_flush)
+                prep_us = host_us_prepared(earm)
                 earm.check_error()
                 del earm
                 entry[kname] = {"us_per_step": us, "partition_kernel_us": kus,
@@ -785,6 +803,7 @@ def run_gpu(args):
                                 "single_call_us": eager_ms * 1e3,
                                 "single_call_kv_gbs": b / (eager_ms * 1e-3) / 1e9,
                                 "host_us_in_pa_decode": host_us,
+                                "host_us_prepared_call": prep_us,
                                 "frac_of_measured_hbm": b / (us * 1e-6) / 1e9 / peak,
                                 "frac_of_nominal_8tbs": b / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS,
                                 "plan": plan_summary(plan)}

@@ -7,8 +7,8 @@ generator) imports without a GPU.
 """
 from .binding import (PAError, decode, load, new_workspace, pa_decode, pa_decode_partitions,
                       pa_decode_static, pa_get_error, pa_get_error_ex, pa_merge, pa_plan,
-                      pa_plan_ex, pa_plan_t, pa_status_string, pa_version)
+                      pa_plan_ex, pa_plan_t, pa_status_string, pa_version, prepare_decode)
 
 __all__ = ["PAError", "decode", "load", "new_workspace", "pa_decode", "pa_decode_partitions",
            "pa_decode_static", "pa_get_error", "pa_get_error_ex", "pa_merge", "pa_plan",
-           "pa_plan_ex", "pa_plan_t", "pa_status_string", "pa_version"]
+           "pa_plan_ex", "pa_plan_t", "pa_status_string", "pa_version", "prepare_decode"]

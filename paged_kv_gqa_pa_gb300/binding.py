@@ -201,6 +201,37 @@ def pa_decode(plan, q, k_cache, v_cache, block_tables, context_lens, scale, wind
         raise PAError("pa_decode", st)
 
 
+class PreparedDecode:
+    """pa_decode with its arguments checked and converted once.
+
+    A decode loop calls pa_decode with the same buffers every step (their
+    contents change, their addresses do not).  This object keeps the checked
+    ctypes arguments and the plan, so each call is the C call alone: a few
+    microseconds of host time instead of the per-tensor checks of pa_decode.
+    The tensors must stay alive and in place while it is used."""
+
+    def __init__(self, plan, q, k_cache, v_cache, block_tables, context_lens, scale, window, out,
+                 lse, workspace, stream=None):
+        self.plan = pa_plan_t.from_buffer_copy(plan)  # the plan as it was when prepared
+        self._keep = (q, k_cache, v_cache, block_tables, context_lens, out, lse, workspace)
+        args = _decode_args(self.plan, q, k_cache, v_cache, block_tables, context_lens, scale,
+                            window, out, lse, workspace, stream)
+        self._fn = load().pa_decode
+        self._args = args
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != PA_OK:
+            raise PAError("pa_decode", st)
+
+
+def prepare_decode(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window, out, lse,
+                   workspace, stream=None) -> PreparedDecode:
+    """Check and convert pa_decode's arguments once; calling the result launches."""
+    return PreparedDecode(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window,
+                          out, lse, workspace, stream)
+
+
 def pa_decode_partitions(plan, q, k_cache, v_cache, block_tables, context_lens, scale, window,
                          out, lse, workspace, stream=None) -> None:
     st = load().pa_decode_partitions(*_decode_args(plan, q, k_cache, v_cache, block_tables,
