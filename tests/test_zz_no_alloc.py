@@ -13,7 +13,8 @@ results must be bitwise equal -- and against the fp64 oracle.  Calls follow
 each other with different plans, so each finds the previous call's contents
 still in the shared scratch: partials of another layout, a device error word
 left set by a timed-out call.  Every merge kind is covered (merge kernel,
-last-CTA merge with its arrival counters, cluster merge).
+last-CTA merge with its arrival counters, a work-balanced plan, cluster
+merge).
 
 The file is named to be collected last, so that a stop-at-first-failure run
 has already run every other test when it gets here."""
@@ -105,7 +106,8 @@ def test_static_scratch_matches_workspace_path_two_calls(kernel):
 
 
 def test_static_scratch_every_merge_kind_in_a_row():
-    """Merge kernel, last-CTA merge (arrival counters in the shared array) and
+    """Merge kernel, last-CTA merge (arrival counters in the shared array),
+    work-balanced plan (partials of the whole batch spread over its CTAs) and
     cluster merge, one after another on the same scratch, the last one through
     the Python wrapper."""
     ensure_built()
@@ -113,8 +115,10 @@ def test_static_scratch_every_merge_kind_in_a_row():
     plans = {
         "merge_kernel": _plan(case, 64, cluster=0, merge_in_kernel=0),
         "last_cta_merge": _plan(case, 128, cluster=0, merge_in_kernel=1),
+        "balanced": _plan(case, binding.PA_PARTITION_BALANCED),
         "cluster_merge": _plan(case, 128, merge_in_kernel=0, parts_per_cta=1),
     }
+    assert plans["balanced"].balanced > 0
     plans["cluster_merge"].cluster = plans["cluster_merge"].num_partitions
     assert 2 <= plans["cluster_merge"].cluster <= 16
     assert plans["last_cta_merge"].num_partitions <= 8
