@@ -212,7 +212,8 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
  * allocated).  They hold the device error word and per-group arrival
  * counters; every call leaves the counters zero again, and the error word
  * keeps its bits until read with pa_get_error_ex(clear = 1).  The rest holds
- * the partition partials between the kernels.  A workspace reused with a
+ * the partition partials between the kernels (and, for a work-balanced plan,
+ * the partition size its partition kernel chose).  A workspace reused with a
  * different plan must have the new plan's ctrl_bytes zeroed first (the
  * counters may then lie where the old plan kept partials).  Concurrent calls
  * must not share a workspace.

@@ -311,7 +311,6 @@ cudaError_t launch_attend(int D, int G, bool split, const AttendParams& p, dim3 
 // griddepcontrol.wait before touching the workspace.
 // ---------------------------------------------------------------------------
 constexpr int kMergeThreads = 128;
-static_assert(kMergeThreads == kThreads, "balanced_pp sums over kWarps warps");
 constexpr int kMergeCols = 16;                          // float4 columns per CTA (64 dims)
 constexpr int kMergeGroups = kMergeThreads / kMergeCols;  // partition groups (8)
 
@@ -362,15 +361,9 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergePara
     const size_t row0 = bh * p.P;
     allow_dependent_launch();  // the next call's partition grid may be scheduled now
     wait_for_prerequisite_grid();
-    int pages_per_part = p.pages_per_part;
-    if (p.balanced) {  // the partition size the partition kernel chose from the lengths
-        __shared__ int s_bal[kWarps];
-        const int t = threadIdx.x;
-        const int pages = t < p.B ? balanced_seq_pages(p.context_lens[t], p.window, p.max_ctx,
-                                                       p.maxp)
-                                  : 0;
-        pages_per_part = balanced_pp(pages, p.B, p.balanced, s_bal);
-    }
+    // A work-balanced plan: the partition size the partition kernel chose from
+    // the lengths, which it left in the workspace's info block.
+    const int pages_per_part = p.balanced ? *p.ws_info : p.pages_per_part;
     const SeqSpan sp = seq_span(p.context_lens[b], p.window, p.max_ctx, p.maxp, pages_per_part);
     T* orow = reinterpret_cast<T*>(p.out) + bh * D + d0;
     const int ncols = min(kMergeCols * 4, D - d0);  // a 96-dim head ends in a half chunk
@@ -479,23 +472,28 @@ cudaError_t launch_merge(int D, const MergeParams& p, cudaStream_t stream) {
 // block's first word is the device error word; it and the counters
 // (ctrl_bytes in all) must start at zero and are left at zero by every call.
 struct WsLayout {
-    size_t ctr_off, ctrl_bytes, m_off, l_off, o_off, total;
+    size_t ctr_off, ctrl_bytes, info_off, m_off, l_off, o_off, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// groups = B * Hkv * head chunks (one arrival counter each).
-static WsLayout ws_layout(int B, int Hq, int D, int P, int R, long long groups) {
+// groups = B * Hkv * head chunks (one arrival counter each).  balanced: a
+// work-balanced plan, whose partition kernel leaves the partition size it
+// chose in a 256-byte info block behind the control bytes for the merge
+// kernel (it need not be zero and is not part of ctrl_bytes).
+static WsLayout ws_layout(int B, int Hq, int D, int P, int R, long long groups,
+                          bool balanced = false) {
     WsLayout w;
     w.ctr_off = kCtrlBytes;
     if (P <= 1) {
-        w.ctrl_bytes = w.m_off = w.l_off = w.o_off = kCtrlBytes;
+        w.ctrl_bytes = w.info_off = w.m_off = w.l_off = w.o_off = kCtrlBytes;
         w.total = kCtrlBytes;
         return w;
     }
     const size_t rows = (size_t)B * Hq * R;
     w.ctrl_bytes = kCtrlBytes + align256((size_t)groups * 4);
-    w.m_off = w.ctrl_bytes;
+    w.info_off = w.ctrl_bytes;
+    w.m_off = w.info_off + (balanced ? 256 : 0);
     w.l_off = w.m_off + align256(rows * 4);
     w.o_off = w.l_off + align256(rows * 4);
     w.total = w.o_off + align256(rows * D * 4);
@@ -690,7 +688,7 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     const long long groups_all = (long long)batch * num_kv_heads * nchunk;
     // Sized for one partial per partition, the most any parts_per_cta needs,
     // so that a caller may lower parts_per_cta in this plan.
-    const WsLayout wl = ws_layout(batch, num_q_heads, head_dim, P, P, groups_all);
+    const WsLayout wl = ws_layout(batch, num_q_heads, head_dim, P, P, groups_all, want_balanced);
     plan->workspace_bytes = wl.total;
     plan->ctrl_bytes = (int)wl.ctrl_bytes;
     plan->kernel = kernel;
@@ -793,7 +791,8 @@ static int check_plan(const pa_plan_t* plan) {
     if (plan->parts_per_cta < 1) return PA_ERR_INVALID_ARG;
     const int R = partials_per_head(plan);
     const WsLayout wl = ws_layout(B, Hq, plan->head_dim, plan->num_partitions, R,
-                                  (long long)B * Hkv * (Hq / Hkv / plan->heads_per_cta));
+                                  (long long)B * Hkv * (Hq / Hkv / plan->heads_per_cta),
+                                  plan->balanced > 0);
     if (plan->workspace_bytes < wl.total) return PA_ERR_INVALID_ARG;
     // The control bytes a caller keeps zero must cover the error word and
     // every arrival counter this plan's launch uses (a plan edited after
@@ -866,7 +865,8 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     const int R = partials_per_head(plan);
     const int nchunk = plan->num_q_heads / plan->num_kv_heads / plan->heads_per_cta;
     const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, D, P, R,
-                                  (long long)plan->batch * plan->num_kv_heads * nchunk);
+                                  (long long)plan->batch * plan->num_kv_heads * nchunk,
+                                  plan->balanced > 0);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     AttendParams p;
     p.q = static_cast<const __half*>(q);
@@ -881,6 +881,7 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     p.ws_o = reinterpret_cast<float*>(ws + wl.o_off);
     p.err = reinterpret_cast<unsigned*>(ws);
     p.counters = reinterpret_cast<unsigned*>(ws + wl.ctr_off);
+    p.ws_info = reinterpret_cast<int*>(ws + wl.info_off);
     p.merge_in_kernel = (plan->kernel == PA_KERNEL_MMA && P > 1 && plan->merge_in_kernel) ? 1 : 0;
     p.cluster = (plan->kernel == PA_KERNEL_MMA && P > 1 && plan->cluster > 1) ? plan->cluster : 0;
     p.B = plan->batch;
@@ -965,7 +966,8 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
     const int nchunk = plan->num_q_heads / plan->num_kv_heads / plan->heads_per_cta;
     const int R = partials_per_head(plan);
     const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, D, plan->num_partitions, R,
-                                  (long long)plan->batch * plan->num_kv_heads * nchunk);
+                                  (long long)plan->batch * plan->num_kv_heads * nchunk,
+                                  plan->balanced > 0);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     MergeParams p;
     p.context_lens = context_lens;
@@ -975,6 +977,7 @@ int pa_merge(const pa_plan_t* plan, const int32_t* context_lens, void* out, floa
     p.out = out;
     p.lse = lse;
     p.err = reinterpret_cast<unsigned*>(ws);
+    p.ws_info = reinterpret_cast<const int*>(ws + wl.info_off);
     p.B = plan->batch;
     p.Hq = plan->num_q_heads;
     p.D = D;
@@ -1043,7 +1046,8 @@ int plan_workspace_extent(const pa_plan_t* plan, size_t* ctrl_bytes, size_t* tot
     const int nchunk = plan->num_q_heads / plan->num_kv_heads / plan->heads_per_cta;
     const WsLayout wl = ws_layout(plan->batch, plan->num_q_heads, plan->head_dim,
                                   plan->num_partitions, partials_per_head(plan),
-                                  (long long)plan->batch * plan->num_kv_heads * nchunk);
+                                  (long long)plan->batch * plan->num_kv_heads * nchunk,
+                                  plan->balanced > 0);
     *ctrl_bytes = wl.ctrl_bytes;
     *total_bytes = wl.total;
     return PA_OK;

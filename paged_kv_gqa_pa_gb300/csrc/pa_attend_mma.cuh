@@ -700,7 +700,10 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
     wait_for_prerequisite_grid();
     if (kBalancedInstance && p.balanced) {
         BalancedItem it;
-        if (!balanced_item(p, blockIdx.x, false, it)) return;  // more CTAs than items
+        const bool has_item = balanced_item(p, blockIdx.x, false, it);
+        // (every CTA finds the same partition size; one leaves it for the merge kernel)
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.ws_info = it.pp;
+        if (!has_item) return;  // more CTAs than items
         b = it.b;
         part0 = it.part;  // (one partition per CTA)
         pp = it.pp;

@@ -47,6 +47,7 @@ struct AttendParams {
     float* ws_l;   // [B, Hq, P] partition exp-sum
     unsigned* err; // device error word
     unsigned* counters;  // per-(sequence, KV head, head chunk) arrival counters (fused merge)
+    int* ws_info;        // work-balanced plans: the partition size chosen, for the merge kernel
     int merge_in_kernel; // 1: the last CTA of each group merges its partials
     int cluster;         // > 1: the group's partitions form one cluster and merge in it
     int B, Hq, Hkv, g, num_pages, maxp, max_ctx, window;
@@ -73,6 +74,7 @@ struct MergeParams {
     const float* ws_o;
     const float* ws_m;
     const float* ws_l;
+    const int* ws_info;      // work-balanced plans: the partition size the partition kernel chose
     void* out;               // fp16 or bf16 (dtype)
     float* lse;
     unsigned* err;
