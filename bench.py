@@ -661,6 +661,12 @@ class OracleSampler:
         byts = 2 * ELEM_BYTES[c.dtype] * c.Hkv * c.D * tokens
         return byts / dt / 1e9, dt, desc, used
 
+    def single_thread_gbs(self):
+        """The oracle on one thread, from the calibration run: KV GB/s."""
+        c = self.case
+        per_token = self.sec_per_unit_1thread * c.Hq  # seconds per attended token, all heads
+        return 2 * ELEM_BYTES[c.dtype] * c.Hkv * c.D / per_token / 1e9
+
 
 def run_reference(args):
     world, rank, local = dist_setup()
@@ -689,7 +695,7 @@ def run_reference(args):
         "config": workload_config(case, world, GB300_L2_BYTES),
         "device": "host CPU (oracle)",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "single_thread_value": sampler.single_thread_gbs()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -814,7 +820,8 @@ def run_gpu(args):
                 sampler = OracleSampler(c)
                 v, dt, desc, used = sampler.run(sampler.plan(args.per_workload_cpu_budget_s))
                 oracle_cpu = {"value": v, "unit": UNIT, "cores": used, "kind": "oracle",
-                              "sample": desc, "seconds": dt}
+                              "sample": desc, "seconds": dt,
+                              "single_thread_value": sampler.single_thread_gbs()}
             entry.update({"kv_bytes": b, "cpu_baseline": oracle_cpu,
                           "timing": "us_per_step: CUDA graph of back-to-back steps over "
                                     "rotating K/V copies; single_call_us: median of "
@@ -835,7 +842,7 @@ def run_gpu(args):
         sampler = OracleSampler(case)
         v, dt, desc, used = sampler.run(sampler.plan(args.cpu_budget_s))
         cpu = {"value": v, "unit": UNIT, "cores": used, "kind": "oracle", "sample": desc,
-               "seconds": dt}
+               "seconds": dt, "single_thread_value": sampler.single_thread_gbs()}
 
     if rank == 0:
         line = {
