@@ -151,3 +151,20 @@ def test_agrees_with_fixed_partitions():
     assert gpu_helpers.rel_l2(a[0], b[0]) <= gpu_helpers.REL_L2_TOL
     assert np.abs(a[1] - b[1]).max() <= gpu_helpers.LSE_TOL
     assert_matches_oracle(case, a[0], a[1], what="balanced gemma2")
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,D", [
+    ([5000], 32, 8, 128),                 # one sequence: X CTAs on it alone
+    ([2000, 700, 3100], 64, 4, 64),       # g = 16: two head chunks of 8 per KV head
+    ([0, 0, 0, 4500], 4, 2, 256),         # only the last sequence attends anything
+])
+def test_edge_shapes(lens, Hq, Hkv, D):
+    case = workloads.make_case("edge", len(lens), Hq, Hkv, D, lens, seed=1410 + len(lens))
+    out, lse, err, plan = run_gpu(case, partition_size=BAL, guard=32)
+    assert err == 0
+    _check_plan(plan, case.B)
+    assert plan.heads_per_cta * (Hq // Hkv // plan.heads_per_cta) == Hq // Hkv
+    empty = [i for i, L in enumerate(lens) if L == 0]
+    if empty:
+        assert np.all(out[empty] == 0) and np.all(np.isneginf(lse[empty]))
+    assert_matches_oracle(case, out, lse, what=f"balanced edge {lens}")
