@@ -266,7 +266,6 @@ static int attended_span_pages(int max_context_len, int window) {
 static int balanced_ctas(int kernel, int dtype, int D, int G, bool rope, int batch,
                          int groups_per_seq, int span, int num_sms) {
     if (kernel != PA_KERNEL_MMA || rope || batch < 1 || batch > kMaxBalancedBatch) return 0;
-    if (G * (D / 4) > kThreads) return 0;  // the last-CTA merge's one item per thread
     const long long slots = (long long)num_sms * attend_ctas_per_sm(kernel, dtype, D, G, rope);
     const long long fill = slots - slots / 64;
     long long x = fill / groups_per_seq;

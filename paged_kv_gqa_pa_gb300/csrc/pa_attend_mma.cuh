@@ -201,90 +201,99 @@ __device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, co
     constexpr int D4 = D / 4;
     const int np = (sp.num_parts + p.parts_per_cta - 1) / p.parts_per_cta;  // partials
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int items = G * D4;               // (head, float4 column) pairs, <= kThreads
-    const int tpi = kThreads / items;        // threads per item, each a stride-tpi slice of partitions
-    const int item = threadIdx.x % items;
-    const int sub = threadIdx.x / items;     // < tpi for active threads
-    const bool active = sub < tpi;
-    const int ih = item / D4;
-    const int id = (item % D4) * 4;
+    const int items = G * D4;  // (head, float4 column) pairs
     const size_t row0 = ((size_t)b * p.Hq + h0) * p.P;
     float* s_m = xbuf;           // [G][np]
     float* s_w = xbuf + G * np;  // [G][np]: exp-sums, then merge weights
     float* s_M = s_small;        // [G]
     float* s_L = s_small + kMaxHeadsPerCta;
 
-    // The (m, l) pairs and this thread's first chunk of o slices go out
-    // together, so a group of up to kFusedLoads x tpi partials costs one
-    // round trip; each further chunk of that many costs one more.
+    // The (m, l) pairs and the first chunk of o slices go out together, so a
+    // group of up to kFusedLoads x tpi partials costs one round trip; each
+    // further chunk of that many costs one more.  Items are taken kThreads at a
+    // time: with fewer items than threads, tpi threads share an item (a
+    // stride-tpi slice of the partials each) and add up in shared memory.
     for (int idx = threadIdx.x; idx < G * np; idx += kThreads) {
         const int h = idx / np, i = idx % np;
         s_m[idx] = __ldcg(p.ws_m + row0 + (size_t)h * p.P + i);
         s_w[idx] = __ldcg(p.ws_l + row0 + (size_t)h * p.P + i);
     }
-    const float* src = p.ws_o + (row0 + (size_t)ih * p.P) * D + id;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = 0; c0 < np; c0 += kFusedLoads * tpi) {
-        float4 ov[kFusedLoads];
+    for (int base = 0; base < items; base += kThreads) {  // (the same rounds in every thread)
+        const int n_it = min(kThreads, items - base);   // items of this round
+        const int tpi = kThreads / n_it;                 // threads per item
+        const int item = threadIdx.x % n_it;
+        const int sub = threadIdx.x / n_it;              // < tpi for active threads
+        const bool active = sub < tpi;
+        const int ih = (base + item) / D4;
+        const int id = ((base + item) % D4) * 4;
+        const float* src = p.ws_o + (row0 + (size_t)ih * p.P) * D + id;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < np; c0 += kFusedLoads * tpi) {
+            float4 ov[kFusedLoads];
 #pragma unroll
-        for (int u = 0; u < kFusedLoads; ++u) {
-            const int i = c0 + sub + u * tpi;
-            ov[u] = (active && i < np)
-                        ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)i * D))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        if (c0 == 0) {  // (the same branch for every thread)
-            __syncthreads();
-            for (int h = warp; h < G; h += kWarps) {
-                float mx = -INFINITY;
-                for (int i = lane; i < np; i += 32) mx = fmaxf(mx, s_m[h * np + i]);
+            for (int u = 0; u < kFusedLoads; ++u) {
+                const int i = c0 + sub + u * tpi;
+                ov[u] = (active && i < np)
+                            ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)i * D))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            if (base == 0 && c0 == 0) {  // (the same branch for every thread)
+                __syncthreads();
+                for (int h = warp; h < G; h += kWarps) {
+                    float mx = -INFINITY;
+                    for (int i = lane; i < np; i += 32) mx = fmaxf(mx, s_m[h * np + i]);
 #pragma unroll
-                for (int mask = 16; mask > 0; mask >>= 1)
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, mask));
-                float sum = 0.f;
-                for (int i = lane; i < np; i += 32) {
-                    const float l = s_w[h * np + i];
-                    // l == 0: nothing attended; a NaN (bad page) is kept so it reaches the output.
-                    const float w = (l == 0.f) ? 0.f : ex2(s_m[h * np + i] - mx) * l;
-                    s_w[h * np + i] = w;
-                    sum += w;
+                    for (int mask = 16; mask > 0; mask >>= 1)
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, mask));
+                    float sum = 0.f;
+                    for (int i = lane; i < np; i += 32) {
+                        const float l = s_w[h * np + i];
+                        // l == 0: nothing attended; a NaN (bad page) is kept so it reaches the output.
+                        const float w = (l == 0.f) ? 0.f : ex2(s_m[h * np + i] - mx) * l;
+                        s_w[h * np + i] = w;
+                        sum += w;
+                    }
+#pragma unroll
+                    for (int mask = 16; mask > 0; mask >>= 1)
+                        sum += __shfl_xor_sync(0xffffffffu, sum, mask);
+                    if (lane == 0) {
+                        s_M[h] = mx;
+                        s_L[h] = sum;
+                    }
                 }
+                __syncthreads();
+            }
 #pragma unroll
-                for (int mask = 16; mask > 0; mask >>= 1)
-                    sum += __shfl_xor_sync(0xffffffffu, sum, mask);
-                if (lane == 0) {
-                    s_M[h] = mx;
-                    s_L[h] = sum;
+            for (int u = 0; u < kFusedLoads; ++u) {
+                const int i = c0 + sub + u * tpi;
+                const float w = (active && i < np) ? s_w[ih * np + i] : 0.f;
+                acc.x += w * ov[u].x;
+                acc.y += w * ov[u].y;
+                acc.z += w * ov[u].z;
+                acc.w += w * ov[u].w;
+            }
+        }
+        if (tpi > 1) {  // (only with fewer items than threads: a single round)
+            if (active) reinterpret_cast<float4*>(scratch)[sub * n_it + item] = acc;
+            __syncthreads();
+            if (sub == 0) {
+                for (int t = 1; t < tpi; ++t) {
+                    const float4 a = reinterpret_cast<const float4*>(scratch)[t * n_it + item];
+                    acc.x += a.x;
+                    acc.y += a.y;
+                    acc.z += a.z;
+                    acc.w += a.w;
                 }
             }
-            __syncthreads();
         }
-#pragma unroll
-        for (int u = 0; u < kFusedLoads; ++u) {
-            const int i = c0 + sub + u * tpi;
-            const float w = (active && i < np) ? s_w[ih * np + i] : 0.f;
-            acc.x += w * ov[u].x;
-            acc.y += w * ov[u].y;
-            acc.z += w * ov[u].z;
-            acc.w += w * ov[u].w;
+        if (sub == 0) {
+            const float lam = s_L[ih];
+            const float inv = 1.f / lam;
+            const size_t bh = (size_t)b * p.Hq + h0 + ih;
+            store4<T>(reinterpret_cast<T*>(p.out) + bh * D + id, acc.x * inv, acc.y * inv,
+                      acc.z * inv, acc.w * inv);
+            if (id == 0) p.lse[bh] = (s_M[ih] + log2f(lam)) * 0.69314718055994531f;
         }
-    }
-    if (active) reinterpret_cast<float4*>(scratch)[sub * items + item] = acc;
-    __syncthreads();
-    if (sub == 0) {
-        for (int t = 1; t < tpi; ++t) {
-            const float4 a = reinterpret_cast<const float4*>(scratch)[t * items + item];
-            acc.x += a.x;
-            acc.y += a.y;
-            acc.z += a.z;
-            acc.w += a.w;
-        }
-        const float lam = s_L[ih];
-        const float inv = 1.f / lam;
-        const size_t bh = (size_t)b * p.Hq + h0 + ih;
-        store4<T>(reinterpret_cast<T*>(p.out) + bh * D + id, acc.x * inv, acc.y * inv,
-                  acc.z * inv, acc.w * inv);
-        if (id == 0) p.lse[bh] = (s_M[ih] + log2f(lam)) * 0.69314718055994531f;
     }
 }
 

@@ -160,11 +160,12 @@ __host__ __device__ constexpr bool kFusedMergeFits(int G, int D, int P) {
            2 * G * P * 4 <= kWarps * kMaxHeadsPerCta * 64 * 4;
 }
 
-// What the last-CTA merge can take at all: one thread (or more) per (head,
-// 4-dim column) item, and the G x R (m, weight) pairs in the combine buffer.
-// Partials beyond kFusedLoads per thread cost one more round trip per chunk.
+// What the last-CTA merge can take at all: the G x R (m, weight) pairs in the
+// combine buffer.  Its threads take the (head, 4-dim column) items kThreads at
+// a time, and partials beyond kFusedLoads per thread cost one more round trip
+// per chunk.
 __host__ __device__ constexpr bool kFusedMergeLegal(int G, int D, int R) {
-    return G * (D / 4) <= kThreads && G * R <= kFusedMaxStaged;
+    return D > 0 && G * R <= kFusedMaxStaged;
 }
 static_assert(2 * kFusedMaxStaged * 4 <= kWarps * kMaxHeadsPerCta * 64 * 4,
               "the staged (m, weight) pairs fit the combine buffer");

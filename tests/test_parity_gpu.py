@@ -408,8 +408,6 @@ def test_rotary_tensor_core_plan_shapes(plan_kind, D, Hq, Hkv, dtype):
     if gpu_helpers.KERNEL != "mma":
         pytest.skip("tensor-core plan shapes")
     kw = dict(ROPE_PLANS[plan_kind])
-    if kw.get("merge_in_kernel") == 1 and (Hq // Hkv) * (D // 4) > 128:
-        pytest.skip("the last-CTA merge serves at most 128 (head, 4-dim column) items")
     lens = [1, 17, 700, 2049, 3333]
     case = workloads.make_case("ropep", len(lens), Hq, Hkv, D, lens, seed=1600 + D, q_std=2.0,
                                rope_theta=500000.0, window=3000 if plan_kind == "cluster" else 0,
