@@ -781,11 +781,15 @@ def run_gpu(args):
     arm.check_error()
 
     per = None
-    summary = None
+    summary = summary_extra = None
     if not args.no_per_workload and rank == 0:
         per = {}
-        summary = {"fields": ["kernel", "us/step", "KV GB/s", "frac of measured HBM",
-                              "single-call us", "oracle GB/s", "plan"]}
+        # One compact row per workload: the five named configs early in the
+        # line ("configs"), the further workloads at its end ("configs_extra").
+        fields = ["us/step", "KV GB/s", "frac measured HBM", "frac nominal 8 TB/s",
+                  "single-call us", "oracle GB/s", "plan"]
+        summary = {"fields": fields, "oracle_cores": None}
+        summary_extra = {"fields": ["kernel"] + fields}
         wl_flush = flush if flush is not None else l2_flush_buffer(torch, device)
         for name in workloads.WORKLOAD_ORDER + workloads.EXTRA_ORDER:
             c = case if name == args.workload else workloads.workload(name)
@@ -831,11 +835,17 @@ def run_gpu(args):
             per[name] = entry
             k0 = kernels[0]
             e0 = entry[k0]
-            summary[name] = [k0, round(e0["us_per_step"], 2), round(e0["kv_gbs"]),
-                             round(e0["frac_of_measured_hbm"], 3),
-                             round(e0["single_call_us"], 1),
-                             round(oracle_cpu["value"], 3) if oracle_cpu else None,
-                             e0["plan"]["short"]]
+            row = [round(e0["us_per_step"], 2), round(e0["kv_gbs"]),
+                   round(e0["frac_of_measured_hbm"], 3), round(e0["frac_of_nominal_8tbs"], 3),
+                   round(e0["single_call_us"], 1),
+                   round(oracle_cpu["value"], 3) if oracle_cpu else None,
+                   e0["plan"]["short"]]
+            if name in workloads.WORKLOAD_ORDER:
+                summary[name] = row
+                if oracle_cpu:
+                    summary["oracle_cores"] = oracle_cpu["cores"]
+            else:
+                summary_extra[name] = [k0] + row
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -851,6 +861,11 @@ def run_gpu(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
             "data": "synthetic",
             "config": workload_config(case, world, l2),
+            # Early, so that a record keeping only the head of the line has
+            # them: each named config's figures beside the oracle's, and the
+            # pages' own figures (context only).
+            "configs": summary,
+            "context": PAGES_CONTEXT,
             "plan": plan_summary(arm.plan),
             "roofline": {"bound": "hbm", "achieved": kern_gbs, "peak": peak, "unit": "GB/s",
                          "frac": kern_gbs / peak, "traffic": traffic,
@@ -867,10 +882,7 @@ def run_gpu(args):
                           "per-step launches, L2 flushed between steps",
             "clocks": clk.summary(),
             "per_workload": per,
-            # Last, so that a tail of the output keeps them: the pages' own
-            # figures (context only) and one compact line per workload.
-            "context": PAGES_CONTEXT,
-            "configs": summary,
+            "configs_extra": summary_extra,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

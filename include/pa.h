@@ -143,8 +143,10 @@ typedef struct pa_plan {
                                b gets max(1, ceil(pages_b / pp)) CTAs, so a long
                                sequence gets more CTAs than a short one.  Its partials
                                are merged by the last CTA of each group
-                               (merge_in_kernel = 1, the choice pa_plan_ex makes) or
-                               by the merge kernel (0); cluster 0, parts_per_cta 1.
+                               (merge_in_kernel = 1) or by the merge kernel (0);
+                               pa_plan_ex takes the merge kernel when one group could
+                               leave its last CTA more than 128 KiB of partials to
+                               merge.  cluster 0, parts_per_cta 1.
                                num_partitions then holds X (the most partials a
                                sequence can have) and partition_size the largest pp
                                any lengths within max_context_len can give.  Set by

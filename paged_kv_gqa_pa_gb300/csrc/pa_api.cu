@@ -707,7 +707,20 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
             ? 1
             : 0;
     plan->balanced = want_balanced ? bal_x : 0;
-    if (want_balanced) plan->merge_in_kernel = 1;
+    if (want_balanced) {
+        // The merge of a balanced plan: the last CTA of each group, unless a
+        // group can leave it too much to merge alone -- one sequence taking
+        // all but B - 1 of the X CTAs, X - B + 1 partials of G x D floats --
+        // when the merge kernel, which spreads a group over many CTAs, wins.
+        // Measured on GB300 (graph-timed, last CTA vs merge kernel): 24/4
+        // heads at D 256 with one long sequence 51.5 vs 44.5 us (442 KB
+        // worst case), 64/8 heads at D 128 43.1 vs 40.8 us (217 KB); 16
+        // sequences, 32/8 heads at D 128 16.4 vs 22.4 us (84 KB), 32/8 heads
+        // at D 96 66.9 vs 67.2 us (81 KB).
+        constexpr long long kLastCtaMergeMaxBytes = 128 << 10;
+        const long long worst = (long long)(bal_x - batch + 1) * G * head_dim * 4;
+        plan->merge_in_kernel = worst <= kLastCtaMergeMaxBytes ? 1 : 0;
+    }
     // Partitions per CTA (tensor-core kernel, split plans without a
     // cluster): a CTA may serve 2 or 4 consecutive partitions and merge them
     // into one partial, which cuts CTA prologues and epilogues, the partials

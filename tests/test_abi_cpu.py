@@ -459,3 +459,11 @@ def test_balanced_plans():
         assert _call_decode(bad) == binding.PA_ERR_INVALID_ARG, (field, value)
     # a fixed-size plan never sets it
     assert pa.pa_plan_ex(8, 32, 8, 128, 16, 1250, 256, 4096, 0, 512, 152).balanced == 0
+    # The merge: the last CTA of each group, unless one group could leave it
+    # more than 128 KiB of partials (X - B + 1 partials of G x D floats).
+    wide = pa.pa_plan_ex(4, 64, 8, 128, 16, 5000, 3125, 50000, 0, BAL, 152)
+    assert wide.balanced == 56 and (56 - 4 + 1) * 8 * 128 * 4 > 128 << 10
+    assert wide.merge_in_kernel == 0
+    narrow = pa.pa_plan_ex(16, 32, 8, 128, 16, 5000, 750, 12000, 0, BAL, 152)
+    assert narrow.balanced == 56 and (56 - 16 + 1) * 4 * 128 * 4 <= 128 << 10
+    assert narrow.merge_in_kernel == 1

@@ -170,14 +170,16 @@ def test_edge_shapes(lens, Hq, Hkv, D):
     assert_matches_oracle(case, out, lse, what=f"balanced edge {lens}")
 
 
+@pytest.mark.parametrize("fused", [1, 0])
 @pytest.mark.parametrize("Hq,Hkv,D", [(64, 8, 128), (24, 4, 256)])
-def test_wide_groups(Hq, Hkv, D):
+def test_wide_groups(Hq, Hkv, D, fused):
     """8 heads at D 128 (256 head-column items) and 6 at D 256 (384): the
-    last CTA of a group merges its items kThreads at a time."""
+    last CTA of a group merges its items kThreads at a time (fused 1); the
+    planner gives these shapes the merge kernel (fused 0)."""
     lens = [9000, 120, 40, 2600]
     case = workloads.make_case("wide", len(lens), Hq, Hkv, D, lens, seed=1420 + D)
-    out, lse, err, plan = run_gpu(case, partition_size=BAL)
+    out, lse, err, plan = run_gpu(case, partition_size=BAL, merge_in_kernel=fused)
     assert err == 0
-    _check_plan(plan, case.B, 1)
+    _check_plan(plan, case.B, fused)
     assert plan.heads_per_cta * (D // 4) > 128
     assert_matches_oracle(case, out, lse, what=f"balanced wide group Hq{Hq} D{D}")
