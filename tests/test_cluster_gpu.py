@@ -52,6 +52,22 @@ def test_cluster_merge_matches_oracle(D, Hq, Hkv, dtype, lens, S):
     assert_matches_oracle(case, o2, l2, ref=ref, what=f"no cluster D{D} {dtype} P{P}")
 
 
+@pytest.mark.parametrize("Hq,Hkv,D,lens,S", [
+    (16, 2, 256, [700, 1024, 513], 512),   # 8 heads x 64 columns over 2 CTAs: 256 items each
+    (24, 4, 256, [900, 1000], 512),        # 6 heads: 192 items each
+    (32, 4, 128, [300, 2000], 1024),       # 8 heads at D 128: 128 items each
+])
+def test_cluster_of_two_merges_two_rounds_per_thread(Hq, Hkv, D, lens, S):
+    """The smallest cluster gives each CTA the most (head, column) items to
+    merge: more than one per thread at D = 256, held in registers across the
+    second cluster barrier and stored after it."""
+    case = workloads.make_case("cl2", len(lens), Hq, Hkv, D, lens, seed=1230 + D, q_std=2.0,
+                               partition_size=S)
+    out, lse, err, plan = run_gpu(case, cluster=True)
+    assert err == 0 and plan.cluster == 2
+    assert_matches_oracle(case, out, lse, what=f"cluster of 2, {Hq}/{Hkv} heads, D {D}")
+
+
 def test_cluster_ragged_batch_with_empty_sequences():
     # Sequences shorter than the cluster's span leave CTAs with nothing to
     # attend; empty sequences give out = 0, lse = -inf.
