@@ -54,10 +54,10 @@ FALLBACK_HBM_GBS = 6800.0
 # `src_sha` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     # One ncu capture of this kernel on the same workload cut to its first
-    # sequence (B = 1): (409.72 + 3.05) MB read + written per launch, scaled by
+    # sequence (B = 1): (409.72 + 3.73) MB read + written per launch, scaled by
     # tokens to the B = 4 launch.
-    ("gqa6_ctx100k", "mma"): {"src_sha": "fd752d8e638bbaf7", "partition_size": 512,
-                              "bytes_per_launch": 4 * (409.716480e6 + 3.046912e6)},
+    ("gqa6_ctx100k", "mma"): {"src_sha": "e04a6e4381135a1d", "partition_size": 512,
+                              "bytes_per_launch": 4 * (409.718016e6 + 3.732224e6)},
 }
 
 
