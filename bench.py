@@ -405,31 +405,62 @@ def flush_l2(flush):
     return flush.view(torch.int64).sum()
 
 
-def time_flushed(arm, iters, flush):
-    """Single-call time: per iteration, evict L2 (by reading a buffer larger
-    than it), then bracket ONE pa_decode call with CUDA events on its stream.
-    The events and the call are enqueued while the eviction still runs, so
-    the interval holds the call's GPU time from a cold L2 and nothing of the
-    host: the launch of its kernel(s), their run, and none of the overlap with
-    a preceding step that back-to-back steps get.  Returns (median ms per
-    call, median host microseconds spent inside the pa_decode call)."""
+def time_flushed(arm, iters, flush, reps=3):
+    """Single-call time from a cold L2.  `iters` pairs of (an L2 eviction by
+    reading a buffer larger than it, one pa_decode call) run back to back
+    between two events, and so do `iters` evictions alone; the difference
+    per pair is the call's cost on the stream: its launch behind a kernel
+    that does not launch dependents early, its run from a cold L2, and none
+    of the overlap with a preceding step that back-to-back steps get.  No
+    host time is inside (the device never waits for the host: an eviction
+    takes far longer than enqueueing a call).  A difference of two long
+    intervals also averages out the CUDA events' ~2 us granularity.
+    Returns (ms per call, the median of `reps` such differences; median host
+    microseconds spent inside one pa_decode call)."""
     torch = arm.torch
     for _ in range(3):
         arm.step()
     torch.cuda.synchronize()
-    res, host = [], []
+    host = []
+
+    def run(with_call):
+        a, b = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+        flush_l2(flush)
+        a.record(arm.stream)
+        for _ in range(iters):
+            flush_l2(flush)
+            if with_call:
+                t0 = time.perf_counter()
+                arm.step()
+                host.append((time.perf_counter() - t0) * 1e6)
+        b.record(arm.stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    diffs = []
+    for _ in range(reps):
+        t_flush = run(False)
+        t_both = run(True)
+        diffs.append((t_both - t_flush) / iters)
+    return statistics.median(diffs), statistics.median(host)
+
+
+def time_isolated(arm, iters, flush):
+    """One call bracketed by its own pair of CUDA events, per iteration, after
+    an L2 eviction (events and call enqueued behind the eviction): median ms.
+    The start event keeps the call from starting early behind the eviction
+    kernel, and the events tick in ~2 us steps."""
+    torch = arm.torch
+    res = []
     for _ in range(iters):
         flush_l2(flush)
         a, b = (torch.cuda.Event(enable_timing=True) for _ in range(2))
         a.record(arm.stream)
-        t0 = time.perf_counter()
         arm.step()
-        t1 = time.perf_counter()
         b.record(arm.stream)
         torch.cuda.synchronize()
         res.append(a.elapsed_time(b))
-        host.append((t1 - t0) * 1e6)
-    return statistics.median(res), statistics.median(host)
+    return statistics.median(res)
 
 
 def host_us_prepared(arm, calls=200):
@@ -744,7 +775,7 @@ def run_gpu(args):
         if big:
             ms, timed_steps = time_steps(arm, args.steps, args.warmup)
         else:
-            ms, _ = time_flushed(arm, args.steps, flush)
+            ms, _ = time_flushed(arm, args.steps, flush, reps=1)  # exactly K timed steps
             timed_steps = args.steps
         kern_ms, kern_timing = time_partition_kernel(arm, min(args.steps, 500), flush)
     if world > 1:
@@ -801,17 +832,23 @@ def run_gpu(args):
                 kernels = ("simt",)  # no tensor-core build for fp32 caches
             for kname in kernels:
                 us, kus, copies, l2state, plan = time_graph_rotating(c, device, kname)
-                # single calls: CUDA events around one pa_decode, L2 evicted
-                # (by reading) before each
+                # single calls from a cold L2, each behind a kernel that does
+                # not launch dependents early; then the same plan without the
+                # pre-wait prefetch, which such a caller would choose
                 earm = GpuArm(c, device, kernel=kname)
                 eager_ms, host_us = time_flushed(earm, args.per_workload_iters, wl_flush)
+                iso_ms = time_isolated(earm, args.per_workload_iters, wl_flush)
                 prep_us = host_us_prepared(earm)
+                earm.plan.prewait_prefetch = 0
+                eager0_ms, _ = time_flushed(earm, args.per_workload_iters, wl_flush)
                 earm.check_error()
                 del earm
                 entry[kname] = {"us_per_step": us, "partition_kernel_us": kus,
                                 "kv_gbs": b / (us * 1e-6) / 1e9,
                                 "single_call_us": eager_ms * 1e3,
                                 "single_call_kv_gbs": b / (eager_ms * 1e-3) / 1e9,
+                                "single_call_us_no_prewait": eager0_ms * 1e3,
+                                "single_call_isolated_us": iso_ms * 1e3,
                                 "host_us_in_pa_decode": host_us,
                                 "host_us_prepared_call": prep_us,
                                 "frac_of_measured_hbm": b / (us * 1e-6) / 1e9 / peak,
@@ -828,10 +865,13 @@ def run_gpu(args):
                               "single_thread_value": sampler.single_thread_gbs()}
             entry.update({"kv_bytes": b, "cpu_baseline": oracle_cpu,
                           "timing": "us_per_step: CUDA graph of back-to-back steps over "
-                                    "rotating K/V copies; single_call_us: median of "
-                                    f"{args.per_workload_iters} single pa_decode calls, CUDA "
-                                    "events on the stream, L2 evicted (read) before each, "
-                                    "enqueued behind the eviction so no host time is inside"})
+                                    "rotating K/V copies; single_call_us: "
+                                    f"{args.per_workload_iters} (L2 eviction by reading, one "
+                                    "pa_decode call) pairs back to back minus the evictions "
+                                    "alone, per call (median of 3), CUDA events on the stream; "
+                                    "_no_prewait: the same plan with prewait_prefetch 0; "
+                                    "single_call_isolated_us: median of one call between its "
+                                    "own event pair after each eviction"})
             per[name] = entry
             k0 = kernels[0]
             e0 = entry[k0]

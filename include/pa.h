@@ -127,7 +127,12 @@ typedef struct pa_plan {
                                depends on (programmatic dependent launch).  Each CTA reads
                                its sequence length and first page ids as hints for them;
                                everything is read again after the wait, so a stale hint
-                               only prefetches a page that is not used */
+                               only prefetches a page that is not used.  pa_plan_ex sets 2,
+                               which pays when the preceding kernel on the stream is a
+                               decode step (or any kernel that launches dependents
+                               early): the hints then run while it drains.  Behind a
+                               kernel that does not, 0 is faster (the hints' two
+                               dependent reads come before this call's own) */
     int test_stall_bytes;   /* test hook, 0 in normal use.  > 0 (at most 4096): in the
                                tensor-core kernel each warp's first page copy expects
                                this many bytes more than it carries, so the bounded
