@@ -698,14 +698,25 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     // are many (the one-CTA merge would then trail the grid).
     plan->cluster = (use_cluster && P >= 2 && P <= kMaxClusterParts) ? P : 0;
     // Tensor-core kernel: each warp's first two pages are requested into L2
-    // before the dependency wait (measured on GB300: 0.2-1 us less per step
-    // when decode steps follow each other with programmatic dependent launch,
-    // no cost when they do not).
+    // before the dependency wait.  Measured on GB300: 0.4-1.5 us less per
+    // step when decode steps follow each other with programmatic dependent
+    // launch; 0.5-1 us more per call behind a kernel that does not launch
+    // dependents early (a caller in that case sets 0).
     plan->prewait_prefetch = kernel == PA_KERNEL_MMA ? 2 : 0;
     plan->merge_in_kernel =
         (kernel == PA_KERNEL_MMA && P > 1 && plan->cluster == 0 && kFusedMergeFits(G, head_dim, P))
             ? 1
             : 0;
+    // Rotary instances (fixed partitions): the last CTA of each group merges
+    // whenever a group's partials are at most 128 KiB.  Measured on GB300
+    // (graph-timed, last CTA vs merge kernel): 4 x 32K tokens, 32/8 heads,
+    // D 128, P 9: 96.1 vs 97.4 us; 24/4 heads, D 256, P 18 (110 KB): 99.9 vs
+    // 103.6 us.  The same 24/4-head shape without rotary embedding is faster
+    // with the merge kernel (82.6 vs 84.9 us), so the rule is for these
+    // instances only.
+    if (kernel == PA_KERNEL_MMA && rope_theta > 0.f && P > 1 && plan->cluster == 0 &&
+        (long long)P * G * head_dim * 4 <= (128 << 10) && kFusedMergeLegal(G, head_dim, P))
+        plan->merge_in_kernel = 1;
     plan->balanced = want_balanced ? bal_x : 0;
     if (want_balanced) {
         // The merge of a balanced plan: the last CTA of each group, unless a

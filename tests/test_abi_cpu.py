@@ -470,3 +470,22 @@ def test_balanced_plans():
     narrow = pa.pa_plan_ex(16, 32, 8, 128, 16, 5000, 750, 12000, 0, BAL, 152)
     assert narrow.balanced == 56 and (56 - 16 + 1) * 4 * 128 * 4 <= 128 << 10
     assert narrow.merge_in_kernel == 1
+
+
+def test_rotary_plans_merge_in_the_last_cta_when_partials_are_small():
+    """Rotary instances with fixed partitions: the last CTA of each group
+    merges when a group's partials (P x G x D floats) are at most 128 KiB,
+    the merge kernel otherwise."""
+    def plan(B, Hq, Hkv, D, L):
+        pages = -(-L // 16)
+        return pa.pa_plan_ex(B, Hq, Hkv, D, 16, B * pages + 8, pages, L, 0, 0, 152,
+                             rope_theta=1e4)
+    small = plan(4, 24, 4, 256, 32768)  # P 18: 18 x 6 x 256 x 4 B = 110.6 KB
+    assert small.cluster == 0 and small.num_partitions * 6 * 256 * 4 <= 128 << 10
+    assert small.merge_in_kernel == 1
+    big = plan(1, 24, 4, 256, 65536)    # P 75: 460.8 KB
+    assert big.cluster == 0 and big.num_partitions * 6 * 256 * 4 > 128 << 10
+    assert big.merge_in_kernel == 0
+    # without rotary embedding the same small shape keeps the merge kernel
+    plain = pa.pa_plan_ex(4, 24, 4, 256, 16, 4 * 2048 + 8, 2048, 32768, 0, 1824, 152)
+    assert plain.num_partitions == 18 and plain.merge_in_kernel == 0
