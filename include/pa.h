@@ -101,7 +101,10 @@ typedef struct pa_plan {
     int merge_in_kernel;    /* 1: with the tensor-core kernel, the last CTA of each
                                (sequence, KV head) merges that group's partials and
                                pa_merge has nothing to do; 0: pa_merge launches the
-                               merge kernel */
+                               merge kernel.  pa_plan_ex sets 1 for fixed partitions of
+                               up to 8 partials per group, for rotary plans whose
+                               group partials fit 128 KiB, and for work-balanced plans
+                               as described under balanced */
     int ctrl_bytes;         /* leading workspace bytes that must be zero before the
                                first call (error word, per-group arrival counters).
                                Every call leaves the counters zero; the error word
