@@ -62,8 +62,8 @@ NCU_TRAFFIC = {
 
 
 KERNEL_SOURCES = {
-    "mma": ("pa_attend_mma.cuh", "pa_attend_mma_page.inc", "pa_attend_mma_f16.cu",
-            "pa_attend_mma_bf16.cu", "pa_attend_mma_rope.cu", "pa_common.cuh"),
+    "mma": ("pa_attend_mma.cuh", "pa_attend_mma_f16.cu", "pa_attend_mma_bf16.cu",
+            "pa_attend_mma_rope.cu", "pa_common.cuh"),
     "simt": ("pa_attend.cuh", "pa_attend_d64.cu", "pa_attend_d128.cu", "pa_attend_d256.cu",
              "pa_attend_bf16_d64.cu", "pa_attend_bf16_d128.cu", "pa_attend_bf16_d256.cu",
              "pa_attend_f32_d64.cu", "pa_attend_f32_d128.cu", "pa_attend_f32_d256.cu",

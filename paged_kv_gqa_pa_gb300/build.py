@@ -35,7 +35,7 @@ def sources():
 
 
 def _deps():
-    return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.inc")) + [
+    return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [
         os.path.join(ROOT, "include", "pa.h"), os.path.abspath(__file__)]
 
 

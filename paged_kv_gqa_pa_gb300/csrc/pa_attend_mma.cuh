@@ -919,35 +919,177 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
         float l_run[2] = {0.f, 0.f};   // exp-sum of the fp32 weights
         float n_run[2] = {0.f, 0.f};   // exp-sum of the fp16-rounded weights
 
-        // The page loop.  Rotary instances at D = 128 (3 CTAs per SM, 168
-        // registers) walk the pages in chunks of 32 and evaluate the rotary
-        // state exactly at each chunk's first page before the chunk's loop,
-        // which keeps that evaluation's temporaries out of the loop's
-        // register peak (their fp16 instances spill otherwise).  Every other
-        // instance keeps the one loop with the evaluation inside (the same
-        // code as before; the chunked form measured slower for them).
-        constexpr bool kChunked = ROPE && D == 128;
-        if constexpr (kChunked) {
-            while (ok && k < nk) {
-                const int pos0 = (pgA + wpage(k)) * kPageSize + tok0;
+        for (; ok && k < nk; ++k) {
+            const int page_pos = (pgA + wpage(k)) * kPageSize;
+            // ---------------- K page: S^T = K . Q^T
+            {
+                const int item = 2 * k;
+                const bool got = mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                consumed = item + 1;
+            }
+            const uint32_t kaddr = ring_w + ((2 * k) % NS) * PB;
+            float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (ROPE) {
+                // the rotary state at this page's row tok0 (rc, rs); row tok0 + 8
+                // is derived per k-step below, for the two slots it uses
 #pragma unroll
                 for (int i = 0; i < KT; ++i) {
                     const int f = (i >> 1) * 16 + (lane & 3) * 2 + (i & 1) * 8;
-                    float c0, s0, c1, s1;
-                    rope_twiddle(pos0, p.rope_phi[0][f], p.rope_phi[1][f], c0, s0);
-                    rope_twiddle(pos0, p.rope_phi[0][f + 1], p.rope_phi[1][f + 1], c1, s1);
-                    rc[i] = make_float2(c0, c1);
-                    rs[i] = make_float2(s0, s1);
+                    if ((k & 31) == 0) {
+                        float c0, s0, c1, s1;
+                        rope_twiddle(page_pos + tok0, p.rope_phi[0][f], p.rope_phi[1][f], c0, s0);
+                        rope_twiddle(page_pos + tok0, p.rope_phi[0][f + 1], p.rope_phi[1][f + 1],
+                                     c1, s1);
+                        rc[i] = make_float2(c0, c1);
+                        rs[i] = make_float2(s0, s1);
+                    } else {
+                        rope_turn_pair(rc[i], rs[i], *reinterpret_cast<const float4*>(s_r64 + f));
+                    }
                 }
-                const int k_end = min(nk, k + 32);
-                for (; ok && k < k_end; ++k) {
-#include "pa_attend_mma_page.inc"
+#pragma unroll
+                for (int kk = 0; kk < KT / 2; ++kk) {
+                    // fragments: a0/a2 row tok0, a1/a3 row tok0 + 8; a0/a1 slot r = 0, a2/a3 r = 1
+                    const int f0 = kk * 16 + (lane & 3) * 2;
+                    float2 c8a = rc[2 * kk], s8a = rs[2 * kk];
+                    float2 c8b = rc[2 * kk + 1], s8b = rs[2 * kk + 1];
+                    rope_turn_pair(c8a, s8a, *reinterpret_cast<const float4*>(s_r8 + f0));
+                    rope_turn_pair(c8b, s8b, *reinterpret_cast<const float4*>(s_r8 + f0 + 8));
+                    uint32_t x[4], y[4], xh[4], xl[4], yh[4], yl[4];
+                    ldsm_x4(kaddr + swz<D>(k_row, kk * 2 + k_chk), x[0], x[1], x[2], x[3]);
+                    ldsm_x4(kaddr + swz<D>(k_row, (kk + KT / 2) * 2 + k_chk), y[0], y[1], y[2],
+                            y[3]);
+                    rope_rot_split<T>(x[0], y[0], rc[2 * kk], rs[2 * kk], xh[0], xl[0], yh[0], yl[0]);
+                    rope_rot_split<T>(x[1], y[1], c8a, s8a, xh[1], xl[1], yh[1], yl[1]);
+                    rope_rot_split<T>(x[2], y[2], rc[2 * kk + 1], rs[2 * kk + 1], xh[2], xl[2], yh[2],
+                                      yl[2]);
+                    rope_rot_split<T>(x[3], y[3], c8b, s8b, xh[3], xl[3], yh[3], yl[3]);
+                    const int k2 = kk + KT / 2;
+                    Elem<T>::mma(ca, xh[0], xh[1], xh[2], xh[3], qb[kk][0], qb[kk][1]);
+                    Elem<T>::mma(ca, xh[0], xh[1], xh[2], xh[3], ql[kk][0], ql[kk][1]);
+                    Elem<T>::mma(ca, xl[0], xl[1], xl[2], xl[3], qb[kk][0], qb[kk][1]);
+                    Elem<T>::mma(cb, yh[0], yh[1], yh[2], yh[3], qb[k2][0], qb[k2][1]);
+                    Elem<T>::mma(cb, yh[0], yh[1], yh[2], yh[3], ql[k2][0], ql[k2][1]);
+                    Elem<T>::mma(cb, yl[0], yl[1], yl[2], yl[3], qb[k2][0], qb[k2][1]);
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < KT; ++kk) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(kaddr + swz<D>(k_row, kk * 2 + k_chk), a0, a1, a2, a3);
+                    if (kk & 1)
+                        Elem<T>::mma(cb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+                    else
+                        Elem<T>::mma(ca, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
                 }
             }
-        } else {
-            for (; ok && k < nk; ++k) {
-#include "pa_attend_mma_page.inc"
+            __syncwarp();
+            if (lane == 0 && 2 * k + NS < n_items) {
+                fence_proxy_async_smem();
+                issue(2 * k + NS);
             }
+            if (2 * k + NS < n_items) issued = 2 * k + NS + 1;
+
+            // ---------------- online softmax (log2 domain); lane: tokens tok0, tok0+8; heads hA, hA+1
+            const bool v0 = page_pos + tok0 >= sp.start && page_pos + tok0 < sp.L;
+            const bool v1 = page_pos + tok0 + 8 >= sp.start && page_pos + tok0 + 8 < sp.L;
+            float s00 = v0 ? (ca[0] + cb[0]) * p.scale_log2 : -INFINITY;  // token0, head A
+            float s01 = v0 ? (ca[1] + cb[1]) * p.scale_log2 : -INFINITY;  // token0, head B
+            float s10 = v1 ? (ca[2] + cb[2]) * p.scale_log2 : -INFINITY;  // token1, head A
+            float s11 = v1 ? (ca[3] + cb[3]) * p.scale_log2 : -INFINITY;  // token1, head B
+            float mA = fmaxf(s00, s10), mB = fmaxf(s01, s11);
+#pragma unroll
+            for (int mask = 4; mask < 32; mask <<= 1) {
+                mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, mask));
+                mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, mask));
+            }
+            if (__any_sync(0xffffffffu, mA > m_run[0] || mB > m_run[1])) {
+                const float nA = fmaxf(m_run[0], mA), nB = fmaxf(m_run[1], mB);
+                const float aA = (nA == -INFINITY) ? 1.f : ex2(m_run[0] - nA);
+                const float aB = (nB == -INFINITY) ? 1.f : ex2(m_run[1] - nB);
+                m_run[0] = nA;
+                m_run[1] = nB;
+                l_run[0] *= aA;
+                l_run[1] *= aB;
+                n_run[0] *= aA;
+                n_run[1] *= aB;
+#pragma unroll
+                for (int mt = 0; mt < KT; ++mt) {
+                    o[mt][0] *= aA;
+                    o[mt][2] *= aA;
+                    o[mt][1] *= aB;
+                    o[mt][3] *= aB;
+                }
+            }
+            const float p00 = (s00 == -INFINITY) ? 0.f : ex2(s00 - m_run[0]);
+            const float p01 = (s01 == -INFINITY) ? 0.f : ex2(s01 - m_run[1]);
+            const float p10 = (s10 == -INFINITY) ? 0.f : ex2(s10 - m_run[0]);
+            const float p11 = (s11 == -INFINITY) ? 0.f : ex2(s11 - m_run[1]);
+            float r00, r01, r10, r11;
+            const uint32_t top = Elem<T>::pack2(p00, p01, r00, r01);  // P[tok0][hA, hB]
+            const uint32_t bot = Elem<T>::pack2(p10, p11, r10, r11);  // P[tok0 + 8][hA, hB]
+            l_run[0] += p00 + p10;
+            l_run[1] += p01 + p11;
+            // P^T fragments: lane gets P[tokens (lane%4)*2 + {0,1} (+8)][head lane/4]
+            const uint32_t pb0 = movmatrix_trans(top);
+            const uint32_t pb1 = movmatrix_trans(bot);
+            uint32_t pc0 = 0u, pc1 = 0u;  // bf16 only: the remainders P - head
+            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                float e00, e01, e10, e11;
+                const uint32_t ltop = Elem<T>::pack2(p00 - r00, p01 - r01, e00, e01);
+                const uint32_t lbot = Elem<T>::pack2(p10 - r10, p11 - r11, e10, e11);
+                r00 += e00;
+                r01 += e01;
+                r10 += e10;
+                r11 += e11;
+                pc0 = movmatrix_trans(ltop);
+                pc1 = movmatrix_trans(lbot);
+            }
+            n_run[0] += r00 + r10;
+            n_run[1] += r01 + r11;
+
+            // ---------------- V page: O^T += V^T . P^T
+            {
+                const int item = 2 * k + 1;
+                const bool got = mbar_wait_bounded(bar_w + (item % NS) * 8, (item / NS) & 1);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                consumed = item + 1;
+            }
+            const uint32_t vaddr = ring_w + ((2 * k + 1) % NS) * PB;
+            if (page_pos < sp.start || page_pos + kPageSize > sp.L) {
+                // Boundary page: zero the V rows of tokens outside [start, L) so
+                // that whatever those slots hold (never-written cache slots may
+                // hold NaN) cannot reach the output through a zero weight.
+                unsigned char* vgen = ring + warp * NS * PB + ((2 * k + 1) % NS) * PB;
+                for (int idx = lane; idx < kPageSize * (D / 8); idx += 32) {
+                    const int row = idx / (D / 8);
+                    const int pos = page_pos + row;
+                    if (pos < sp.start || pos >= sp.L)
+                        *reinterpret_cast<uint4*>(vgen + swz<D>(row, idx % (D / 8))) =
+                            make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(vaddr + swz<D>(v_row, mt * 2 + v_chk), a0, a1, a2, a3);
+                Elem<T>::mma(o[mt], a0, a1, a2, a3, pb0, pb1);
+                if constexpr (std::is_same<T, __nv_bfloat16>::value)
+                    Elem<T>::mma(o[mt], a0, a1, a2, a3, pc0, pc1);
+            }
+            __syncwarp();
+            if (lane == 0 && 2 * k + 1 + NS < n_items) {
+                fence_proxy_async_smem();
+                issue(2 * k + 1 + NS);
+            }
+            if (2 * k + 1 + NS < n_items) issued = 2 * k + 1 + NS + 1;
         }
         if (!ok) {
             if (lane == 0) {
