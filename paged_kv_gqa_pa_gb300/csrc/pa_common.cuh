@@ -117,7 +117,7 @@ struct MmaCfg {
     static constexpr int kPageBytes = kPageSize * D * 2;
     // pages in flight per warp; with the fixed buffers below this keeps
     // kMinBlocks CTAs per SM within 228 KiB of shared memory
-    static constexpr int kStages = ROPE ? (D == 256 ? 3 : (D == 128 ? 6 : (D == 96 ? 5 : 6)))
+    static constexpr int kStages = ROPE ? (D == 256 ? 3 : (D == 128 ? 6 : (D == 96 ? 8 : 6)))
                                         : (D == 256 ? 3 : (D == 128 ? 4 : (D == 96 ? 5 : 6)));
     static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
     // scratch of the last-CTA merge ((m, weight) pairs of a group's partials);
@@ -138,7 +138,7 @@ struct MmaCfg {
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes + kXBytes +
                                       kWarps * kMaxHeadsPerCta * 3 * 4 + kWarps * kStages * 8 +
                                       kRopeBytes + 16;
-    static constexpr int kMinBlocks = ROPE ? (D == 64 || D == 96 ? 3 : 2) : (D == 256 ? 2 : 3);
+    static constexpr int kMinBlocks = ROPE ? (D == 64 ? 3 : 2) : (D == 256 ? 2 : 3);
     static_assert(kMinBlocks * (kSmemBytes + 1024) <= 228 * 1024, "CTAs per SM by shared memory");
     static_assert(kRows64 || kPageBytes == kFullSlabs * kSlabBytes, "slab layout");
     static_assert(kPageBytes % 1024 == 0, "page slots keep the 1 KiB swizzle alignment");
