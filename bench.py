@@ -234,17 +234,19 @@ PAGES_CONTEXT = {
 def plan_summary(plan):
     """The plan fields that shape a launch, plus a short label."""
     # P<n>: no split; S<tokens> P<partitions> then cl<C> (cluster merge of C
-    # CTAs), or x<partitions per CTA> with lc (last-CTA merge) or mk (merge kernel)
+    # CTAs; "d": the deep-ring instance), or x<partitions per CTA> with lc
+    # (last-CTA merge) or mk (merge kernel)
     if plan.num_partitions == 1:
         short = "P1"
     elif plan.cluster > 1:
-        short = f"S{plan.partition_size} P{plan.num_partitions} cl{plan.cluster}"
+        short = (f"S{plan.partition_size} P{plan.num_partitions} cl{plan.cluster}"
+                 + ("d" if plan.deep_ring else ""))
     else:
         short = (f"S{plan.partition_size} P{plan.num_partitions} x{plan.parts_per_cta} "
                  + ("lc" if plan.merge_in_kernel else "mk"))
     return {"partitions": plan.num_partitions, "partition_size": plan.partition_size,
             "ctas": plan.ctas, "cluster": plan.cluster, "merge_in_kernel": plan.merge_in_kernel,
-            "parts_per_cta": plan.parts_per_cta, "short": short}
+            "parts_per_cta": plan.parts_per_cta, "deep_ring": plan.deep_ring, "short": short}
 
 
 KERNEL_IDS = {"simt": 1, "mma": 2}

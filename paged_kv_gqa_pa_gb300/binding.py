@@ -64,6 +64,7 @@ class pa_plan_t(ctypes.Structure):
         ("prewait_prefetch", ctypes.c_int),
         ("test_stall_bytes", ctypes.c_int),
         ("balanced", ctypes.c_int),
+        ("deep_ring", ctypes.c_int),
     ]
 
     def as_dict(self):

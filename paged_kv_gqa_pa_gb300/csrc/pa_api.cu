@@ -27,7 +27,7 @@ cudaError_t launch_attend_mma_rope_d(bool split, const AttendParams& p, const CU
                                      dim3 grid, cudaStream_t stream);
 
 template <int D, typename T, bool ROPE>
-cudaError_t attend_mma_cluster_occupancy(int c, int* clusters);
+cudaError_t attend_mma_cluster_occupancy(int c, int* clusters, bool deep);
 
 template <typename T>
 static cudaError_t launch_attend_mma_t(int D, bool split, const AttendParams& p,
@@ -176,11 +176,11 @@ static long long clusters_per_wave(int num_sms, int per_sm, int c) {
 }
 
 // cudaOccupancyMaxActiveClusters of the cluster-merge instance for (head
-// dim, element type, rotary) and clusters of c CTAs on the current device,
-// queried once per device and cached; -1 if the query fails.
-static long long device_clusters_per_wave(int D, int dtype, bool rope, int c) {
+// dim, element type, rotary, deep rings) and clusters of c CTAs on the
+// current device, queried once per device and cached; -1 if the query fails.
+static long long device_clusters_per_wave(int D, int dtype, bool rope, int c, bool deep = false) {
     constexpr int kMaxDevices = 64;
-    static std::atomic<int> cache[kMaxDevices][4][2][2][kMaxClusterParts];  // value + 1; 0 = unknown
+    static std::atomic<int> cache[kMaxDevices][4][2][2][2][kMaxClusterParts];  // value + 1; 0 = unknown
     int dev = 0;
     if (c < 2 || c > kMaxClusterParts || cudaGetDevice(&dev) != cudaSuccess || dev < 0 ||
         dev >= kMaxDevices) {
@@ -189,12 +189,12 @@ static long long device_clusters_per_wave(int D, int dtype, bool rope, int c) {
     }
     const int di = D == 64 ? 0 : D == 96 ? 1 : D == 128 ? 2 : 3;
     const int ti = dtype == PA_DTYPE_BF16 ? 1 : 0;
-    std::atomic<int>& slot = cache[dev][di][ti][rope ? 1 : 0][c - 1];
+    std::atomic<int>& slot = cache[dev][di][ti][rope ? 1 : 0][deep ? 1 : 0][c - 1];
     const int known = slot.load();
     if (known > 0) return known - 1;
     int n = 0;
     cudaError_t e = cudaErrorInvalidValue;
-#define PA_OCC(DD, TT, RR) e = attend_mma_cluster_occupancy<DD, TT, RR>(c, &n)
+#define PA_OCC(DD, TT, RR) e = attend_mma_cluster_occupancy<DD, TT, RR>(c, &n, deep)
 #define PA_OCC_D(TT, RR)                                                          \
     switch (D) {                                                                  \
         case 64: PA_OCC(64, TT, RR); break;                                       \
@@ -697,6 +697,24 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     // (its last CTA merges them, no second launch); the merge kernel when they
     // are many (the one-CTA merge would then trail the grid).
     plan->cluster = (use_cluster && P >= 2 && P <= kMaxClusterParts) ? P : 0;
+    // Deep page rings for cluster grids that do not fill the GPU (head dims
+    // 96 and 128 without rotary embedding; the others have one instance):
+    // with at most one CTA per SM each CTA streams alone, and 6 pages in
+    // flight per warp beat 4.  Measured on GB300 (graph-timed, 4-page rings
+    // at 3 CTAs per SM vs 6-page rings at 2, 32/8 heads at D 128): one
+    // sequence of 16K tokens 18.0 vs 16.1 us, of 8K 11.15 vs 10.43 us, two
+    // of 8K 14.4 vs 14.0 us; a full grid (8 ragged sequences) 14.3 vs 15.6 us.
+    plan->deep_ring = 0;
+    if (plan->cluster > 1 && kernel == PA_KERNEL_MMA && rope_theta <= 0.f &&
+        (head_dim == 96 || head_dim == 128)) {
+        const long long groups = (long long)batch * num_kv_heads * nchunk;
+        if (groups * plan->cluster <= num_sms) {
+            long long held = -1;
+            if (this_device) held = device_clusters_per_wave(head_dim, dtype, false, plan->cluster, true);
+            if (held < 0) held = clusters_per_wave(num_sms, 2, plan->cluster);
+            if (held >= groups) plan->deep_ring = 1;
+        }
+    }
     // Tensor-core kernel: each warp's first two pages are requested into L2
     // before the dependency wait.  Measured on GB300: 0.4-1.5 us less per
     // step when decode steps follow each other with programmatic dependent
@@ -841,6 +859,11 @@ static int check_plan(const pa_plan_t* plan) {
             return PA_ERR_INVALID_ARG;
     }
     if (plan->cluster < 0) return PA_ERR_INVALID_ARG;
+    if (plan->deep_ring != 0 && plan->deep_ring != 1) return PA_ERR_INVALID_ARG;
+    if (plan->deep_ring == 1 && plan->cluster > 1 &&
+        (plan->kernel != PA_KERNEL_MMA || plan->rope_theta > 0.f ||
+         (plan->head_dim != 96 && plan->head_dim != 128)))
+        return PA_ERR_INVALID_ARG;
     if (plan->prewait_prefetch < 0 || plan->prewait_prefetch > kMaxPrewaitPrefetch)
         return PA_ERR_INVALID_ARG;
     if (plan->test_stall_bytes < 0 || plan->test_stall_bytes > 4096) return PA_ERR_INVALID_ARG;
@@ -907,6 +930,7 @@ int pa_decode_partitions(const pa_plan_t* plan, const void* q, const void* k_cac
     p.ws_info = reinterpret_cast<int*>(ws + wl.info_off);
     p.merge_in_kernel = (plan->kernel == PA_KERNEL_MMA && P > 1 && plan->merge_in_kernel) ? 1 : 0;
     p.cluster = (plan->kernel == PA_KERNEL_MMA && P > 1 && plan->cluster > 1) ? plan->cluster : 0;
+    p.deep = p.cluster > 1 && plan->deep_ring == 1 ? 1 : 0;
     p.B = plan->batch;
     p.Hq = plan->num_q_heads;
     p.Hkv = plan->num_kv_heads;

@@ -603,11 +603,11 @@ static_assert(ClusterPartial<64>::kMaxBytes <= MmaCfg<64>::kWideXOff &&
 // the partitions of a group form one cluster and merge in it; a separate
 // instance, so that the other instances carry none of its code.  ROPE: q and
 // each K row are rotated to their positions before q.K.
-template <int D, typename T, bool SPLIT, bool CLUSTER, bool ROPE>
-__global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
+template <int D, typename T, bool SPLIT, bool CLUSTER, bool ROPE, bool DEEP = false>
+__global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE, DEEP>::kMinBlocks)
     attend_mma_kernel(const AttendParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
-    using Cfg = MmaCfg<D, ROPE>;
+    using Cfg = MmaCfg<D, ROPE, DEEP>;
     constexpr int NS = Cfg::kStages;
     constexpr int PB = Cfg::kPageBytes;
     constexpr int KT = D / 16;  // k-steps of q.K, m-tiles of P.V
@@ -1213,38 +1213,50 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE>::kMinBlocks)
                                             reinterpret_cast<float*>(ring));
 }
 
+// Whether (D, ROPE) has a deep-ring cluster instance (MmaCfg DEEP).
+template <int D, bool ROPE>
+constexpr bool kHasDeep = !ROPE && (D == 96 || D == 128);
+
 template <int D, typename T, bool ROPE>
 cudaError_t launch_attend_mma_dr(bool split, const AttendParams& p, const CUtensorMap* maps,
                                  dim3 grid, cudaStream_t stream) {
     const bool clustered = split && p.cluster > 1;
+    const bool deep = clustered && p.deep && kHasDeep<D, ROPE>;
     const void* fn =
         !split ? reinterpret_cast<const void*>(&attend_mma_kernel<D, T, false, false, ROPE>)
         : clustered ? reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true, true, ROPE>)
                     : reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true, false, ROPE>);
+    int smem = MmaCfg<D, ROPE>::kSmemBytes;
+    if constexpr (kHasDeep<D, ROPE>) {
+        if (deep) {
+            fn = reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true, true, ROPE, true>);
+            smem = MmaCfg<D, ROPE, true>::kSmemBytes;
+        }
+    }
     constexpr int kMaxDevices = 64;
     static std::atomic<uint32_t> configured[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const uint32_t bit = !split ? 1u : (clustered ? 8u : 2u);
+    const uint32_t bit = !split ? 1u : (clustered ? (deep ? 16u : 8u) : 2u);
+    const uint32_t nonportable_bit = deep ? 32u : 4u;
     if (dev < 0 || dev >= kMaxDevices || !(configured[dev].load() & bit)) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 MmaCfg<D, ROPE>::kSmemBytes);
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDevices) configured[dev].fetch_or(bit);
     }
     void* args[] = {const_cast<AttendParams*>(&p), const_cast<CUtensorMap*>(&maps[0]),
                     const_cast<CUtensorMap*>(&maps[1])};
     if (clustered && p.cluster > 8 &&
-        (dev < 0 || dev >= kMaxDevices || !(configured[dev].load() & 4u))) {
+        (dev < 0 || dev >= kMaxDevices || !(configured[dev].load() & nonportable_bit))) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDevices) configured[dev].fetch_or(4u);
+        if (dev >= 0 && dev < kMaxDevices) configured[dev].fetch_or(nonportable_bit);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = MmaCfg<D, ROPE>::kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1264,10 +1276,18 @@ cudaError_t launch_attend_mma_dr(bool split, const AttendParams& p, const CUtens
 // for this device (its SM count and GPC layout), where a table measured on one
 // part would only be a guess on another.
 template <int D, typename T, bool ROPE>
-cudaError_t attend_mma_cluster_occupancy(int c, int* clusters) {
+cudaError_t attend_mma_cluster_occupancy(int c, int* clusters, bool deep) {
     const void* fn = reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true, true, ROPE>);
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         MmaCfg<D, ROPE>::kSmemBytes);
+    int smem = MmaCfg<D, ROPE>::kSmemBytes;
+    if constexpr (kHasDeep<D, ROPE>) {
+        if (deep) {
+            fn = reinterpret_cast<const void*>(&attend_mma_kernel<D, T, true, true, ROPE, true>);
+            smem = MmaCfg<D, ROPE, true>::kSmemBytes;
+        }
+    } else if (deep) {
+        return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (c > 8) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1276,7 +1296,7 @@ cudaError_t attend_mma_cluster_occupancy(int c, int* clusters) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)c, 1, 1);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = MmaCfg<D, ROPE>::kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)c;

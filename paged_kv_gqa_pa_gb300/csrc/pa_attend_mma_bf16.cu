@@ -13,8 +13,8 @@ template cudaError_t launch_attend_mma_d<128, __nv_bfloat16>(bool, const AttendP
                                                    dim3, cudaStream_t);
 template cudaError_t launch_attend_mma_d<256, __nv_bfloat16>(bool, const AttendParams&, const CUtensorMap*,
                                                    dim3, cudaStream_t);
-template cudaError_t attend_mma_cluster_occupancy<64, __nv_bfloat16, false>(int, int*);
-template cudaError_t attend_mma_cluster_occupancy<96, __nv_bfloat16, false>(int, int*);
-template cudaError_t attend_mma_cluster_occupancy<128, __nv_bfloat16, false>(int, int*);
-template cudaError_t attend_mma_cluster_occupancy<256, __nv_bfloat16, false>(int, int*);
+template cudaError_t attend_mma_cluster_occupancy<64, __nv_bfloat16, false>(int, int*, bool);
+template cudaError_t attend_mma_cluster_occupancy<96, __nv_bfloat16, false>(int, int*, bool);
+template cudaError_t attend_mma_cluster_occupancy<128, __nv_bfloat16, false>(int, int*, bool);
+template cudaError_t attend_mma_cluster_occupancy<256, __nv_bfloat16, false>(int, int*, bool);
 }  // namespace pa

@@ -13,8 +13,8 @@ template cudaError_t launch_attend_mma_d<128, __half>(bool, const AttendParams&,
                                                    dim3, cudaStream_t);
 template cudaError_t launch_attend_mma_d<256, __half>(bool, const AttendParams&, const CUtensorMap*,
                                                    dim3, cudaStream_t);
-template cudaError_t attend_mma_cluster_occupancy<64, __half, false>(int, int*);
-template cudaError_t attend_mma_cluster_occupancy<96, __half, false>(int, int*);
-template cudaError_t attend_mma_cluster_occupancy<128, __half, false>(int, int*);
-template cudaError_t attend_mma_cluster_occupancy<256, __half, false>(int, int*);
+template cudaError_t attend_mma_cluster_occupancy<64, __half, false>(int, int*, bool);
+template cudaError_t attend_mma_cluster_occupancy<96, __half, false>(int, int*, bool);
+template cudaError_t attend_mma_cluster_occupancy<128, __half, false>(int, int*, bool);
+template cudaError_t attend_mma_cluster_occupancy<256, __half, false>(int, int*, bool);
 }  // namespace pa

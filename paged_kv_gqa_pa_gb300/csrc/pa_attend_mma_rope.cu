@@ -16,7 +16,7 @@ PA_ROPE_INSTANCE(96, __nv_bfloat16)
 PA_ROPE_INSTANCE(128, __nv_bfloat16)
 PA_ROPE_INSTANCE(256, __nv_bfloat16)
 #undef PA_ROPE_INSTANCE
-#define PA_ROPE_OCCUPANCY(D, T) template cudaError_t attend_mma_cluster_occupancy<D, T, true>(int, int*);
+#define PA_ROPE_OCCUPANCY(D, T) template cudaError_t attend_mma_cluster_occupancy<D, T, true>(int, int*, bool);
 PA_ROPE_OCCUPANCY(64, __half)
 PA_ROPE_OCCUPANCY(96, __half)
 PA_ROPE_OCCUPANCY(128, __half)

@@ -52,7 +52,7 @@ def to_device(case, device="cuda"):
 
 def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=None,
             guard=0, parts_per_cta=None, merge_in_kernel=None, ws=None, cluster=None,
-            prewait_prefetch=None, test_stall_bytes=None):
+            prewait_prefetch=None, test_stall_bytes=None, deep_ring=None):
     """Plan + pa_decode through the C ABI.  Returns (out fp64 numpy, lse fp64
     numpy, device error word, plan).  With guard > 0 the outputs and the
     workspace sit inside larger NaN/0xA5-filled buffers whose guard regions are
@@ -60,7 +60,8 @@ def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=N
     partition count must be 2..16), False forbids it, None keeps the planner's
     choice; forcing several partitions per CTA or the last-CTA merge drops it.
     prewait_prefetch overrides the plan's pre-wait L2 prefetch (pages per warp);
-    test_stall_bytes sets the plan's copy-timeout test hook."""
+    test_stall_bytes sets the plan's copy-timeout test hook; deep_ring picks
+    the cluster instance with deeper page rings (1) or not (0)."""
     ensure_built()
     dev = dev or to_device(case)
     B, Hq, D = case.q.shape
@@ -94,6 +95,8 @@ def run_gpu(case, partition_size=None, max_context_len=None, dev=None, num_sms=N
         plan.prewait_prefetch = prewait_prefetch
     if test_stall_bytes is not None:
         plan.test_stall_bytes = test_stall_bytes
+    if deep_ring is not None:
+        plan.deep_ring = deep_ring
     n_out = B * Hq * D
     et = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[case.dtype]
     out_buf = torch.full((n_out + 2 * guard,), float("nan"), dtype=et, device="cuda")

@@ -53,12 +53,13 @@ def test_plan_struct_layout_matches_header():
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     fields = re.findall(r"\b(?:int|size_t|float)\s+([a-z_0-9]+)(?:\[\d+\])?\s*;", body)
     assert fields == [f for f, _ in binding.pa_plan_t._fields_]
-    # 14 ints, a size_t, then 10 four-byte fields (kernel ... balanced).
+    # 14 ints, a size_t, then 11 four-byte fields (kernel ... deep_ring).
     assert binding.pa_plan_t.workspace_bytes.offset == 56
     assert binding.pa_plan_t.kernel.offset == 64
     assert binding.pa_plan_t.parts_per_cta.offset == 68
     assert binding.pa_plan_t.prewait_prefetch.offset == 92
-    assert ctypes.sizeof(binding.pa_plan_t) == 104
+    assert binding.pa_plan_t.deep_ring.offset == 104
+    assert ctypes.sizeof(binding.pa_plan_t) == 112
 
 
 def test_status_strings_and_version():
@@ -489,3 +490,36 @@ def test_rotary_plans_merge_in_the_last_cta_when_partials_are_small():
     # without rotary embedding the same small shape keeps the merge kernel
     plain = pa.pa_plan_ex(4, 24, 4, 256, 16, 4 * 2048 + 8, 2048, 32768, 0, 1824, 152)
     assert plain.num_partitions == 18 and plain.merge_in_kernel == 0
+
+
+def test_deep_ring_cluster_instance_for_small_cluster_grids():
+    """Cluster plans of plain head dims 96 and 128 whose grid has at most one
+    CTA per SM take the instance with deeper page rings (2 CTAs per SM)."""
+    def plan(B, D, L, **kw):
+        pages = -(-L // 16)
+        return pa.pa_plan_ex(B, 32, 8, D, 16, B * pages + 8, pages, L, 0, 0, 152, **kw)
+    for D in (96, 128):
+        one = plan(1, D, 16384)
+        assert one.cluster == 16 and one.ctas == 128 and one.deep_ring == 1
+    # a grid that needs more than one CTA per SM, other head dims, rotary
+    # plans and plans without a cluster keep the default instance
+    assert plan(8, 128, 4096).cluster == 6 and plan(8, 128, 4096).deep_ring == 0
+    assert plan(2, 128, 8192).ctas > 152 and plan(2, 128, 8192).deep_ring == 0
+    assert plan(1, 64, 16384).cluster == 16 and plan(1, 64, 16384).deep_ring == 0
+    assert plan(1, 128, 16384, rope_theta=1e4).deep_ring == 0
+    assert plan(1, 128, 32768).cluster == 0 and plan(1, 128, 32768).deep_ring == 0
+    # the ABI: 0 or 1; with a cluster, 1 only where the instance exists; it is
+    # ignored without a cluster
+    ok = plan(1, 128, 16384)
+    for field, value, status in (("deep_ring", 2, binding.PA_ERR_INVALID_ARG),
+                                 ("deep_ring", -1, binding.PA_ERR_INVALID_ARG)):
+        bad = binding.pa_plan_t.from_buffer_copy(ok)
+        setattr(bad, field, value)
+        assert _call_decode(bad) == status
+    rope = plan(1, 128, 16384, rope_theta=1e4)
+    assert rope.cluster > 1
+    rope.deep_ring = 1
+    assert _call_decode(rope) == binding.PA_ERR_INVALID_ARG
+    d64 = plan(1, 64, 16384)
+    d64.deep_ring = 1
+    assert _call_decode(d64) == binding.PA_ERR_INVALID_ARG

@@ -183,3 +183,20 @@ def test_plan_for_this_device_asks_it_and_agrees_with_the_gb300_table(D, dtype, 
         assert asked.num_sms == 152
         assert (asked.cluster, asked.num_partitions, asked.partition_size) == \
             (table.cluster, table.num_partitions, table.partition_size), (B, D, dtype, rope)
+
+
+@pytest.mark.parametrize("D,dtype", [(128, "f16"), (96, "f16"), (128, "bf16"), (96, "bf16")])
+@pytest.mark.parametrize("lens,window", [([16384], 0), ([8000], 0), ([12345], 4096), ([1], 0)])
+def test_deep_ring_cluster_instance_matches_the_default_one(D, dtype, lens, window):
+    """The deep-ring cluster instance (2 CTAs per SM, more pages in flight per
+    warp) walks the same pages in the same order as the default one: results
+    are bitwise equal, and match the oracle."""
+    case = workloads.make_case("deep", len(lens), 32, 8, D, lens, seed=1240 + D, window=window,
+                               dtype=dtype, q_std=2.0)
+    a = run_gpu(case, guard=32, deep_ring=1)
+    b = run_gpu(case, guard=32, deep_ring=0)
+    assert a[2] == 0 and b[2] == 0
+    if lens[0] > 1:
+        assert a[3].cluster > 1 and a[3].deep_ring == 1
+    assert np.array_equal(a[0], b[0], equal_nan=True) and np.array_equal(a[1], b[1], equal_nan=True)
+    assert_matches_oracle(case, a[0], a[1], what=f"deep ring D{D} {dtype} {lens}")
