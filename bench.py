@@ -54,10 +54,10 @@ FALLBACK_HBM_GBS = 6800.0
 # `src_sha` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     # One ncu capture of this kernel on the same workload cut to its first
-    # sequence (B = 1): (409.71 + 3.25) MB read + written per launch, scaled by
+    # sequence (B = 1): (409.72 + 3.68) MB read + written per launch, scaled by
     # tokens to the B = 4 launch.
-    ("gqa6_ctx100k", "mma"): {"src_sha": "fbee60bc20e96684", "partition_size": 512,
-                              "bytes_per_launch": 4 * (409.710592e6 + 3.251712e6)},
+    ("gqa6_ctx100k", "mma"): {"src_sha": "7f5d6b9564eec3d6", "partition_size": 512,
+                              "bytes_per_launch": 4 * (409.718784e6 + 3.684608e6)},
 }
 
 
