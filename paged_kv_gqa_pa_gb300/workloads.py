@@ -214,6 +214,9 @@ EXTRA_WORKLOADS = {
                                 seed=1011),
     "skewed16_d128_ctx12k": dict(B=16, Hq=32, Hkv=8, D=128, lens=[12000] + [200] * 15,
                                  seed=1012),
+    # One sequence of 16K tokens (Llama-3-8B-style heads): a cluster grid of
+    # 128 CTAs, fewer than the SMs, which the deep-ring instance serves.
+    "single16k_d128": dict(B=1, Hq=32, Hkv=8, D=128, lens=[16384], seed=1013),
 }
 EXTRA_ORDER = list(EXTRA_WORKLOADS)
 ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}
