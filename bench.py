@@ -54,10 +54,10 @@ FALLBACK_HBM_GBS = 6800.0
 # `src_sha` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     # One ncu capture of this kernel on the same workload cut to its first
-    # sequence (B = 1): (409.72 + 3.68) MB read + written per launch, scaled by
+    # sequence (B = 1): (409.72 + 3.71) MB read + written per launch, scaled by
     # tokens to the B = 4 launch.
-    ("gqa6_ctx100k", "mma"): {"src_sha": "7f5d6b9564eec3d6", "partition_size": 512,
-                              "bytes_per_launch": 4 * (409.718784e6 + 3.684608e6)},
+    ("gqa6_ctx100k", "mma"): {"src_sha": "42f47dba44d6b3c6", "partition_size": 512,
+                              "bytes_per_launch": 4 * (409.715712e6 + 3.714304e6)},
 }
 
 

@@ -164,13 +164,14 @@ typedef struct pa_plan {
                                cluster merge, not unsplit); 0 = fixed-size
                                partitions */
     int deep_ring;          /* 1: with a cluster (tensor-core kernel, no rotary
-                               embedding, head_dim 96 or 128), the instance with deeper
-                               page rings at 2 CTAs per SM instead of 3, for cluster
-                               grids that do not fill the GPU: a CTA streaming alone on
-                               its SM is bound by what its own ring keeps in flight.
-                               pa_plan_ex sets it when the grid has at most one CTA per
-                               SM and one wave of the instance holds every cluster;
-                               0 otherwise.  Ignored without a cluster; with one, 1 is
+                               embedding, head_dim 96, 128 or 256), the instance with
+                               deeper page rings at 2 CTAs per SM instead of 3 (at
+                               head_dim 256: 1 instead of 2), for cluster grids that do
+                               not fill the GPU: a CTA streaming alone on its SM is
+                               bound by what its own ring keeps in flight.  pa_plan_ex
+                               sets it when the grid has at most one CTA per SM (at
+                               head_dim 256 at most one per two SMs) and one wave of the
+                               instance holds every cluster; 0 otherwise.  Ignored without a cluster; with one, 1 is
                                rejected for other kernels, head dims or rotary plans */
 } pa_plan_t;
 

@@ -698,20 +698,26 @@ int pa_plan_ex(int batch, int num_q_heads, int num_kv_heads, int head_dim, int p
     // are many (the one-CTA merge would then trail the grid).
     plan->cluster = (use_cluster && P >= 2 && P <= kMaxClusterParts) ? P : 0;
     // Deep page rings for cluster grids that do not fill the GPU (head dims
-    // 96 and 128 without rotary embedding; the others have one instance):
-    // with at most one CTA per SM each CTA streams alone, and 6 pages in
-    // flight per warp beat 4.  Measured on GB300 (graph-timed, 4-page rings
-    // at 3 CTAs per SM vs 6-page rings at 2, 32/8 heads at D 128): one
-    // sequence of 16K tokens 18.0 vs 16.1 us, of 8K 11.15 vs 10.43 us, two
-    // of 8K 14.4 vs 14.0 us; a full grid (8 ragged sequences) 14.3 vs 15.6 us.
+    // 96, 128 and 256 without rotary embedding; the others have one
+    // instance): with at most one CTA per SM each CTA streams alone, and more
+    // pages in flight per warp win.  Measured on GB300 (graph-timed, default
+    // vs deep instance): 32/8 heads at D 128, one sequence of 16K tokens
+    // 18.0 vs 16.1 us, of 8K 11.15 vs 10.43 us, two of 8K 14.4 vs 14.0 us; a
+    // full grid (8 ragged sequences) 14.3 vs 15.6 us.  At D 256 the deep
+    // instance runs 1 CTA per SM with 6-page rings: one sequence of 16K
+    // tokens, 24/4 heads (64 CTAs) 18.9 vs 17.05 us, but 128 CTAs (8/4 heads,
+    // two sequences; or 16/8 heads) 10.6 vs 16.2 and 15.6 vs 21.6 us, so
+    // there it is taken only for grids of at most half the SMs.
     plan->deep_ring = 0;
     if (plan->cluster > 1 && kernel == PA_KERNEL_MMA && rope_theta <= 0.f &&
-        (head_dim == 96 || head_dim == 128)) {
+        (head_dim == 96 || head_dim == 128 || head_dim == 256)) {
         const long long groups = (long long)batch * num_kv_heads * nchunk;
-        if (groups * plan->cluster <= num_sms) {
+        const int deep_per_sm = head_dim == 256 ? 1 : 2;
+        const long long max_ctas = head_dim == 256 ? num_sms / 2 : num_sms;
+        if (groups * plan->cluster <= max_ctas) {
             long long held = -1;
             if (this_device) held = device_clusters_per_wave(head_dim, dtype, false, plan->cluster, true);
-            if (held < 0) held = clusters_per_wave(num_sms, 2, plan->cluster);
+            if (held < 0) held = clusters_per_wave(num_sms, deep_per_sm, plan->cluster);
             if (held >= groups) plan->deep_ring = 1;
         }
     }
@@ -862,7 +868,7 @@ static int check_plan(const pa_plan_t* plan) {
     if (plan->deep_ring != 0 && plan->deep_ring != 1) return PA_ERR_INVALID_ARG;
     if (plan->deep_ring == 1 && plan->cluster > 1 &&
         (plan->kernel != PA_KERNEL_MMA || plan->rope_theta > 0.f ||
-         (plan->head_dim != 96 && plan->head_dim != 128)))
+         (plan->head_dim != 96 && plan->head_dim != 128 && plan->head_dim != 256)))
         return PA_ERR_INVALID_ARG;
     if (plan->prewait_prefetch < 0 || plan->prewait_prefetch > kMaxPrewaitPrefetch)
         return PA_ERR_INVALID_ARG;

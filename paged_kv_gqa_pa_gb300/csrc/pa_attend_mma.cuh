@@ -1215,7 +1215,7 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<D, ROPE, DEEP>::kMinBlocks)
 
 // Whether (D, ROPE) has a deep-ring cluster instance (MmaCfg DEEP).
 template <int D, bool ROPE>
-constexpr bool kHasDeep = !ROPE && (D == 96 || D == 128);
+constexpr bool kHasDeep = !ROPE && (D == 96 || D == 128 || D == 256);
 
 template <int D, typename T, bool ROPE>
 cudaError_t launch_attend_mma_dr(bool split, const AttendParams& p, const CUtensorMap* maps,

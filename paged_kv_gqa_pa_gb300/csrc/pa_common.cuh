@@ -108,13 +108,14 @@ struct AttendCfg {
 // ROPE: the rotary instances, which keep the rotated q (hi + lo) and the
 // lane's rotary state in registers; they run 2 CTAs per SM (3 at D = 64) with
 // deeper rings, plus the per-CTA tables of the 8- and 64-token rotations.
-// DEEP: the cluster-merge instances of plain head dims 96 and 128 for grids
-// that do not fill the GPU: 2 CTAs per SM with the deeper rings, since a CTA
-// that streams alone on its SM is bound by the bytes its own ring keeps in
-// flight.
+// DEEP: the cluster-merge instances of plain head dims 96, 128 and 256 for
+// grids that do not fill the GPU: 2 CTAs per SM with the deeper rings (1 with
+// 6-page rings at D = 256), since a CTA that streams alone on its SM is bound
+// by the bytes its own ring keeps in flight.
 template <int D, bool ROPE = false, bool DEEP = false>
 struct MmaCfg {
-    static_assert(!DEEP || (!ROPE && (D == 96 || D == 128)), "deep rings: plain D 96 / 128");
+    static_assert(!DEEP || (!ROPE && (D == 96 || D == 128 || D == 256)),
+                  "deep rings: plain head dims 96, 128 and 256");
     static_assert(D % 64 == 0 || (D % 64 == 32 && (D / 32) % 2 == 1),
                   "head dim: 64-column slabs, or an odd number of 32-column units");
     static constexpr bool kRows64 = (D % 64) != 0;  // one 3-D box, 64-byte units, 64-byte swizzle
@@ -124,7 +125,7 @@ struct MmaCfg {
     // pages in flight per warp; with the fixed buffers below this keeps
     // kMinBlocks CTAs per SM within 228 KiB of shared memory
     static constexpr int kStages = ROPE || DEEP
-                                       ? (D == 256 ? 3 : (D == 128 ? 6 : (D == 96 ? 8 : 6)))
+                                       ? (D == 256 ? (DEEP ? 6 : 3) : (D == 128 ? 6 : (D == 96 ? 8 : 6)))
                                        : (D == 256 ? 3 : (D == 128 ? 4 : (D == 96 ? 5 : 6)));
     static constexpr int kRingBytes = kWarps * kStages * kPageBytes;
     // scratch of the last-CTA merge ((m, weight) pairs of a group's partials);
@@ -145,7 +146,8 @@ struct MmaCfg {
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes + kXBytes +
                                       kWarps * kMaxHeadsPerCta * 3 * 4 + kWarps * kStages * 8 +
                                       kRopeBytes + 16;
-    static constexpr int kMinBlocks = ROPE ? (D == 64 ? 3 : 2) : (D == 256 || DEEP ? 2 : 3);
+    static constexpr int kMinBlocks =
+        ROPE ? (D == 64 ? 3 : 2) : (DEEP && D == 256 ? 1 : (D == 256 || DEEP ? 2 : 3));
     static_assert(kMinBlocks * (kSmemBytes + 1024) <= 228 * 1024, "CTAs per SM by shared memory");
     static_assert(kRows64 || kPageBytes == kFullSlabs * kSlabBytes, "slab layout");
     static_assert(kPageBytes % 1024 == 0, "page slots keep the 1 KiB swizzle alignment");

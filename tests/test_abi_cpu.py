@@ -494,7 +494,8 @@ def test_rotary_plans_merge_in_the_last_cta_when_partials_are_small():
 
 def test_deep_ring_cluster_instance_for_small_cluster_grids():
     """Cluster plans of plain head dims 96 and 128 whose grid has at most one
-    CTA per SM take the instance with deeper page rings (2 CTAs per SM)."""
+    CTA per SM take the instance with deeper page rings (2 CTAs per SM); at
+    head dim 256 (1 CTA per SM) grids of at most half the SMs."""
     def plan(B, D, L, **kw):
         pages = -(-L // 16)
         return pa.pa_plan_ex(B, 32, 8, D, 16, B * pages + 8, pages, L, 0, 0, 152, **kw)
@@ -506,6 +507,13 @@ def test_deep_ring_cluster_instance_for_small_cluster_grids():
     assert plan(8, 128, 4096).cluster == 6 and plan(8, 128, 4096).deep_ring == 0
     assert plan(2, 128, 8192).ctas > 152 and plan(2, 128, 8192).deep_ring == 0
     assert plan(1, 64, 16384).cluster == 16 and plan(1, 64, 16384).deep_ring == 0
+    # head dim 256: 1 CTA per SM, only for grids of at most half the SMs
+    def plan256(B, Hq, Hkv, L, window=0):
+        pages = -(-L // 16)
+        return pa.pa_plan_ex(B, Hq, Hkv, 256, 16, B * pages + 8, pages, L, window, 0, 152)
+    assert plan256(1, 24, 4, 16384).ctas == 64 and plan256(1, 24, 4, 16384).deep_ring == 1
+    assert plan256(1, 16, 8, 8192).ctas == 128 and plan256(1, 16, 8, 8192).deep_ring == 0
+    assert plan256(4, 8, 4, 8192, 4096).deep_ring == 0  # the Gemma-2 workload
     assert plan(1, 128, 16384, rope_theta=1e4).deep_ring == 0
     assert plan(1, 128, 32768).cluster == 0 and plan(1, 128, 32768).deep_ring == 0
     # the ABI: 0 or 1; with a cluster, 1 only where the instance exists; it is

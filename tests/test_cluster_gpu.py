@@ -185,7 +185,8 @@ def test_plan_for_this_device_asks_it_and_agrees_with_the_gb300_table(D, dtype, 
             (table.cluster, table.num_partitions, table.partition_size), (B, D, dtype, rope)
 
 
-@pytest.mark.parametrize("D,dtype", [(128, "f16"), (96, "f16"), (128, "bf16"), (96, "bf16")])
+@pytest.mark.parametrize("D,dtype", [(128, "f16"), (96, "f16"), (128, "bf16"), (96, "bf16"),
+                                     (256, "f16"), (256, "bf16")])
 @pytest.mark.parametrize("lens,window", [([16384], 0), ([8000], 0), ([12345], 4096), ([1], 0)])
 def test_deep_ring_cluster_instance_matches_the_default_one(D, dtype, lens, window):
     """The deep-ring cluster instance (2 CTAs per SM, more pages in flight per
