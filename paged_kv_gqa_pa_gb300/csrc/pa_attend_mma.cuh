@@ -218,8 +218,8 @@ __device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, co
         s_m[idx] = __ldcg(p.ws_m + row0 + (size_t)h * p.P + i);
         s_w[idx] = __ldcg(p.ws_l + row0 + (size_t)h * p.P + i);
     }
-    for (int base = 0; base < items; base += kThreads) {  // (the same rounds in every thread)
-        const int n_it = min(kThreads, items - base);   // items of this round
+    for (int base = 0; base < items; base += kThreads) {  // (the same passes in every thread)
+        const int n_it = min(kThreads, items - base);   // items of this pass
         const int tpi = kThreads / n_it;                 // threads per item
         const int item = threadIdx.x % n_it;
         const int sub = threadIdx.x / n_it;              // < tpi for active threads
@@ -273,7 +273,7 @@ __device__ __forceinline__ void group_arrive_and_merge(const AttendParams& p, co
                 acc.w += w * ov[u].w;
             }
         }
-        if (tpi > 1) {  // (only with fewer items than threads: a single round)
+        if (tpi > 1) {  // (only with fewer items than threads: a single pass)
             if (active) reinterpret_cast<float4*>(scratch)[sub * n_it + item] = acc;
             __syncthreads();
             if (sub == 0) {
